@@ -1,0 +1,214 @@
+"""Python binding of libtwell.so, the TwELL activation-sparse FFN for GB300.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels (include/twell.h documents each call).  torch supplies device memory
+and the current stream; bf16 tensors are passed by pointer.  If the library
+has not been built, every call raises -- there is no CPU or eager fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtwell.so")
+
+TWELL_OK = 0
+KERNELS = {
+    "up_pack": 0, "route": 1, "fb_gather": 2, "fb_up": 3, "spmm": 4, "fb_down": 5, "pack": 6,
+    "unpack": 7, "sddmm": 8, "dx": 9, "dw": 10, "dense_gemm": 11, "aux": 12,
+}
+EXPORTED = [
+    "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",
+    "twell_bwd_workspace_bytes", "twell_dense_ffn_fwd", "twell_read_status", "twell_status_string",
+    "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
+]
+
+
+class TwellError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class twell_t(ctypes.Structure):
+    _fields_ = [
+        ("n_rows", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("tile", ctypes.c_int32),
+        ("cap", ctypes.c_int32), ("fb_cap", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("values", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+        ("row_fb", ctypes.c_void_p), ("fb_rows", ctypes.c_void_p), ("fb_dense", ctypes.c_void_p),
+        ("n_fb", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
+_lib_handle = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads libtwell.so; raises if it is missing (build it with __graft_entry__.build())."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    L = ctypes.POINTER(twell_t)
+    sig = {
+        "twell_pack": (ctypes.c_int, [P, I64, L, P]),
+        "twell_unpack": (ctypes.c_int, [L, P, I64, P]),
+        "twell_ffn_fwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
+        "twell_fwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+        "twell_ffn_bwd": (ctypes.c_int, [P, P, P, L, I32, P, ctypes.c_float, P, P, P, P, P, SZ, P]),
+        "twell_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+        "twell_dense_ffn_fwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, P, P, P]),
+        "twell_read_status": (ctypes.c_int, [L, P]),
+        "twell_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "twell_launch_count": (I64, []),
+        "twell_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+        "twell_profile_reset": (ctypes.c_int, []),
+        "twell_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib_handle = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().twell_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != TWELL_OK:
+        raise TwellError(code, where)
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("tensors passed to libtwell must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+@dataclass
+class Packed:
+    """Device buffers of one TwELL hybrid layout and the twell_t that names them."""
+    values: "object"
+    idx: "object"
+    counts: "object"
+    row_fb: "object"
+    fb_rows: "object"
+    fb_dense: "object"
+    n_fb: "object"
+    status: "object"
+    n_rows: int
+    d_ff: int
+    tile: int
+    cap: int
+    fb_cap: int
+
+    def struct(self) -> twell_t:
+        p = lambda t: t.data_ptr() if t is not None and t.numel() else None
+        return twell_t(self.n_rows, self.d_ff, self.tile, self.cap, self.fb_cap, 0,
+                       p(self.values), p(self.idx), p(self.counts), p(self.row_fb), p(self.fb_rows),
+                       p(self.fb_dense), p(self.n_fb), p(self.status))
+
+
+def alloc_packed(n_rows: int, d_ff: int, tile: int, cap: int, fb_cap: int, device="cuda") -> Packed:
+    import torch
+    nt = d_ff // tile
+    kw = dict(device=device)
+    return Packed(
+        values=torch.empty((n_rows, nt, cap), dtype=torch.bfloat16, **kw),
+        idx=torch.empty((n_rows, nt, cap), dtype=torch.uint8, **kw),
+        counts=torch.empty((n_rows, nt), dtype=torch.uint8, **kw),
+        row_fb=torch.empty((max(n_rows, 1),), dtype=torch.int32, **kw),
+        fb_rows=torch.empty((max(fb_cap, 1),), dtype=torch.int32, **kw),
+        fb_dense=torch.empty((max(fb_cap, 1), d_ff), dtype=torch.bfloat16, **kw),
+        n_fb=torch.zeros((4,), dtype=torch.int32, **kw),
+        status=torch.zeros((4,), dtype=torch.int32, **kw),
+        n_rows=n_rows, d_ff=d_ff, tile=tile, cap=cap, fb_cap=fb_cap,
+    )
+
+
+def twell_pack(H, packed: Packed, stream=None) -> None:
+    """Dense bf16 H [n_rows, >= d_ff] -> TwELL hybrid (asynchronous)."""
+    st = packed.struct()
+    _check(load_library().twell_pack(_ptr(H), H.stride(0), ctypes.byref(st), _stream(stream)), "twell_pack")
+
+
+def twell_unpack(packed: Packed, H, stream=None) -> None:
+    st = packed.struct()
+    _check(load_library().twell_unpack(ctypes.byref(st), _ptr(H), H.stride(0), _stream(stream)), "twell_unpack")
+
+
+def fwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
+    return int(load_library().twell_fwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
+
+
+def bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
+    return int(load_library().twell_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
+
+
+def twell_ffn_fwd(X, W_inT, b, W_down, packed: Packed, Y, workspace, stream=None) -> None:
+    n, d = X.shape
+    f = W_inT.shape[0]
+    st = packed.struct()
+    _check(load_library().twell_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, ctypes.byref(st),
+                                        _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "twell_ffn_fwd")
+
+
+def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW_inT, dW_down, db, workspace,
+                  stream=None) -> None:
+    d = X.shape[1]
+    st = packed.struct()
+    _check(load_library().twell_ffn_bwd(_ptr(X), _ptr(W_inT), _ptr(W_down), ctypes.byref(st), d, _ptr(dY),
+                                        float(l1_lambda), _ptr(dX), _ptr(dW_inT), _ptr(dW_down), _ptr(db),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "twell_ffn_bwd")
+
+
+def twell_dense_ffn_fwd(X, W_inT, b, W_downT, Hbuf, Y, stream=None) -> None:
+    n, d = X.shape
+    f = W_inT.shape[0]
+    _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_downT), n, d, f, _ptr(Hbuf),
+                                              _ptr(Y), _stream(stream)), "twell_dense_ffn_fwd")
+
+
+def twell_read_status(packed: Packed, stream=None) -> int:
+    st = packed.struct()
+    return int(load_library().twell_read_status(ctypes.byref(st), _stream(stream)))
+
+
+def twell_launch_count() -> int:
+    return int(load_library().twell_launch_count())
+
+
+def twell_profile_enable(on: bool) -> None:
+    _check(load_library().twell_profile_enable(1 if on else 0), "twell_profile_enable")
+
+
+def twell_profile_reset() -> None:
+    _check(load_library().twell_profile_reset(), "twell_profile_reset")
+
+
+def twell_profile_read(kernel) -> tuple:
+    """(launches, total_ms) of one kernel id or name since the last reset."""
+    k = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(load_library().twell_profile_read(k, ctypes.byref(n), ctypes.byref(ms)), "twell_profile_read")
+    return int(n.value), float(ms.value)

@@ -1,0 +1,351 @@
+// Host side of the C ABI declared in include/twell.h: argument checks,
+// TMA descriptor encoding, the launch sequence of each call, the device
+// status word, launch counting and optional per-kernel event timing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "twell_internal.h"
+
+namespace twell {
+
+// ---------------------------------------------------------------- launches
+namespace {
+struct Pending {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_mu;
+int64_t g_launches = 0;
+bool g_profiling = false;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+int64_t g_prof_launches[TWELL_KERNEL_COUNT] = {};
+double g_prof_ms[TWELL_KERNEL_COUNT] = {};
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+LaunchScope::LaunchScope(int kernel_id, cudaStream_t stream) : kernel_(kernel_id), stream_(stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  ++g_launches;
+  if (g_profiling) {
+    start_ = take_event();
+    cudaEventRecord(start_, stream_);
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  if (!start_) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  cudaEvent_t stop = take_event();
+  cudaEventRecord(stop, stream_);
+  g_pending.push_back(Pending{kernel_, start_, stop});
+}
+
+// ---------------------------------------------------------------- device facts
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+bool device_is_sm103() {
+  static int cached[64] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+  return ok;
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return TWELL_ERR_CUDA;
+  cuuint64_t dims[2] = {inner_elems, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace twell
+
+using namespace twell;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layout(const twell_t* L) {
+  if (!L) return TWELL_ERR_INVALID_ARG;
+  if (L->n_rows < 0 || L->d_ff <= 0 || L->fb_cap < 0 || L->reserved != 0) return TWELL_ERR_INVALID_ARG;
+  const int T = L->tile;
+  if (T != 32 && T != 64 && T != 128 && T != 256) return TWELL_ERR_INVALID_ARG;
+  if (L->cap < 1 || L->cap > T || L->cap > 32) return TWELL_ERR_INVALID_ARG;
+  if (L->d_ff % T != 0) return TWELL_ERR_INVALID_ARG;
+  if (L->d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (!L->n_fb || !L->status) return TWELL_ERR_INVALID_ARG;
+  if (L->n_rows > 0 && (!L->values || !L->idx || !L->counts || !L->row_fb)) return TWELL_ERR_INVALID_ARG;
+  if (L->fb_cap > 0 && (!L->fb_rows || !L->fb_dense)) return TWELL_ERR_INVALID_ARG;
+  if (!aligned16(L->values) || !aligned16(L->idx) || !aligned16(L->counts) || !aligned16(L->row_fb))
+    return TWELL_ERR_MISALIGNED;
+  if (L->fb_cap > 0 && (!aligned16(L->fb_rows) || !aligned16(L->fb_dense))) return TWELL_ERR_MISALIGNED;
+  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
+  return TWELL_OK;
+}
+
+int check_dense(const void* p) {
+  if (!p) return TWELL_ERR_INVALID_ARG;
+  if (!aligned16(p)) return TWELL_ERR_MISALIGNED;
+  return TWELL_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+#define TW_TRY(expr)             \
+  do {                           \
+    const int rc_ = (expr);      \
+    if (rc_ != TWELL_OK) return rc_; \
+  } while (0)
+
+#define TW_CUDA(expr)                                  \
+  do {                                                 \
+    if ((expr) != cudaSuccess) return TWELL_ERR_CUDA;  \
+  } while (0)
+
+int reset_words(const twell_t* L, cudaStream_t s) {
+  TW_CUDA(cudaMemsetAsync(L->status, 0, sizeof(int32_t), s));
+  if (L->n_rows > 0) TW_CUDA(cudaMemsetAsync(L->row_fb, 0, sizeof(int32_t) * static_cast<size_t>(L->n_rows), s));
+  return TWELL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int twell_pack(const uint16_t* H, int64_t ldh, const twell_t* out, twell_stream_t stream) {
+  TW_TRY(check_layout(out));
+  TW_TRY(check_dense(H));
+  if (ldh < out->d_ff || ldh % 8 != 0) return TWELL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TW_TRY(reset_words(out, s));
+  TW_TRY(launch_pack_cells(H, ldh, *out, s));
+  TW_TRY(launch_route(*out, s));
+  TW_TRY(launch_fb_copy(H, ldh, *out, s));
+  return TWELL_OK;
+}
+
+int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t stream) {
+  TW_TRY(check_layout(in));
+  TW_TRY(check_dense(H));
+  if (ldh < in->d_ff || ldh % 8 != 0) return TWELL_ERR_INVALID_ARG;
+  return launch_unpack(*in, H, ldh, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
+                                 int32_t fb_cap) {
+  (void)n_rows;
+  (void)d_ff;
+  (void)tile;
+  (void)cap;
+  if (fb_cap <= 0 || d_model <= 0) return 256;
+  return align256(sizeof(uint16_t) * static_cast<size_t>(fb_cap) * static_cast<size_t>(d_model));
+}
+
+int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
+                  int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y, void* workspace,
+                  size_t workspace_bytes, twell_stream_t stream) {
+  TW_TRY(check_layout(H));
+  if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
+  if (H->n_rows != n_rows || H->d_ff != d_ff) return TWELL_ERR_INVALID_ARG;
+  if (d_model % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+  TW_TRY(check_dense(X));
+  TW_TRY(check_dense(W_inT));
+  TW_TRY(check_dense(b));
+  TW_TRY(check_dense(W_down));
+  TW_TRY(check_dense(Y));
+  const size_t need = twell_fwd_workspace_bytes(n_rows, d_model, d_ff, H->tile, H->cap, H->fb_cap);
+  if (H->fb_cap > 0 && (!workspace || workspace_bytes < need)) return TWELL_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TWELL_ERR_MISALIGNED;
+  if (n_rows == 0) return TWELL_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  TW_TRY(reset_words(H, s));
+  PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, d_ff / H->tile, H->tile, H->cap};
+  TW_TRY(launch_gemm_pack(X, W_inT, n_rows, nullptr, d_ff, d_model, pp, H->status, s));
+  TW_TRY(launch_route(*H, s));
+  if (H->fb_cap > 0) {
+    uint16_t* Xfb = static_cast<uint16_t*>(workspace);
+    TW_TRY(launch_fb_gather(*H, X, d_model, Xfb, s));
+    DenseEpiParams dp{b, H->fb_dense, d_ff, 1};
+    TW_TRY(launch_gemm_dense(Xfb, W_inT, H->fb_cap, H->n_fb, d_ff, d_model, dp, H->status, TWELL_KERNEL_FB_UP, s));
+  }
+  TW_TRY(launch_spmm(*H, W_down, d_model, Y, s));
+  TW_TRY(launch_fb_down(*H, W_down, d_model, Y, s));
+  return TWELL_OK;
+}
+
+size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
+                                 int32_t fb_cap) {
+  if (n_rows < 0 || d_ff <= 0 || tile <= 0 || cap <= 0 || fb_cap < 0) return 0;
+  return bwd_workspace_layout(n_rows, d_model, d_ff, tile, cap, fb_cap, nullptr, nullptr);
+}
+
+int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t* H,
+                  int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX, float* dW_inT,
+                  float* dW_down, float* db, void* workspace, size_t workspace_bytes, twell_stream_t stream) {
+  TW_TRY(check_layout(H));
+  if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
+  if (d_model % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+  TW_TRY(check_dense(X));
+  TW_TRY(check_dense(W_inT));
+  TW_TRY(check_dense(W_down));
+  TW_TRY(check_dense(dY));
+  TW_TRY(check_dense(dX));
+  TW_TRY(check_dense(dW_inT));
+  TW_TRY(check_dense(dW_down));
+  TW_TRY(check_dense(db));
+  const size_t need = twell_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
+  BwdWorkspace ws{};
+  bwd_workspace_layout(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap, &ws, workspace);
+  return launch_bwd(X, W_inT, W_down, *H, dY, l1_lambda, dX, dW_inT, dW_down, db, d_model, ws,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_downT,
+                        int32_t n_rows, int32_t d_model, int32_t d_ff, uint16_t* Hbuf, uint16_t* Y,
+                        twell_stream_t stream) {
+  if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
+  if (d_model % 128 != 0 || d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  TW_TRY(check_dense(X));
+  TW_TRY(check_dense(W_inT));
+  TW_TRY(check_dense(b));
+  TW_TRY(check_dense(W_downT));
+  TW_TRY(check_dense(Hbuf));
+  TW_TRY(check_dense(Y));
+  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
+  if (n_rows == 0) return TWELL_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DenseEpiParams up{b, Hbuf, d_ff, 1};
+  TW_TRY(launch_gemm_dense(X, W_inT, n_rows, nullptr, d_ff, d_model, up, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
+  DenseEpiParams down{nullptr, Y, d_model, 0};
+  TW_TRY(launch_gemm_dense(Hbuf, W_downT, n_rows, nullptr, d_model, d_ff, down, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
+  return TWELL_OK;
+}
+
+int twell_read_status(const twell_t* layout, twell_stream_t stream) {
+  if (!layout || !layout->status || !layout->n_fb) return TWELL_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return TWELL_ERR_CUDA;
+  int32_t st = 0, nfb = 0;
+  if (cudaMemcpy(&st, layout->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return TWELL_ERR_CUDA;
+  if (cudaMemcpy(&nfb, layout->n_fb, sizeof nfb, cudaMemcpyDeviceToHost) != cudaSuccess) return TWELL_ERR_CUDA;
+  if (st != 0) return st;
+  if (nfb > layout->fb_cap) return TWELL_ERR_FALLBACK_OVERFLOW;
+  return TWELL_OK;
+}
+
+const char* twell_status_string(int code) {
+  switch (code) {
+    case TWELL_OK: return "ok";
+    case TWELL_ERR_INVALID_ARG: return "invalid argument";
+    case TWELL_ERR_MISALIGNED: return "pointer not aligned as required";
+    case TWELL_ERR_UNSUPPORTED: return "shape not supported by the kernels' tiling";
+    case TWELL_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case TWELL_ERR_WORKSPACE: return "workspace missing or too small";
+    case TWELL_ERR_FALLBACK_OVERFLOW: return "more dense-fallback rows than fb_cap";
+    case TWELL_ERR_WAIT_TIMEOUT: return "a bounded pipeline wait on the GPU expired";
+    case TWELL_ERR_NO_DEVICE: return "no sm_103a device is current";
+    default: return "unknown status";
+  }
+}
+
+int64_t twell_launch_count(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_launches;
+}
+
+int twell_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_profiling = on != 0;
+  return TWELL_OK;
+}
+
+int twell_profile_reset(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return TWELL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& p : g_pending) {
+    g_event_pool.push_back(p.start);
+    g_event_pool.push_back(p.stop);
+  }
+  g_pending.clear();
+  for (int k = 0; k < TWELL_KERNEL_COUNT; ++k) {
+    g_prof_launches[k] = 0;
+    g_prof_ms[k] = 0.0;
+  }
+  return TWELL_OK;
+}
+
+int twell_profile_read(int kernel, int64_t* launches, double* total_ms) {
+  if (kernel < 0 || kernel >= TWELL_KERNEL_COUNT) return TWELL_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TWELL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& p : g_pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.start, p.stop) == cudaSuccess) {
+      g_prof_launches[p.kernel] += 1;
+      g_prof_ms[p.kernel] += ms;
+    }
+    g_event_pool.push_back(p.start);
+    g_event_pool.push_back(p.stop);
+  }
+  g_pending.clear();
+  if (launches) *launches = g_prof_launches[kernel];
+  if (total_ms) *total_ms = g_prof_ms[kernel];
+  return TWELL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,443 @@
+// Backward of the TwELL layer for  L = sum(Y * dY) + lambda * sum|H|
+// (L1 on the activations: bayesiansapien note, TL;DR; training kernels are
+// part of the release, "What it claims").
+//
+//   sddmm_kernel    dZ[n][j] = dY[n] . W_down[j] + lambda, formed only at the
+//                   stored non-zeros of H (the ReLU mask is the pattern)
+//   dx_kernel       dX[n] = sum_j dZ[n][j] W_in^T[j]   (gather over stored j)
+//   unit lists      the stored entries regrouped by hidden unit, rows
+//                   ascending, built deterministically (block histogram,
+//                   scans, ordered fill -- no atomics)
+//   dw_kernel       dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] =
+//                   sum_n dZ[n][j] X[n], db[j] = sum_n dZ[n][j]
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sm103.cuh"
+#include "twell_internal.h"
+
+namespace twell {
+namespace {
+
+struct Layout {
+  int32_t N, f, T, C, fb_cap, nt;
+  const uint16_t* values;
+  const uint8_t* idx;
+  const uint8_t* counts;
+  const int32_t* row_fb;
+  const int32_t* fb_rows;
+  const uint16_t* fb_dense;
+  const int32_t* n_fb;
+};
+
+Layout flat(const twell_t& L) {
+  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.values, L.idx,
+                L.counts, L.row_fb, L.fb_rows, L.fb_dense, L.n_fb};
+}
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// dot(dY row staged in shared memory, W[j]) across the warp; every lane gets it.
+__device__ __forceinline__ float row_dot(const uint16_t* __restrict__ sdy, const uint16_t* __restrict__ W, int j,
+                                         int d, int lane) {
+  float acc = 0.f;
+  const uint16_t* wr = W + static_cast<int64_t>(j) * d;
+  for (int c = lane * 8; c < d; c += 256) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wr + c));
+    const uint4 g = *reinterpret_cast<const uint4*>(sdy + c);
+    acc = fmaf(bf16_lo(g.x), bf16_lo(w.x), acc);
+    acc = fmaf(bf16_hi(g.x), bf16_hi(w.x), acc);
+    acc = fmaf(bf16_lo(g.y), bf16_lo(w.y), acc);
+    acc = fmaf(bf16_hi(g.y), bf16_hi(w.y), acc);
+    acc = fmaf(bf16_lo(g.z), bf16_lo(w.z), acc);
+    acc = fmaf(bf16_hi(g.z), bf16_hi(w.z), acc);
+    acc = fmaf(bf16_lo(g.w), bf16_lo(w.w), acc);
+    acc = fmaf(bf16_hi(g.w), bf16_hi(w.w), acc);
+  }
+  return warp_sum(acc);
+}
+
+// Warp per row; dynamic shared memory holds one dY row per warp.
+__global__ void __launch_bounds__(kWarps * 32)
+    sddmm_kernel(Layout L, const uint16_t* __restrict__ dY, const uint16_t* __restrict__ W_down, int d, float lambda,
+                 float* __restrict__ dz_cells, float* __restrict__ dz_fb) {
+  extern __shared__ uint4 sdy_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= L.N) return;
+  uint16_t* sdy = reinterpret_cast<uint16_t*>(sdy_raw) + static_cast<int64_t>(warp) * d;
+  const uint4* src = reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(row) * d);
+  for (int i = lane; i < d / 8; i += 32) reinterpret_cast<uint4*>(sdy)[i] = src[i];
+  const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+  float* dzr = dz_cells + cell0 * L.C;
+  for (int i = lane; i < L.nt * L.C; i += 32) dzr[i] = 0.f;
+  __syncwarp();
+  const int fb = L.row_fb[row];
+  if (fb < 0) {
+    for (int t0 = 0; t0 < L.nt; t0 += 32) {
+      const int t = t0 + lane;
+      const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
+      unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int c = __shfl_sync(0xffffffffu, cnt, b);
+        const int64_t cell = cell0 + t0 + b;
+        for (int s = 0; s < c; ++s) {
+          const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
+          const float dot = row_dot(sdy, W_down, j, d, lane);
+          const float h = bf16_bits_to_float(L.values[cell * L.C + s]);
+          if (lane == 0) dz_cells[cell * L.C + s] = h > 0.f ? dot + lambda : 0.f;
+        }
+      }
+    }
+  } else if (fb < L.fb_cap) {
+    const uint16_t* hr = L.fb_dense + static_cast<int64_t>(fb) * L.f;
+    float* out = dz_fb + static_cast<int64_t>(fb) * L.f;
+    for (int j0 = 0; j0 < L.f; j0 += 32) {
+      const uint16_t hv = hr[j0 + lane];
+      unsigned mask = __ballot_sync(0xffffffffu, bf16_bits_to_float(hv) != 0.f);
+      float mine = 0.f;
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float dot = row_dot(sdy, W_down, j0 + b, d, lane);
+        if (lane == b) mine = bf16_bits_to_float(hv) > 0.f ? dot + lambda : 0.f;
+      }
+      out[j0 + lane] = mine;
+    }
+  }
+}
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
+  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
+  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
+  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
+  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
+  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
+  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
+  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
+  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
+}
+
+// dX: warp per (row, 256 columns), terms in ascending hidden unit.
+__global__ void __launch_bounds__(kWarps * 32)
+    dx_kernel(Layout L, const float* __restrict__ dz_cells, const float* __restrict__ dz_fb,
+              const uint16_t* __restrict__ W_inT, int d, uint16_t* __restrict__ dX) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= L.N) return;
+  const int c0 = blockIdx.y * 256 + lane * 8;
+  const bool active = c0 < d;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int fb = L.row_fb[row];
+  if (fb < 0) {
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+    for (int t0 = 0; t0 < L.nt; t0 += 32) {
+      const int t = t0 + lane;
+      const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
+      unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int c = __shfl_sync(0xffffffffu, cnt, b);
+        const int64_t cell = cell0 + t0 + b;
+        for (int s = 0; s < c; ++s) {
+          const float v = dz_cells[cell * L.C + s];
+          const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
+          if (active) fma8(acc, v, __ldg(reinterpret_cast<const uint4*>(W_inT + static_cast<int64_t>(j) * d + c0)));
+        }
+      }
+    }
+  } else if (fb < L.fb_cap) {
+    const float* zr = dz_fb + static_cast<int64_t>(fb) * L.f;
+    for (int j0 = 0; j0 < L.f; j0 += 32) {
+      const float zv = zr[j0 + lane];
+      unsigned mask = __ballot_sync(0xffffffffu, zv != 0.f);
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float v = __shfl_sync(0xffffffffu, zv, b);
+        if (active)
+          fma8(acc, v, __ldg(reinterpret_cast<const uint4*>(W_inT + static_cast<int64_t>(j0 + b) * d + c0)));
+      }
+    }
+  }
+  if (active) {
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
+             (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(dX + static_cast<int64_t>(row) * d + c0) = make_uint4(p[0], p[1], p[2], p[3]);
+  }
+}
+
+// Pass 1 of the unit-major regrouping: per block of kBwdRowsPerBlock rows,
+// the number of stored entries of every hidden unit.
+__global__ void unit_hist_kernel(Layout L, int32_t* __restrict__ blk_count) {
+  extern __shared__ int32_t hist[];
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x) hist[j] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * kBwdRowsPerBlock;
+  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
+  for (int row = r0; row < r1; ++row) {
+    if (L.row_fb[row] >= 0) continue;  // uniform across the block
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+    for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
+      const int cnt = L.counts[cell0 + t];
+      for (int s = 0; s < cnt; ++s) atomicAdd(&hist[t * L.T + L.idx[(cell0 + t) * L.C + s]], 1);
+    }
+  }
+  __syncthreads();
+  int32_t* out = blk_count + static_cast<int64_t>(blockIdx.x) * L.f;
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x) out[j] = hist[j];
+}
+
+// Exclusive scan over row blocks for every unit (in place), totals to col_ptr[j].
+__global__ void unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f, int32_t* __restrict__ col_ptr) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= f) return;
+  int run = 0;
+  for (int b = 0; b < n_blocks; ++b) {
+    int32_t* p = blk_count + static_cast<int64_t>(b) * f + j;
+    const int c = *p;
+    *p = run;
+    run += c;
+  }
+  col_ptr[j] = run;
+}
+
+// Exclusive scan of the per-unit totals: col_ptr[j] = start, col_ptr[f] = all.
+__global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ col_ptr, int f) {
+  __shared__ int warp_tot[32];
+  __shared__ int base_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) base_s = 0;
+  __syncthreads();
+  for (int start = 0; start < f; start += 1024) {
+    const int j = start + tid;
+    const int v = j < f ? col_ptr[j] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_tot[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += x;
+      }
+      warp_tot[lane] = wi - w;
+    }
+    __syncthreads();
+    const int excl = base_s + warp_tot[warp] + incl - v;
+    if (j < f) col_ptr[j] = excl;
+    __syncthreads();
+    if (tid == 1023) base_s = excl + v;
+    __syncthreads();
+  }
+  if (tid == 0) col_ptr[f] = base_s;
+}
+
+// Pass 2: rows of a block in ascending order; within one row every unit
+// appears at most once, so the per-unit cursors need no atomics.
+__global__ void unit_fill_kernel(Layout L, const float* __restrict__ dz_cells, const int32_t* __restrict__ blk_count,
+                                 const int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_rows,
+                                 float* __restrict__ col_h, float* __restrict__ col_dz) {
+  extern __shared__ int32_t cursor[];
+  const int32_t* off = blk_count + static_cast<int64_t>(blockIdx.x) * L.f;
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x) cursor[j] = col_ptr[j] + off[j];
+  __syncthreads();
+  const int r0 = blockIdx.x * kBwdRowsPerBlock;
+  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
+  for (int row = r0; row < r1; ++row) {
+    if (L.row_fb[row] >= 0) continue;
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+    for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
+      const int64_t cell = cell0 + t;
+      const int cnt = L.counts[cell];
+      for (int s = 0; s < cnt; ++s) {
+        const int j = t * L.T + L.idx[cell * L.C + s];
+        const int pos = cursor[j]++;
+        col_rows[pos] = row;
+        col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + s]);
+        col_dz[pos] = dz_cells[cell * L.C + s];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Warp per hidden unit j and 256 columns.  TwELL entries in ascending row,
+// then fallback rows in ascending slot.
+__global__ void __launch_bounds__(kWarps * 32)
+    dw_kernel(Layout L, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
+              const float* __restrict__ col_h, const float* __restrict__ col_dz, const float* __restrict__ dz_fb,
+              const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT,
+              float* __restrict__ dW_down, float* __restrict__ db) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kWarps + warp;
+  if (j >= L.f) return;
+  const int c0 = blockIdx.y * 256 + lane * 8;
+  const bool active = c0 < d;
+  float a_down[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float gb = 0.f;
+  const int e1 = col_ptr[j + 1];
+  for (int e = col_ptr[j]; e < e1; ++e) {
+    const int n = col_rows[e];
+    const float h = col_h[e], dz = col_dz[e];
+    gb += dz;
+    if (active) {
+      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(n) * d + c0)));
+      fma8(a_in, dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(n) * d + c0)));
+    }
+  }
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  for (int slot = 0; slot < nfb; ++slot) {
+    const float h = bf16_bits_to_float(L.fb_dense[static_cast<int64_t>(slot) * L.f + j]);
+    if (h == 0.f) continue;
+    const int n = L.fb_rows[slot];
+    const float dz = dz_fb[static_cast<int64_t>(slot) * L.f + j];
+    gb += dz;
+    if (active) {
+      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(n) * d + c0)));
+      fma8(a_in, dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(n) * d + c0)));
+    }
+  }
+  if (active) {
+    float4* od = reinterpret_cast<float4*>(dW_down + static_cast<int64_t>(j) * d + c0);
+    float4* oi = reinterpret_cast<float4*>(dW_inT + static_cast<int64_t>(j) * d + c0);
+    od[0] = make_float4(a_down[0], a_down[1], a_down[2], a_down[3]);
+    od[1] = make_float4(a_down[4], a_down[5], a_down[6], a_down[7]);
+    oi[0] = make_float4(a_in[0], a_in[1], a_in[2], a_in[3]);
+    oi[1] = make_float4(a_in[4], a_in[5], a_in[6], a_in[7]);
+  }
+  if (blockIdx.y == 0 && lane == 0) db[j] = gb;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t bwd_workspace_layout(int N, int /*d_model*/, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
+                            void* base) {
+  const int nt = d_ff / T;
+  const int64_t cells = static_cast<int64_t>(N) * nt * C;
+  const int n_blocks = (N + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t o_dzc = take(sizeof(float) * cells);
+  const size_t o_dzf = take(sizeof(float) * static_cast<size_t>(fb_cap) * d_ff);
+  const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
+  const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
+  const size_t o_rows = take(sizeof(int32_t) * cells);
+  const size_t o_h = take(sizeof(float) * cells);
+  const size_t o_dz = take(sizeof(float) * cells);
+  if (ws && base) {
+    uint8_t* b = static_cast<uint8_t*>(base);
+    ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
+    ws->dz_fb = reinterpret_cast<float*>(b + o_dzf);
+    ws->blk_count = reinterpret_cast<int32_t*>(b + o_blk);
+    ws->col_ptr = reinterpret_cast<int32_t*>(b + o_ptr);
+    ws->col_rows = reinterpret_cast<int32_t*>(b + o_rows);
+    ws->col_h = reinterpret_cast<float*>(b + o_h);
+    ws->col_dz = reinterpret_cast<float*>(b + o_dz);
+    ws->n_blocks = n_blocks;
+  }
+  return off;
+}
+
+#define TW_CHECK_LAUNCH()                                         \
+  do {                                                            \
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA; \
+  } while (0)
+
+int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& Lh,
+               const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
+               int d, const BwdWorkspace& ws, cudaStream_t s) {
+  const Layout L = flat(Lh);
+  const int f = Lh.d_ff;
+  const int N = Lh.n_rows;
+  const int row_blocks = (N + kWarps - 1) / kWarps;
+  const int col_blocks = (d + 255) / 256;
+  if (N > 0) {
+    const size_t smem = static_cast<size_t>(kWarps) * d * sizeof(uint16_t);
+    static bool attr[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr[dev]) {
+      if (cudaFuncSetAttribute(sddmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+        return TWELL_ERR_CUDA;
+      attr[dev] = true;
+    }
+    {
+      LaunchScope ls(TWELL_KERNEL_SDDMM, s);
+      sddmm_kernel<<<row_blocks, kWarps * 32, smem, s>>>(L, dY, W_down, d, lambda, ws.dz_cells, ws.dz_fb);
+    }
+    TW_CHECK_LAUNCH();
+    {
+      LaunchScope ls(TWELL_KERNEL_DX, s);
+      dx_kernel<<<dim3(row_blocks, col_blocks), kWarps * 32, 0, s>>>(L, ws.dz_cells, ws.dz_fb, W_inT, d, dX);
+    }
+    TW_CHECK_LAUNCH();
+  }
+  const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
+  static bool attr2[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr2[dev]) {
+    if (cudaFuncSetAttribute(unit_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+        cudaFuncSetAttribute(unit_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+      return TWELL_ERR_CUDA;
+    attr2[dev] = true;
+  }
+  if (ws.n_blocks > 0) {
+    LaunchScope ls(TWELL_KERNEL_AUX, s);
+    unit_hist_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.blk_count);
+  }
+  TW_CHECK_LAUNCH();
+  {
+    LaunchScope ls(TWELL_KERNEL_AUX, s);
+    unit_block_scan_kernel<<<(f + 255) / 256, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
+  }
+  TW_CHECK_LAUNCH();
+  {
+    LaunchScope ls(TWELL_KERNEL_AUX, s);
+    unit_scan_kernel<<<1, 1024, 0, s>>>(ws.col_ptr, f);
+  }
+  TW_CHECK_LAUNCH();
+  if (ws.n_blocks > 0) {
+    LaunchScope ls(TWELL_KERNEL_AUX, s);
+    unit_fill_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.dz_cells, ws.blk_count, ws.col_ptr, ws.col_rows, ws.col_h,
+                                                    ws.col_dz);
+  }
+  TW_CHECK_LAUNCH();
+  {
+    LaunchScope ls(TWELL_KERNEL_DW, s);
+    dw_kernel<<<dim3((f + kWarps - 1) / kWarps, col_blocks), kWarps * 32, 0, s>>>(
+        L, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, ws.dz_fb, X, dY, d, dW_inT, dW_down, db);
+  }
+  TW_CHECK_LAUNCH();
+  return TWELL_OK;
+}
+
+}  // namespace twell

@@ -1,0 +1,242 @@
+// Forward-pass kernels around the tensor-core up-projection:
+//   route_kernel     hybrid routing: rows whose tiles overflowed C become
+//                    fallback rows, numbered in ascending row order
+//                    (ifai.io news, "Reshaping math for the GPU": a dense
+//                    matrix catches the rare dense tokens; bayesiansapien note,
+//                    Figure 1 "hybrid" splits rows between formats)
+//   fb_gather_kernel copies the fallback rows of X together for the dense
+//                    recompute and clears their TwELL cells
+//   spmm_kernel      Y = H . W_down over TwELL rows, reading only the W_down
+//                    rows named by the stored tile-local indices
+//   fb_down_kernel   Y rows of the fallback rows from their dense H rows
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sm103.cuh"
+#include "twell_internal.h"
+
+namespace twell {
+namespace {
+
+// Flat copy of the layout for kernel parameters.
+struct Layout {
+  int32_t N, f, T, C, fb_cap, nt;
+  uint16_t* values;
+  uint8_t* idx;
+  uint8_t* counts;
+  int32_t* row_fb;
+  int32_t* fb_rows;
+  uint16_t* fb_dense;
+  int32_t* n_fb;
+  int32_t* status;
+};
+
+Layout flat(const twell_t& L) {
+  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.values, L.idx,
+                L.counts, L.row_fb, L.fb_rows, L.fb_dense, L.n_fb, L.status};
+}
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteRows = 8;  // rows per thread per pass
+
+// row_fb holds 0/1 overflow flags on entry and -1 / fallback slot on exit.
+// One CTA: an exclusive block scan of the flags gives every fallback row its
+// slot in ascending row order, so the result is deterministic.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
+  __shared__ int warp_tot[kRouteThreads / 32];
+  __shared__ int base_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) base_s = 0;
+  __syncthreads();
+  for (int start = 0; start < L.N; start += kRouteThreads * kRouteRows) {
+    const int r0 = start + tid * kRouteRows;
+    int flags = 0, local = 0;
+#pragma unroll
+    for (int i = 0; i < kRouteRows; ++i) {
+      const int r = r0 + i;
+      const int fl = (r < L.N && L.row_fb[r] != 0) ? 1 : 0;
+      flags |= fl << i;
+      local += fl;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    int slot = base_s + warp_tot[warp] + incl - local;
+#pragma unroll
+    for (int i = 0; i < kRouteRows; ++i) {
+      const int r = r0 + i;
+      if (r >= L.N) break;
+      if ((flags >> i) & 1) {
+        L.row_fb[r] = slot;
+        if (slot < L.fb_cap) L.fb_rows[slot] = r;
+        ++slot;
+      } else {
+        L.row_fb[r] = -1;
+      }
+    }
+    __syncthreads();
+    if (tid == kRouteThreads - 1) base_s = slot;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *L.n_fb = base_s;
+    if (base_s > L.fb_cap) report_error(L.status, TWELL_ERR_FALLBACK_OVERFLOW);
+  }
+}
+
+// One CTA per fallback slot (grid-stride): X row -> Xfb[slot], and the row's
+// TwELL cells (written with truncated contents by the up-projection) become
+// count 0 with canonical padding.
+__global__ void fb_gather_kernel(Layout L, const uint16_t* __restrict__ X, int d, uint16_t* __restrict__ Xfb) {
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
+    const int row = L.fb_rows[slot];
+    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * d);
+    uint4* dst = reinterpret_cast<uint4*>(Xfb + static_cast<int64_t>(slot) * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+    for (int i = threadIdx.x; i < L.nt; i += blockDim.x) L.counts[cell0 + i] = 0;
+    for (int i = threadIdx.x; i < L.nt * L.C; i += blockDim.x) {
+      L.values[cell0 * L.C + i] = 0;
+      L.idx[cell0 * L.C + i] = 0;
+    }
+  }
+}
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
+  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
+  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
+  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
+  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
+  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
+  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
+  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
+  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&a)[8]) {
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p[i] = static_cast<uint32_t>(float_to_bf16_bits(a[2 * i])) |
+           (static_cast<uint32_t>(float_to_bf16_bits(a[2 * i + 1])) << 16);
+  return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+constexpr int kSpmmWarps = 8;
+
+// Gather-SpMM over TwELL rows.  A warp owns one row and 256 output columns
+// (8 per lane, one 16-byte W_down load per lane per stored entry).  Cells are
+// visited tile by tile and slot by slot, so every output sums its terms in
+// ascending hidden-unit order.  Fallback rows are skipped here.
+__global__ void __launch_bounds__(kSpmmWarps * 32)
+    spmm_kernel(Layout L, const uint16_t* __restrict__ W, int d, uint16_t* __restrict__ Y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kSpmmWarps + warp;
+  if (row >= L.N) return;
+  if (L.row_fb[row] >= 0) return;
+  const int c0 = blockIdx.y * 256 + lane * 8;
+  const bool active = c0 < d;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+  for (int t0 = 0; t0 < L.nt; t0 += 32) {
+    const int t = t0 + lane;
+    const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
+    unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
+    while (mask) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int c = __shfl_sync(0xffffffffu, cnt, b);
+      const int64_t cell = cell0 + t0 + b;
+      for (int s = 0; s < c; ++s) {
+        const float v = bf16_bits_to_float(L.values[cell * L.C + s]);
+        const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
+        if (active) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(j) * d + c0));
+          fma8(acc, v, w);
+        }
+      }
+    }
+  }
+  if (active) *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c0) = pack8_bf16(acc);
+}
+
+// Fallback rows: warp per (slot, 256 columns); walks the dense h row in
+// ascending j, skipping zeros.
+__global__ void __launch_bounds__(128)
+    fb_down_kernel(Layout L, const uint16_t* __restrict__ W, int d, uint16_t* __restrict__ Y) {
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = (blockIdx.y * 4 + warp) * 256 + lane * 8;
+  const bool active = c0 < d;
+  for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
+    const int row = L.fb_rows[slot];
+    const uint16_t* h = L.fb_dense + static_cast<int64_t>(slot) * L.f;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < L.f; j0 += 32) {
+      const uint16_t hv = h[j0 + lane];
+      unsigned mask = __ballot_sync(0xffffffffu, bf16_bits_to_float(hv) != 0.0f);
+      while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float v = bf16_bits_to_float(static_cast<uint16_t>(__shfl_sync(0xffffffffu, hv, b)));
+        if (active) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(j0 + b) * d + c0));
+          fma8(acc, v, w);
+        }
+      }
+    }
+    if (active) *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c0) = pack8_bf16(acc);
+  }
+}
+
+}  // namespace
+
+int launch_route(const twell_t& L, cudaStream_t s) {
+  LaunchScope ls(TWELL_KERNEL_ROUTE, s);
+  route_kernel<<<1, kRouteThreads, 0, s>>>(flat(L));
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_fb_gather(const twell_t& L, const uint16_t* X, int d_model, uint16_t* Xfb, cudaStream_t s) {
+  if (L.fb_cap <= 0) return TWELL_OK;
+  const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
+  LaunchScope ls(TWELL_KERNEL_FB_GATHER, s);
+  fb_gather_kernel<<<grid, 256, 0, s>>>(flat(L), X, d_model, Xfb);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
+  if (L.n_rows <= 0) return TWELL_OK;
+  dim3 grid((L.n_rows + kSpmmWarps - 1) / kSpmmWarps, (d_model + 255) / 256);
+  LaunchScope ls(TWELL_KERNEL_SPMM, s);
+  spmm_kernel<<<grid, kSpmmWarps * 32, 0, s>>>(flat(L), W_down, d_model, Y);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
+  if (L.fb_cap <= 0) return TWELL_OK;
+  dim3 grid(std::max(1, std::min(L.fb_cap, 4 * sm_count())), (d_model + 1023) / 1024);
+  LaunchScope ls(TWELL_KERNEL_FB_DOWN, s);
+  fb_down_kernel<<<grid, 128, 0, s>>>(flat(L), W_down, d_model, Y);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace twell

@@ -1,0 +1,178 @@
+// Standalone dense <-> TwELL conversions (the pages' "dense-to-TwELL and
+// TwELL-to-dense paths", repo-explainer "TwELL: The Packing Format That Fits
+// the Machine"; format per the bayesiansapien note's Figure 1 description).
+//
+// pack_cells_kernel: a warp reads 256 consecutive bf16 of one row with
+//   16-byte loads (8 columns per lane); the T/8 lanes of each tile compact
+//   their non-zeros with a segmented popcount prefix over per-lane 8-bit
+//   masks, write them to the cell in ascending column order, pad the rest,
+//   store the count and flag the row (row_fb = 1) when the tile overflows C.
+// fb_copy_kernel: dense rows of fallback rows -> fb_dense, their cells cleared.
+// unpack_kernel: each lane rebuilds 8 output columns from its tile's cell (or
+//   from fb_dense) and writes them with one 16-byte store.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sm103.cuh"
+#include "twell_internal.h"
+
+namespace twell {
+namespace {
+
+struct Layout {
+  int32_t N, f, T, C, fb_cap, nt;
+  uint16_t* values;
+  uint8_t* idx;
+  uint8_t* counts;
+  int32_t* row_fb;
+  int32_t* fb_rows;
+  uint16_t* fb_dense;
+  int32_t* n_fb;
+  int32_t* status;
+};
+
+Layout flat(const twell_t& L) {
+  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.values, L.idx,
+                L.counts, L.row_fb, L.fb_rows, L.fb_dense, L.n_fb, L.status};
+}
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ uint16_t half_word(const uint32_t (&w)[4], int k) {
+  return static_cast<uint16_t>((k & 1) ? (w[k / 2] >> 16) : (w[k / 2] & 0xFFFFu));
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    pack_cells_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int segs = (L.f + 255) / 256;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (gw >= static_cast<int64_t>(L.N) * segs) return;  // whole warp leaves together
+  const int row = static_cast<int>(gw / segs);
+  const int seg = static_cast<int>(gw % segs);
+  const int col = seg * 256 + lane * 8;
+  const bool in = col < L.f;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (in) v = __ldg(reinterpret_cast<const uint4*>(H + static_cast<int64_t>(row) * ldh + col));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t nzmask = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if ((half_word(w, k) & 0x7FFFu) != 0) nzmask |= 1u << k;  // +0 and -0 are zeros
+  const int G = L.T / 8;  // lanes per tile: 4, 8, 16 or 32
+  const int gl = lane % G;
+  const int local = __popc(nzmask);
+  int incl = local;
+  for (int o = 1; o < G; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (gl >= o) incl += x;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, (lane / G) * G + G - 1);
+  if (!in) return;
+  const int C = L.C;
+  const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
+  int slot = incl - local;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if ((nzmask >> k) & 1u) {
+      if (slot < C) {
+        L.values[cell * C + slot] = half_word(w, k);
+        L.idx[cell * C + slot] = static_cast<uint8_t>(gl * 8 + k);
+      }
+      ++slot;
+    }
+  }
+  const int stored = total < C ? total : C;
+  for (int s = stored + gl; s < C; s += G) {
+    L.values[cell * C + s] = 0;
+    L.idx[cell * C + s] = 0;
+  }
+  if (gl == 0) {
+    L.counts[cell] = static_cast<uint8_t>(stored);
+    if (total > C) L.row_fb[row] = 1;
+  }
+}
+
+// Fallback rows: copy the dense row, clear the row's cells.
+__global__ void fb_copy_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
+    const int row = L.fb_rows[slot];
+    const uint4* src = reinterpret_cast<const uint4*>(H + static_cast<int64_t>(row) * ldh);
+    uint4* dst = reinterpret_cast<uint4*>(L.fb_dense + static_cast<int64_t>(slot) * L.f);
+    for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) dst[i] = src[i];
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
+    for (int i = threadIdx.x; i < L.nt; i += blockDim.x) L.counts[cell0 + i] = 0;
+    for (int i = threadIdx.x; i < L.nt * L.C; i += blockDim.x) {
+      L.values[cell0 * L.C + i] = 0;
+      L.idx[cell0 * L.C + i] = 0;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    unpack_kernel(Layout L, uint16_t* __restrict__ H, int64_t ldh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int segs = (L.f + 255) / 256;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (gw >= static_cast<int64_t>(L.N) * segs) return;
+  const int row = static_cast<int>(gw / segs);
+  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
+  if (col >= L.f) return;
+  uint4 out;
+  const int fb = L.row_fb[row];
+  if (fb >= 0) {
+    out = *reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f + col);
+  } else {
+    const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
+    const int lo = col % L.T;
+    const int cnt = L.counts[cell];
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int s = 0; s < cnt; ++s) {
+      const int i = static_cast<int>(L.idx[cell * L.C + s]) - lo;
+      if (i >= 0 && i < 8) {
+        const uint32_t val = L.values[cell * L.C + s];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (i == k) w[k / 2] |= (k & 1) ? (val << 16) : val;
+      }
+    }
+    out = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + col) = out;
+}
+
+int64_t warps_needed(const twell_t& L) {
+  return static_cast<int64_t>(L.n_rows) * ((L.d_ff + 255) / 256);
+}
+
+}  // namespace
+
+int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s) {
+  const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
+  if (blocks <= 0) return TWELL_OK;
+  if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
+  LaunchScope ls(TWELL_KERNEL_PACK, s);
+  pack_cells_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s) {
+  if (L.fb_cap <= 0) return TWELL_OK;
+  const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
+  LaunchScope ls(TWELL_KERNEL_PACK, s);
+  fb_copy_kernel<<<grid, 256, 0, s>>>(flat(L), H, ldh);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s) {
+  const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
+  if (blocks <= 0) return TWELL_OK;
+  if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
+  LaunchScope ls(TWELL_KERNEL_UNPACK, s);
+  unpack_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace twell

@@ -1,0 +1,92 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/twell.h"
+
+namespace twell {
+
+// Pipeline waits inside kernels give up after this much global time and
+// report TWELL_ERR_WAIT_TIMEOUT instead of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------- launches
+// Counts every kernel launch and, while profiling is on, brackets it with a
+// pair of CUDA events on its stream.
+class LaunchScope {
+ public:
+  LaunchScope(int kernel_id, cudaStream_t stream);
+  ~LaunchScope();
+
+ private:
+  int kernel_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
+int sm_count();                      // SMs of the current device (cached per device)
+bool device_is_sm103();              // current device is compute capability 10.3
+int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+
+// ---------------------------------------------------------------- kernels
+struct PackEpiParams {
+  const uint16_t* bias;   // [d_ff]
+  uint16_t* values;       // [M][n_tiles][C]
+  uint8_t* idx;
+  uint8_t* counts;        // [M][n_tiles]
+  int32_t* row_flag;      // [M], set to 1 where a tile overflows C (pre-zeroed)
+  int32_t n_tiles;
+  int32_t tile;           // T
+  int32_t cap;            // C
+};
+
+struct DenseEpiParams {
+  const uint16_t* bias;   // [N] or null
+  uint16_t* out;          // [M][ldo]
+  int64_t ldo;
+  int32_t relu;           // 1: out = bf16(z) where z > 0 else +0
+};
+
+// C[M, N] = A[M, K] . B[N, K]^T on tcgen05 with the epilogue named by the
+// function.  A rows beyond min(M, *M_dev) are not stored.  `n_blk` is the N
+// tile width (128 or 256).
+int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
+                     const PackEpiParams& p, int32_t* status, cudaStream_t s);
+int launch_gemm_dense(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
+                      const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+
+// forward helpers (fwd_kernels.cu)
+int launch_route(const twell_t& L, cudaStream_t s);
+int launch_fb_gather(const twell_t& L, const uint16_t* X, int d_model, uint16_t* Xfb, cudaStream_t s);
+int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
+int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
+
+// standalone pack / unpack (pack_kernels.cu)
+int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);
+int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);
+int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
+
+// backward (bwd_kernels.cu)
+struct BwdWorkspace {
+  float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries (0 in padding)
+  float* dz_fb;           // [fb_cap][d_ff] fp32: dZ of the fallback rows (0 off the pattern)
+  int32_t* blk_count;     // [n_blocks][d_ff] entries per (row block, hidden unit), then offsets
+  int32_t* col_ptr;       // [d_ff + 1] start of each hidden unit's entry list
+  int32_t* col_rows;      // [capacity] row of each entry, grouped by unit, rows ascending
+  float* col_h;           // [capacity] h of each entry
+  float* col_dz;          // [capacity] dZ of each entry
+  int32_t n_blocks;       // row blocks of kBwdRowsPerBlock rows
+};
+constexpr int kBwdRowsPerBlock = 32;
+size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
+                            void* base);
+int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,
+               const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
+               int d_model, const BwdWorkspace& ws, cudaStream_t s);
+
+}  // namespace twell

@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Throughput of the TwELL activation-sparse FFN layer on one GB300.
+
+One step = the whole layer: twell_ffn_fwd (tensor-core up-projection with the
+fused bias/ReLU/TwELL-pack epilogue, hybrid routing, dense-fallback recompute,
+gather-SpMM down-projection) followed by twell_ffn_bwd (SDDMM with the L1
+term, dX gather, unit-major weight gradients), on the 1B-model FFN shape
+N=4096, d_model=2048, d_ff=8192, T=128, C=8 with synthetic seeded inputs.
+
+Prints one JSON line.  `value` is tokens/s of the step with inputs resident in
+HBM (L2 flushed between steps by writing a 2x-L2 buffer); `e2e` is the same
+step through the same C-ABI calls with X and dY copied in from pinned host
+memory and Y and dX copied back inside the timed region.  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN tokens/s (TwELL fwd/bwd, 99% sparse) + % of HBM/tensor roofline"
+UNIT = "tokens/s"
+WORKLOAD = "1B-scale FFN fwd+bwd: N=4096 d_model=2048 d_ff=8192 T=128 C=8, lognormal row activity (mean 1%), 2% rows at 20%"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source
+    has not changed since (the capture stores the source digest)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None, None
+    src = os.path.join(ROOT, "activation_sparse_transformer_gb300", "csrc", "gemm_tcgen05.cu")
+    with open(src, "rb") as fh:
+        digest = hashlib.sha256(fh.read()).hexdigest()[:16]
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) >= 5 and parts[0] == kernel and parts[1] == workload:
+                if parts[2] == digest:
+                    return float(parts[3]), parts[4]
+                return None, "stale: kernel changed since the capture"
+    return None, None
+
+
+def bench_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import activation_sparse_transformer_gb300 as tw
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tw.load_library()
+    cfg = synth.CONFIGS[args.config]
+    base = synth.make_ffn_inputs(cfg)
+    # every rank draws its own batch (weak scaling: per-GPU work is fixed)
+    if rank:
+        shifted = synth.FFNConfig(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
+        base = synth.make_ffn_inputs(shifted)
+    N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
+    lam = cfg.l1_lambda or 1e-4
+    dY_np = synth.make_grad_output(N, d, seed=cfg.seed + 77 + rank)
+
+    def dt(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    X, Wi, b, Wd, dY = dt(base["X"]), dt(base["W_inT"]), dt(base["b"]), dt(base["W_down"]), dt(dY_np)
+    packed = tw.alloc_packed(N, f, T, C, fb, dev)
+    Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dWi = torch.empty((f, d), dtype=torch.float32, device=dev)
+    dWd = torch.empty((f, d), dtype=torch.float32, device=dev)
+    db = torch.empty((f,), dtype=torch.float32, device=dev)
+    wsf = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(tw.bwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, wsf, stream)
+
+    def step():
+        fwd()
+        tw.twell_ffn_bwd(X, Wi, Wd, packed, dY, lam, dX, dWi, dWd, db, wsb, stream)
+
+    # correctness of the routing on this batch (status word, fallback count)
+    step()
+    rc = tw.twell_read_status(packed, stream)
+    if rc != 0:
+        raise RuntimeError(f"layer status {rc}: {tw.status_string(rc)}")
+    n_fb = int(packed.n_fb[0].item())
+    counts = packed.counts.to(torch.int32)
+    nnz_tw = int(counts.sum().item())
+    nnz_fb = int((packed.fb_dense[:n_fb].view(torch.int16) & 0x7FFF).ne(0).sum().item()) if n_fb else 0
+    density = (nnz_tw + nnz_fb) / float(N * f)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def timed(fn, k, profile=False):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        if profile:
+            tw.twell_profile_reset()
+            tw.twell_profile_enable(True)
+        for i in range(k):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if profile:
+            tw.twell_profile_enable(False)
+        return [a.elapsed_time(bb) for a, bb in ev]
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches0 = tw.twell_launch_count()
+    t_wall = time.perf_counter()
+    step_ms = timed(step, args.steps, profile=True)
+    wall = time.perf_counter() - t_wall
+    launches = tw.twell_launch_count() - launches0
+    clk = clocks.stop()
+    per_kernel = {}
+    for name in tw.KERNELS:
+        n, ms = tw.twell_profile_read(name)
+        if n:
+            per_kernel[name] = {"launches": n, "avg_us": 1000.0 * ms / n, "share": 0.0}
+    tot = sum(v["avg_us"] * v["launches"] for v in per_kernel.values()) or 1.0
+    for v in per_kernel.values():
+        v["share"] = round(v["avg_us"] * v["launches"] / tot, 4)
+        v["avg_us"] = round(v["avg_us"], 2)
+
+    # forward alone (the layer's inference path) and the dense comparator
+    fwd_ms = timed(fwd, args.steps)
+    WdT = Wd.t().contiguous()
+    Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+
+    def dense():
+        tw.twell_dense_ffn_fwd(X, Wi, b, WdT, Hbuf, Y, stream)
+
+    dense()
+    dense_ms = timed(dense, max(3, args.steps // 2))
+    del Hbuf, WdT
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    hX = torch.from_numpy(base["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hdY = torch.from_numpy(dY_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hY = torch.empty((N, d), dtype=torch.bfloat16).pin_memory()
+    hdX = torch.empty((N, d), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        X.copy_(hX, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        step()
+        hY.copy_(Y, non_blocking=True)
+        hdX.copy_(dX, non_blocking=True)
+
+    e2e_step()
+    e2e_ms = timed(e2e_step, args.steps)
+    h2d = hX.numel() * 2 + hdY.numel() * 2
+    d2h = hY.numel() * 2 + hdX.numel() * 2
+
+    def med(v):
+        return statistics.median(v)
+
+    ms = med(step_ms)
+    if world > 1:
+        t = torch.tensor([ms, med(e2e_ms)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_m = float(t[0]), float(t[1])
+    else:
+        e2e_m = med(e2e_ms)
+
+    peaks, peak_src = load_peaks()
+    flops_up = 2.0 * N * d * f
+    up = per_kernel.get("up_pack")
+    roof = None
+    if up:
+        achieved = flops_up / (up["avg_us"] * 1e-6) / 1e12
+        traffic, note = ncu_traffic("up_pack", "1b")
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)",
+                "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+                "kernel": "up_pack (tcgen05 GEMM + bias/ReLU/TwELL-pack epilogue)",
+                "algorithmic": "2*N*d_model*d_ff flops per launch"}
+        if note:
+            roof["traffic_note"] = note
+    fwd_m = med(fwd_ms)
+    roof_fwd_us = max(flops_up / (peaks["bf16_tflops"] * 1e12),
+                      (N * d * 2 * 2 + f * d * 2 * 2 + N * (f // T) * (3 * C + 1)) / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    result = {
+        "metric": METRIC, "value": round(world * N / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
+        "config": {"workload": WORKLOAD, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
+                   "fb_cap": fb, "l1_lambda": lam, "l2": "flushed between steps (2x L2 write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "fwd": {"tokens_per_s": round(world * N / (fwd_m * 1e-3), 1), "ms": round(fwd_m, 4),
+                "roofline_us": round(roof_fwd_us, 2), "roofline_frac": round(roof_fwd_us / (fwd_m * 1e3), 4)},
+        "dense_ffn_fwd": {"tokens_per_s": round(world * N / (med(dense_ms) * 1e-3), 1), "ms": round(med(dense_ms), 4),
+                          "note": "same tcgen05 GEMM, no sparsity: reported baseline"},
+        "kernels": per_kernel,
+        "layer": {"n_fb": n_fb, "density": round(density, 5), "sparsity": round(1 - density, 5),
+                  "packed_h_bytes": int(packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel()
+                                        + fb * f * 2),
+                  "dense_h_bytes": N * f * 2},
+        "e2e": {"value": round(world * N / (e2e_m * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_m, 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "timed_wall_s": round(wall, 3),
+    }
+    return result
+
+
+def cpu_sample_rows(default):
+    return int(os.environ.get("TWELL_CPU_SAMPLE_ROWS", default))
+
+
+def oracle_step(base, dY, rows, cfg, lam):
+    """One fwd+bwd of the oracle on the first `rows` tokens treated as a batch."""
+    import oracle
+    X = base["X"][:rows]
+    Z, H = oracle.hidden(X, base["W_inT"], base["b"])
+    packed = oracle.pack(H, cfg.tile, cfg.cap, max(1, rows))
+    oracle.down_packed(packed, base["W_down"])
+    _, dZ = oracle.grad_hidden(dY[:rows], base["W_down"], H, lam)
+    oracle.grad_input(dZ, base["W_inT"])
+    oracle.grad_weights(X, base["W_down"], H, dY[:rows], lam)
+
+
+def cpu_baseline(rows=None):
+    import numpy as np
+
+    import oracle
+    import synth
+    cfg = synth.CONFIGS["1b"]
+    base = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
+    rows = rows or cpu_sample_rows(384)
+    oracle.build()
+    t = time.perf_counter()
+    oracle_step(base, dY, rows, cfg, cfg.l1_lambda or 1e-4)
+    el = time.perf_counter() - t
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(rows / el, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fwd+bwd of the first {rows} tokens of the 1B-shape layer as one batch "
+                      f"(plain C fp32 loops, OpenMP over {cores} threads), {el:.1f} s"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    import synth
+    cfg = synth.CONFIGS["1b"]
+    base = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
+    lam = cfg.l1_lambda or 1e-4
+    rows = cpu_sample_rows(32)
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_step(base, dY, rows, cfg, lam)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle_step(base, dY, rows, cfg, lam)
+        times.append(time.perf_counter() - t)
+    s = statistics.median(times)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    value = round(rows / s, 3)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * s * cfg.n_rows / rows, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded, see synth/)",
+            "config": {"workload": WORKLOAD, "sample_rows": rows},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: fwd+bwd of the first {rows} tokens as one batch"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="1b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        res = bench_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = bench_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * twell.h -- C ABI of the TwELL activation-sparse feed-forward layer for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (from "Sparser, Faster, Lighter Transformer Language Models",
+ * Sakana AI + NVIDIA, as the pages describe it):
+ *     H = ReLU(X . W_in + b)          (the nonlinearity zeroes most units:
+ *                                      ifai.io news, opening; iaexpertos blog,
+ *                                      "The Challenge of Sparsity Ignored by GPUs")
+ *     H is stored in the Tile-wise ELLPACK (TwELL) hybrid format
+ *                                     (ifai.io news, "Reshaping math for the GPU";
+ *                                      repo-explainer, "TwELL: The Packing Format
+ *                                      That Fits the Machine"; bayesiansapien note,
+ *                                      flowchart and the description of Figure 1)
+ *     Y = H . W_down                  computed from the packed form
+ *     plus the backward pass, with the gradient of an L1 penalty on H
+ *                                     (bayesiansapien note, TL;DR).
+ * The repo-explainer page ("TwELL: The Packing Format...") names the kernel
+ * layer's jobs: dense-to-TwELL, TwELL-to-dense, and fused MLP execution.
+ *
+ * Conventions for every call
+ *   - bf16 tensors are passed as uint16_t bit patterns; all tensors are
+ *     row-major and dense (the leading dimension equals the row length unless
+ *     an ld argument says otherwise).
+ *   - Pointers named in a call are DEVICE pointers owned by the caller unless
+ *     the comment says host.  The library allocates no device memory inside
+ *     these calls; scratch comes from the caller's workspace.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     and never synchronise, except twell_read_status.
+ *   - Return value: TWELL_OK or a negative TWELL_ERR_* code found on the host
+ *     before any launch (nothing is launched then).  Errors found on the GPU
+ *     are written to the layout's device status word (see twell_t.status) and
+ *     read with twell_read_status; kernels never trap.
+ *   - Shapes: n_rows >= 0 (0 is a no-op), d_model % 64 == 0, d_ff % 128 == 0,
+ *     tile T in {32, 64, 128, 256} with T | d_ff, 1 <= cap C <= min(T, 32).
+ *     Device pointers must be 16-byte aligned.
+ *
+ * Hybrid layout (this build's reading of the pages; capacity C, the overflow
+ * rule and byte layouts are not given there):
+ *   - d_ff is cut into n_tiles = d_ff / T tiles of T consecutive hidden units.
+ *   - Per (row n, tile t) a cell holds up to C non-zero values, their
+ *     tile-local indices (strictly increasing, in [0, T)) and a count.
+ *   - A row with any tile holding more than C non-zeros is a fallback row: its
+ *     dense H row lives in fb_dense, its cells have count 0.  Fallback rows
+ *     take slots 0, 1, ... in ascending row order.
+ *   - Unused slots are padding: value +0.0 (0x0000), index 0.
+ *   - "Non-zero" means the bf16 value compares unequal to zero.
+ */
+#ifndef TWELL_H
+#define TWELL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TWELL_API __attribute__((visibility("default")))
+#else
+#define TWELL_API
+#endif
+
+typedef struct CUstream_st* twell_stream_t; /* same type as cudaStream_t */
+
+enum {
+  TWELL_OK = 0,
+  TWELL_ERR_INVALID_ARG = -1,        /* null pointer, negative size, bad T/C */
+  TWELL_ERR_MISALIGNED = -2,         /* pointer not 16-byte aligned */
+  TWELL_ERR_UNSUPPORTED = -3,        /* shape outside the kernels' tiling */
+  TWELL_ERR_CUDA = -4,               /* a CUDA runtime/driver call failed */
+  TWELL_ERR_WORKSPACE = -5,          /* workspace missing or too small */
+  TWELL_ERR_FALLBACK_OVERFLOW = -6,  /* device: more fallback rows than fb_cap */
+  TWELL_ERR_WAIT_TIMEOUT = -7,       /* device: a bounded pipeline wait expired */
+  TWELL_ERR_NO_DEVICE = -8           /* no sm_103a device current */
+};
+
+/* A packed activation matrix H [n_rows][d_ff].  The struct itself lives in
+ * host memory and is read during the call; every pointer in it is a device
+ * pointer to caller-owned memory of the stated size. */
+typedef struct twell_t {
+  int32_t n_rows;     /* N */
+  int32_t d_ff;       /* f */
+  int32_t tile;       /* T */
+  int32_t cap;        /* C */
+  int32_t fb_cap;     /* rows the dense fallback can hold (>= 0) */
+  int32_t reserved;   /* must be 0 */
+  uint16_t* values;   /* [N][f/T][C] bf16 */
+  uint8_t* idx;       /* [N][f/T][C] tile-local index */
+  uint8_t* counts;    /* [N][f/T] non-zeros stored in the cell (0 for fallback rows) */
+  int32_t* row_fb;    /* [N] -1 = TwELL row, else slot in fb_dense */
+  int32_t* fb_rows;   /* [fb_cap] row of each fallback slot, ascending */
+  uint16_t* fb_dense; /* [fb_cap][f] bf16 dense rows */
+  int32_t* n_fb;      /* device scalar: number of fallback rows found (may exceed fb_cap) */
+  int32_t* status;    /* device scalar: 0 or a TWELL_ERR_* code set by a kernel */
+} twell_t;
+
+/* Dense -> TwELL (the pages' "dense-to-TwELL" kernel path; repo-explainer,
+ * "TwELL: The Packing Format That Fits the Machine").
+ * H: device, [out->n_rows][ldh] bf16, ldh >= d_ff and ldh % 8 == 0.
+ * Writes every array of *out, *out->n_fb and resets *out->status to 0 (then
+ * TWELL_ERR_FALLBACK_OVERFLOW if n_fb > fb_cap; rows past fb_cap are not
+ * stored).  Bit-exact: the output is a pure function of H's bits. */
+TWELL_API int twell_pack(const uint16_t* H, int64_t ldh, const twell_t* out, twell_stream_t stream);
+
+/* TwELL -> dense (the pages' "TwELL-to-dense" path).
+ * H: device, [in->n_rows][ldh] bf16 output, ldh >= d_ff, ldh % 8 == 0.
+ * Every element of the first d_ff columns is written (zeros included). */
+TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t stream);
+
+/* Forward of the layer ("fused MLP execution", repo-explainer page; the
+ * dense matrix for rare dense tokens, ifai.io news "Reshaping math for the GPU").
+ *   X      [n_rows][d_model] bf16      W_inT  [d_ff][d_model] bf16 (W_in transposed,
+ *   b      [d_ff] bf16                                             nn.Linear layout)
+ *   W_down [d_ff][d_model] bf16 (row j = hidden unit j)
+ *   H      packed output; H->n_rows == n_rows, H->d_ff == d_ff
+ *   Y      [n_rows][d_model] bf16 output
+ * h = bf16(z) where z = X.W_in + b > 0 (fp32 accumulation), else +0; Y is the
+ * fp32 sum over h's non-zeros rounded once to bf16.  Fallback rows get their
+ * dense h recomputed and stored in fb_dense.
+ * workspace: device, >= twell_fwd_workspace_bytes(...) bytes, 256-byte aligned. */
+TWELL_API int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
+                  const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
+                  const twell_t* H, uint16_t* Y, void* workspace, size_t workspace_bytes,
+                  twell_stream_t stream);
+
+TWELL_API size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
+                                 int32_t cap, int32_t fb_cap);
+
+/* Backward of  L = sum(Y * dY) + l1_lambda * sum|H|  (the L1 penalty of the
+ * bayesiansapien note's TL;DR, its gradient taken as l1_lambda wherever h > 0).
+ *   H    the packed forward activations (pattern = ReLU mask); n_rows = H->n_rows
+ *   X [n_rows][d_model], W_inT and W_down [d_ff][d_model]: the forward's inputs
+ *   dY   [n_rows][d_model] bf16
+ * Outputs (all overwritten):
+ *   dX      [n_rows][d_model] bf16      dZ = (dY.W_down^T + l1_lambda) at the pattern
+ *   dW_inT  [d_ff][d_model] fp32        dW_inT[j] = sum_n dZ[n][j] X[n]
+ *   dW_down [d_ff][d_model] fp32        dW_down[j] = sum_n h[n][j] dY[n]
+ *   db      [d_ff] fp32                 db[j] = sum_n dZ[n][j]
+ * dH is only formed at H's non-zeros (SDDMM).  Deterministic: no atomics.
+ * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned. */
+TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
+                  const twell_t* H, int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
+                  float* dW_inT, float* dW_down, float* db, void* workspace,
+                  size_t workspace_bytes, twell_stream_t stream);
+
+TWELL_API size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
+                                 int32_t cap, int32_t fb_cap);
+
+/* Dense comparator (not part of the method): Y = ReLU(X.W_in + b).W_down with
+ * the same tensor-core GEMM and no sparsity.  W_downT is [d_model][d_ff] bf16
+ * (W_down transposed); Hbuf is caller scratch [n_rows][d_ff] bf16 that receives
+ * the dense H. */
+TWELL_API int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
+                        const uint16_t* W_downT, int32_t n_rows, int32_t d_model, int32_t d_ff,
+                        uint16_t* Hbuf, uint16_t* Y, twell_stream_t stream);
+
+/* Synchronises `stream`, then returns *layout->status if non-zero, else
+ * TWELL_ERR_FALLBACK_OVERFLOW when *layout->n_fb > fb_cap, else TWELL_OK. */
+TWELL_API int twell_read_status(const twell_t* layout, twell_stream_t stream);
+
+/* Static string for a TWELL_* code. */
+TWELL_API const char* twell_status_string(int code);
+
+/* Number of kernels this library has launched in this process (all calls). */
+TWELL_API int64_t twell_launch_count(void);
+
+/* Per-kernel device timing.  While enabled (on != 0) every launch is bracketed
+ * by CUDA events on its stream.  twell_profile_read synchronises the device,
+ * accumulates the pending event pairs and returns, for the kernel named by
+ * `kernel` (a TWELL_KERNEL_* id), the launches and total milliseconds since
+ * the last reset.  twell_profile_reset clears the totals. */
+enum {
+  TWELL_KERNEL_UP_PACK = 0,      /* tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue */
+  TWELL_KERNEL_ROUTE = 1,        /* fallback routing scan */
+  TWELL_KERNEL_FB_GATHER = 2,    /* gather of fallback X rows + clearing their cells */
+  TWELL_KERNEL_FB_UP = 3,        /* tcgen05 recompute of dense fallback rows */
+  TWELL_KERNEL_SPMM = 4,         /* TwELL gather-SpMM down-projection */
+  TWELL_KERNEL_FB_DOWN = 5,      /* fallback rows' down-projection */
+  TWELL_KERNEL_PACK = 6,         /* standalone dense -> TwELL */
+  TWELL_KERNEL_UNPACK = 7,       /* TwELL -> dense */
+  TWELL_KERNEL_SDDMM = 8,        /* backward: dZ at the pattern */
+  TWELL_KERNEL_DX = 9,           /* backward: dX gather */
+  TWELL_KERNEL_DW = 10,          /* backward: dW_down, dW_inT, db */
+  TWELL_KERNEL_DENSE_GEMM = 11,  /* dense comparator GEMMs */
+  TWELL_KERNEL_AUX = 12,         /* small helpers (clears, transposed indexes) */
+  TWELL_KERNEL_COUNT = 13
+};
+TWELL_API int twell_profile_enable(int on);
+TWELL_API int twell_profile_reset(void);
+TWELL_API int twell_profile_read(int kernel, int64_t* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_H */

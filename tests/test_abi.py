@@ -1,0 +1,76 @@
+"""The C-ABI library loads and exports every entry point include/twell.h
+declares; host-side argument checks return their codes without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "twell.h")) as fh:
+        src = fh.read()
+    return sorted(set(re.findall(r"TWELL_API\s+[\w\s\*]+?\b(twell_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    import activation_sparse_transformer_gb300 as tw
+    return tw.load_library()
+
+
+def test_header_declares_the_four_layer_calls():
+    names = _declared()
+    for n in ("twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_ffn_bwd"):
+        assert n in names
+    assert len(names) >= 13
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import activation_sparse_transformer_gb300 as tw
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert sorted(tw.EXPORTED) == _declared()
+
+
+def test_status_strings(lib):
+    import activation_sparse_transformer_gb300 as tw
+    for code in range(0, -9, -1):
+        s = tw.status_string(code)
+        assert s and s != "unknown status"
+    assert tw.status_string(-100) == "unknown status"
+
+
+def test_host_argument_checks_without_gpu(lib):
+    import activation_sparse_transformer_gb300 as tw
+    L = tw.twell_t(16, 1024, 64, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    # null layout
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, None, None) == -1
+    # bad tile
+    bad = tw.twell_t(16, 1024, 48, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -1
+    # capacity above T
+    bad = tw.twell_t(16, 1024, 32, 33, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -1
+    # misaligned pointer in the layout
+    bad = tw.twell_t(16, 1024, 64, 8, 4, 0, 0x1001, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -2
+    # d_ff not a multiple of 128 (but of T)
+    bad = tw.twell_t(16, 960, 64, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -3
+    # a well-formed call reaches the device check and stops there on a CPU-only host
+    rc = lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(L), None)
+    try:
+        import torch
+        gpu = torch.cuda.is_available()
+    except Exception:
+        gpu = False
+    if not gpu:
+        assert rc == -8
+    # workspace sizes are pure host arithmetic
+    assert tw.fwd_workspace_bytes(4096, 2048, 8192, 128, 8, 512) == 512 * 2048 * 2
+    assert tw.bwd_workspace_bytes(4096, 2048, 8192, 128, 8, 512) > 4096 * 64 * 8 * 4

@@ -1,0 +1,180 @@
+"""Fused forward on the GPU (tcgen05 up-projection with the TwELL-pack
+epilogue, routing, dense-fallback recompute, gather-SpMM) against the oracle.
+
+* integer inputs: every sum is exact, so the GPU must match bit for bit;
+* random bf16 layers: the packed output is exactly the oracle's packing of the
+  H the GPU computed; H agrees with the oracle's except where |z| < 1e-3;
+  Y is within the stated tolerance;
+* the 1B-scale layer in the bench's launch configuration, checked on sampled
+  rows plus every fallback row.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from twell_check import assert_close, from_dev_bits, from_dev_f32, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tw():
+    import __graft_entry__ as g
+    g.build()
+    import activation_sparse_transformer_gb300 as m
+    return m
+
+
+def run_fwd(tw, torch, inp, T, C, fb_cap):
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    N, d = inp["X"].shape
+    f = inp["W_inT"].shape[0]
+    p = tw.alloc_packed(N, f, T, C, fb_cap, dev)
+    p.values.view(torch.int16).fill_(0x7777)
+    p.idx.fill_(0xAB)
+    p.counts.fill_(0xCD)
+    Y = torch.full((N, d), 3.0, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb_cap), dtype=torch.uint8, device=dev)
+    tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws)
+    rc = tw.twell_read_status(p)
+    return p, Y, rc
+
+
+def gpu_h(tw, torch, p):
+    H = torch.empty((p.n_rows, p.d_ff), dtype=torch.bfloat16, device="cuda")
+    tw.twell_unpack(p, H)
+    torch.cuda.synchronize()
+    return from_dev_bits(H)
+
+
+def check_packing_of(p, H, T, C, fb_cap):
+    ref = oracle.pack(H, T, C, fb_cap)
+    assert int(p.n_fb[0].item()) == ref["n_fb"]
+    assert np.array_equal(from_dev_bits(p.values).reshape(ref["values"].shape), ref["values"])
+    assert np.array_equal(from_dev_bits(p.idx), ref["idx"])
+    assert np.array_equal(from_dev_bits(p.counts), ref["counts"])
+    assert np.array_equal(from_dev_bits(p.row_fb)[:H.shape[0]], ref["row_fb"])
+    k = min(ref["n_fb"], fb_cap)
+    assert np.array_equal(from_dev_bits(p.fb_rows)[:k], ref["fb_rows"][:k])
+    assert np.array_equal(from_dev_bits(p.fb_dense)[:k], ref["fb_dense"][:k])
+    return ref
+
+
+INT_CASES = [
+    # N, d, f, T, C, sparsity, seed
+    (256, 256, 1024, 64, 8, 0.97, 1),
+    (200, 128, 1152, 128, 8, 0.95, 2),    # ragged N, d_ff % 256 == 128 (128-wide N tiles)
+    (130, 64, 512, 32, 4, 0.9, 3),        # K = one 64-wide step, many overflow rows
+    (384, 512, 2048, 256, 16, 0.98, 4),
+]
+
+
+@pytest.mark.parametrize("N,d,f,T,C,sp,seed", INT_CASES)
+def test_fwd_integer_bit_exact(tw, N, d, f, T, C, sp, seed):
+    import torch
+    inp = synth.make_integer_inputs(N, d, f, seed=seed, sparsity=sp)
+    fb_cap = N
+    ref = oracle.forward(inp["X"], inp["W_inT"], inp["b"], inp["W_down"], T, C, fb_cap)
+    assert np.abs(ref["Y"]).max() < 2 ** 24
+    p, Y, rc = run_fwd(tw, torch, inp, T, C, fb_cap)
+    assert rc == 0, tw.status_string(rc)
+    H = gpu_h(tw, torch, p)
+    assert np.array_equal(H, ref["H"])
+    check_packing_of(p, ref["H"], T, C, fb_cap)
+    assert np.array_equal(from_dev_bits(Y), ref["Y_bf16"])
+
+
+def _check_random_layer(tw, torch, cfg, inp, rows=None):
+    T, C, fb = cfg.tile, cfg.cap, cfg.fallback_capacity
+    p, Y, rc = run_fwd(tw, torch, inp, T, C, fb)
+    assert rc == 0, tw.status_string(rc)
+    Hg = gpu_h(tw, torch, p)
+    ref_pack = check_packing_of(p, Hg, T, C, fb)
+    if rows is None:
+        rows = np.arange(cfg.n_rows, dtype=np.int32)
+    rows = np.unique(np.concatenate([rows, np.nonzero(ref_pack["row_fb"] >= 0)[0]])).astype(np.int32)
+    Z, Hr = oracle.hidden(inp["X"], inp["W_inT"], inp["b"], rows=rows)
+    mism = Hg[rows] != Hr
+    if mism.any():
+        assert np.abs(Z[mism]).max() < 1e-3, np.abs(Z[mism]).max()
+        assert mism.mean() < 1e-4
+    assert_close(synth.bf16_bits_to_f32(Hg[rows]), synth.bf16_bits_to_f32(Hr), "H")
+    Yr = oracle.down_dense(Hr, inp["W_down"])
+    assert_close(from_dev_f32(Y)[rows], Yr, "Y")
+    return p, ref_pack
+
+
+def test_fwd_pr1(tw):
+    import torch
+    cfg = synth.CONFIGS["pr1"]
+    inp = synth.make_ffn_inputs(cfg)
+    _check_random_layer(tw, torch, cfg, inp)
+
+
+@pytest.mark.parametrize("N,T,C", [(333, 64, 8), (129, 128, 8), (513, 32, 4), (64, 256, 16)])
+def test_fwd_ragged_lognormal(tw, N, T, C):
+    import torch
+    cfg = synth.FFNConfig("t", N, 256, 1024, T, C, seed=N, row_spread="lognormal", forced_frac_rows=0.03,
+                          fb_cap=N // 4 + 4)
+    inp = synth.make_ffn_inputs(cfg)
+    p, ref = _check_random_layer(tw, torch, cfg, inp)
+    assert ref["n_fb"] >= 1
+
+
+def test_fwd_1b_full_size_sampled(tw):
+    import torch
+    cfg = synth.CONFIGS["1b"]
+    inp = synth.make_ffn_inputs(cfg)
+    rows = np.random.default_rng(0).choice(cfg.n_rows, size=256, replace=False)
+    rows = np.concatenate([rows, [0, cfg.n_rows - 1]])
+    p, ref = _check_random_layer(tw, torch, cfg, inp, rows=rows)
+    assert ref["n_fb"] >= len(inp["forced_rows"])
+    assert set(inp["forced_rows"].tolist()) <= set(np.nonzero(ref["row_fb"] >= 0)[0].tolist())
+
+
+def test_fwd_fallback_overflow_status(tw):
+    import torch
+    cfg = synth.FFNConfig("t", 256, 256, 1024, 64, 8, seed=3, row_spread="lognormal", forced_frac_rows=0.1,
+                          fb_cap=4)
+    inp = synth.make_ffn_inputs(cfg)
+    p, Y, rc = run_fwd(tw, torch, inp, 64, 8, 4)
+    assert rc == -6
+    assert int(p.n_fb[0].item()) > 4
+
+
+def test_fwd_empty_batch(tw):
+    import torch
+    inp = synth.make_integer_inputs(16, 64, 256, seed=1, sparsity=0.9)
+    dev = torch.device("cuda")
+    p = tw.alloc_packed(0, 256, 64, 8, 4, dev)
+    X = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(0, 64, 256, 64, 8, 4), dtype=torch.uint8, device=dev)
+    Wi, b, Wd = (to_dev(inp[k], torch) for k in ("W_inT", "b", "W_down"))
+    # zero rows: a no-op that still validates its arguments
+    st = p.struct()
+    lib = tw.load_library()
+    import ctypes
+    rc = lib.twell_ffn_fwd(0x100, Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), 0, 64, 256, ctypes.byref(st),
+                           0x100, ws.data_ptr(), ws.numel(), None)
+    assert rc == 0
+
+
+def test_dense_comparator(tw):
+    import torch
+    cfg = synth.CONFIGS["pr1"]
+    inp = synth.make_ffn_inputs(cfg)
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    WdT = Wd.t().contiguous()
+    Hb = torch.empty((cfg.n_rows, cfg.d_ff), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((cfg.n_rows, cfg.d_model), dtype=torch.bfloat16, device=dev)
+    tw.twell_dense_ffn_fwd(X, Wi, b, WdT, Hb, Y)
+    torch.cuda.synchronize()
+    Z, Hr = oracle.hidden(inp["X"], inp["W_inT"], inp["b"])
+    Hg = from_dev_bits(Hb)
+    mism = Hg != Hr
+    assert not mism.any() or np.abs(Z[mism]).max() < 1e-3
+    assert_close(from_dev_f32(Y), oracle.down_dense(Hr, inp["W_down"]), "dense Y")
