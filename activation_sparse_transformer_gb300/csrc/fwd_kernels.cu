@@ -85,7 +85,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
       if (r >= L.N) break;
       if ((flags >> i) & 1) {
         L.row_fb[r] = slot;
-        if (slot < L.fb_cap) L.fb_rows[slot] = r;
+        if (slot < L.fb_cap) {
+          L.fb_rows[slot] = r;
+        } else {
+          // past the capacity (an error the status word reports): the row is
+          // not stored anywhere, but its cells still become empty
+          const int64_t cell0 = static_cast<int64_t>(r) * L.nt;
+          for (int c = 0; c < L.nt; ++c) L.counts[cell0 + c] = 0;
+          for (int c = 0; c < L.nt * L.C; ++c) {
+            L.values[cell0 * L.C + c] = 0;
+            L.idx[cell0 * L.C + c] = 0;
+          }
+        }
         ++slot;
       } else {
         L.row_fb[r] = -1;

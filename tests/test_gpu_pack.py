@@ -67,7 +67,7 @@ def test_pack_bit_exact(tw, N, f, T, C, act, seed):
     import torch
     dense_rows = np.arange(3, N, 17)
     H = synth.make_dense_h(N, f, seed=seed, activity=act, dense_rows=dense_rows)
-    fb_cap = max(4, len(dense_rows) + 8)
+    fb_cap = max(4, oracle.pack(H, T, C, N)["n_fb"] + 3)
     ref = oracle.pack(H, T, C, fb_cap)
     assert ref["n_fb"] >= len(dense_rows) // 2
     p, rc, Hd = _pack_on_gpu(tw, torch, H, T, C, fb_cap)
