@@ -24,6 +24,7 @@ EXPORTED = [
     "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",
     "twell_bwd_workspace_bytes", "twell_dense_ffn_fwd", "twell_read_status", "twell_status_string",
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
+    "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch",
 ]
 
 
@@ -70,6 +71,8 @@ def load_library() -> ctypes.CDLL:
         "twell_profile_enable": (ctypes.c_int, [ctypes.c_int]),
         "twell_profile_reset": (ctypes.c_int, []),
         "twell_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]),
+        "twell_ffn_fwd_noalloc": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P]),
+        "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -169,6 +172,17 @@ def twell_ffn_fwd(X, W_inT, b, W_down, packed: Packed, Y, workspace, stream=None
     _check(load_library().twell_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, ctypes.byref(st),
                                         _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "twell_ffn_fwd")
+
+
+def twell_ffn_fwd_noalloc(X, W_inT, b, W_down, packed: Packed, Y, stream=None) -> None:
+    """twell_ffn_fwd without a workspace argument: the library's fixed scratch
+    array is used (for callers that cannot allocate device memory)."""
+    n, d = X.shape
+    f = W_inT.shape[0]
+    st = packed.struct()
+    _check(load_library().twell_ffn_fwd_noalloc(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f,
+                                                ctypes.byref(st), _ptr(Y), _stream(stream)),
+           "twell_ffn_fwd_noalloc")
 
 
 def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW_inT, dW_down, db, workspace,

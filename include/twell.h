@@ -128,6 +128,33 @@ TWELL_API int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint
 TWELL_API size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
                                  int32_t cap, int32_t fb_cap);
 
+/* The forward pass for callers that cannot allocate device memory.  (The
+ * paper and its pages have no counterpart: this is a deployment convenience
+ * of this library.)  Some callers have no allocator of their own to hand --
+ * code running inside another framework's memory pool, plugins whose host
+ * application owns every cudaMalloc, real-time paths where a cudaMalloc (which
+ * may synchronise the device) is not allowed -- so they cannot supply the
+ * workspace twell_ffn_fwd needs.  This call takes the same arguments minus the
+ * workspace and uses a fixed scratch array compiled into the library instead
+ * (twell_ffn_fwd_noalloc_max_scratch() bytes, 4 MiB; every GPU that loads the
+ * library holds it until the process exits).  It allocates nothing.
+ *   - Sizes: twell_fwd_workspace_bytes(...) must not exceed that maximum
+ *     (fb_cap * d_model <= 2 Mi); otherwise TWELL_ERR_WORKSPACE is returned
+ *     and nothing is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero): calls that overlap on the GPU,
+ *     e.g. on two streams, race on it and must be ordered by the caller.
+ * Results are identical to twell_ffn_fwd with a caller-provided workspace. */
+TWELL_API int twell_ffn_fwd_noalloc(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
+                                    const uint16_t* W_down, int32_t n_rows, int32_t d_model,
+                                    int32_t d_ff, const twell_t* H, uint16_t* Y,
+                                    twell_stream_t stream);
+
+TWELL_API size_t twell_ffn_fwd_noalloc_max_scratch(void);
+
 /* Backward of  L = sum(Y * dY) + l1_lambda * sum|H|  (the L1 penalty of the
  * bayesiansapien note's TL;DR, its gradient taken as l1_lambda wherever h > 0).
  *   H    the packed forward activations (pattern = ReLU mask); n_rows = H->n_rows
