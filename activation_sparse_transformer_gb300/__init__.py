@@ -195,10 +195,11 @@ def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW
                                         _stream(stream)), "twell_ffn_bwd")
 
 
-def twell_dense_ffn_fwd(X, W_inT, b, W_downT, Hbuf, Y, stream=None) -> None:
+def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
+    """Dense comparator: Y = ReLU(X.W_in + b).W_down on the same tensor-core GEMM."""
     n, d = X.shape
     f = W_inT.shape[0]
-    _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_downT), n, d, f, _ptr(Hbuf),
+    _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, _ptr(Hbuf),
                                               _ptr(Y), _stream(stream)), "twell_dense_ffn_fwd")
 
 

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -184,14 +185,34 @@ int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t str
   return launch_unpack(*in, H, ldh, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Forward workspace: [spill tiles][spill counter][fallback down-projection partials]
+struct FwdWorkspace {
+  size_t spill_off, count_off, part_off, total;
+  int32_t spill_cap;
+  int ksplit;
+};
+
+FwdWorkspace fwd_workspace_layout(int32_t d_model, int32_t d_ff, int32_t tile, int32_t fb_cap) {
+  FwdWorkspace w{};
+  const int64_t nt = d_ff / tile;
+  w.spill_cap = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(fb_cap) * nt, 0xFFFFFF));
+  w.ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
+  w.spill_off = 0;
+  w.count_off = align256(sizeof(uint16_t) * static_cast<size_t>(w.spill_cap) * static_cast<size_t>(tile));
+  w.part_off = w.count_off + 256;
+  w.total = w.part_off +
+            align256(sizeof(float) * static_cast<size_t>(w.ksplit) * static_cast<size_t>(fb_cap) * d_model);
+  return w;
+}
+}  // namespace
+
 size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
                                  int32_t fb_cap) {
   (void)n_rows;
-  (void)d_ff;
-  (void)tile;
   (void)cap;
-  if (fb_cap <= 0 || d_model <= 0) return 256;
-  return align256(sizeof(uint16_t) * static_cast<size_t>(fb_cap) * static_cast<size_t>(d_model));
+  if (d_model <= 0 || d_ff <= 0 || tile <= 0 || fb_cap < 0) return 0;
+  return fwd_workspace_layout(d_model, d_ff, tile, fb_cap).total;
 }
 
 int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
@@ -200,29 +221,30 @@ int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, c
   TW_TRY(check_layout(H));
   if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
   if (H->n_rows != n_rows || H->d_ff != d_ff) return TWELL_ERR_INVALID_ARG;
-  if (d_model % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
   TW_TRY(check_dense(b));
   TW_TRY(check_dense(W_down));
   TW_TRY(check_dense(Y));
-  const size_t need = twell_fwd_workspace_bytes(n_rows, d_model, d_ff, H->tile, H->cap, H->fb_cap);
-  if (H->fb_cap > 0 && (!workspace || workspace_bytes < need)) return TWELL_ERR_WORKSPACE;
-  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TWELL_ERR_MISALIGNED;
+  const FwdWorkspace w = fwd_workspace_layout(d_model, d_ff, H->tile, H->fb_cap);
+  if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
   if (n_rows == 0) return TWELL_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* spill = reinterpret_cast<uint16_t*>(ws + w.spill_off);
+  int32_t* spill_count = reinterpret_cast<int32_t*>(ws + w.count_off);
+  float* part = reinterpret_cast<float*>(ws + w.part_off);
   TW_TRY(reset_words(H, s));
-  PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, d_ff / H->tile, H->tile, H->cap};
-  TW_TRY(launch_gemm_pack(X, W_inT, n_rows, nullptr, d_ff, d_model, pp, H->status, s));
+  TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
+  PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
+                   d_ff / H->tile, H->tile, H->cap};
+  TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
   TW_TRY(launch_route(*H, s));
-  if (H->fb_cap > 0) {
-    uint16_t* Xfb = static_cast<uint16_t*>(workspace);
-    TW_TRY(launch_fb_gather(*H, X, d_model, Xfb, s));
-    DenseEpiParams dp{b, H->fb_dense, d_ff, 1};
-    TW_TRY(launch_gemm_dense(Xfb, W_inT, H->fb_cap, H->n_fb, d_ff, d_model, dp, H->status, TWELL_KERNEL_FB_UP, s));
-  }
+  TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, s));
   TW_TRY(launch_spmm(*H, W_down, d_model, Y, s));
-  TW_TRY(launch_fb_down(*H, W_down, d_model, Y, s));
+  TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, s));
   return TWELL_OK;
 }
 
@@ -237,7 +259,7 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
                   float* dW_down, float* db, void* workspace, size_t workspace_bytes, twell_stream_t stream) {
   TW_TRY(check_layout(H));
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
-  if (d_model % 64 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
   TW_TRY(check_dense(W_down));
@@ -255,7 +277,7 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_downT,
+int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
                         int32_t n_rows, int32_t d_model, int32_t d_ff, uint16_t* Hbuf, uint16_t* Y,
                         twell_stream_t stream) {
   if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
@@ -263,16 +285,17 @@ int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
   TW_TRY(check_dense(b));
-  TW_TRY(check_dense(W_downT));
+  TW_TRY(check_dense(W_down));
   TW_TRY(check_dense(Hbuf));
   TW_TRY(check_dense(Y));
   if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
   if (n_rows == 0) return TWELL_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   DenseEpiParams up{b, Hbuf, d_ff, 1};
-  TW_TRY(launch_gemm_dense(X, W_inT, n_rows, nullptr, d_ff, d_model, up, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
+  TW_TRY(launch_gemm_dense(X, W_inT, false, n_rows, nullptr, d_ff, d_model, up, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
   DenseEpiParams down{nullptr, Y, d_model, 0};
-  TW_TRY(launch_gemm_dense(Hbuf, W_downT, n_rows, nullptr, d_model, d_ff, down, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
+  TW_TRY(launch_gemm_dense(Hbuf, W_down, true, n_rows, nullptr, d_model, d_ff, down, nullptr, TWELL_KERNEL_DENSE_GEMM,
+                           s));
   return TWELL_OK;
 }
 

@@ -2,8 +2,10 @@
 // (L1 on the activations: bayesiansapien note, TL;DR; training kernels are
 // part of the release, "What it claims").
 //
-//   sddmm_kernel    dZ[n][j] = dY[n] . W_down[j] + lambda, formed only at the
-//                   stored non-zeros of H (the ReLU mask is the pattern)
+//   SDDMM           dZ[n][j] = dY[n] . W_down[j] + lambda, kept only at the
+//                   stored non-zeros of H (the ReLU mask is the pattern): a
+//                   tcgen05 GEMM dY . W_down^T whose epilogue samples the
+//                   accumulator at the TwELL pattern (gemm_tcgen05.cu)
 //   dx_kernel       dX[n] = sum_j dZ[n][j] W_in^T[j]   (gather over stored j)
 //   unit lists      the stored entries regrouped by hidden unit, rows
 //                   ascending, built deterministically (block histogram,
@@ -42,78 +44,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// dot(dY row staged in shared memory, W[j]) across the warp; every lane gets it.
-__device__ __forceinline__ float row_dot(const uint16_t* __restrict__ sdy, const uint16_t* __restrict__ W, int j,
-                                         int d, int lane) {
-  float acc = 0.f;
-  const uint16_t* wr = W + static_cast<int64_t>(j) * d;
-  for (int c = lane * 8; c < d; c += 256) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(wr + c));
-    const uint4 g = *reinterpret_cast<const uint4*>(sdy + c);
-    acc = fmaf(bf16_lo(g.x), bf16_lo(w.x), acc);
-    acc = fmaf(bf16_hi(g.x), bf16_hi(w.x), acc);
-    acc = fmaf(bf16_lo(g.y), bf16_lo(w.y), acc);
-    acc = fmaf(bf16_hi(g.y), bf16_hi(w.y), acc);
-    acc = fmaf(bf16_lo(g.z), bf16_lo(w.z), acc);
-    acc = fmaf(bf16_hi(g.z), bf16_hi(w.z), acc);
-    acc = fmaf(bf16_lo(g.w), bf16_lo(w.w), acc);
-    acc = fmaf(bf16_hi(g.w), bf16_hi(w.w), acc);
-  }
-  return warp_sum(acc);
-}
-
-// Warp per row; dynamic shared memory holds one dY row per warp.
-__global__ void __launch_bounds__(kWarps * 32)
-    sddmm_kernel(Layout L, const uint16_t* __restrict__ dY, const uint16_t* __restrict__ W_down, int d, float lambda,
-                 float* __restrict__ dz_cells, float* __restrict__ dz_fb) {
-  extern __shared__ uint4 sdy_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + warp;
-  if (row >= L.N) return;
-  uint16_t* sdy = reinterpret_cast<uint16_t*>(sdy_raw) + static_cast<int64_t>(warp) * d;
-  const uint4* src = reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(row) * d);
-  for (int i = lane; i < d / 8; i += 32) reinterpret_cast<uint4*>(sdy)[i] = src[i];
-  const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-  float* dzr = dz_cells + cell0 * L.C;
-  for (int i = lane; i < L.nt * L.C; i += 32) dzr[i] = 0.f;
-  __syncwarp();
-  const int fb = L.row_fb[row];
-  if (fb < 0) {
-    for (int t0 = 0; t0 < L.nt; t0 += 32) {
-      const int t = t0 + lane;
-      const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
-      unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int c = __shfl_sync(0xffffffffu, cnt, b);
-        const int64_t cell = cell0 + t0 + b;
-        for (int s = 0; s < c; ++s) {
-          const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
-          const float dot = row_dot(sdy, W_down, j, d, lane);
-          const float h = bf16_bits_to_float(L.values[cell * L.C + s]);
-          if (lane == 0) dz_cells[cell * L.C + s] = h > 0.f ? dot + lambda : 0.f;
-        }
-      }
-    }
-  } else if (fb < L.fb_cap) {
-    const uint16_t* hr = L.fb_dense + static_cast<int64_t>(fb) * L.f;
-    float* out = dz_fb + static_cast<int64_t>(fb) * L.f;
-    for (int j0 = 0; j0 < L.f; j0 += 32) {
-      const uint16_t hv = hr[j0 + lane];
-      unsigned mask = __ballot_sync(0xffffffffu, bf16_bits_to_float(hv) != 0.f);
-      float mine = 0.f;
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const float dot = row_dot(sdy, W_down, j0 + b, d, lane);
-        if (lane == b) mine = bf16_bits_to_float(hv) > 0.f ? dot + lambda : 0.f;
-      }
-      out[j0 + lane] = mine;
-    }
-  }
 }
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
@@ -380,20 +310,10 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const int row_blocks = (N + kWarps - 1) / kWarps;
   const int col_blocks = (d + 255) / 256;
   if (N > 0) {
-    const size_t smem = static_cast<size_t>(kWarps) * d * sizeof(uint16_t);
-    static bool attr[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr[dev]) {
-      if (cudaFuncSetAttribute(sddmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-        return TWELL_ERR_CUDA;
-      attr[dev] = true;
-    }
-    {
-      LaunchScope ls(TWELL_KERNEL_SDDMM, s);
-      sddmm_kernel<<<row_blocks, kWarps * 32, smem, s>>>(L, dY, W_down, d, lambda, ws.dz_cells, ws.dz_fb);
-    }
-    TW_CHECK_LAUNCH();
+    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile, Lh.tile,
+                       Lh.cap, f, lambda, ws.dz_cells, ws.dz_fb};
+    const int rc = launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s);
+    if (rc != TWELL_OK) return rc;
     {
       LaunchScope ls(TWELL_KERNEL_DX, s);
       dx_kernel<<<dim3(row_blocks, col_blocks), kWarps * 32, 0, s>>>(L, ws.dz_cells, ws.dz_fb, W_inT, d, dX);

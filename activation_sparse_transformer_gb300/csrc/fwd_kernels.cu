@@ -4,11 +4,14 @@
 //                    (ifai.io news, "Reshaping math for the GPU": a dense
 //                    matrix catches the rare dense tokens; bayesiansapien note,
 //                    Figure 1 "hybrid" splits rows between formats)
-//   fb_gather_kernel copies the fallback rows of X together for the dense
-//                    recompute and clears their TwELL cells
+//   fb_assemble_kernel builds each fallback row of fb_dense from its cells:
+//                    tiles that overflowed were spilled densely by the
+//                    up-projection's epilogue, the others hold <= C entries;
+//                    the row's cells are then cleared
 //   spmm_kernel      Y = H . W_down over TwELL rows, reading only the W_down
 //                    rows named by the stored tile-local indices
-//   fb_down_kernel   Y rows of the fallback rows from their dense H rows
+//   fb_reduce_kernel Y rows of the fallback rows: the K-split partial sums of
+//                    fb_dense . W_down (tensor cores) added in split order
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -112,21 +115,38 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
   }
 }
 
-// One CTA per fallback slot (grid-stride): X row -> Xfb[slot], and the row's
-// TwELL cells (written with truncated contents by the up-projection) become
-// count 0 with canonical padding.
-__global__ void fb_gather_kernel(Layout L, const uint16_t* __restrict__ X, int d, uint16_t* __restrict__ Xfb) {
+// One CTA per fallback slot (grid-stride), a warp per tile: the dense tile
+// comes from the spill buffer when the cell overflowed, else it is rebuilt
+// from the cell's entries; then the cell becomes empty (count 0, padding).
+__global__ void __launch_bounds__(256)
+    fb_assemble_kernel(Layout L, const uint16_t* __restrict__ spill, int32_t spill_cap) {
   const int nfb = min(*L.n_fb, L.fb_cap);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int vec = L.T / 8;  // 16-byte vectors per tile
   for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
     const int row = L.fb_rows[slot];
-    const uint4* src = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * d);
-    uint4* dst = reinterpret_cast<uint4*>(Xfb + static_cast<int64_t>(slot) * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
-    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-    for (int i = threadIdx.x; i < L.nt; i += blockDim.x) L.counts[cell0 + i] = 0;
-    for (int i = threadIdx.x; i < L.nt * L.C; i += blockDim.x) {
-      L.values[cell0 * L.C + i] = 0;
-      L.idx[cell0 * L.C + i] = 0;
+    uint16_t* out_row = L.fb_dense + static_cast<int64_t>(slot) * L.f;
+    for (int t = warp; t < L.nt; t += 8) {
+      const int64_t cell = static_cast<int64_t>(row) * L.nt + t;
+      const int cnt = L.counts[cell];
+      uint4* dst = reinterpret_cast<uint4*>(out_row + static_cast<int64_t>(t) * L.T);
+      if (cnt == kSpilledCell) {
+        const uint32_t s24 = static_cast<uint32_t>(L.values[cell * L.C]) |
+                             (static_cast<uint32_t>(L.idx[cell * L.C]) << 16);
+        const bool have = s24 < static_cast<uint32_t>(spill_cap);
+        const uint4* src = reinterpret_cast<const uint4*>(spill + static_cast<int64_t>(s24) * L.T);
+        for (int q = lane; q < vec; q += 32) dst[q] = have ? src[q] : make_uint4(0, 0, 0, 0);
+      } else {
+        for (int q = lane; q < vec; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        if (lane < cnt) out_row[static_cast<int64_t>(t) * L.T + L.idx[cell * L.C + lane]] = L.values[cell * L.C + lane];
+      }
+      __syncwarp();
+      if (lane == 0) L.counts[cell] = 0;
+      for (int q = lane; q < L.C; q += 32) {
+        L.values[cell * L.C + q] = 0;
+        L.idx[cell * L.C + q] = 0;
+      }
     }
   }
 }
@@ -189,32 +209,23 @@ __global__ void __launch_bounds__(kSpmmWarps * 32)
   if (active) *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c0) = pack8_bf16(acc);
 }
 
-// Fallback rows: warp per (slot, 256 columns); walks the dense h row in
-// ascending j, skipping zeros.
-__global__ void __launch_bounds__(128)
-    fb_down_kernel(Layout L, const uint16_t* __restrict__ W, int d, uint16_t* __restrict__ Y) {
+// Y[fb_rows[r]] = bf16(sum over splits of part[ks][r]), splits in order.
+__global__ void fb_reduce_kernel(Layout L, const float* __restrict__ part, int ksplit, int d,
+                                 uint16_t* __restrict__ Y) {
   const int nfb = min(*L.n_fb, L.fb_cap);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c0 = (blockIdx.y * 4 + warp) * 256 + lane * 8;
-  const bool active = c0 < d;
+  const int64_t stride = static_cast<int64_t>(L.fb_cap) * d;
   for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
     const int row = L.fb_rows[slot];
-    const uint16_t* h = L.fb_dense + static_cast<int64_t>(slot) * L.f;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < L.f; j0 += 32) {
-      const uint16_t hv = h[j0 + lane];
-      unsigned mask = __ballot_sync(0xffffffffu, bf16_bits_to_float(hv) != 0.0f);
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const float v = bf16_bits_to_float(static_cast<uint16_t>(__shfl_sync(0xffffffffu, hv, b)));
-        if (active) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(j0 + b) * d + c0));
-          fma8(acc, v, w);
-        }
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int ks = 0; ks < ksplit; ++ks) {
+        const float4* src = reinterpret_cast<const float4*>(part + ks * stride + static_cast<int64_t>(slot) * d + c);
+        const float4 x = src[0], y = src[1];
+        a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+        a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
       }
+      *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c) = pack8_bf16(a);
     }
-    if (active) *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c0) = pack8_bf16(acc);
   }
 }
 
@@ -226,11 +237,12 @@ int launch_route(const twell_t& L, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-int launch_fb_gather(const twell_t& L, const uint16_t* X, int d_model, uint16_t* Xfb, cudaStream_t s) {
+int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* /*spill_count*/,
+                       int32_t spill_cap, cudaStream_t s) {
   if (L.fb_cap <= 0) return TWELL_OK;
   const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
   LaunchScope ls(TWELL_KERNEL_FB_GATHER, s);
-  fb_gather_kernel<<<grid, 256, 0, s>>>(flat(L), X, d_model, Xfb);
+  fb_assemble_kernel<<<grid, 256, 0, s>>>(flat(L), spill, spill_cap);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -242,11 +254,16 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
+int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int ksplit,
+                   cudaStream_t s) {
   if (L.fb_cap <= 0) return TWELL_OK;
-  dim3 grid(std::max(1, std::min(L.fb_cap, 4 * sm_count())), (d_model + 1023) / 1024);
+  PartialEpiParams pp{part, d_model, static_cast<int64_t>(L.fb_cap) * d_model};
+  int rc = launch_gemm_partial_nmajor(L.fb_dense, W_down, L.fb_cap, L.n_fb, d_model, L.d_ff, ksplit, pp, L.status,
+                                      TWELL_KERNEL_FB_DOWN, s);
+  if (rc != TWELL_OK) return rc;
+  const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
   LaunchScope ls(TWELL_KERNEL_FB_DOWN, s);
-  fb_down_kernel<<<grid, 128, 0, s>>>(flat(L), W_down, d_model, Y);
+  fb_reduce_kernel<<<grid, 256, 0, s>>>(flat(L), part, ksplit, d_model, Y);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -1,19 +1,28 @@
 // Persistent warp-specialised bf16 GEMM on the 5th-generation tensor cores
-// (tcgen05 + TMEM), fed by TMA, with two epilogues:
+// (tcgen05 + TMEM), fed by TMA, with four epilogues:
 //   * PackEpi: z = acc + b, h = bf16(z) where z > 0, compaction of each
 //     (row, T-column tile) into TwELL cells (values, tile-local indices,
-//     count) and a per-row overflow flag -- the up-projection of the sparse
-//     layer with its pack fused in (the pages' "fused MLP execution" and
-//     "dense-to-TwELL" paths, repo-explainer "TwELL: The Packing Format...").
-//   * DenseEpi: bf16 rows with optional bias and ReLU (dense fallback rows,
-//     dense comparator).
+//     count) and a per-row overflow flag -- the layer's up-projection with its
+//     dense-to-TwELL pack fused in (repo-explainer, "TwELL: The Packing Format
+//     That Fits the Machine": dense-to-TwELL and fused MLP execution).  A tile
+//     that overflows C also spills its dense bf16 values so that the hybrid's
+//     dense fallback row can be assembled without recomputation (ifai.io news,
+//     "Reshaping math for the GPU": a dense matrix catches the rare dense
+//     tokens).
+//   * DenseEpi: bf16 rows with optional bias and ReLU (dense comparator).
+//   * PartialEpi: fp32 partial sums of one K split (fallback rows'
+//     down-projection).
+//   * SampleEpi: dH = dY . W_down^T kept only at the TwELL pattern, plus the
+//     L1 term's gradient (bayesiansapien note, TL;DR) -- the backward SDDMM.
 //
-// C[M, N] = A[M, K] . B[N, K]^T, A and B row-major bf16 (both K-major).
-// CTA tile 128 x BN, K step 64, one CTA per SM, tiles strided over CTAs.
-// Warp roles: 0 = TMA producer, 1 = MMA issuer, 2 = TMEM owner, 4..7 =
-// epilogue (warp 4+i reads TMEM lanes 32i..32i+31, i.e. tile rows 32i..).
-// Accumulators are double-buffered in TMEM so the epilogue of one tile runs
-// under the MMAs of the next.
+// C[M, N] = A[M, K] . B^T; A row-major [M][K] (K-major).  B is either
+// row-major [N][K] (K-major) or row-major [K][N] (N-major, e.g. W_down read as
+// the B operand of H . W_down).  CTA tile 128 x BN, K step 64, one CTA per SM,
+// work units (m, n, k-split) strided over CTAs.  Warp roles: 0 = TMA
+// producer, 1 = MMA issuer, 2 = TMEM owner, 4..7 = epilogue (warp 4+i reads
+// TMEM lanes 32i..32i+31, i.e. tile rows 32i..).  Accumulators are
+// double-buffered in TMEM so one tile's epilogue runs under the next tile's
+// MMAs.  Every pipeline wait is bounded and reports TWELL_ERR_WAIT_TIMEOUT.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -44,9 +53,29 @@ struct GemmArgs {
   const int32_t* M_dev;  // optional device-side row count (clamped to M)
   int N;
   int K;
+  int ksplit;            // K ranges per output tile (partial sums when > 1)
   int32_t* status;
   uint64_t wait_limit_ns;
 };
+
+// Row i of a 32-column TMEM chunk, picked with a select tree (no local memory).
+__device__ __forceinline__ uint32_t pick32(const uint32_t (&r)[32], int k) {
+  uint32_t a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = (k & 16) ? r[i + 16] : r[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = (k & 8) ? a[i + 8] : a[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (k & 4) ? b[i + 4] : b[i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) d[i] = (k & 2) ? c[i + 2] : c[i];
+  return (k & 1) ? d[1] : d[0];
+}
+
+__device__ __forceinline__ float bias_at(const uint4 (&bq)[4], int i) {
+  const uint32_t bw = (&bq[i / 8].x)[(i % 8) / 2];
+  return (i & 1) ? bf16_hi(bw) : bf16_lo(bw);
+}
 
 // ------------------------------------------------------------ epilogues
 struct PackEpi {
@@ -54,9 +83,19 @@ struct PackEpi {
   static constexpr int kMaxCap = 32;
   static constexpr uint32_t kSmemBytes = 128 * kMaxCap * 3;  // per thread: C values (u16) + C indices (u8)
 
+  // h of 32 columns [col, col + 32) of this thread's row, from TMEM.
+  static __device__ __forceinline__ void load_h32(const Params& p, uint32_t taddr, int col, uint32_t (&r)[32],
+                                                  uint4 (&bq)[4]) {
+    tmem_ld32(taddr, r);
+    const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bq[q] = __ldg(bp + q);
+    tmem_ld_wait();
+  }
+
   // One thread = one accumulator row; processes columns [col0, col0 + BN).
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0,
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
                                                uint8_t* smem, int et) {
     uint16_t* sv = reinterpret_cast<uint16_t*>(smem) + et * kMaxCap;
     uint8_t* si = smem + 128 * kMaxCap * 2 + et * kMaxCap;
@@ -66,16 +105,12 @@ struct PackEpi {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0 + c * 32);
       uint4 bq[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) bq[q] = __ldg(bp + q);
-      tmem_ld_wait();
+      load_h32(p, taddr + c * 32, col0 + c * 32, r, bq);
       const int j0 = (c * 32) % T;
       if (j0 == 0) {
         cnt = 0;
-        uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int q = 0; q < kMaxCap * 2 / 16; ++q) reinterpret_cast<uint4*>(sv)[q] = z;
 #pragma unroll
@@ -83,9 +118,7 @@ struct PackEpi {
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint32_t bw = (&bq[i / 8].x)[(i % 8) / 2];
-        const float bias = (i & 1) ? bf16_hi(bw) : bf16_lo(bw);
-        const float z = __uint_as_float(r[i]) + bias;
+        const float z = __uint_as_float(r[i]) + bias_at(bq, i);
         if (z > 0.0f) {
           const uint16_t h = float_to_bf16_bits(z);
           if (h != 0) {
@@ -97,10 +130,14 @@ struct PackEpi {
           }
         }
       }
-      if (((c + 1) * 32) % T == 0 && valid) {
-        const int t = (col0 + c * 32) / T;
-        const int64_t cell = static_cast<int64_t>(row) * p.n_tiles + t;
-        p.counts[cell] = static_cast<uint8_t>(cnt < C ? cnt : C);
+      if (((c + 1) * 32) % T != 0) continue;
+      // ---- the T-column tile [tile_c0, tile_c0 + T) is complete
+      const int tile_c0 = (c + 1) * 32 - T;
+      const int t = (col0 + tile_c0) / T;
+      const int64_t cell = static_cast<int64_t>(row) * p.n_tiles + t;
+      const bool ovf = valid && cnt > C;
+      if (valid && !ovf) {
+        p.counts[cell] = static_cast<uint8_t>(cnt);
         if ((C & 7) == 0) {
           uint4* gv = reinterpret_cast<uint4*>(p.values + cell * C);
           uint2* gi = reinterpret_cast<uint2*>(p.idx + cell * C);
@@ -114,7 +151,43 @@ struct PackEpi {
             p.idx[cell * C + q] = si[q];
           }
         }
-        if (cnt > C) p.row_flag[row] = 1;
+      }
+      if (__any_sync(0xffffffffu, ovf)) {
+        // The row becomes a fallback row: keep this tile's dense h so the
+        // dense row can be assembled later.  TMEM still holds the tile.
+        int slot = -1;
+        if (ovf) {
+          p.row_flag[row] = 1;
+          slot = atomicAdd(p.spill_count, 1);
+          if (slot >= p.spill_cap) {
+            report_error(p.status, TWELL_ERR_FALLBACK_OVERFLOW);
+            slot = -1;
+          }
+          p.counts[cell] = kSpilledCell;
+          const uint32_t s24 = slot < 0 ? 0xFFFFFFu : static_cast<uint32_t>(slot);
+          p.values[cell * C] = static_cast<uint16_t>(s24 & 0xFFFFu);
+          p.idx[cell * C] = static_cast<uint8_t>(s24 >> 16);
+        }
+        for (int cc = tile_c0; cc < tile_c0 + T; cc += 32) {
+          uint32_t rr[32];
+          uint4 bb[4];
+          load_h32(p, taddr + cc, col0 + cc, rr, bb);
+          if (slot >= 0) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float z0 = __uint_as_float(rr[i]) + bias_at(bb, i);
+              const float z1 = __uint_as_float(rr[i + 1]) + bias_at(bb, i + 1);
+              const uint32_t h0 = z0 > 0.0f ? float_to_bf16_bits(z0) : 0u;
+              const uint32_t h1 = z1 > 0.0f ? float_to_bf16_bits(z1) : 0u;
+              packed[i / 2] = h0 | (h1 << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.spill + static_cast<int64_t>(slot) * T + (cc - tile_c0));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
       }
     }
   }
@@ -125,7 +198,7 @@ struct DenseEpi {
   static constexpr uint32_t kSmemBytes = 0;
 
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0,
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
                                                uint8_t*, int) {
     const bool valid = row < M;
 #pragma unroll 1
@@ -144,9 +217,8 @@ struct DenseEpi {
       for (int i = 0; i < 32; i += 2) {
         float z0 = __uint_as_float(r[i]), z1 = __uint_as_float(r[i + 1]);
         if (p.bias) {
-          const uint32_t bw = (&bq[i / 8].x)[(i % 8) / 2];
-          z0 += bf16_lo(bw);
-          z1 += bf16_hi(bw);
+          z0 += bias_at(bq, i);
+          z1 += bias_at(bq, i + 1);
         }
         if (p.relu) {
           z0 = z0 > 0.0f ? z0 : 0.0f;
@@ -165,8 +237,87 @@ struct DenseEpi {
   }
 };
 
+struct PartialEpi {
+  using Params = PartialEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int ks,
+                                               uint8_t*, int) {
+    const bool valid = row < M;
+    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + static_cast<int64_t>(row) * p.ld + col0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      if (valid) {
+        float4* dst = reinterpret_cast<float4*>(base + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+      }
+    }
+  }
+};
+
+struct SampleEpi {
+  using Params = SampleEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
+                                               uint8_t*, int) {
+    const bool valid = row < M;
+    const int fb = valid ? p.row_fb[row] : -1;
+    const int T = p.tile, C = p.cap;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      const int col = col0 + c * 32;
+      if (!valid) continue;
+      if (fb < 0) {
+        // TwELL row: the stored entries of this chunk's tile that fall in it
+        const int t = col / T;
+        const int64_t cell = static_cast<int64_t>(row) * p.n_tiles + t;
+        const int cnt = p.counts[cell];
+        const int lo = col - t * T;
+        for (int s = 0; s < cnt; ++s) {
+          const int j = static_cast<int>(p.idx[cell * C + s]) - lo;
+          if (j >= 0 && j < 32) {
+            const float h = bf16_bits_to_float(p.values[cell * C + s]);
+            const float dh = __uint_as_float(pick32(r, j));
+            p.dz_cells[cell * C + s] = h > 0.0f ? dh + p.lambda : 0.0f;
+          }
+        }
+      } else if (fb < p.fb_cap) {
+        // fallback row: dense dZ over all 32 columns
+        const uint4* hp = reinterpret_cast<const uint4*>(p.fb_dense + static_cast<int64_t>(fb) * p.d_ff + col);
+        uint4 hq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hq[q] = hp[q];
+        float4* dst = reinterpret_cast<float4*>(p.dz_fb + static_cast<int64_t>(fb) * p.d_ff + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * q + e;
+            const float h = bias_at(hq, i);
+            o[e] = h > 0.0f ? __uint_as_float(r[i]) + p.lambda : 0.0f;
+          }
+          dst[q] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+};
+
 // ------------------------------------------------------------ kernel
-template <int BN, class Epi>
+template <int BN, class Epi, bool kBNMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args, const typename Epi::Params ep) {
@@ -193,8 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (args.M_dev) M = min(M, max(0, *args.M_dev));
   const int num_m = (M + kBM - 1) / kBM;
   const int num_n = args.N / BN;
-  const int num_tiles = num_m * num_n;
+  const int num_units = num_m * num_n * args.ksplit;
   const int num_k = (args.K + kBK - 1) / kBK;
+  const int k_per = (num_k + args.ksplit - 1) / args.ksplit;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -222,21 +374,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t limit = args.wait_limit_ns;
 
   if (warp == 0) {
-    if (lane == 0 && num_tiles > 0) {
+    if (lane == 0 && num_units > 0) {
       // ---------------- TMA producer
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m_blk = tile % num_m, n_blk = tile / num_m;
-        for (int kb = 0; kb < num_k; ++kb) {
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const int m_blk = u % num_m, rest = u / num_m;
+        const int n_blk = rest % num_n, ks = rest / num_n;
+        const int kb0 = ks * k_per, kb1 = min(num_k, kb0 + k_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], Cfg::kABytes + Cfg::kBBytes);
           tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kBK, m_blk * kBM);
-          tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], kb * kBK, n_blk * BN);
+          if (kBNMajor) {
+            // B is [K][N]: BN/64 boxes of 64 N-columns x 64 K-rows, 8 KB apart
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_2d(sB + stage * Cfg::kBBytes + q * 8192, &tmB, &full[stage], n_blk * BN + q * 64, kb * kBK);
+          } else {
+            tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], kb * kBK, n_blk * BN);
+          }
           issued_parity[stage] = static_cast<int>(phase);
           if (++stage == S) {
             stage = 0;
@@ -256,33 +417,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && num_tiles > 0) {
+    if (lane == 0 && num_units > 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN) | (kBNMajor ? (1u << 16) : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const int ks = (u / num_m) / num_n;
+        const int kb0 = ks * k_per, kb1 = min(num_k, kb0 + k_per);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, limit, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * Cfg::kABytes));
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * Cfg::kBBytes));
+          const uint64_t bdesc = kBNMajor ? smem_desc_sw128_nmajor(smem_u32(sB + stage * Cfg::kBBytes), 8192)
+                                          : smem_desc_sw128(smem_u32(sB + stage * Cfg::kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // +32 B per K step of 16 bf16, in 16-byte descriptor units
-            mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            // K step of 16: +32 B along a K-major row, or +16 rows (2 KB) of an N-major tile
+            const uint64_t b_step = kBNMajor ? 128u * k : 2u * k;
+            mma_bf16(d_tmem, adesc + 2u * k, bdesc + b_step, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
           if (++stage == S) {
@@ -309,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 128;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile % num_m, n_blk = tile / num_m;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const int m_blk = u % num_m, rest = u / num_m;
+      const int n_blk = rest % num_n, ks = rest / num_n;
       if (!mbar_wait(&tfull[acc], acc_phase, limit, abort)) {
         report_error(args.status, TWELL_ERR_WAIT_TIMEOUT);
         break;
@@ -318,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row = m_blk * kBM + lg * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::template apply<BN>(ep, taddr, row, M, n_blk * BN, epi_smem, et);
+      Epi::template apply<BN>(ep, taddr, row, M, n_blk * BN, ks, epi_smem, et);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -333,20 +499,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, class Epi>
-int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
+template <int BN, class Epi, bool kBNMajor>
+int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
+  const int num_k = (K + kBK - 1) / kBK;
+  if (ksplit < 1 || ksplit > num_k) return TWELL_ERR_UNSUPPORTED;
+  const int k_per = (num_k + ksplit - 1) / ksplit;
+  if (k_per * (ksplit - 1) >= num_k) return TWELL_ERR_UNSUPPORTED;  // every split must own a K block
   CUtensorMap ta, tb;
   int rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2,
                           kBK, kBM);
   if (rc) return rc;
-  rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kBK,
-                      BN);
+  if (kBNMajor)
+    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
+                        kBK);
+  else
+    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kBK,
+                        BN);
   if (rc) return rc;
   const uint32_t smem = 1024 + Cfg::kPipeBytes + Cfg::kBarBytes + Epi::kSmemBytes;
-  auto kern = tc_gemm_kernel<BN, Epi>;
+  auto kern = tc_gemm_kernel<BN, Epi, kBNMajor>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -355,9 +529,9 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
       return TWELL_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
-  const int grid = std::max(1, std::min(tiles, sm_count()));
-  GemmArgs args{M, M_dev, N, K, status, kWaitLimitNs};
+  const int units = ((M + kBM - 1) / kBM) * (N / BN) * ksplit;
+  const int grid = std::max(1, std::min(units, sm_count()));
+  GemmArgs args{M, M_dev, N, K, ksplit, status, kWaitLimitNs};
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kThreads, smem, s>>>(ta, tb, args, p);
@@ -367,19 +541,52 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
 
 }  // namespace
 
-int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
-                     const PackEpiParams& p, int32_t* status, cudaStream_t s) {
+int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, int N, int K, const PackEpiParams& p,
+                     int32_t* status, cudaStream_t s) {
   if (p.cap > PackEpi::kMaxCap) return TWELL_ERR_UNSUPPORTED;
-  if (N % 256 == 0) return launch_gemm<256, PackEpi>(A, B, M, M_dev, N, K, p, status, TWELL_KERNEL_UP_PACK, s);
+  if (N % 256 == 0)
+    return launch_gemm<256, PackEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
   if (N % 128 == 0 && p.tile <= 128)
-    return launch_gemm<128, PackEpi>(A, B, M, M_dev, N, K, p, status, TWELL_KERNEL_UP_PACK, s);
+    return launch_gemm<128, PackEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
   return TWELL_ERR_UNSUPPORTED;
 }
 
-int launch_gemm_dense(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
-                      const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
-  if (N % 256 == 0) return launch_gemm<256, DenseEpi>(A, B, M, M_dev, N, K, p, status, kernel_id, s);
-  if (N % 128 == 0) return launch_gemm<128, DenseEpi>(A, B, M, M_dev, N, K, p, status, kernel_id, s);
+int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int M, const int32_t* M_dev, int N,
+                      int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
+  if (b_n_major) {
+    if (N % 256 == 0) return launch_gemm<256, DenseEpi, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+    if (N % 128 == 0) return launch_gemm<128, DenseEpi, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+    return TWELL_ERR_UNSUPPORTED;
+  }
+  if (N % 256 == 0) return launch_gemm<256, DenseEpi, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+  if (N % 128 == 0) return launch_gemm<128, DenseEpi, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+  return TWELL_ERR_UNSUPPORTED;
+}
+
+int choose_fb_ksplit(int K) {
+  const int num_k = (K + kBK - 1) / kBK;
+  int ks = std::min(4, num_k);
+  while (ks > 1) {
+    const int per = (num_k + ks - 1) / ks;
+    if (per * (ks - 1) < num_k) break;
+    --ks;
+  }
+  return ks;
+}
+
+int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
+                               int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
+                               cudaStream_t s) {
+  if (N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  return launch_gemm<128, PartialEpi, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s);
+}
+
+int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
+                       int32_t* status, cudaStream_t s) {
+  if (N % 256 == 0)
+    return launch_gemm<256, SampleEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
+  if (N % 128 == 0)
+    return launch_gemm<128, SampleEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
   return TWELL_ERR_UNSUPPORTED;
 }
 

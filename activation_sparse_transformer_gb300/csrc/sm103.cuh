@@ -159,7 +159,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N tile.
+// Shared-memory matrix descriptor for an N-major operand tile (B stored as
+// [K][N]) written by TMA with 128-byte swizzling in boxes of 64 N-elements by
+// 64 K-rows: each K-row of a box is 128 B, 8-row K groups are 1024 B apart
+// (stride offset) and consecutive 64-wide N blocks are `lbo_bytes` apart
+// (leading offset).  Stepping K by 16 rows adds 2048 B to the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128_nmajor(uint32_t saddr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N
+// tile (bit 16 set separately marks an N-major B operand).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4)                                   // D format fp32
          | (1u << 7)                                 // A format bf16

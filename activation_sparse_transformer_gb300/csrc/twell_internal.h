@@ -34,12 +34,23 @@ int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uin
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
 // ---------------------------------------------------------------- kernels
+// A cell whose tile held more than C non-zeros during the fused
+// up-projection: its count byte holds this marker and its first slot holds a
+// 24-bit index into the spill buffer (value bits 0..15, index byte 16..23),
+// where the tile's dense bf16 values were written.  Only fallback rows carry
+// such cells, and the fallback assembly clears them.
+constexpr uint8_t kSpilledCell = 255;
+
 struct PackEpiParams {
   const uint16_t* bias;   // [d_ff]
   uint16_t* values;       // [M][n_tiles][C]
   uint8_t* idx;
   uint8_t* counts;        // [M][n_tiles]
   int32_t* row_flag;      // [M], set to 1 where a tile overflows C (pre-zeroed)
+  uint16_t* spill;        // [spill_cap][T] dense tiles of overflowing cells
+  int32_t* spill_count;   // device counter, pre-zeroed
+  int32_t spill_cap;
+  int32_t* status;
   int32_t n_tiles;
   int32_t tile;           // T
   int32_t cap;            // C
@@ -52,19 +63,49 @@ struct DenseEpiParams {
   int32_t relu;           // 1: out = bf16(z) where z > 0 else +0
 };
 
-// C[M, N] = A[M, K] . B[N, K]^T on tcgen05 with the epilogue named by the
-// function.  A rows beyond min(M, *M_dev) are not stored.  `n_blk` is the N
-// tile width (128 or 256).
-int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
-                     const PackEpiParams& p, int32_t* status, cudaStream_t s);
-int launch_gemm_dense(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
-                      const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+// fp32 partial sums of one K split: part[ks * split_stride + row * ld + col]
+struct PartialEpiParams {
+  float* part;
+  int64_t ld;
+  int64_t split_stride;
+};
+
+// dH = dY . W_down^T sampled at the TwELL pattern (the ReLU mask), plus the
+// L1 gradient: dZ = dH + lambda where h > 0.
+struct SampleEpiParams {
+  const uint16_t* values;   // the packed forward activations
+  const uint8_t* idx;
+  const uint8_t* counts;
+  const int32_t* row_fb;
+  const uint16_t* fb_dense;
+  int32_t fb_cap;
+  int32_t n_tiles, tile, cap, d_ff;
+  float lambda;
+  float* dz_cells;          // [M][n_tiles][C] fp32, stored slots only
+  float* dz_fb;             // [fb_cap][d_ff] fp32, dense (0 where h == 0)
+};
+
+// C[M, N] = A[M, K] . B^T with A row-major [M][K] (K-major).  B is row-major
+// [N][K] (K-major) for the pack / dense / sample GEMMs and row-major [K][N]
+// (N-major) for the partial GEMM.  Rows beyond min(M, *M_dev) are not stored.
+int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, int N, int K, const PackEpiParams& p,
+                     int32_t* status, cudaStream_t s);
+int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int M, const int32_t* M_dev, int N,
+                      int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
+                               int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
+                               cudaStream_t s);
+int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
+                       int32_t* status, cudaStream_t s);
+int choose_fb_ksplit(int K);   // K splits used for the fallback rows' down-projection
 
 // forward helpers (fwd_kernels.cu)
 int launch_route(const twell_t& L, cudaStream_t s);
-int launch_fb_gather(const twell_t& L, const uint16_t* X, int d_model, uint16_t* Xfb, cudaStream_t s);
+int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* spill_count, int32_t spill_cap,
+                       cudaStream_t s);
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
-int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
+int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int ksplit,
+                   cudaStream_t s);
 
 // standalone pack / unpack (pack_kernels.cu)
 int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);

@@ -221,15 +221,14 @@ def bench_ours(args, rank, world, local):
 
     # forward alone (the layer's inference path) and the dense comparator
     fwd_ms = timed(fwd, args.steps)
-    WdT = Wd.t().contiguous()
     Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
 
     def dense():
-        tw.twell_dense_ffn_fwd(X, Wi, b, WdT, Hbuf, Y, stream)
+        tw.twell_dense_ffn_fwd(X, Wi, b, Wd, Hbuf, Y, stream)
 
     dense()
     dense_ms = timed(dense, max(3, args.steps // 2))
-    del Hbuf, WdT
+    del Hbuf
 
     # end to end through the C ABI with host buffers (pinned), copies timed
     hX = torch.from_numpy(base["X"].view(np.int16)).view(torch.bfloat16).pin_memory()

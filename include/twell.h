@@ -31,7 +31,7 @@
  *     before any launch (nothing is launched then).  Errors found on the GPU
  *     are written to the layout's device status word (see twell_t.status) and
  *     read with twell_read_status; kernels never trap.
- *   - Shapes: n_rows >= 0 (0 is a no-op), d_model % 64 == 0, d_ff % 128 == 0,
+ *   - Shapes: n_rows >= 0 (0 is a no-op), d_model % 128 == 0, d_ff % 128 == 0,
  *     tile T in {32, 64, 128, 256} with T | d_ff, 1 <= cap C <= min(T, 32).
  *     Device pointers must be 16-byte aligned.
  *
@@ -117,9 +117,11 @@ TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_st
  *   H      packed output; H->n_rows == n_rows, H->d_ff == d_ff
  *   Y      [n_rows][d_model] bf16 output
  * h = bf16(z) where z = X.W_in + b > 0 (fp32 accumulation), else +0; Y is the
- * fp32 sum over h's non-zeros rounded once to bf16.  Fallback rows get their
- * dense h recomputed and stored in fb_dense.
- * workspace: device, >= twell_fwd_workspace_bytes(...) bytes, 256-byte aligned. */
+ * fp32 sum over h's non-zeros rounded once to bf16.  A tile that overflows C
+ * has its dense h kept by the up-projection, so the fallback rows of fb_dense
+ * hold exactly the h the GEMM produced.
+ * workspace: device, >= twell_fwd_workspace_bytes(...) bytes (always > 0),
+ * 256-byte aligned; its contents need no initialisation. */
 TWELL_API int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
                   const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
                   const twell_t* H, uint16_t* Y, void* workspace, size_t workspace_bytes,
@@ -139,8 +141,8 @@ TWELL_API size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int3
  * (twell_ffn_fwd_noalloc_max_scratch() bytes, 4 MiB; every GPU that loads the
  * library holds it until the process exits).  It allocates nothing.
  *   - Sizes: twell_fwd_workspace_bytes(...) must not exceed that maximum
- *     (fb_cap * d_model <= 2 Mi); otherwise TWELL_ERR_WORKSPACE is returned
- *     and nothing is launched.
+ *     (it grows with fb_cap * d_ff and fb_cap * d_model); otherwise
+ *     TWELL_ERR_WORKSPACE is returned and nothing is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -176,11 +178,11 @@ TWELL_API size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int3
                                  int32_t cap, int32_t fb_cap);
 
 /* Dense comparator (not part of the method): Y = ReLU(X.W_in + b).W_down with
- * the same tensor-core GEMM and no sparsity.  W_downT is [d_model][d_ff] bf16
- * (W_down transposed); Hbuf is caller scratch [n_rows][d_ff] bf16 that receives
+ * the same tensor-core GEMM and no sparsity.  W_down is [d_ff][d_model] bf16 as
+ * for twell_ffn_fwd; Hbuf is caller scratch [n_rows][d_ff] bf16 that receives
  * the dense H. */
 TWELL_API int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
-                        const uint16_t* W_downT, int32_t n_rows, int32_t d_model, int32_t d_ff,
+                        const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
                         uint16_t* Hbuf, uint16_t* Y, twell_stream_t stream);
 
 /* Synchronises `stream`, then returns *layout->status if non-zero, else

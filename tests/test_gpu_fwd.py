@@ -66,7 +66,7 @@ INT_CASES = [
     # N, d, f, T, C, sparsity, seed
     (256, 256, 1024, 64, 8, 0.97, 1),
     (200, 128, 1152, 128, 8, 0.95, 2),    # ragged N, d_ff % 256 == 128 (128-wide N tiles)
-    (130, 64, 512, 32, 4, 0.9, 3),        # K = one 64-wide step, many overflow rows
+    (130, 128, 512, 32, 4, 0.9, 3),       # K = two 64-wide steps, many overflow rows
     (384, 512, 2048, 256, 16, 0.98, 4),
 ]
 
@@ -148,20 +148,33 @@ def test_fwd_fallback_overflow_status(tw):
 
 def test_fwd_empty_batch(tw):
     import torch
-    inp = synth.make_integer_inputs(16, 64, 256, seed=1, sparsity=0.9)
+    inp = synth.make_integer_inputs(16, 128, 256, seed=1, sparsity=0.9)
     dev = torch.device("cuda")
     p = tw.alloc_packed(0, 256, 64, 8, 4, dev)
-    X = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
-    Y = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(tw.fwd_workspace_bytes(0, 64, 256, 64, 8, 4), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(0, 128, 256, 64, 8, 4), dtype=torch.uint8, device=dev)
     Wi, b, Wd = (to_dev(inp[k], torch) for k in ("W_inT", "b", "W_down"))
     # zero rows: a no-op that still validates its arguments
     st = p.struct()
     lib = tw.load_library()
     import ctypes
-    rc = lib.twell_ffn_fwd(0x100, Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), 0, 64, 256, ctypes.byref(st),
+    rc = lib.twell_ffn_fwd(0x100, Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), 0, 128, 256, ctypes.byref(st),
                            0x100, ws.data_ptr(), ws.numel(), None)
     assert rc == 0
+
+
+def test_dense_comparator_integer_exact(tw):
+    # N-major B operand (W_down read as [K][N]) through the tensor cores
+    import torch
+    inp = synth.make_integer_inputs(200, 256, 1536, seed=6, sparsity=0.97)
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    Hb = torch.empty((200, 1536), dtype=torch.bfloat16, device=dev)
+    Y = torch.empty((200, 256), dtype=torch.bfloat16, device=dev)
+    tw.twell_dense_ffn_fwd(X, Wi, b, Wd, Hb, Y)
+    torch.cuda.synchronize()
+    ref = oracle.forward(inp["X"], inp["W_inT"], inp["b"], inp["W_down"], 64, 8, 200)
+    assert np.array_equal(from_dev_bits(Hb), ref["H"])
+    assert np.array_equal(from_dev_bits(Y), oracle.round_bf16(oracle.down_dense(ref["H"], inp["W_down"])))
 
 
 def test_dense_comparator(tw):
@@ -170,10 +183,9 @@ def test_dense_comparator(tw):
     inp = synth.make_ffn_inputs(cfg)
     dev = torch.device("cuda")
     X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
-    WdT = Wd.t().contiguous()
     Hb = torch.empty((cfg.n_rows, cfg.d_ff), dtype=torch.bfloat16, device=dev)
     Y = torch.empty((cfg.n_rows, cfg.d_model), dtype=torch.bfloat16, device=dev)
-    tw.twell_dense_ffn_fwd(X, Wi, b, WdT, Hb, Y)
+    tw.twell_dense_ffn_fwd(X, Wi, b, Wd, Hb, Y)
     torch.cuda.synchronize()
     Z, Hr = oracle.hidden(inp["X"], inp["W_inT"], inp["b"])
     Hg = from_dev_bits(Hb)
