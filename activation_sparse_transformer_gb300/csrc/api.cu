@@ -97,8 +97,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
-                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+namespace {
+int encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows, uint64_t row_stride_bytes,
+                   uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
   auto fn = encode_fn();
   if (!fn) return TWELL_ERR_CUDA;
   cuuint64_t dims[2] = {inner_elems, rows};
@@ -106,9 +107,22 @@ int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uin
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TWELL_OK : TWELL_ERR_CUDA;
+}
+}  // namespace
+
+int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return encode_bf16_2d(map, base, inner_elems, rows, row_stride_bytes, box_inner, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int encode_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return encode_bf16_2d(map, base, inner_elems, rows, row_stride_bytes, box_inner, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace twell

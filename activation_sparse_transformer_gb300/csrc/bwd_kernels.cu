@@ -6,7 +6,10 @@
 //                   stored non-zeros of H (the ReLU mask is the pattern): a
 //                   tcgen05 GEMM dY . W_down^T whose epilogue samples the
 //                   accumulator at the TwELL pattern (gemm_tcgen05.cu)
-//   dx_kernel       dX[n] = sum_j dZ[n][j] W_in^T[j]   (gather over stored j)
+//   dX              dX[n] = sum_j dZ[n][j] W_in^T[j]: the gather-SpMM (spmm.cu)
+//                   with fp32 values for TwELL rows; for fallback rows a
+//                   split-K tcgen05 GEMM of dZ (as bf16 high + low parts)
+//                   with W_in^T read N-major, reduced in split order
 //   unit lists      the stored entries regrouped by hidden unit, rows
 //                   ascending, built deterministically (block histogram,
 //                   scans, ordered fill -- no atomics)
@@ -55,59 +58,6 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
   acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
   acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
   acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
-}
-
-// dX: warp per (row, 256 columns), terms in ascending hidden unit.
-__global__ void __launch_bounds__(kWarps * 32)
-    dx_kernel(Layout L, const float* __restrict__ dz_cells, const float* __restrict__ dz_fb,
-              const uint16_t* __restrict__ W_inT, int d, uint16_t* __restrict__ dX) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarps + warp;
-  if (row >= L.N) return;
-  const int c0 = blockIdx.y * 256 + lane * 8;
-  const bool active = c0 < d;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const int fb = L.row_fb[row];
-  if (fb < 0) {
-    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-    for (int t0 = 0; t0 < L.nt; t0 += 32) {
-      const int t = t0 + lane;
-      const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
-      unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int c = __shfl_sync(0xffffffffu, cnt, b);
-        const int64_t cell = cell0 + t0 + b;
-        for (int s = 0; s < c; ++s) {
-          const float v = dz_cells[cell * L.C + s];
-          const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
-          if (active) fma8(acc, v, __ldg(reinterpret_cast<const uint4*>(W_inT + static_cast<int64_t>(j) * d + c0)));
-        }
-      }
-    }
-  } else if (fb < L.fb_cap) {
-    const float* zr = dz_fb + static_cast<int64_t>(fb) * L.f;
-    for (int j0 = 0; j0 < L.f; j0 += 32) {
-      const float zv = zr[j0 + lane];
-      unsigned mask = __ballot_sync(0xffffffffu, zv != 0.f);
-      while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const float v = __shfl_sync(0xffffffffu, zv, b);
-        if (active)
-          fma8(acc, v, __ldg(reinterpret_cast<const uint4*>(W_inT + static_cast<int64_t>(j0 + b) * d + c0)));
-      }
-    }
-  }
-  if (active) {
-    uint32_t p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
-             (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
-    *reinterpret_cast<uint4*>(dX + static_cast<int64_t>(row) * d + c0) = make_uint4(p[0], p[1], p[2], p[3]);
-  }
 }
 
 // Pass 1 of the unit-major regrouping: per block of kBwdRowsPerBlock rows,
@@ -264,19 +214,24 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
 
-size_t bwd_workspace_layout(int N, int /*d_model*/, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
+size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
                             void* base) {
   const int nt = d_ff / T;
   const int64_t cells = static_cast<int64_t>(N) * nt * C;
   const int n_blocks = (N + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
+  const int ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off += align256(bytes);
     return o;
   };
+  const size_t fbf = static_cast<size_t>(fb_cap) * d_ff;
   const size_t o_dzc = take(sizeof(float) * cells);
-  const size_t o_dzf = take(sizeof(float) * static_cast<size_t>(fb_cap) * d_ff);
+  const size_t o_dzf = take(sizeof(float) * fbf);
+  const size_t o_hi = take(sizeof(uint16_t) * fbf);
+  const size_t o_lo = take(sizeof(uint16_t) * fbf);
+  const size_t o_part = take(sizeof(float) * 2 * ksplit * static_cast<size_t>(fb_cap) * d_model);
   const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
   const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
   const size_t o_rows = take(sizeof(int32_t) * cells);
@@ -286,6 +241,10 @@ size_t bwd_workspace_layout(int N, int /*d_model*/, int d_ff, int T, int C, int 
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
     ws->dz_fb = reinterpret_cast<float*>(b + o_dzf);
+    ws->dz_fb_hi = reinterpret_cast<uint16_t*>(b + o_hi);
+    ws->dz_fb_lo = reinterpret_cast<uint16_t*>(b + o_lo);
+    ws->part = reinterpret_cast<float*>(b + o_part);
+    ws->ksplit = ksplit;
     ws->blk_count = reinterpret_cast<int32_t*>(b + o_blk);
     ws->col_ptr = reinterpret_cast<int32_t*>(b + o_ptr);
     ws->col_rows = reinterpret_cast<int32_t*>(b + o_rows);
@@ -307,18 +266,28 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const Layout L = flat(Lh);
   const int f = Lh.d_ff;
   const int N = Lh.n_rows;
-  const int row_blocks = (N + kWarps - 1) / kWarps;
   const int col_blocks = (d + 255) / 256;
   if (N > 0) {
-    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile, Lh.tile,
-                       Lh.cap, f, lambda, ws.dz_cells, ws.dz_fb};
-    const int rc = launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s);
+    SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile, Lh.tile,
+                       Lh.cap,    f,        lambda,    ws.dz_cells, ws.dz_fb,  ws.dz_fb_hi, ws.dz_fb_lo};
+    int rc = launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s);
     if (rc != TWELL_OK) return rc;
-    {
-      LaunchScope ls(TWELL_KERNEL_DX, s);
-      dx_kernel<<<dim3(row_blocks, col_blocks), kWarps * 32, 0, s>>>(L, ws.dz_cells, ws.dz_fb, W_inT, d, dX);
+    // dX of TwELL rows (fallback rows get 0 here and are overwritten below)
+    rc = launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s);
+    if (rc != TWELL_OK) return rc;
+    if (Lh.fb_cap > 0) {
+      const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
+      PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
+      PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
+      rc = launch_gemm_partial_nmajor(ws.dz_fb_hi, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
+                                      TWELL_KERNEL_DX, s);
+      if (rc != TWELL_OK) return rc;
+      rc = launch_gemm_partial_nmajor(ws.dz_fb_lo, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
+                                      TWELL_KERNEL_DX, s);
+      if (rc != TWELL_OK) return rc;
+      rc = launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, s);
+      if (rc != TWELL_OK) return rc;
     }
-    TW_CHECK_LAUNCH();
   }
   const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
   static bool attr2[64] = {};

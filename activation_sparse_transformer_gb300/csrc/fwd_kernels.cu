@@ -8,8 +8,6 @@
 //                    tiles that overflowed were spilled densely by the
 //                    up-projection's epilogue, the others hold <= C entries;
 //                    the row's cells are then cleared
-//   spmm_kernel      Y = H . W_down over TwELL rows, reading only the W_down
-//                    rows named by the stored tile-local indices
 //   fb_reduce_kernel Y rows of the fallback rows: the K-split partial sums of
 //                    fb_dense . W_down (tensor cores) added in split order
 #include <cuda_runtime.h>
@@ -151,17 +149,6 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
-  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
-  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
-  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
-  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
-  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
-  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
-  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
-  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
-}
-
 __device__ __forceinline__ uint4 pack8_bf16(const float (&a)[8]) {
   uint32_t p[4];
 #pragma unroll
@@ -169,44 +156,6 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&a)[8]) {
     p[i] = static_cast<uint32_t>(float_to_bf16_bits(a[2 * i])) |
            (static_cast<uint32_t>(float_to_bf16_bits(a[2 * i + 1])) << 16);
   return make_uint4(p[0], p[1], p[2], p[3]);
-}
-
-constexpr int kSpmmWarps = 8;
-
-// Gather-SpMM over TwELL rows.  A warp owns one row and 256 output columns
-// (8 per lane, one 16-byte W_down load per lane per stored entry).  Cells are
-// visited tile by tile and slot by slot, so every output sums its terms in
-// ascending hidden-unit order.  Fallback rows are skipped here.
-__global__ void __launch_bounds__(kSpmmWarps * 32)
-    spmm_kernel(Layout L, const uint16_t* __restrict__ W, int d, uint16_t* __restrict__ Y) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kSpmmWarps + warp;
-  if (row >= L.N) return;
-  if (L.row_fb[row] >= 0) return;
-  const int c0 = blockIdx.y * 256 + lane * 8;
-  const bool active = c0 < d;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-  for (int t0 = 0; t0 < L.nt; t0 += 32) {
-    const int t = t0 + lane;
-    const int cnt = t < L.nt ? L.counts[cell0 + t] : 0;
-    unsigned mask = __ballot_sync(0xffffffffu, cnt > 0);
-    while (mask) {
-      const int b = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const int c = __shfl_sync(0xffffffffu, cnt, b);
-      const int64_t cell = cell0 + t0 + b;
-      for (int s = 0; s < c; ++s) {
-        const float v = bf16_bits_to_float(L.values[cell * L.C + s]);
-        const int j = (t0 + b) * L.T + L.idx[cell * L.C + s];
-        if (active) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(W + static_cast<int64_t>(j) * d + c0));
-          fma8(acc, v, w);
-        }
-      }
-    }
-  }
-  if (active) *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * d + c0) = pack8_bf16(acc);
 }
 
 // Y[fb_rows[r]] = bf16(sum over splits of part[ks][r]), splits in order.
@@ -246,14 +195,6 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* /
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
-  if (L.n_rows <= 0) return TWELL_OK;
-  dim3 grid((L.n_rows + kSpmmWarps - 1) / kSpmmWarps, (d_model + 255) / 256);
-  LaunchScope ls(TWELL_KERNEL_SPMM, s);
-  spmm_kernel<<<grid, kSpmmWarps * 32, 0, s>>>(flat(L), W_down, d_model, Y);
-  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
-}
-
 int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int ksplit,
                    cudaStream_t s) {
   if (L.fb_cap <= 0) return TWELL_OK;
@@ -261,9 +202,15 @@ int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16
   int rc = launch_gemm_partial_nmajor(L.fb_dense, W_down, L.fb_cap, L.n_fb, d_model, L.d_ff, ksplit, pp, L.status,
                                       TWELL_KERNEL_FB_DOWN, s);
   if (rc != TWELL_OK) return rc;
+  return launch_fb_reduce(L, part, ksplit, d_model, Y, TWELL_KERNEL_FB_DOWN, s);
+}
+
+int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_model, uint16_t* out, int kernel_id,
+                     cudaStream_t s) {
+  if (L.fb_cap <= 0) return TWELL_OK;
   const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
-  LaunchScope ls(TWELL_KERNEL_FB_DOWN, s);
-  fb_reduce_kernel<<<grid, 256, 0, s>>>(flat(L), part, ksplit, d_model, Y);
+  LaunchScope ls(kernel_id, s);
+  fb_reduce_kernel<<<grid, 256, 0, s>>>(flat(L), part, nsplit, d_model, out);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -299,7 +299,9 @@ struct SampleEpi {
         uint4 hq[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) hq[q] = hp[q];
-        float4* dst = reinterpret_cast<float4*>(p.dz_fb + static_cast<int64_t>(fb) * p.d_ff + col);
+        const int64_t off = static_cast<int64_t>(fb) * p.d_ff + col;
+        float4* dst = reinterpret_cast<float4*>(p.dz_fb + off);
+        uint32_t hi[16], lo[16];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float o[4];
@@ -308,8 +310,26 @@ struct SampleEpi {
             const int i = 4 * q + e;
             const float h = bias_at(hq, i);
             o[e] = h > 0.0f ? __uint_as_float(r[i]) + p.lambda : 0.0f;
+            // dz = hi + lo with both halves in bf16 (the fallback rows' dX runs
+            // on the tensor cores as two bf16 products)
+            const uint16_t hb = float_to_bf16_bits(o[e]);
+            const uint16_t lb = float_to_bf16_bits(o[e] - bf16_bits_to_float(hb));
+            if (i & 1) {
+              hi[i / 2] |= static_cast<uint32_t>(hb) << 16;
+              lo[i / 2] |= static_cast<uint32_t>(lb) << 16;
+            } else {
+              hi[i / 2] = hb;
+              lo[i / 2] = lb;
+            }
           }
           dst[q] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+        uint4* dh = reinterpret_cast<uint4*>(p.dz_fb_hi + off);
+        uint4* dl = reinterpret_cast<uint4*>(p.dz_fb_lo + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
       }
     }

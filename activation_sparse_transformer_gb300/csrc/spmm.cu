@@ -1,0 +1,158 @@
+// TwELL gather-SpMM:  out[n, :] = sum_t sum_{s < count[n,t]} v[n,t,s] * W[t*T + idx[n,t,s], :]
+//
+// The down-projection Y = H . W_down of the sparse layer reads only the W_down
+// rows named by the stored tile-local indices (repo-explainer, "TwELL: The
+// Packing Format That Fits the Machine": fused MLP execution from the packed
+// form); the backward's dX = dZ . W_in^T has the same shape with fp32 values.
+//
+// At ~1% density a W row is used by ~1% of the tokens, so staging W slabs for
+// a token block buys almost no reuse unless the block holds thousands of
+// tokens (far more accumulators than an SM has registers).  The kernel is
+// therefore built for memory-level parallelism instead: a warp owns one token
+// row and 256 output columns.  It first flattens the row's stored entries
+// (tile-major, slots ascending, so hidden units ascend) into its shared-memory
+// list -- counts of 32 tiles per round, a warp prefix sum, each lane
+// expanding its own cell -- then streams the named W rows with coalesced
+// 16-byte loads, kU independent loads in flight per lane, and accumulates in
+// fp32 registers.  Each output sums its terms in ascending hidden-unit order.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sm103.cuh"
+#include "twell_internal.h"
+
+namespace twell {
+namespace {
+
+constexpr int kWarps = 8;  // rows per CTA
+constexpr int kU = 4;      // W row loads in flight per lane
+
+struct SpmmArgs {
+  const void* values;     // [N][nt][C] VT
+  const uint8_t* idx;     // [N][nt][C]
+  const uint8_t* counts;  // [N][nt]
+  uint16_t* out;          // [N][d] bf16
+  int N, d, nt, T, C;
+  int32_t* status;
+};
+
+template <typename VT>
+__device__ __forceinline__ float as_f32(VT v);
+template <>
+__device__ __forceinline__ float as_f32<uint16_t>(uint16_t v) { return bf16_bits_to_float(v); }
+template <>
+__device__ __forceinline__ float as_f32<float>(float v) { return v; }
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
+  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
+  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
+  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
+  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
+  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
+  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
+  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
+  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
+}
+
+// max_entries = n_tiles * C bounds the entries a row can store.
+template <typename VT>
+__global__ void __launch_bounds__(kWarps * 32)
+    spmm_row_kernel(const SpmmArgs a, const uint16_t* __restrict__ W, int max_entries) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* lj = reinterpret_cast<int32_t*>(smem_raw) + warp * max_entries;
+  float* lv = reinterpret_cast<float*>(smem_raw) + kWarps * max_entries + warp * max_entries;
+  const int row = blockIdx.x * kWarps + warp;
+  if (row >= a.N) return;
+  const int c0 = blockIdx.y * 256 + lane * 8;
+  const bool active = c0 < a.d;
+  const VT* vals = static_cast<const VT*>(a.values);
+  const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+
+  // ---- flatten: tiles in order, 32 per round
+  int total = 0;
+  for (int t0 = 0; t0 < a.nt; t0 += 32) {
+    const int t = t0 + lane;
+    const int cnt = t < a.nt ? a.counts[cell0 + t] : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const int base = total + incl - cnt;
+    const int64_t cell = cell0 + t;
+    for (int s = 0; s < cnt; ++s) {
+      lj[base + s] = t * a.T + a.idx[cell * a.C + s];
+      lv[base + s] = as_f32<VT>(vals[cell * a.C + s]);
+    }
+    total += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+
+  // ---- stream the named W rows, kU loads in flight
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (active) {
+    const uint16_t* wcol = W + c0;
+    int e = 0;
+    for (; e + kU <= total; e += kU) {
+      uint4 w[kU];
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(lj[e + u]) * a.d));
+        v[u] = lv[e + u];
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) fma8(acc, v[u], w[u]);
+    }
+    for (; e < total; ++e)
+      fma8(acc, lv[e], __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(lj[e]) * a.d)));
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
+             (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = make_uint4(p[0], p[1], p[2], p[3]);
+  }
+}
+
+template <typename VT>
+int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaStream_t s) {
+  if (a.N <= 0) return TWELL_OK;
+  if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  const int max_entries = a.nt * a.C;
+  const size_t smem = static_cast<size_t>(kWarps) * max_entries * 8;
+  if (smem > 227 * 1024) return TWELL_ERR_UNSUPPORTED;
+  auto kern = spmm_row_kernel<VT>;
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+      return TWELL_ERR_CUDA;
+    attr[dev] = true;
+  }
+  dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256);
+  {
+    LaunchScope ls(kernel_id, s);
+    kern<<<grid, kWarps * 32, smem, s>>>(a, W, max_entries);
+  }
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
+  SpmmArgs a{L.values, L.idx, L.counts, Y, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
+  return launch_spmm_rows<uint16_t>(a, W_down, TWELL_KERNEL_SPMM, s);
+}
+
+int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
+                    int kernel_id, cudaStream_t s) {
+  SpmmArgs a{vals, L.idx, L.counts, out, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
+  return launch_spmm_rows<float>(a, W, kernel_id, s);
+}
+
+}  // namespace twell

@@ -30,8 +30,12 @@ class LaunchScope {
 
 int sm_count();                      // SMs of the current device (cached per device)
 bool device_is_sm103();              // current device is compute capability 10.3
+// bf16 2-D tensor maps: 128-byte swizzled (tensor-core operands) or plain
+// row-major boxes (shared-memory slabs read by CUDA cores).
 int encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+int encode_tmap_2d_plain(CUtensorMap* map, const void* base, uint64_t inner_elems, uint64_t rows,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
 // ---------------------------------------------------------------- kernels
 // A cell whose tile held more than C non-zeros during the fused
@@ -83,6 +87,8 @@ struct SampleEpiParams {
   float lambda;
   float* dz_cells;          // [M][n_tiles][C] fp32, stored slots only
   float* dz_fb;             // [fb_cap][d_ff] fp32, dense (0 where h == 0)
+  uint16_t* dz_fb_hi;       // [fb_cap][d_ff] bf16(dz_fb)
+  uint16_t* dz_fb_lo;       // [fb_cap][d_ff] bf16(dz_fb - hi): hi + lo carries dz to ~2^-17
 };
 
 // C[M, N] = A[M, K] . B^T with A row-major [M][K] (K-major).  B is row-major
@@ -104,6 +110,11 @@ int launch_route(const twell_t& L, cudaStream_t s);
 int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* spill_count, int32_t spill_cap,
                        cudaStream_t s);
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
+int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
+                    int kernel_id, cudaStream_t s);
+// out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
+int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_model, uint16_t* out, int kernel_id,
+                     cudaStream_t s);
 int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int ksplit,
                    cudaStream_t s);
 
@@ -114,8 +125,12 @@ int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 
 // backward (bwd_kernels.cu)
 struct BwdWorkspace {
-  float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries (0 in padding)
+  float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries
   float* dz_fb;           // [fb_cap][d_ff] fp32: dZ of the fallback rows (0 off the pattern)
+  uint16_t* dz_fb_hi;     // [fb_cap][d_ff] bf16 high part of dz_fb
+  uint16_t* dz_fb_lo;     // [fb_cap][d_ff] bf16 low part of dz_fb
+  float* part;            // [2 * ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
+  int32_t ksplit;
   int32_t* blk_count;     // [n_blocks][d_ff] entries per (row block, hidden unit), then offsets
   int32_t* col_ptr;       // [d_ff + 1] start of each hidden unit's entry list
   int32_t* col_rows;      // [capacity] row of each entry, grouped by unit, rows ascending
