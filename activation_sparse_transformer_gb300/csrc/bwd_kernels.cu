@@ -2,19 +2,21 @@
 // (L1 on the activations: bayesiansapien note, TL;DR; training kernels are
 // part of the release, "What it claims").
 //
-//   SDDMM           dZ[n][j] = dY[n] . W_down[j] + lambda, kept only at the
-//                   stored non-zeros of H (the ReLU mask is the pattern): a
-//                   tcgen05 GEMM dY . W_down^T whose epilogue samples the
-//                   accumulator at the TwELL pattern (gemm_tcgen05.cu)
-//   dX              dX[n] = sum_j dZ[n][j] W_in^T[j]: the gather-SpMM (spmm.cu)
-//                   with fp32 values for TwELL rows; for fallback rows a
-//                   split-K tcgen05 GEMM of dZ (as bf16 high + low parts)
-//                   with W_in^T read N-major, reduced in split order
-//   unit lists      the stored entries regrouped by hidden unit, rows
-//                   ascending, built deterministically (block histogram,
-//                   scans, ordered fill -- no atomics)
-//   dw_kernel       dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] =
-//                   sum_n dZ[n][j] X[n], db[j] = sum_n dZ[n][j]
+//   SDDMM     dZ[n][j] = dY[n] . W_down[j] + lambda, kept only at the stored
+//             non-zeros of H (the ReLU mask is the pattern): a tcgen05 GEMM
+//             dY . W_down^T whose epilogue samples the accumulator at the TwELL
+//             pattern (gemm_tcgen05.cu)
+//   dX        dX[n] = sum_j dZ[n][j] W_in^T[j]: the gather-SpMM (spmm.cu) with
+//             fp32 values for TwELL rows; for fallback rows a split-K tcgen05
+//             GEMM of dZ (as bf16 high + low parts) with W_in^T read N-major
+//   unit lists  the TwELL entries regrouped by hidden unit, rows ascending,
+//             built deterministically (block histograms, scans, ordered fill)
+//   dw_kernel dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] = sum_n dZ[n][j] X[n],
+//             db[j] = sum_n dZ[n][j] over the TwELL entries
+//   fallback  the dense fallback rows' share added by tcgen05 GEMMs with both
+//             operands M/N-major (H_fb^T . dY_fb and dZ_fb^T . X_fb, dZ as
+//             high + low bf16 parts) plus a column sum for db
+// No atomics on outputs, so every result is deterministic.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -42,12 +44,7 @@ Layout flat(const twell_t& L) {
 }
 
 constexpr int kWarps = 8;
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
+constexpr int kU = 4;  // rows in flight per lane in dw_kernel
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
   acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
@@ -61,38 +58,47 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
 }
 
 // Pass 1 of the unit-major regrouping: per block of kBwdRowsPerBlock rows,
-// the number of stored entries of every hidden unit.
-__global__ void unit_hist_kernel(Layout L, int32_t* __restrict__ blk_count) {
+// the number of stored entries of every hidden unit, written unit-major
+// (blk_count[j][b]) so that each unit's block counts are contiguous.
+__global__ void unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
   extern __shared__ int32_t hist[];
   for (int j = threadIdx.x; j < L.f; j += blockDim.x) hist[j] = 0;
   __syncthreads();
   const int r0 = blockIdx.x * kBwdRowsPerBlock;
   const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
-  for (int row = r0; row < r1; ++row) {
-    if (L.row_fb[row] >= 0) continue;  // uniform across the block
-    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-    for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
-      const int cnt = L.counts[cell0 + t];
-      for (int s = 0; s < cnt; ++s) atomicAdd(&hist[t * L.T + L.idx[(cell0 + t) * L.C + s]], 1);
-    }
+  for (int i = threadIdx.x; i < (r1 - r0) * L.nt; i += blockDim.x) {
+    const int64_t cell = static_cast<int64_t>(r0) * L.nt + i;
+    const int cnt = L.counts[cell];
+    const int t = i % L.nt;
+    for (int s = 0; s < cnt; ++s) atomicAdd(&hist[t * L.T + L.idx[cell * L.C + s]], 1);
   }
   __syncthreads();
-  int32_t* out = blk_count + static_cast<int64_t>(blockIdx.x) * L.f;
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x) out[j] = hist[j];
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x)
+    blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] = hist[j];
 }
 
-// Exclusive scan over row blocks for every unit (in place), totals to col_ptr[j].
-__global__ void unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f, int32_t* __restrict__ col_ptr) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+// Warp per unit: exclusive scan over its row blocks (in place); the total goes
+// to col_ptr[j].
+__global__ void unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f,
+                                       int32_t* __restrict__ col_ptr) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (blockDim.x >> 5) + warp;
   if (j >= f) return;
+  int32_t* p = blk_count + static_cast<int64_t>(j) * n_blocks;
   int run = 0;
-  for (int b = 0; b < n_blocks; ++b) {
-    int32_t* p = blk_count + static_cast<int64_t>(b) * f + j;
-    const int c = *p;
-    *p = run;
-    run += c;
+  for (int b0 = 0; b0 < n_blocks; b0 += 32) {
+    const int b = b0 + lane;
+    const int c = b < n_blocks ? p[b] : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (b < n_blocks) p[b] = run + incl - c;
+    run += __shfl_sync(0xffffffffu, incl, 31);
   }
-  col_ptr[j] = run;
+  if (lane == 0) col_ptr[j] = run;
 }
 
 // Exclusive scan of the per-unit totals: col_ptr[j] = start, col_ptr[f] = all.
@@ -133,19 +139,19 @@ __global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ c
   if (tid == 0) col_ptr[f] = base_s;
 }
 
-// Pass 2: rows of a block in ascending order; within one row every unit
+// Pass 2: the rows of a block in ascending order; within one row every unit
 // appears at most once, so the per-unit cursors need no atomics.
-__global__ void unit_fill_kernel(Layout L, const float* __restrict__ dz_cells, const int32_t* __restrict__ blk_count,
-                                 const int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_rows,
-                                 float* __restrict__ col_h, float* __restrict__ col_dz) {
+__global__ void unit_fill_kernel(Layout L, int n_blocks, const float* __restrict__ dz_cells,
+                                 const int32_t* __restrict__ blk_count, const int32_t* __restrict__ col_ptr,
+                                 int32_t* __restrict__ col_rows, float* __restrict__ col_h,
+                                 float* __restrict__ col_dz) {
   extern __shared__ int32_t cursor[];
-  const int32_t* off = blk_count + static_cast<int64_t>(blockIdx.x) * L.f;
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x) cursor[j] = col_ptr[j] + off[j];
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x)
+    cursor[j] = col_ptr[j] + blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x];
   __syncthreads();
   const int r0 = blockIdx.x * kBwdRowsPerBlock;
   const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
   for (int row = r0; row < r1; ++row) {
-    if (L.row_fb[row] >= 0) continue;
     const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
     for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
       const int64_t cell = cell0 + t;
@@ -162,41 +168,52 @@ __global__ void unit_fill_kernel(Layout L, const float* __restrict__ dz_cells, c
   }
 }
 
-// Warp per hidden unit j and 256 columns.  TwELL entries in ascending row,
-// then fallback rows in ascending slot.
+// Warp per hidden unit j and 256 columns: TwELL entries in ascending row,
+// kU rows of dY and X in flight per lane.
 __global__ void __launch_bounds__(kWarps * 32)
-    dw_kernel(Layout L, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
-              const float* __restrict__ col_h, const float* __restrict__ col_dz, const float* __restrict__ dz_fb,
-              const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT,
-              float* __restrict__ dW_down, float* __restrict__ db) {
+    dw_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
+              const float* __restrict__ col_h, const float* __restrict__ col_dz, const uint16_t* __restrict__ X,
+              const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT, float* __restrict__ dW_down,
+              float* __restrict__ db) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + warp;
-  if (j >= L.f) return;
+  if (j >= f) return;
   const int c0 = blockIdx.y * 256 + lane * 8;
   const bool active = c0 < d;
   float a_down[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float gb = 0.f;
-  const int e1 = col_ptr[j + 1];
-  for (int e = col_ptr[j]; e < e1; ++e) {
-    const int n = col_rows[e];
-    const float h = col_h[e], dz = col_dz[e];
-    gb += dz;
-    if (active) {
-      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(n) * d + c0)));
-      fma8(a_in, dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(n) * d + c0)));
+  const int e0 = col_ptr[j], e1 = col_ptr[j + 1];
+  int e = e0;
+  for (; e + kU <= e1; e += kU) {
+    uint4 g[kU], x[kU];
+    float h[kU], z[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t n = col_rows[e + u];
+      h[u] = col_h[e + u];
+      z[u] = col_dz[e + u];
+      if (active) {
+        g[u] = __ldg(reinterpret_cast<const uint4*>(dY + n * d + c0));
+        x[u] = __ldg(reinterpret_cast<const uint4*>(X + n * d + c0));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      gb += z[u];
+      if (active) {
+        fma8(a_down, h[u], g[u]);
+        fma8(a_in, z[u], x[u]);
+      }
     }
   }
-  const int nfb = min(*L.n_fb, L.fb_cap);
-  for (int slot = 0; slot < nfb; ++slot) {
-    const float h = bf16_bits_to_float(L.fb_dense[static_cast<int64_t>(slot) * L.f + j]);
-    if (h == 0.f) continue;
-    const int n = L.fb_rows[slot];
-    const float dz = dz_fb[static_cast<int64_t>(slot) * L.f + j];
-    gb += dz;
+  for (; e < e1; ++e) {
+    const int64_t n = col_rows[e];
+    const float h = col_h[e], z = col_dz[e];
+    gb += z;
     if (active) {
-      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(n) * d + c0)));
-      fma8(a_in, dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(n) * d + c0)));
+      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + n * d + c0)));
+      fma8(a_in, z, __ldg(reinterpret_cast<const uint4*>(X + n * d + c0)));
     }
   }
   if (active) {
@@ -210,6 +227,51 @@ __global__ void __launch_bounds__(kWarps * 32)
   if (blockIdx.y == 0 && lane == 0) db[j] = gb;
 }
 
+// Operands of the fallback rows' weight-gradient GEMMs, K = fallback slot:
+// hfb[s] = fb_dense[s], dyg[s] = dY[fb_rows[s]], xg[s] = X[fb_rows[s]] for
+// s < n_fb; rows n_fb .. (next multiple of 64) - 1 are zero in these and in
+// the dZ high / low parts, as the GEMM's device-side K requires.
+__global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
+                                   uint16_t* __restrict__ hfb, uint16_t* __restrict__ dyg, uint16_t* __restrict__ xg,
+                                   uint16_t* __restrict__ dz_hi, uint16_t* __restrict__ dz_lo, int fb_pad) {
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  const int kpad = min(fb_pad, (nfb + 63) & ~63);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int slot = blockIdx.x; slot < kpad; slot += gridDim.x) {
+    const bool real = slot < nfb;
+    const int row = real ? L.fb_rows[slot] : 0;
+    uint4* h = reinterpret_cast<uint4*>(hfb + static_cast<int64_t>(slot) * L.f);
+    const uint4* hs = reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(real ? slot : 0) * L.f);
+    for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) h[i] = real ? hs[i] : z;
+    if (!real) {
+      uint4* a = reinterpret_cast<uint4*>(dz_hi + static_cast<int64_t>(slot) * L.f);
+      uint4* b = reinterpret_cast<uint4*>(dz_lo + static_cast<int64_t>(slot) * L.f);
+      for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) {
+        a[i] = z;
+        b[i] = z;
+      }
+    }
+    uint4* g = reinterpret_cast<uint4*>(dyg + static_cast<int64_t>(slot) * d);
+    uint4* x = reinterpret_cast<uint4*>(xg + static_cast<int64_t>(slot) * d);
+    const uint4* gs = reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(row) * d);
+    const uint4* xs = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+      g[i] = real ? gs[i] : z;
+      x[i] = real ? xs[i] : z;
+    }
+  }
+}
+
+// db[j] += sum over fallback slots (ascending) of dZ_fb[slot][j].
+__global__ void fb_db_kernel(Layout L, const float* __restrict__ dz_fb, float* __restrict__ db) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= L.f) return;
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  float s = 0.f;
+  for (int slot = 0; slot < nfb; ++slot) s += dz_fb[static_cast<int64_t>(slot) * L.f + j];
+  db[j] += s;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -220,17 +282,22 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const int64_t cells = static_cast<int64_t>(N) * nt * C;
   const int n_blocks = (N + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
   const int ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
+  const int fb_pad = (fb_cap + 63) & ~63;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
     off += align256(bytes);
     return o;
   };
-  const size_t fbf = static_cast<size_t>(fb_cap) * d_ff;
+  const size_t padf = static_cast<size_t>(fb_pad) * d_ff;
+  const size_t padd = static_cast<size_t>(fb_pad) * d_model;
   const size_t o_dzc = take(sizeof(float) * cells);
-  const size_t o_dzf = take(sizeof(float) * fbf);
-  const size_t o_hi = take(sizeof(uint16_t) * fbf);
-  const size_t o_lo = take(sizeof(uint16_t) * fbf);
+  const size_t o_dzf = take(sizeof(float) * static_cast<size_t>(fb_cap) * d_ff);
+  const size_t o_hi = take(sizeof(uint16_t) * padf);
+  const size_t o_lo = take(sizeof(uint16_t) * padf);
+  const size_t o_hfb = take(sizeof(uint16_t) * padf);
+  const size_t o_dyg = take(sizeof(uint16_t) * padd);
+  const size_t o_xg = take(sizeof(uint16_t) * padd);
   const size_t o_part = take(sizeof(float) * 2 * ksplit * static_cast<size_t>(fb_cap) * d_model);
   const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
   const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
@@ -243,6 +310,10 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->dz_fb = reinterpret_cast<float*>(b + o_dzf);
     ws->dz_fb_hi = reinterpret_cast<uint16_t*>(b + o_hi);
     ws->dz_fb_lo = reinterpret_cast<uint16_t*>(b + o_lo);
+    ws->hfb = reinterpret_cast<uint16_t*>(b + o_hfb);
+    ws->dyg = reinterpret_cast<uint16_t*>(b + o_dyg);
+    ws->xg = reinterpret_cast<uint16_t*>(b + o_xg);
+    ws->fb_pad = fb_pad;
     ws->part = reinterpret_cast<float*>(b + o_part);
     ws->ksplit = ksplit;
     ws->blk_count = reinterpret_cast<int32_t*>(b + o_blk);
@@ -259,6 +330,11 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   do {                                                            \
     if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA; \
   } while (0)
+#define TW_TRY_RC(expr)              \
+  do {                               \
+    const int rc_ = (expr);          \
+    if (rc_ != TWELL_OK) return rc_; \
+  } while (0)
 
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& Lh,
                const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
@@ -268,45 +344,42 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const int N = Lh.n_rows;
   const int col_blocks = (d + 255) / 256;
   if (N > 0) {
-    SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile, Lh.tile,
-                       Lh.cap,    f,        lambda,    ws.dz_cells, ws.dz_fb,  ws.dz_fb_hi, ws.dz_fb_lo};
-    int rc = launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s);
-    if (rc != TWELL_OK) return rc;
+    // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
+    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts,   Lh.row_fb, Lh.fb_dense,  Lh.fb_cap,  f / Lh.tile, Lh.tile,
+                       Lh.cap,    f,      lambda,      ws.dz_cells, ws.dz_fb,   ws.dz_fb_hi, ws.dz_fb_lo};
+    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
     // dX of TwELL rows (fallback rows get 0 here and are overwritten below)
-    rc = launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s);
-    if (rc != TWELL_OK) return rc;
+    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s));
     if (Lh.fb_cap > 0) {
       const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
       PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
-      rc = launch_gemm_partial_nmajor(ws.dz_fb_hi, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
-                                      TWELL_KERNEL_DX, s);
-      if (rc != TWELL_OK) return rc;
-      rc = launch_gemm_partial_nmajor(ws.dz_fb_lo, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
-                                      TWELL_KERNEL_DX, s);
-      if (rc != TWELL_OK) return rc;
-      rc = launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, s);
-      if (rc != TWELL_OK) return rc;
+      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_hi, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
+                                           TWELL_KERNEL_DX, s));
+      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_lo, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
+                                           TWELL_KERNEL_DX, s));
+      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, s));
     }
   }
+  // ---- weight gradients: TwELL entries regrouped by hidden unit
   const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
-  static bool attr2[64] = {};
+  static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr2[dev]) {
+  if (dev < 64 && !attr[dev]) {
     if (cudaFuncSetAttribute(unit_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
         cudaFuncSetAttribute(unit_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return TWELL_ERR_CUDA;
-    attr2[dev] = true;
+    attr[dev] = true;
   }
   if (ws.n_blocks > 0) {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_hist_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.blk_count);
+    unit_hist_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.n_blocks, ws.blk_count);
   }
   TW_CHECK_LAUNCH();
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_block_scan_kernel<<<(f + 255) / 256, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
+    unit_block_scan_kernel<<<(f + 7) / 8, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
   }
   TW_CHECK_LAUNCH();
   {
@@ -316,16 +389,36 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   if (ws.n_blocks > 0) {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_fill_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.dz_cells, ws.blk_count, ws.col_ptr, ws.col_rows, ws.col_h,
-                                                    ws.col_dz);
+    unit_fill_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.n_blocks, ws.dz_cells, ws.blk_count, ws.col_ptr,
+                                                    ws.col_rows, ws.col_h, ws.col_dz);
   }
   TW_CHECK_LAUNCH();
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
     dw_kernel<<<dim3((f + kWarps - 1) / kWarps, col_blocks), kWarps * 32, 0, s>>>(
-        L, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, ws.dz_fb, X, dY, d, dW_inT, dW_down, db);
+        f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d, dW_inT, dW_down, db);
   }
   TW_CHECK_LAUNCH();
+  // ---- the fallback rows' share, on the tensor cores
+  if (Lh.fb_cap > 0 && N > 0) {
+    {
+      const int grid = std::max(1, std::min(ws.fb_pad, 2 * sm_count()));
+      LaunchScope ls(TWELL_KERNEL_DW, s);
+      fb_operands_kernel<<<grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg, ws.dz_fb_hi, ws.dz_fb_lo,
+                                               ws.fb_pad);
+    }
+    TW_CHECK_LAUNCH();
+    AddEpiParams down{dW_down, d};
+    AddEpiParams in{dW_inT, d};
+    TW_TRY_RC(launch_gemm_add_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, down, Lh.status, TWELL_KERNEL_DW, s));
+    TW_TRY_RC(launch_gemm_add_mn(ws.dz_fb_hi, ws.xg, f, d, ws.fb_pad, Lh.n_fb, in, Lh.status, TWELL_KERNEL_DW, s));
+    TW_TRY_RC(launch_gemm_add_mn(ws.dz_fb_lo, ws.xg, f, d, ws.fb_pad, Lh.n_fb, in, Lh.status, TWELL_KERNEL_DW, s));
+    {
+      LaunchScope ls(TWELL_KERNEL_DW, s);
+      fb_db_kernel<<<(f + 255) / 256, 256, 0, s>>>(L, ws.dz_fb, db);
+    }
+    TW_CHECK_LAUNCH();
+  }
   return TWELL_OK;
 }
 

@@ -54,6 +54,8 @@ struct GemmArgs {
   int N;
   int K;
   int ksplit;            // K ranges per output tile (partial sums when > 1)
+  const int32_t* K_dev;  // optional device-side K (clamped to K); operand rows/cols up to the next
+                         // multiple of 64 past it must be zero
   int32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -262,6 +264,38 @@ struct PartialEpi {
   }
 };
 
+// out[row][col] += acc (fp32): contributions added onto a result another
+// kernel wrote first (the fallback rows' share of the weight gradients).
+struct AddEpi {
+  using Params = AddEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
+                                               uint8_t*, int) {
+    const bool valid = row < M;
+    float* base = p.out + static_cast<int64_t>(row) * p.ld + col0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      if (valid) {
+        float4* dst = reinterpret_cast<float4*>(base + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 o = dst[q];
+          o.x += __uint_as_float(r[4 * q]);
+          o.y += __uint_as_float(r[4 * q + 1]);
+          o.z += __uint_as_float(r[4 * q + 2]);
+          o.w += __uint_as_float(r[4 * q + 3]);
+          dst[q] = o;
+        }
+      }
+    }
+  }
+};
+
 struct SampleEpi {
   using Params = SampleEpiParams;
   static constexpr uint32_t kSmemBytes = 0;
@@ -337,7 +371,7 @@ struct SampleEpi {
 };
 
 // ------------------------------------------------------------ kernel
-template <int BN, class Epi, bool kBNMajor>
+template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args, const typename Epi::Params ep) {
@@ -364,8 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (args.M_dev) M = min(M, max(0, *args.M_dev));
   const int num_m = (M + kBM - 1) / kBM;
   const int num_n = args.N / BN;
-  const int num_units = num_m * num_n * args.ksplit;
-  const int num_k = (args.K + kBK - 1) / kBK;
+  const int K = args.K_dev ? min(args.K, max(0, *args.K_dev)) : args.K;
+  const int num_k = (K + kBK - 1) / kBK;
+  const int num_units = num_k > 0 ? num_m * num_n * args.ksplit : 0;
   const int k_per = (num_k + args.ksplit - 1) / args.ksplit;
 
   if (threadIdx.x == 0) {
@@ -409,7 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], Cfg::kABytes + Cfg::kBBytes);
-          tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kBK, m_blk * kBM);
+          if (kANMajor) {
+            // A is [K][M]: two boxes of 64 M-columns x 64 K-rows, 8 KB apart
+            tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], m_blk * kBM, kb * kBK);
+            tma_load_2d(sA + stage * Cfg::kABytes + 8192, &tmA, &full[stage], m_blk * kBM + 64, kb * kBK);
+          } else {
+            tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kBK, m_blk * kBM);
+          }
           if (kBNMajor) {
             // B is [K][N]: BN/64 boxes of 64 N-columns x 64 K-rows, 8 KB apart
 #pragma unroll
@@ -439,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && num_units > 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN) | (kBNMajor ? (1u << 16) : 0u);
+      constexpr uint32_t idesc =
+          idesc_bf16_f32(kBM, BN) | (kANMajor ? (1u << 15) : 0u) | (kBNMajor ? (1u << 16) : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -460,14 +502,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * Cfg::kABytes));
+          const uint64_t adesc = kANMajor ? smem_desc_sw128_nmajor(smem_u32(sA + stage * Cfg::kABytes), 8192)
+                                          : smem_desc_sw128(smem_u32(sA + stage * Cfg::kABytes));
           const uint64_t bdesc = kBNMajor ? smem_desc_sw128_nmajor(smem_u32(sB + stage * Cfg::kBBytes), 8192)
                                           : smem_desc_sw128(smem_u32(sB + stage * Cfg::kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // K step of 16: +32 B along a K-major row, or +16 rows (2 KB) of an N-major tile
+            const uint64_t a_step = kANMajor ? 128u * k : 2u * k;
             const uint64_t b_step = kBNMajor ? 128u * k : 2u * k;
-            mma_bf16(d_tmem, adesc + 2u * k, bdesc + b_step, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            mma_bf16(d_tmem, adesc + a_step, bdesc + b_step, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
           if (++stage == S) {
@@ -519,9 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, class Epi, bool kBNMajor>
+template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
-                const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s) {
+                const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
+                const int32_t* K_dev = nullptr) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
@@ -529,8 +574,13 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   const int k_per = (num_k + ksplit - 1) / ksplit;
   if (k_per * (ksplit - 1) >= num_k) return TWELL_ERR_UNSUPPORTED;  // every split must own a K block
   CUtensorMap ta, tb;
-  int rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2,
-                          kBK, kBM);
+  int rc;
+  if (kANMajor)
+    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), static_cast<uint64_t>(M) * 2, 64,
+                        kBK);
+  else
+    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kBK,
+                        kBM);
   if (rc) return rc;
   if (kBNMajor)
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
@@ -540,7 +590,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
                         BN);
   if (rc) return rc;
   const uint32_t smem = 1024 + Cfg::kPipeBytes + Cfg::kBarBytes + Epi::kSmemBytes;
-  auto kern = tc_gemm_kernel<BN, Epi, kBNMajor>;
+  auto kern = tc_gemm_kernel<BN, Epi, kANMajor, kBNMajor>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -551,7 +601,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   }
   const int units = ((M + kBM - 1) / kBM) * (N / BN) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
-  GemmArgs args{M, M_dev, N, K, ksplit, status, kWaitLimitNs};
+  GemmArgs args{M, M_dev, N, K, ksplit, K_dev, status, kWaitLimitNs};
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kThreads, smem, s>>>(ta, tb, args, p);
@@ -565,21 +615,21 @@ int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, int N, int K, 
                      int32_t* status, cudaStream_t s) {
   if (p.cap > PackEpi::kMaxCap) return TWELL_ERR_UNSUPPORTED;
   if (N % 256 == 0)
-    return launch_gemm<256, PackEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
+    return launch_gemm<256, PackEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
   if (N % 128 == 0 && p.tile <= 128)
-    return launch_gemm<128, PackEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
+    return launch_gemm<128, PackEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s);
   return TWELL_ERR_UNSUPPORTED;
 }
 
 int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int M, const int32_t* M_dev, int N,
                       int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
   if (b_n_major) {
-    if (N % 256 == 0) return launch_gemm<256, DenseEpi, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
-    if (N % 128 == 0) return launch_gemm<128, DenseEpi, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+    if (N % 256 == 0) return launch_gemm<256, DenseEpi, false, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+    if (N % 128 == 0) return launch_gemm<128, DenseEpi, false, true>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
     return TWELL_ERR_UNSUPPORTED;
   }
-  if (N % 256 == 0) return launch_gemm<256, DenseEpi, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
-  if (N % 128 == 0) return launch_gemm<128, DenseEpi, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+  if (N % 256 == 0) return launch_gemm<256, DenseEpi, false, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
+  if (N % 128 == 0) return launch_gemm<128, DenseEpi, false, false>(A, B, M, M_dev, N, K, 1, p, status, kernel_id, s);
   return TWELL_ERR_UNSUPPORTED;
 }
 
@@ -598,15 +648,25 @@ int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, cons
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
                                cudaStream_t s) {
   if (N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
-  return launch_gemm<128, PartialEpi, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s);
+  return launch_gemm<128, PartialEpi, false, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s);
+}
+
+int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev,
+                       const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
+  if (M % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (N % 256 == 0)
+    return launch_gemm<256, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev);
+  if (N % 128 == 0)
+    return launch_gemm<128, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev);
+  return TWELL_ERR_UNSUPPORTED;
 }
 
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s) {
   if (N % 256 == 0)
-    return launch_gemm<256, SampleEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
+    return launch_gemm<256, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
   if (N % 128 == 0)
-    return launch_gemm<128, SampleEpi, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
+    return launch_gemm<128, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
   return TWELL_ERR_UNSUPPORTED;
 }
 

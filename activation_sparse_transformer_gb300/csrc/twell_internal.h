@@ -74,6 +74,12 @@ struct PartialEpiParams {
   int64_t split_stride;
 };
 
+// out[row][col] += acc, fp32 (row-major, leading dimension ld)
+struct AddEpiParams {
+  float* out;
+  int64_t ld;
+};
+
 // dH = dY . W_down^T sampled at the TwELL pattern (the ReLU mask), plus the
 // L1 gradient: dZ = dH + lambda where h > 0.
 struct SampleEpiParams {
@@ -103,6 +109,11 @@ int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, cons
                                cudaStream_t s);
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s);
+// out[M][N] += A^T . B with A row-major [K][M] and B row-major [K][N] (both
+// M/N-major); only the first *K_dev rows of K count, and rows up to the next
+// multiple of 64 past *K_dev must be zero in both operands.
+int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev,
+                       const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 int choose_fb_ksplit(int K);   // K splits used for the fallback rows' down-projection
 
 // forward helpers (fwd_kernels.cu)
@@ -127,8 +138,12 @@ int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 struct BwdWorkspace {
   float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries
   float* dz_fb;           // [fb_cap][d_ff] fp32: dZ of the fallback rows (0 off the pattern)
-  uint16_t* dz_fb_hi;     // [fb_cap][d_ff] bf16 high part of dz_fb
-  uint16_t* dz_fb_lo;     // [fb_cap][d_ff] bf16 low part of dz_fb
+  uint16_t* dz_fb_hi;     // [fb_pad][d_ff] bf16 high part of dz_fb (zero past n_fb)
+  uint16_t* dz_fb_lo;     // [fb_pad][d_ff] bf16 low part of dz_fb (zero past n_fb)
+  uint16_t* hfb;          // [fb_pad][d_ff] fallback rows of H (zero past n_fb)
+  uint16_t* dyg;          // [fb_pad][d_model] dY of the fallback rows (zero past n_fb)
+  uint16_t* xg;           // [fb_pad][d_model] X of the fallback rows (zero past n_fb)
+  int32_t fb_pad;         // fb_cap rounded up to 64
   float* part;            // [2 * ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
   int32_t ksplit;
   int32_t* blk_count;     // [n_blocks][d_ff] entries per (row block, hidden unit), then offsets
