@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libtwell.so")
 
 TWELL_OK = 0
 KERNELS = {
-    "up_pack": 0, "route": 1, "fb_gather": 2, "fb_up": 3, "spmm": 4, "fb_down": 5, "pack": 6,
+    "up_pack": 0, "route": 1, "fb_assemble": 2, "spmm": 4, "fb_down": 5, "pack": 6,
     "unpack": 7, "sddmm": 8, "dx": 9, "dw": 10, "dense_gemm": 11, "aux": 12,
 }
 EXPORTED = [

@@ -56,6 +56,51 @@ LaunchScope::~LaunchScope() {
   g_pending.push_back(Pending{kernel_, start_, stop});
 }
 
+// ---------------------------------------------------------------- aux stream
+namespace {
+struct AuxState {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+AuxState g_aux[64];
+std::mutex g_aux_mu;
+}  // namespace
+
+AuxFork::AuxFork(cudaStream_t s) : s_(s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    rc_ = TWELL_ERR_CUDA;
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_aux_mu);
+  AuxState& a = g_aux[dev];
+  if (!a.stream) {
+    if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+      rc_ = TWELL_ERR_CUDA;
+      return;
+    }
+  }
+  aux_ = a.stream;
+  if (cudaEventRecord(a.fork, s_) != cudaSuccess || cudaStreamWaitEvent(aux_, a.fork, 0) != cudaSuccess)
+    rc_ = TWELL_ERR_CUDA;
+}
+
+int AuxFork::join() {
+  if (joined_ || rc_ != 0) return rc_;
+  joined_ = true;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_aux_mu);
+  AuxState& a = g_aux[dev];
+  if (cudaEventRecord(a.join, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, a.join, 0) != cudaSuccess)
+    rc_ = TWELL_ERR_CUDA;
+  return rc_;
+}
+
+AuxFork::~AuxFork() { join(); }
+
 // ---------------------------------------------------------------- device facts
 int sm_count() {
   static int cached[64] = {};
@@ -256,9 +301,16 @@ int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, c
                    d_ff / H->tile, H->tile, H->cap};
   TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
   TW_TRY(launch_route(*H, s));
-  TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, s));
-  TW_TRY(launch_spmm(*H, W_down, d_model, Y, s));
-  TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, s));
+  {
+    // the dense-fallback rows (assembly + tensor-core down-projection) run on
+    // a second stream while the gather-SpMM handles the TwELL rows
+    AuxFork fork(s);
+    TW_TRY(fork.status());
+    TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
+    TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
+    TW_TRY(launch_spmm(*H, W_down, d_model, Y, s));
+    TW_TRY(fork.join());
+  }
   return TWELL_OK;
 }
 

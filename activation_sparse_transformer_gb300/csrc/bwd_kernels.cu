@@ -348,18 +348,22 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts,   Lh.row_fb, Lh.fb_dense,  Lh.fb_cap,  f / Lh.tile, Lh.tile,
                        Lh.cap,    f,      lambda,      ws.dz_cells, ws.dz_fb,   ws.dz_fb_hi, ws.dz_fb_lo};
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
-    // dX of TwELL rows (fallback rows get 0 here and are overwritten below)
-    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s));
+    // dX: TwELL rows by the gather-SpMM, fallback rows on a second stream
+    AuxFork fork(s);
+    TW_TRY_RC(fork.status());
     if (Lh.fb_cap > 0) {
+      cudaStream_t a = fork.aux();
       const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
       PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
       TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_hi, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
-                                           TWELL_KERNEL_DX, s));
+                                           TWELL_KERNEL_DX, a));
       TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_lo, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
-                                           TWELL_KERNEL_DX, s));
-      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, s));
+                                           TWELL_KERNEL_DX, a));
+      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
     }
+    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s));
+    TW_TRY_RC(fork.join());
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit
   const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);

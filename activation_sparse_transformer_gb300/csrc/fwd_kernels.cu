@@ -190,7 +190,7 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* /
                        int32_t spill_cap, cudaStream_t s) {
   if (L.fb_cap <= 0) return TWELL_OK;
   const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
-  LaunchScope ls(TWELL_KERNEL_FB_GATHER, s);
+  LaunchScope ls(TWELL_KERNEL_FB_ASSEMBLE, s);
   fb_assemble_kernel<<<grid, 256, 0, s>>>(flat(L), spill, spill_cap);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

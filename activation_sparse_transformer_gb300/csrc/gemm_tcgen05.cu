@@ -19,10 +19,12 @@
 // row-major [N][K] (K-major) or row-major [K][N] (N-major, e.g. W_down read as
 // the B operand of H . W_down).  CTA tile 128 x BN, K step 64, one CTA per SM,
 // work units (m, n, k-split) strided over CTAs.  Warp roles: 0 = TMA
-// producer, 1 = MMA issuer, 2 = TMEM owner, 4..7 = epilogue (warp 4+i reads
-// TMEM lanes 32i..32i+31, i.e. tile rows 32i..).  Accumulators are
-// double-buffered in TMEM so one tile's epilogue runs under the next tile's
-// MMAs.  Every pipeline wait is bounded and reports TWELL_ERR_WAIT_TIMEOUT.
+// producer, 1 = MMA issuer, 2 = TMEM owner, 4..11 = epilogue: warps 4+i and
+// 8+i read TMEM lanes 32i..32i+31 (tile rows 32i..), the first taking the
+// tile's left half of the columns and the second the right half.
+// Accumulators are double-buffered in TMEM so one tile's epilogue runs under
+// the next tile's MMAs.  Every pipeline wait is bounded and reports
+// TWELL_ERR_WAIT_TIMEOUT.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,7 +38,8 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // 4 role warps + 8 epilogue warps
+constexpr int kEpiThreads = 256;
 
 template <int BN>
 struct GemmCfg {
@@ -83,7 +86,12 @@ __device__ __forceinline__ float bias_at(const uint4 (&bq)[4], int i) {
 struct PackEpi {
   using Params = PackEpiParams;
   static constexpr int kMaxCap = 32;
-  static constexpr uint32_t kSmemBytes = 128 * kMaxCap * 3;  // per thread: C values (u16) + C indices (u8)
+  static constexpr uint32_t kSmemBytes = kEpiThreads * kMaxCap * 3;  // per thread: C values (u16) + C indices (u8)
+
+  // A positive z rounds (to nearest, ties to even) to a non-zero bf16 exactly
+  // when z > 2^-134: half of the smallest bf16 subnormal, itself a tie that
+  // rounds to the even neighbour 0.  So one compare decides "non-zero".
+  static __device__ __forceinline__ float nonzero_threshold() { return __uint_as_float(0x00008000u); }
 
   // h of 32 columns [col, col + 32) of this thread's row, from TMEM.
   static __device__ __forceinline__ void load_h32(const Params& p, uint32_t taddr, int col, uint32_t (&r)[32],
@@ -95,21 +103,30 @@ struct PackEpi {
     tmem_ld_wait();
   }
 
-  // One thread = one accumulator row; processes columns [col0, col0 + BN).
+  // One thread = one accumulator row; this warp handles whole T-column tiles:
+  // the left or right half of the CTA tile, or all of it (second warp idle)
+  // when one T-tile is wider than half.
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
-                                               uint8_t* smem, int et) {
-    uint16_t* sv = reinterpret_cast<uint16_t*>(smem) + et * kMaxCap;
-    uint8_t* si = smem + 128 * kMaxCap * 2 + et * kMaxCap;
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int, uint8_t* smem, int et) {
     const int T = p.tile, C = p.cap;
+    int cb = half * (BN / 2), ce = cb + BN / 2;
+    if (T > BN / 2) {
+      if (half) return;
+      cb = 0;
+      ce = BN;
+    }
+    uint16_t* sv = reinterpret_cast<uint16_t*>(smem) + et * kMaxCap;
+    uint8_t* si = smem + kEpiThreads * kMaxCap * 2 + et * kMaxCap;
     const bool valid = row < M;
+    const float thr = nonzero_threshold();
     int cnt = 0;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = cb; c < ce; c += 32) {
       uint32_t r[32];
       uint4 bq[4];
-      load_h32(p, taddr + c * 32, col0 + c * 32, r, bq);
-      const int j0 = (c * 32) % T;
+      load_h32(p, taddr + c, col0 + c, r, bq);
+      const int j0 = c % T;
       if (j0 == 0) {
         cnt = 0;
         const uint4 z = make_uint4(0, 0, 0, 0);
@@ -118,23 +135,28 @@ struct PackEpi {
 #pragma unroll
         for (int q = 0; q < kMaxCap / 16; ++q) reinterpret_cast<uint4*>(si)[q] = z;
       }
+      uint32_t mask = 0;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float z = __uint_as_float(r[i]) + bias_at(bq, i);
-        if (z > 0.0f) {
-          const uint16_t h = float_to_bf16_bits(z);
-          if (h != 0) {
-            if (cnt < C) {
-              sv[cnt] = h;
-              si[cnt] = static_cast<uint8_t>(j0 + i);
-            }
-            ++cnt;
-          }
-        }
+        r[i] = __float_as_uint(z);
+        mask |= (z > thr ? 1u : 0u) << i;
       }
-      if (((c + 1) * 32) % T != 0) continue;
+      const int k = __popc(mask);
+      if (cnt + k <= C) {
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1;
+          sv[cnt] = float_to_bf16_bits(__uint_as_float(pick32(r, i)));
+          si[cnt] = static_cast<uint8_t>(j0 + i);
+          ++cnt;
+        }
+      } else {
+        cnt += k;  // the tile overflows: its entries are spilled below instead
+      }
+      if ((c + 32) % T != 0) continue;
       // ---- the T-column tile [tile_c0, tile_c0 + T) is complete
-      const int tile_c0 = (c + 1) * 32 - T;
+      const int tile_c0 = c + 32 - T;
       const int t = (col0 + tile_c0) / T;
       const int64_t cell = static_cast<int64_t>(row) * p.n_tiles + t;
       const bool ovf = valid && cnt > C;
@@ -200,11 +222,12 @@ struct DenseEpi {
   static constexpr uint32_t kSmemBytes = 0;
 
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
-                                               uint8_t*, int) {
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int ks, uint8_t*, int) {
+    (void)ks;
     const bool valid = row < M;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       uint4 bq[4] = {};
@@ -244,12 +267,12 @@ struct PartialEpi {
   static constexpr uint32_t kSmemBytes = 0;
 
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int ks,
-                                               uint8_t*, int) {
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int ks, uint8_t*, int) {
     const bool valid = row < M;
     float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + static_cast<int64_t>(row) * p.ld + col0;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
@@ -271,12 +294,13 @@ struct AddEpi {
   static constexpr uint32_t kSmemBytes = 0;
 
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
-                                               uint8_t*, int) {
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int ks, uint8_t*, int) {
+    (void)ks;
     const bool valid = row < M;
     float* base = p.out + static_cast<int64_t>(row) * p.ld + col0;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
@@ -301,13 +325,14 @@ struct SampleEpi {
   static constexpr uint32_t kSmemBytes = 0;
 
   template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int,
-                                               uint8_t*, int) {
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int ks, uint8_t*, int) {
+    (void)ks;
     const bool valid = row < M;
     const int fb = valid ? p.row_fb[row] : -1;
     const int T = p.tile, C = p.cap;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
@@ -411,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], kEpiThreads);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -534,7 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue
-    const int lg = warp & 3;
+    const int lg = warp & 3;              // TMEM lane quarter
+    const int half = (warp - 4) >> 2;     // column half of the tile
     const int et = threadIdx.x - 128;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -548,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row = m_blk * kBM + lg * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::template apply<BN>(ep, taddr, row, M, n_blk * BN, ks, epi_smem, et);
+      Epi::template apply<BN>(ep, taddr, row, M, n_blk * BN, half, ks, epi_smem, et);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;

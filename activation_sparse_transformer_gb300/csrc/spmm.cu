@@ -15,6 +15,8 @@
 // expanding its own cell -- then streams the named W rows with coalesced
 // 16-byte loads, kU independent loads in flight per lane, and accumulates in
 // fp32 registers.  Each output sums its terms in ascending hidden-unit order.
+// Fallback rows are skipped: their rows of the output belong to the dense
+// fallback path, which may run at the same time on another stream.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,6 +34,7 @@ struct SpmmArgs {
   const void* values;     // [N][nt][C] VT
   const uint8_t* idx;     // [N][nt][C]
   const uint8_t* counts;  // [N][nt]
+  const int32_t* row_fb;  // [N]: rows >= 0 are fallback rows, left to the fallback path
   uint16_t* out;          // [N][d] bf16
   int N, d, nt, T, C;
   int32_t* status;
@@ -65,6 +68,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   float* lv = reinterpret_cast<float*>(smem_raw) + kWarps * max_entries + warp * max_entries;
   const int row = blockIdx.x * kWarps + warp;
   if (row >= a.N) return;
+  if (a.row_fb[row] >= 0) return;  // written by the fallback path, which may run concurrently
   const int c0 = blockIdx.y * 256 + lane * 8;
   const bool active = c0 < a.d;
   const VT* vals = static_cast<const VT*>(a.values);
@@ -145,13 +149,13 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaSt
 }  // namespace
 
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
-  SpmmArgs a{L.values, L.idx, L.counts, Y, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
+  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
   return launch_spmm_rows<uint16_t>(a, W_down, TWELL_KERNEL_SPMM, s);
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s) {
-  SpmmArgs a{vals, L.idx, L.counts, out, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
+  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
   return launch_spmm_rows<float>(a, W, kernel_id, s);
 }
 

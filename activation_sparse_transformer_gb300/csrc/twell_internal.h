@@ -29,6 +29,24 @@ class LaunchScope {
 };
 
 int sm_count();                      // SMs of the current device (cached per device)
+
+// A second stream per device for work that can overlap the caller's stream
+// (the dense-fallback path).  fork(): aux waits for everything queued on s so
+// far; join(): s waits for everything queued on aux.  Both are asynchronous.
+class AuxFork {
+ public:
+  explicit AuxFork(cudaStream_t s);
+  ~AuxFork();
+  int status() const { return rc_; }
+  cudaStream_t aux() const { return aux_; }
+  int join();
+
+ private:
+  cudaStream_t s_;
+  cudaStream_t aux_ = nullptr;
+  int rc_ = 0;
+  bool joined_ = false;
+};
 bool device_is_sm103();              // current device is compute capability 10.3
 // bf16 2-D tensor maps: 128-byte swizzled (tensor-core operands) or plain
 // row-major boxes (shared-memory slabs read by CUDA cores).

@@ -203,8 +203,8 @@ TWELL_API int64_t twell_launch_count(void);
 enum {
   TWELL_KERNEL_UP_PACK = 0,      /* tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue */
   TWELL_KERNEL_ROUTE = 1,        /* fallback routing scan */
-  TWELL_KERNEL_FB_GATHER = 2,    /* gather of fallback X rows + clearing their cells */
-  TWELL_KERNEL_FB_UP = 3,        /* tcgen05 recompute of dense fallback rows */
+  TWELL_KERNEL_FB_ASSEMBLE = 2,  /* dense fallback rows from spilled tiles + cells */
+  TWELL_KERNEL_RESERVED3 = 3,    /* unused */
   TWELL_KERNEL_SPMM = 4,         /* TwELL gather-SpMM down-projection */
   TWELL_KERNEL_FB_DOWN = 5,      /* fallback rows' down-projection */
   TWELL_KERNEL_PACK = 6,         /* standalone dense -> TwELL */
