@@ -168,13 +168,24 @@ __global__ void unit_fill_kernel(Layout L, int n_blocks, const float* __restrict
   }
 }
 
-// Warp per hidden unit j and 256 columns: TwELL entries in ascending row,
-// kU rows of dY and X in flight per lane.
+// Warp per hidden unit j and 256 columns: TwELL entries in ascending row.
+// The warp stages 32 entries at a time (row, h, dZ) in its shared-memory
+// slot with one coalesced load per lane, then walks them with kU rows of dY
+// and X in flight per lane.  h is exactly a bf16 value, so the dW_down update
+// uses the mixed bf16 x bf16 + fp32 fma.
+struct UnitEntry {
+  int32_t row;
+  uint32_t h_bits;  // bf16 bits of h in the low half
+  float dz;
+  float pad;
+};
+
 __global__ void __launch_bounds__(kWarps * 32)
     dw_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
               const float* __restrict__ col_h, const float* __restrict__ col_dz, const uint16_t* __restrict__ X,
               const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT, float* __restrict__ dW_down,
               float* __restrict__ db) {
+  __shared__ UnitEntry stage[kWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + warp;
   if (j >= f) return;
@@ -184,37 +195,45 @@ __global__ void __launch_bounds__(kWarps * 32)
   float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float gb = 0.f;
   const int e0 = col_ptr[j], e1 = col_ptr[j + 1];
-  int e = e0;
-  for (; e + kU <= e1; e += kU) {
-    uint4 g[kU], x[kU];
-    float h[kU], z[kU];
+  UnitEntry* st = stage[warp];
+  for (int b = e0; b < e1; b += 32) {
+    const int m = min(32, e1 - b);
+    if (lane < m) {
+      const float h = col_h[b + lane];
+      st[lane] = UnitEntry{col_rows[b + lane], static_cast<uint32_t>(__float_as_uint(h) >> 16), col_dz[b + lane], 0.f};
+    }
+    __syncwarp();
+    int e = 0;
+    for (; e + kU <= m; e += kU) {
+      uint4 g[kU], x[kU];
+      UnitEntry en[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t n = col_rows[e + u];
-      h[u] = col_h[e + u];
-      z[u] = col_dz[e + u];
-      if (active) {
-        g[u] = __ldg(reinterpret_cast<const uint4*>(dY + n * d + c0));
-        x[u] = __ldg(reinterpret_cast<const uint4*>(X + n * d + c0));
+      for (int u = 0; u < kU; ++u) {
+        en[u] = st[e + u];
+        if (active) {
+          g[u] = __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en[u].row) * d + c0));
+          x[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en[u].row) * d + c0));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        gb += en[u].dz;
+        if (active) {
+          fma8_bf16(a_down, static_cast<uint16_t>(en[u].h_bits), g[u]);
+          fma8(a_in, en[u].dz, x[u]);
+        }
       }
     }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      gb += z[u];
+    for (; e < m; ++e) {
+      const UnitEntry en = st[e];
+      gb += en.dz;
       if (active) {
-        fma8(a_down, h[u], g[u]);
-        fma8(a_in, z[u], x[u]);
+        fma8_bf16(a_down, static_cast<uint16_t>(en.h_bits),
+                  __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en.row) * d + c0)));
+        fma8(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
       }
     }
-  }
-  for (; e < e1; ++e) {
-    const int64_t n = col_rows[e];
-    const float h = col_h[e], z = col_dz[e];
-    gb += z;
-    if (active) {
-      fma8(a_down, h, __ldg(reinterpret_cast<const uint4*>(dY + n * d + c0)));
-      fma8(a_in, z, __ldg(reinterpret_cast<const uint4*>(X + n * d + c0)));
-    }
+    __syncwarp();
   }
   if (active) {
     float4* od = reinterpret_cast<float4*>(dW_down + static_cast<int64_t>(j) * d + c0);

@@ -190,6 +190,22 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
+// acc[0..7] += v * w[0..7] with v and the eight w bf16, accumulators fp32:
+// the mixed-precision fma forms the exact product and rounds once, exactly as
+// fmaf(float(v), float(w), acc) does, without unpacking w.
+__device__ __forceinline__ void fma8_bf16(float (&acc)[8], uint16_t v, const uint4& w) {
+  asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      "mov.b32 {l0, h0}, %9;\n\tmov.b32 {l1, h1}, %10;\n\t"
+      "mov.b32 {l2, h2}, %11;\n\tmov.b32 {l3, h3}, %12;\n\t"
+      "fma.rn.f32.bf16 %0, %8, l0, %0;\n\tfma.rn.f32.bf16 %1, %8, h0, %1;\n\t"
+      "fma.rn.f32.bf16 %2, %8, l1, %2;\n\tfma.rn.f32.bf16 %3, %8, h1, %3;\n\t"
+      "fma.rn.f32.bf16 %4, %8, l2, %4;\n\tfma.rn.f32.bf16 %5, %8, h2, %5;\n\t"
+      "fma.rn.f32.bf16 %6, %8, l3, %6;\n\tfma.rn.f32.bf16 %7, %8, h3, %7;\n\t}"
+      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]),
+        "+f"(acc[7])
+      : "h"(v), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
+}
+
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   __nv_bfloat16 b = __float2bfloat16_rn(x);
   return *reinterpret_cast<uint16_t*>(&b);

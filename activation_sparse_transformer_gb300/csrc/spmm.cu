@@ -28,7 +28,7 @@ namespace twell {
 namespace {
 
 constexpr int kWarps = 8;  // rows per CTA
-constexpr int kU = 4;      // W row loads in flight per lane
+constexpr int kU = 8;      // W row loads in flight per lane
 
 struct SpmmArgs {
   const void* values;     // [N][nt][C] VT
@@ -58,14 +58,37 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
   acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
 }
 
+// Entry of the per-warp list.  bf16 values: one word, hidden unit j in the low
+// 16 bits and the value's bits in the high 16.  fp32 values: (j, value).
+template <typename VT>
+struct RowEntry;
+template <>
+struct RowEntry<uint16_t> {
+  uint32_t w;
+  static __device__ __forceinline__ RowEntry make(int j, uint16_t v) {
+    return RowEntry{static_cast<uint32_t>(j) | (static_cast<uint32_t>(v) << 16)};
+  }
+  __device__ __forceinline__ int j() const { return static_cast<int>(w & 0xFFFFu); }
+  __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const {
+    fma8_bf16(acc, static_cast<uint16_t>(w >> 16), wr);
+  }
+};
+template <>
+struct RowEntry<float> {
+  int32_t jj;
+  float v;
+  static __device__ __forceinline__ RowEntry make(int j, float val) { return RowEntry{j, val}; }
+  __device__ __forceinline__ int j() const { return jj; }
+  __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const { fma8(acc, v, wr); }
+};
+
 // max_entries = n_tiles * C bounds the entries a row can store.
 template <typename VT>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     spmm_row_kernel(const SpmmArgs a, const uint16_t* __restrict__ W, int max_entries) {
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int32_t* lj = reinterpret_cast<int32_t*>(smem_raw) + warp * max_entries;
-  float* lv = reinterpret_cast<float*>(smem_raw) + kWarps * max_entries + warp * max_entries;
+  RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw) + warp * max_entries;
   const int row = blockIdx.x * kWarps + warp;
   if (row >= a.N) return;
   if (a.row_fb[row] >= 0) return;  // written by the fallback path, which may run concurrently
@@ -87,10 +110,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     const int base = total + incl - cnt;
     const int64_t cell = cell0 + t;
-    for (int s = 0; s < cnt; ++s) {
-      lj[base + s] = t * a.T + a.idx[cell * a.C + s];
-      lv[base + s] = as_f32<VT>(vals[cell * a.C + s]);
-    }
+    for (int s = 0; s < cnt; ++s) list[base + s] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s], vals[cell * a.C + s]);
     total += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncwarp();
@@ -102,17 +122,19 @@ __global__ void __launch_bounds__(kWarps * 32)
     int e = 0;
     for (; e + kU <= total; e += kU) {
       uint4 w[kU];
-      float v[kU];
+      RowEntry<VT> en[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
-        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(lj[e + u]) * a.d));
-        v[u] = lv[e + u];
+        en[u] = list[e + u];
+        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
       }
 #pragma unroll
-      for (int u = 0; u < kU; ++u) fma8(acc, v[u], w[u]);
+      for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
     }
-    for (; e < total; ++e)
-      fma8(acc, lv[e], __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(lj[e]) * a.d)));
+    for (; e < total; ++e) {
+      const RowEntry<VT> en = list[e];
+      en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+    }
     uint32_t p[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -126,8 +148,9 @@ template <typename VT>
 int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaStream_t s) {
   if (a.N <= 0) return TWELL_OK;
   if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;  // hidden unit fits the entry's 16 bits
   const int max_entries = a.nt * a.C;
-  const size_t smem = static_cast<size_t>(kWarps) * max_entries * 8;
+  const size_t smem = static_cast<size_t>(kWarps) * max_entries * sizeof(RowEntry<VT>);
   if (smem > 227 * 1024) return TWELL_ERR_UNSUPPORTED;
   auto kern = spmm_row_kernel<VT>;
   static bool attr[64] = {};
