@@ -247,36 +247,39 @@ __global__ void __launch_bounds__(kWarps * 32)
 }
 
 // Operands of the fallback rows' weight-gradient GEMMs, K = fallback slot:
-// hfb[s] = fb_dense[s], dyg[s] = dY[fb_rows[s]], xg[s] = X[fb_rows[s]] for
-// s < n_fb; rows n_fb .. (next multiple of 64) - 1 are zero in these and in
-// the dZ high / low parts, as the GEMM's device-side K requires.
+// hfb[s] = fb_dense[s], dyg[s] = dY[fb_rows[s]] for s < n_fb, and
+// xg2[2s] = xg2[2s+1] = X[fb_rows[s]] (paired with the high and low parts of
+// dZ, interleaved the same way).  Rows from n_fb (2 n_fb for the paired
+// buffers) up to the next multiple of 64 are zero, as the GEMM's device-side K
+// requires.
 __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
-                                   uint16_t* __restrict__ hfb, uint16_t* __restrict__ dyg, uint16_t* __restrict__ xg,
-                                   uint16_t* __restrict__ dz_hi, uint16_t* __restrict__ dz_lo, int fb_pad) {
+                                   uint16_t* __restrict__ hfb, uint16_t* __restrict__ dyg, uint16_t* __restrict__ xg2,
+                                   uint16_t* __restrict__ dz_hl, int fb_pad) {
   const int nfb = min(*L.n_fb, L.fb_cap);
-  const int kpad = min(fb_pad, (nfb + 63) & ~63);
+  const int k1 = min(fb_pad, (nfb + 63) & ~63);
+  const int k2 = min(2 * fb_pad, (2 * nfb + 63) & ~63);
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int slot = blockIdx.x; slot < kpad; slot += gridDim.x) {
+  // single rows: hfb, dyg
+  for (int slot = blockIdx.x; slot < k1; slot += gridDim.x) {
     const bool real = slot < nfb;
     const int row = real ? L.fb_rows[slot] : 0;
     uint4* h = reinterpret_cast<uint4*>(hfb + static_cast<int64_t>(slot) * L.f);
     const uint4* hs = reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(real ? slot : 0) * L.f);
     for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) h[i] = real ? hs[i] : z;
-    if (!real) {
-      uint4* a = reinterpret_cast<uint4*>(dz_hi + static_cast<int64_t>(slot) * L.f);
-      uint4* b = reinterpret_cast<uint4*>(dz_lo + static_cast<int64_t>(slot) * L.f);
-      for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) {
-        a[i] = z;
-        b[i] = z;
-      }
-    }
     uint4* g = reinterpret_cast<uint4*>(dyg + static_cast<int64_t>(slot) * d);
-    uint4* x = reinterpret_cast<uint4*>(xg + static_cast<int64_t>(slot) * d);
     const uint4* gs = reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(row) * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) g[i] = real ? gs[i] : z;
+  }
+  // paired rows: xg2 (X twice), dz_hl padding
+  for (int k = blockIdx.x; k < k2; k += gridDim.x) {
+    const bool real = k < 2 * nfb;
+    const int row = real ? L.fb_rows[k >> 1] : 0;
+    uint4* x = reinterpret_cast<uint4*>(xg2 + static_cast<int64_t>(k) * d);
     const uint4* xs = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-      g[i] = real ? gs[i] : z;
-      x[i] = real ? xs[i] : z;
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) x[i] = real ? xs[i] : z;
+    if (!real) {
+      uint4* a = reinterpret_cast<uint4*>(dz_hl + static_cast<int64_t>(k) * L.f);
+      for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) a[i] = z;
     }
   }
 }
@@ -312,11 +315,10 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t padd = static_cast<size_t>(fb_pad) * d_model;
   const size_t o_dzc = take(sizeof(float) * cells);
   const size_t o_dzf = take(sizeof(float) * static_cast<size_t>(fb_cap) * d_ff);
-  const size_t o_hi = take(sizeof(uint16_t) * padf);
-  const size_t o_lo = take(sizeof(uint16_t) * padf);
+  const size_t o_hl = take(sizeof(uint16_t) * 2 * padf);
   const size_t o_hfb = take(sizeof(uint16_t) * padf);
   const size_t o_dyg = take(sizeof(uint16_t) * padd);
-  const size_t o_xg = take(sizeof(uint16_t) * padd);
+  const size_t o_xg = take(sizeof(uint16_t) * 2 * padd);
   const size_t o_part = take(sizeof(float) * 2 * ksplit * static_cast<size_t>(fb_cap) * d_model);
   const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
   const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
@@ -327,11 +329,10 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
     ws->dz_fb = reinterpret_cast<float*>(b + o_dzf);
-    ws->dz_fb_hi = reinterpret_cast<uint16_t*>(b + o_hi);
-    ws->dz_fb_lo = reinterpret_cast<uint16_t*>(b + o_lo);
+    ws->dz_hl = reinterpret_cast<uint16_t*>(b + o_hl);
     ws->hfb = reinterpret_cast<uint16_t*>(b + o_hfb);
     ws->dyg = reinterpret_cast<uint16_t*>(b + o_dyg);
-    ws->xg = reinterpret_cast<uint16_t*>(b + o_xg);
+    ws->xg2 = reinterpret_cast<uint16_t*>(b + o_xg);
     ws->fb_pad = fb_pad;
     ws->part = reinterpret_cast<float*>(b + o_part);
     ws->ksplit = ksplit;
@@ -364,8 +365,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const int col_blocks = (d + 255) / 256;
   if (N > 0) {
     // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
-    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts,   Lh.row_fb, Lh.fb_dense,  Lh.fb_cap,  f / Lh.tile, Lh.tile,
-                       Lh.cap,    f,      lambda,      ws.dz_cells, ws.dz_fb,   ws.dz_fb_hi, ws.dz_fb_lo};
+    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb,   Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
+                       Lh.tile,   Lh.cap, f,         lambda,      ws.dz_cells, ws.dz_fb,  ws.dz_hl};
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
     // dX: TwELL rows by the gather-SpMM, fallback rows on a second stream
     AuxFork fork(s);
@@ -375,10 +376,11 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
       const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
       PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
-      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_hi, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
-                                           TWELL_KERNEL_DX, a));
-      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_fb_lo, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
-                                           TWELL_KERNEL_DX, a));
+      // the high and low parts are every other row of dz_hl
+      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
+                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f)));
+      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl + f, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
+                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f)));
       TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
     }
     TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s));
@@ -425,17 +427,16 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   // ---- the fallback rows' share, on the tensor cores
   if (Lh.fb_cap > 0 && N > 0) {
     {
-      const int grid = std::max(1, std::min(ws.fb_pad, 2 * sm_count()));
+      const int grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
       LaunchScope ls(TWELL_KERNEL_DW, s);
-      fb_operands_kernel<<<grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg, ws.dz_fb_hi, ws.dz_fb_lo,
-                                               ws.fb_pad);
+      fb_operands_kernel<<<grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad);
     }
     TW_CHECK_LAUNCH();
     AddEpiParams down{dW_down, d};
     AddEpiParams in{dW_inT, d};
-    TW_TRY_RC(launch_gemm_add_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, down, Lh.status, TWELL_KERNEL_DW, s));
-    TW_TRY_RC(launch_gemm_add_mn(ws.dz_fb_hi, ws.xg, f, d, ws.fb_pad, Lh.n_fb, in, Lh.status, TWELL_KERNEL_DW, s));
-    TW_TRY_RC(launch_gemm_add_mn(ws.dz_fb_lo, ws.xg, f, d, ws.fb_pad, Lh.n_fb, in, Lh.status, TWELL_KERNEL_DW, s));
+    TW_TRY_RC(launch_gemm_add_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, 1, down, Lh.status, TWELL_KERNEL_DW, s));
+    // K = (slot, part): the high and low parts of dZ against X twice
+    TW_TRY_RC(launch_gemm_add_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, in, Lh.status, TWELL_KERNEL_DW, s));
     {
       LaunchScope ls(TWELL_KERNEL_DW, s);
       fb_db_kernel<<<(f + 255) / 256, 256, 0, s>>>(L, ws.dz_fb, db);

@@ -57,8 +57,9 @@ struct GemmArgs {
   int N;
   int K;
   int ksplit;            // K ranges per output tile (partial sums when > 1)
-  const int32_t* K_dev;  // optional device-side K (clamped to K); operand rows/cols up to the next
-                         // multiple of 64 past it must be zero
+  const int32_t* K_dev;  // optional device-side K (times k_mul, clamped to K); operand rows/cols up to
+                         // the next multiple of 64 past it must be zero
+  int k_mul;
   int32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -383,8 +384,8 @@ struct SampleEpi {
           }
           dst[q] = make_float4(o[0], o[1], o[2], o[3]);
         }
-        uint4* dh = reinterpret_cast<uint4*>(p.dz_fb_hi + off);
-        uint4* dl = reinterpret_cast<uint4*>(p.dz_fb_lo + off);
+        uint4* dh = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
+        uint4* dl = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           dh[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (args.M_dev) M = min(M, max(0, *args.M_dev));
   const int num_m = (M + kBM - 1) / kBM;
   const int num_n = args.N / BN;
-  const int K = args.K_dev ? min(args.K, max(0, *args.K_dev)) : args.K;
+  const int K = args.K_dev ? min(args.K, max(0, *args.K_dev) * args.k_mul) : args.K;
   const int num_k = (K + kBK - 1) / kBK;
   const int num_units = num_k > 0 ? num_m * num_n * args.ksplit : 0;
   const int k_per = (num_k + args.ksplit - 1) / args.ksplit;
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
-                const int32_t* K_dev = nullptr) {
+                const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
@@ -602,11 +603,11 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   CUtensorMap ta, tb;
   int rc;
   if (kANMajor)
-    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), static_cast<uint64_t>(M) * 2, 64,
-                        kBK);
+    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
+                        static_cast<uint64_t>(lda ? lda : M) * 2, 64, kBK);
   else
-    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2, kBK,
-                        kBM);
+    rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                        static_cast<uint64_t>(lda ? lda : K) * 2, kBK, kBM);
   if (rc) return rc;
   if (kBNMajor)
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
@@ -627,7 +628,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   }
   const int units = ((M + kBM - 1) / kBM) * (N / BN) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
-  GemmArgs args{M, M_dev, N, K, ksplit, K_dev, status, kWaitLimitNs};
+  GemmArgs args{M, M_dev, N, K, ksplit, K_dev, k_mul, status, kWaitLimitNs};
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kThreads, smem, s>>>(ta, tb, args, p);
@@ -672,18 +673,19 @@ int choose_fb_ksplit(int K) {
 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
-                               cudaStream_t s) {
+                               cudaStream_t s, int64_t lda) {
   if (N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
-  return launch_gemm<128, PartialEpi, false, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s);
+  return launch_gemm<128, PartialEpi, false, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s, nullptr, 1,
+                                                   lda);
 }
 
-int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev,
+int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
                        const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
   if (M % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   if (N % 256 == 0)
-    return launch_gemm<256, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev);
+    return launch_gemm<256, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
   if (N % 128 == 0)
-    return launch_gemm<128, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev);
+    return launch_gemm<128, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
   return TWELL_ERR_UNSUPPORTED;
 }
 

@@ -111,8 +111,9 @@ struct SampleEpiParams {
   float lambda;
   float* dz_cells;          // [M][n_tiles][C] fp32, stored slots only
   float* dz_fb;             // [fb_cap][d_ff] fp32, dense (0 where h == 0)
-  uint16_t* dz_fb_hi;       // [fb_cap][d_ff] bf16(dz_fb)
-  uint16_t* dz_fb_lo;       // [fb_cap][d_ff] bf16(dz_fb - hi): hi + lo carries dz to ~2^-17
+  uint16_t* dz_hl;          // [2 * fb_pad][d_ff] bf16: row 2s = bf16(dz_fb[s]) (high part),
+                            // row 2s+1 = bf16(dz_fb[s] - high) (low part); high + low carry
+                            // dz to ~2^-17 relative
 };
 
 // C[M, N] = A[M, K] . B^T with A row-major [M][K] (K-major).  B is row-major
@@ -124,13 +125,13 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
                       int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
-                               cudaStream_t s);
+                               cudaStream_t s, int64_t lda = 0);
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s);
 // out[M][N] += A^T . B with A row-major [K][M] and B row-major [K][N] (both
-// M/N-major); only the first *K_dev rows of K count, and rows up to the next
-// multiple of 64 past *K_dev must be zero in both operands.
-int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev,
+// M/N-major); only the first k_mul * (*K_dev) rows of K count, and rows up to
+// the next multiple of 64 past them must be zero in both operands.
+int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
                        const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 int choose_fb_ksplit(int K);   // K splits used for the fallback rows' down-projection
 
@@ -156,11 +157,10 @@ int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 struct BwdWorkspace {
   float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries
   float* dz_fb;           // [fb_cap][d_ff] fp32: dZ of the fallback rows (0 off the pattern)
-  uint16_t* dz_fb_hi;     // [fb_pad][d_ff] bf16 high part of dz_fb (zero past n_fb)
-  uint16_t* dz_fb_lo;     // [fb_pad][d_ff] bf16 low part of dz_fb (zero past n_fb)
+  uint16_t* dz_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of dz_fb, interleaved by row
   uint16_t* hfb;          // [fb_pad][d_ff] fallback rows of H (zero past n_fb)
   uint16_t* dyg;          // [fb_pad][d_model] dY of the fallback rows (zero past n_fb)
-  uint16_t* xg;           // [fb_pad][d_model] X of the fallback rows (zero past n_fb)
+  uint16_t* xg2;          // [2 * fb_pad][d_model] X of the fallback rows, each row twice
   int32_t fb_pad;         // fb_cap rounded up to 64
   float* part;            // [2 * ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
   int32_t ksplit;
@@ -171,7 +171,7 @@ struct BwdWorkspace {
   float* col_dz;          // [capacity] dZ of each entry
   int32_t n_blocks;       // row blocks of kBwdRowsPerBlock rows
 };
-constexpr int kBwdRowsPerBlock = 32;
+constexpr int kBwdRowsPerBlock = 16;
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
                             void* base);
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,
