@@ -24,7 +24,7 @@ EXPORTED = [
     "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",
     "twell_bwd_workspace_bytes", "twell_dense_ffn_fwd", "twell_read_status", "twell_status_string",
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
-    "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch",
+    "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
 ]
 
 
@@ -73,6 +73,7 @@ def load_library() -> ctypes.CDLL:
         "twell_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]),
         "twell_ffn_fwd_noalloc": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P]),
         "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
+        "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -172,6 +173,17 @@ def twell_ffn_fwd(X, W_inT, b, W_down, packed: Packed, Y, workspace, stream=None
     _check(load_library().twell_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, ctypes.byref(st),
                                         _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "twell_ffn_fwd")
+
+
+def twell_gated_ffn_fwd(X, W_gT, W_uT, b, W_down, packed: Packed, Y, workspace, stream=None) -> None:
+    """Gated ReLU layer: H = ReLU(X.W_g + b) * (X.W_u) packed in TwELL, Y = H.W_down."""
+    n, d = X.shape
+    f = W_gT.shape[0]
+    st = packed.struct()
+    _check(load_library().twell_gated_ffn_fwd(_ptr(X), _ptr(W_gT), _ptr(W_uT), _ptr(b), _ptr(W_down), n, d, f,
+                                              ctypes.byref(st), _ptr(Y), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "twell_gated_ffn_fwd")
 
 
 def twell_ffn_fwd_noalloc(X, W_inT, b, W_down, packed: Packed, Y, stream=None) -> None:

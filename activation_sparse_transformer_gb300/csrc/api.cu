@@ -274,18 +274,26 @@ size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, 
   return fwd_workspace_layout(d_model, d_ff, tile, fb_cap).total;
 }
 
-int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
-                  int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y, void* workspace,
-                  size_t workspace_bytes, twell_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// The forward of both layer kinds: the fused up-projection (plain ReLU, or
+// gated when W_uT is given), routing, then the TwELL rows' gather-SpMM on the
+// caller's stream and the dense-fallback rows on a second stream.
+int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, const uint16_t* b,
+            const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y,
+            void* workspace, size_t workspace_bytes, twell_stream_t stream) {
   TW_TRY(check_layout(H));
   if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
   if (H->n_rows != n_rows || H->d_ff != d_ff) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
+  if (W_uT) TW_TRY(check_dense(W_uT));
   TW_TRY(check_dense(b));
   TW_TRY(check_dense(W_down));
   TW_TRY(check_dense(Y));
+  if (W_uT && 128 % H->tile != 0) return TWELL_ERR_UNSUPPORTED;
   const FwdWorkspace w = fwd_workspace_layout(d_model, d_ff, H->tile, H->fb_cap);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
@@ -299,7 +307,10 @@ int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, c
   TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
   PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
                    d_ff / H->tile, H->tile, H->cap};
-  TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
+  if (W_uT)
+    TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
+  else
+    TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
   TW_TRY(launch_route(*H, s));
   {
     // the dense-fallback rows (assembly + tensor-core down-projection) run on
@@ -312,6 +323,22 @@ int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, c
     TW_TRY(fork.join());
   }
   return TWELL_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
+                  int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y, void* workspace,
+                  size_t workspace_bytes, twell_stream_t stream) {
+  return ffn_fwd(X, W_inT, nullptr, b, W_down, n_rows, d_model, d_ff, H, Y, workspace, workspace_bytes, stream);
+}
+
+int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT, const uint16_t* b,
+                        const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H,
+                        uint16_t* Y, void* workspace, size_t workspace_bytes, twell_stream_t stream) {
+  if (!W_uT) return TWELL_ERR_INVALID_ARG;
+  return ffn_fwd(X, W_gT, W_uT, b, W_down, n_rows, d_model, d_ff, H, Y, workspace, workspace_bytes, stream);
 }
 
 size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,

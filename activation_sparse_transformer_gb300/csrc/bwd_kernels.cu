@@ -57,24 +57,33 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
   acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
 }
 
-// Pass 1 of the unit-major regrouping: per block of kBwdRowsPerBlock rows,
-// the number of stored entries of every hidden unit, written unit-major
-// (blk_count[j][b]) so that each unit's block counts are contiguous.
-__global__ void unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
-  extern __shared__ int32_t hist[];
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x) hist[j] = 0;
+// Unit-major regrouping of the TwELL entries.  A CTA owns a block of
+// kBwdRowsPerBlock (= 32) rows.  For every hidden unit it builds a 32-bit mask
+// with bit r set when row r of the block stores that unit (a unit appears at
+// most once per row), so popc(mask) counts the unit's entries in the block and
+// cursor + popc(mask & ((1 << r) - 1)) is the place of row r's entry: rows
+// ascending, no atomics on the output, every cell processed in parallel.
+__device__ __forceinline__ void build_row_masks(const Layout& L, int r0, int r1, uint32_t* mask) {
+  for (int j = threadIdx.x; j < L.f; j += blockDim.x) mask[j] = 0;
   __syncthreads();
-  const int r0 = blockIdx.x * kBwdRowsPerBlock;
-  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
   for (int i = threadIdx.x; i < (r1 - r0) * L.nt; i += blockDim.x) {
     const int64_t cell = static_cast<int64_t>(r0) * L.nt + i;
     const int cnt = L.counts[cell];
     const int t = i % L.nt;
-    for (int s = 0; s < cnt; ++s) atomicAdd(&hist[t * L.T + L.idx[cell * L.C + s]], 1);
+    const uint32_t bit = 1u << (i / L.nt);
+    for (int s = 0; s < cnt; ++s) atomicOr(&mask[t * L.T + L.idx[cell * L.C + s]], bit);
   }
   __syncthreads();
+}
+
+// Pass 1: entries per (unit, row block), stored unit-major (blk_count[j][b]).
+__global__ void unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
+  extern __shared__ uint32_t mask[];
+  const int r0 = blockIdx.x * kBwdRowsPerBlock;
+  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
+  build_row_masks(L, r0, r1, mask);
   for (int j = threadIdx.x; j < L.f; j += blockDim.x)
-    blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] = hist[j];
+    blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] = __popc(mask[j]);
 }
 
 // Warp per unit: exclusive scan over its row blocks (in place); the total goes
@@ -139,32 +148,29 @@ __global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ c
   if (tid == 0) col_ptr[f] = base_s;
 }
 
-// Pass 2: the rows of a block in ascending order; within one row every unit
-// appears at most once, so the per-unit cursors need no atomics.
+// Pass 2: every entry written at its unit's cursor plus the number of the
+// unit's entries in earlier rows of the block.
 __global__ void unit_fill_kernel(Layout L, int n_blocks, const float* __restrict__ dz_cells,
                                  const int32_t* __restrict__ blk_count, const int32_t* __restrict__ col_ptr,
                                  int32_t* __restrict__ col_rows, float* __restrict__ col_h,
                                  float* __restrict__ col_dz) {
-  extern __shared__ int32_t cursor[];
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x)
-    cursor[j] = col_ptr[j] + blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x];
-  __syncthreads();
+  extern __shared__ uint32_t mask[];
   const int r0 = blockIdx.x * kBwdRowsPerBlock;
   const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
-  for (int row = r0; row < r1; ++row) {
-    const int64_t cell0 = static_cast<int64_t>(row) * L.nt;
-    for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
-      const int64_t cell = cell0 + t;
-      const int cnt = L.counts[cell];
-      for (int s = 0; s < cnt; ++s) {
-        const int j = t * L.T + L.idx[cell * L.C + s];
-        const int pos = cursor[j]++;
-        col_rows[pos] = row;
-        col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + s]);
-        col_dz[pos] = dz_cells[cell * L.C + s];
-      }
+  build_row_masks(L, r0, r1, mask);
+  for (int i = threadIdx.x; i < (r1 - r0) * L.nt; i += blockDim.x) {
+    const int64_t cell = static_cast<int64_t>(r0) * L.nt + i;
+    const int cnt = L.counts[cell];
+    const int t = i % L.nt;
+    const int r = i / L.nt;
+    for (int s = 0; s < cnt; ++s) {
+      const int j = t * L.T + L.idx[cell * L.C + s];
+      const int pos = col_ptr[j] + blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] +
+                      __popc(mask[j] & ((1u << r) - 1u));
+      col_rows[pos] = r0 + r;
+      col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + s]);
+      col_dz[pos] = dz_cells[cell * L.C + s];
     }
-    __syncthreads();
   }
 }
 
@@ -368,11 +374,15 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb,   Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
                        Lh.tile,   Lh.cap, f,         lambda,      ws.dz_cells, ws.dz_fb,  ws.dz_hl};
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
-    // dX: TwELL rows by the gather-SpMM, fallback rows on a second stream
-    AuxFork fork(s);
-    TW_TRY_RC(fork.status());
+  }
+  // dX (gather-SpMM for TwELL rows, tensor-core GEMMs for fallback rows) runs
+  // on a second stream while this stream computes the weight gradients; both
+  // only read the SDDMM's dZ.
+  AuxFork fork(s);
+  TW_TRY_RC(fork.status());
+  if (N > 0) {
+    cudaStream_t a = fork.aux();
     if (Lh.fb_cap > 0) {
-      cudaStream_t a = fork.aux();
       const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
       PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
@@ -383,8 +393,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                                            TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f)));
       TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
     }
-    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, s));
-    TW_TRY_RC(fork.join());
+    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, a));
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit
   const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
@@ -443,6 +452,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     }
     TW_CHECK_LAUNCH();
   }
+  TW_TRY_RC(fork.join());
   return TWELL_OK;
 }
 

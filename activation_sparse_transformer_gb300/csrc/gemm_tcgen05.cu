@@ -85,6 +85,7 @@ __device__ __forceinline__ float bias_at(const uint4 (&bq)[4], int i) {
 
 // ------------------------------------------------------------ epilogues
 struct PackEpi {
+  static constexpr bool kDualB = false;
   using Params = PackEpiParams;
   static constexpr int kMaxCap = 32;
   static constexpr uint32_t kSmemBytes = kEpiThreads * kMaxCap * 3;  // per thread: C values (u16) + C indices (u8)
@@ -218,7 +219,137 @@ struct PackEpi {
   }
 };
 
+// Gated (Llama-style) variant of PackEpi: the CTA's B stage holds 128 gate
+// rows and 128 up rows of the same hidden units, so TMEM columns [0, BN/2)
+// hold z_g = X.W_g and [BN/2, BN) hold z_u = X.W_u for units col0 .. col0+BN/2.
+// h = bf16(z_g' * z_u) where z_g' = z_g + b > 0, else +0; a product of fp32
+// rounds to a non-zero bf16 exactly when its magnitude exceeds 2^-134.
+struct GatedPackEpi {
+  static constexpr bool kDualB = true;
+  using Params = PackEpiParams;
+  static constexpr int kMaxCap = 32;
+  static constexpr uint32_t kSmemBytes = kEpiThreads * kMaxCap * 3;
+
+  // fp32 h of 32 units [c, c + 32) of this thread's row (bias applied to the gate)
+  template <int BN>
+  static __device__ __forceinline__ void load_h32(const Params& p, uint32_t taddr, int col0, int c,
+                                                  uint32_t (&g)[32]) {
+    uint32_t u[32];
+    tmem_ld32(taddr + c, g);
+    tmem_ld32(taddr + BN / 2 + c, u);
+    const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0 + c);
+    uint4 bq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bq[q] = __ldg(bp + q);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float zg = __uint_as_float(g[i]) + bias_at(bq, i);
+      g[i] = __float_as_uint(zg > 0.0f ? zg * __uint_as_float(u[i]) : 0.0f);
+    }
+  }
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int, uint8_t* smem, int et) {
+    constexpr int U = BN / 2;  // hidden units per CTA tile
+    const int T = p.tile, C = p.cap;
+    int cb = half * (U / 2), ce = cb + U / 2;
+    if (T > U / 2) {
+      if (half) return;
+      cb = 0;
+      ce = U;
+    }
+    uint16_t* sv = reinterpret_cast<uint16_t*>(smem) + et * kMaxCap;
+    uint8_t* si = smem + kEpiThreads * kMaxCap * 2 + et * kMaxCap;
+    const bool valid = row < M;
+    const float thr = __uint_as_float(0x00008000u);
+    int cnt = 0;
+#pragma unroll 1
+    for (int c = cb; c < ce; c += 32) {
+      uint32_t h[32];
+      load_h32<BN>(p, taddr, col0, c, h);
+      const int j0 = c % T;
+      if (j0 == 0) {
+        cnt = 0;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < kMaxCap * 2 / 16; ++q) reinterpret_cast<uint4*>(sv)[q] = z;
+#pragma unroll
+        for (int q = 0; q < kMaxCap / 16; ++q) reinterpret_cast<uint4*>(si)[q] = z;
+      }
+      uint32_t mask = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mask |= (fabsf(__uint_as_float(h[i])) > thr ? 1u : 0u) << i;
+      const int k = __popc(mask);
+      if (cnt + k <= C) {
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1;
+          sv[cnt] = float_to_bf16_bits(__uint_as_float(pick32(h, i)));
+          si[cnt] = static_cast<uint8_t>(j0 + i);
+          ++cnt;
+        }
+      } else {
+        cnt += k;
+      }
+      if ((c + 32) % T != 0) continue;
+      const int tile_c0 = c + 32 - T;
+      const int t = (col0 + tile_c0) / T;
+      const int64_t cell = static_cast<int64_t>(row) * p.n_tiles + t;
+      const bool ovf = valid && cnt > C;
+      if (valid && !ovf) {
+        p.counts[cell] = static_cast<uint8_t>(cnt);
+        if ((C & 7) == 0) {
+          uint4* gv = reinterpret_cast<uint4*>(p.values + cell * C);
+          uint2* gi = reinterpret_cast<uint2*>(p.idx + cell * C);
+          for (int q = 0; q < C / 8; ++q) {
+            gv[q] = reinterpret_cast<const uint4*>(sv)[q];
+            gi[q] = reinterpret_cast<const uint2*>(si)[q];
+          }
+        } else {
+          for (int q = 0; q < C; ++q) {
+            p.values[cell * C + q] = sv[q];
+            p.idx[cell * C + q] = si[q];
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, ovf)) {
+        int slot = -1;
+        if (ovf) {
+          p.row_flag[row] = 1;
+          slot = atomicAdd(p.spill_count, 1);
+          if (slot >= p.spill_cap) {
+            report_error(p.status, TWELL_ERR_FALLBACK_OVERFLOW);
+            slot = -1;
+          }
+          p.counts[cell] = kSpilledCell;
+          const uint32_t s24 = slot < 0 ? 0xFFFFFFu : static_cast<uint32_t>(slot);
+          p.values[cell * C] = static_cast<uint16_t>(s24 & 0xFFFFu);
+          p.idx[cell * C] = static_cast<uint8_t>(s24 >> 16);
+        }
+        for (int cc = tile_c0; cc < tile_c0 + T; cc += 32) {
+          uint32_t hh[32];
+          load_h32<BN>(p, taddr, col0, cc, hh);
+          if (slot >= 0) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              packed[i / 2] = static_cast<uint32_t>(float_to_bf16_bits(__uint_as_float(hh[i]))) |
+                              (static_cast<uint32_t>(float_to_bf16_bits(__uint_as_float(hh[i + 1]))) << 16);
+            uint4* dst = reinterpret_cast<uint4*>(p.spill + static_cast<int64_t>(slot) * T + (cc - tile_c0));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+};
+
 struct DenseEpi {
+  static constexpr bool kDualB = false;
   using Params = DenseEpiParams;
   static constexpr uint32_t kSmemBytes = 0;
 
@@ -264,6 +395,7 @@ struct DenseEpi {
 };
 
 struct PartialEpi {
+  static constexpr bool kDualB = false;
   using Params = PartialEpiParams;
   static constexpr uint32_t kSmemBytes = 0;
 
@@ -291,6 +423,7 @@ struct PartialEpi {
 // out[row][col] += acc (fp32): contributions added onto a result another
 // kernel wrote first (the fallback rows' share of the weight gradients).
 struct AddEpi {
+  static constexpr bool kDualB = false;
   using Params = AddEpiParams;
   static constexpr uint32_t kSmemBytes = 0;
 
@@ -322,6 +455,7 @@ struct AddEpi {
 };
 
 struct SampleEpi {
+  static constexpr bool kDualB = false;
   using Params = SampleEpiParams;
   static constexpr uint32_t kSmemBytes = 0;
 
@@ -400,7 +534,7 @@ struct SampleEpi {
 template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args, const typename Epi::Params ep) {
+                   const __grid_constant__ CUtensorMap tmB2, const GemmArgs args, const typename Epi::Params ep) {
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -423,7 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int M = args.M;
   if (args.M_dev) M = min(M, max(0, *args.M_dev));
   const int num_m = (M + kBM - 1) / kBM;
-  const int num_n = args.N / BN;
+  // dual-B tiles cover BN/2 output units (gate and up halves of the B stage)
+  constexpr int kUnitsPerTile = Epi::kDualB ? BN / 2 : BN;
+  const int num_n = args.N / kUnitsPerTile;
   const int K = args.K_dev ? min(args.K, max(0, *args.K_dev) * args.k_mul) : args.K;
   const int num_k = (K + kBK - 1) / kBK;
   const int num_units = num_k > 0 ? num_m * num_n * args.ksplit : 0;
@@ -446,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (Epi::kDualB) tma_prefetch_desc(&tmB2);
   }
   if (warp == 2) tmem_alloc(tmem_holder, Cfg::kTmemCols);
   tc_fence_before();
@@ -477,7 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sA + stage * Cfg::kABytes, &tmA, &full[stage], kb * kBK, m_blk * kBM);
           }
-          if (kBNMajor) {
+          if (Epi::kDualB) {
+            // rows of the two B matrices for the same units stacked in one stage
+            tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], kb * kBK, n_blk * (BN / 2));
+            tma_load_2d(sB + stage * Cfg::kBBytes + Cfg::kBBytes / 2, &tmB2, &full[stage], kb * kBK,
+                        n_blk * (BN / 2));
+          } else if (kBNMajor) {
             // B is [K][N]: BN/64 boxes of 64 N-columns x 64 K-rows, 8 KB apart
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
@@ -575,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int row = m_blk * kBM + lg * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::template apply<BN>(ep, taddr, row, M, n_blk * BN, half, ks, epi_smem, et);
+      Epi::template apply<BN>(ep, taddr, row, M, n_blk * kUnitsPerTile, half, ks, epi_smem, et);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -593,14 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
-                const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0) {
+                const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0, const uint16_t* B2 = nullptr) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
   if (ksplit < 1 || ksplit > num_k) return TWELL_ERR_UNSUPPORTED;
   const int k_per = (num_k + ksplit - 1) / ksplit;
   if (k_per * (ksplit - 1) >= num_k) return TWELL_ERR_UNSUPPORTED;  // every split must own a K block
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tb2;
   int rc;
   if (kANMajor)
     rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
@@ -609,13 +751,22 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
     rc = encode_tmap_2d(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                         static_cast<uint64_t>(lda ? lda : K) * 2, kBK, kBM);
   if (rc) return rc;
-  if (kBNMajor)
+  if (Epi::kDualB) {
+    if (!B2) return TWELL_ERR_INVALID_ARG;
+    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kBK,
+                        BN / 2);
+    if (rc) return rc;
+    rc = encode_tmap_2d(&tb2, B2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2,
+                        kBK, BN / 2);
+  } else if (kBNMajor) {
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
                         kBK);
-  else
+  } else {
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kBK,
                         BN);
+  }
   if (rc) return rc;
+  if (!Epi::kDualB) tb2 = tb;
   const uint32_t smem = 1024 + Cfg::kPipeBytes + Cfg::kBarBytes + Epi::kSmemBytes;
   auto kern = tc_gemm_kernel<BN, Epi, kANMajor, kBNMajor>;
   static bool attr_set[64] = {};
@@ -626,12 +777,12 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
       return TWELL_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int units = ((M + kBM - 1) / kBM) * (N / BN) * ksplit;
+  const int units = ((M + kBM - 1) / kBM) * (N / (Epi::kDualB ? BN / 2 : BN)) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
   GemmArgs args{M, M_dev, N, K, ksplit, K_dev, k_mul, status, kWaitLimitNs};
   {
     LaunchScope ls(kernel_id, s);
-    kern<<<grid, kThreads, smem, s>>>(ta, tb, args, p);
+    kern<<<grid, kThreads, smem, s>>>(ta, tb, tb2, args, p);
   }
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
@@ -687,6 +838,13 @@ int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K
   if (N % 128 == 0)
     return launch_gemm<128, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
   return TWELL_ERR_UNSUPPORTED;
+}
+
+int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t* Bu, int M, int N, int K,
+                           const PackEpiParams& p, int32_t* status, cudaStream_t s) {
+  if (p.cap > GatedPackEpi::kMaxCap || N % 128 != 0 || 128 % p.tile != 0) return TWELL_ERR_UNSUPPORTED;
+  return launch_gemm<256, GatedPackEpi, false, false>(A, Bg, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s,
+                                                      nullptr, 1, 0, Bu);
 }
 
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,

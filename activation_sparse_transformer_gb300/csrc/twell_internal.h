@@ -121,6 +121,10 @@ struct SampleEpiParams {
 // (N-major) for the partial GEMM.  Rows beyond min(M, *M_dev) are not stored.
 int launch_gemm_pack(const uint16_t* A, const uint16_t* B, int M, int N, int K, const PackEpiParams& p,
                      int32_t* status, cudaStream_t s);
+// Gated up-projection: h = bf16((X.W_g + b) * (X.W_u)) where X.W_g + b > 0,
+// packed like launch_gemm_pack; Bg and Bu are [N][K] (K-major).
+int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t* Bu, int M, int N, int K,
+                           const PackEpiParams& p, int32_t* status, cudaStream_t s);
 int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int M, const int32_t* M_dev, int N,
                       int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
@@ -171,7 +175,7 @@ struct BwdWorkspace {
   float* col_dz;          // [capacity] dZ of each entry
   int32_t n_blocks;       // row blocks of kBwdRowsPerBlock rows
 };
-constexpr int kBwdRowsPerBlock = 16;
+constexpr int kBwdRowsPerBlock = 32;  // one bit per row in the unit-list row masks
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
                             void* base);
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,

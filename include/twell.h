@@ -130,6 +130,18 @@ TWELL_API int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint
 TWELL_API size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
                                  int32_t cap, int32_t fb_cap);
 
+/* Forward of the gated (Llama-style) ReLU layer: H = ReLU(X.W_g + b) (.) (X.W_u)
+ * elementwise, then Y = H.W_down, with H packed in TwELL as for twell_ffn_fwd
+ * (the pages name a sparse "sparse_llama" model configuration, repo-explainer
+ * "The Repo's Two Jobs").  W_gT and W_uT are [d_ff][d_model] bf16; b applies to
+ * the gate.  h = bf16(zg * zu) where zg = X.W_g + b > 0 (fp32), else +0, so h
+ * may be negative; "non-zero" is h != 0.  The tile must divide 128.  Same
+ * workspace as twell_ffn_fwd. */
+TWELL_API int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
+                                  const uint16_t* b, const uint16_t* W_down, int32_t n_rows,
+                                  int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y,
+                                  void* workspace, size_t workspace_bytes, twell_stream_t stream);
+
 /* The forward pass for callers that cannot allocate device memory.  (The
  * paper and its pages have no counterpart: this is a deployment convenience
  * of this library.)  Some callers have no allocator of their own to hand --

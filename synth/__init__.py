@@ -23,6 +23,9 @@ Recipe (one config = one seed, numpy PCG64):
     scaled by s_n so that exactly round(p_n * f) units of s_n*u_n + b are > 0,
     then X_n = bf16(s_n * X0_n).
   * dY ~ N(0, 1) in bf16 for training configs.
+  * gated configs add W_u^T ~ N(0, 1/sqrt(d)); the bias places the gate's quantile.
+  * decode configs take the bias from a separate calibration batch (seed + 500)
+    of calib_rows tokens, since a quantile over 16 tokens says little.
 """
 from __future__ import annotations
 
@@ -53,6 +56,8 @@ class FFNConfig:
     forced_activity: float = 0.2
     l1_lambda: float = 0.0
     fb_cap: Optional[int] = None      # dense-fallback capacity; default below
+    gated: bool = False               # Llama-style: H = ReLU(X.W_g + b) * (X.W_u)
+    calib_rows: Optional[int] = None  # bias from a separate calibration batch of this many tokens
 
     @property
     def n_tiles(self) -> int:
@@ -74,7 +79,17 @@ CONFIGS = {
     # training step shape (forward + backward, L1 on H)
     "train": FFNConfig("train", 8192, 2048, 8192, 128, 8, seed=4, row_spread="lognormal",
                        forced_frac_rows=0.01, l1_lambda=1e-4),
+    # gated (Llama-style) layer, bias at the gate's 99th percentile
+    "gated": FFNConfig("gated", 4096, 4096, 14336, 128, 16, seed=2, gated=True),
+    # decode-shaped step: 16 tokens, bias calibrated on 4096 other tokens
+    "decode": FFNConfig("decode", 16, 4096, 14336, 128, 16, seed=3, sparsity=0.995, calib_rows=4096),
 }
+
+
+def decode_sweep():
+    """The decode shape at the sweep's sparsity levels."""
+    return [dataclasses.replace(CONFIGS["decode"], name=f"decode_{int(round(s * 1000))}", sparsity=s)
+            for s in (0.90, 0.95, 0.99, 0.995)]
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -131,7 +146,15 @@ def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None) -> dict:
     x0 = f32_to_bf16_bits(rng.standard_normal((n, d), dtype=np.float32))
     w_in_t = f32_to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32) / np.float32(math.sqrt(d)))
     w_down = f32_to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32) / np.float32(math.sqrt(f)))
-    u = bf16_bits_to_f32(x0) @ bf16_bits_to_f32(w_in_t).T
+    w_u_t = None
+    if cfg.gated:
+        w_u_t = f32_to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32) / np.float32(math.sqrt(d)))
+    if cfg.calib_rows:
+        crng = np.random.default_rng(cfg.seed + 500)
+        xc = f32_to_bf16_bits(crng.standard_normal((cfg.calib_rows, d), dtype=np.float32))
+        u = bf16_bits_to_f32(xc) @ bf16_bits_to_f32(w_in_t).T
+    else:
+        u = bf16_bits_to_f32(x0) @ bf16_bits_to_f32(w_in_t).T
     b = _column_bias(u, cfg.sparsity)
     target = np.full(n, 1.0 - cfg.sparsity)
     forced = np.zeros(0, dtype=np.int64)
@@ -150,6 +173,8 @@ def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None) -> dict:
         x = x0
     out = {"X": x, "W_inT": w_in_t, "b": b, "W_down": w_down, "target_activity": target,
            "forced_rows": forced}
+    if w_u_t is not None:
+        out["W_uT"] = w_u_t
     if cfg.l1_lambda or cfg.name == "train":
         out["dY"] = make_grad_output(n, d, cfg.seed + 1000)
     return out
@@ -161,7 +186,7 @@ def make_grad_output(n: int, d: int, seed: int) -> np.ndarray:
 
 
 def make_integer_inputs(n: int, d: int, f: int, seed: int, lo: int = -2, hi: int = 2,
-                        sparsity: float = 0.99) -> dict:
+                        sparsity: float = 0.99, gated: bool = False) -> dict:
     """Small-integer layer inputs.  Every product and partial sum is an exact
     float32 integer, so any summation order gives the same bits (the exact
     parity case).  The bias is the negated integer column quantile, so about
@@ -171,8 +196,11 @@ def make_integer_inputs(n: int, d: int, f: int, seed: int, lo: int = -2, hi: int
     w_in_t = rng.integers(lo, hi + 1, size=(f, d)).astype(np.float32)
     w_down = rng.integers(lo, hi + 1, size=(f, d)).astype(np.float32)
     b = _column_bias(x @ w_in_t.T, sparsity)
-    return {"X": f32_to_bf16_bits(x), "W_inT": f32_to_bf16_bits(w_in_t), "b": b,
-            "W_down": f32_to_bf16_bits(w_down)}
+    out = {"X": f32_to_bf16_bits(x), "W_inT": f32_to_bf16_bits(w_in_t), "b": b,
+           "W_down": f32_to_bf16_bits(w_down)}
+    if gated:
+        out["W_uT"] = f32_to_bf16_bits(rng.integers(lo, hi + 1, size=(f, d)).astype(np.float32))
+    return out
 
 
 def make_dense_h(n: int, f: int, seed: int, activity: float = 0.01,
