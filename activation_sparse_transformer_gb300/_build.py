@@ -65,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     tmp = LIB + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
-        "-Xlinker", f"-rpath,{libdir}"]
+        "-Xlinker", f"-rpath,{libdir}", "-Xlinker", "--no-undefined"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")

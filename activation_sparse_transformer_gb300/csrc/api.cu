@@ -60,7 +60,7 @@ LaunchScope::~LaunchScope() {
 namespace {
 struct AuxState {
   cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr;
 };
 AuxState g_aux[64];
 std::mutex g_aux_mu;
@@ -77,7 +77,8 @@ AuxFork::AuxFork(cudaStream_t s) : s_(s) {
   if (!a.stream) {
     if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.mid, cudaEventDisableTiming) != cudaSuccess) {
       rc_ = TWELL_ERR_CUDA;
       return;
     }
@@ -95,6 +96,17 @@ int AuxFork::join() {
   std::lock_guard<std::mutex> lk(g_aux_mu);
   AuxState& a = g_aux[dev];
   if (cudaEventRecord(a.join, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, a.join, 0) != cudaSuccess)
+    rc_ = TWELL_ERR_CUDA;
+  return rc_;
+}
+
+int AuxFork::aux_to_main() {
+  if (joined_ || rc_ != 0) return rc_;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_aux_mu);
+  AuxState& a = g_aux[dev];
+  if (cudaEventRecord(a.mid, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, a.mid, 0) != cudaSuccess)
     rc_ = TWELL_ERR_CUDA;
   return rc_;
 }

@@ -13,9 +13,11 @@
 //             built deterministically (block histograms, scans, ordered fill)
 //   dw_kernel dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] = sum_n dZ[n][j] X[n],
 //             db[j] = sum_n dZ[n][j] over the TwELL entries
-//   fallback  the dense fallback rows' share added by tcgen05 GEMMs with both
-//             operands M/N-major (H_fb^T . dY_fb and dZ_fb^T . X_fb, dZ as
-//             high + low bf16 parts) plus a column sum for db
+//   fallback  the dense fallback rows' share of dW_down and dW_in^T stored
+//             first by tcgen05 GEMMs with both operands M/N-major (H_fb^T .
+//             dY_fb and dZ_fb^T . X_fb, dZ as high + low bf16 parts) on the
+//             second stream; dw_kernel adds the TwELL share on top; a column
+//             sum adds the fallback share of db
 // No atomics on outputs, so every result is deterministic.
 #include <cuda_runtime.h>
 
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     dw_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
               const float* __restrict__ col_h, const float* __restrict__ col_dz, const uint16_t* __restrict__ X,
               const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT, float* __restrict__ dW_down,
-              float* __restrict__ db) {
+              float* __restrict__ db, const int32_t* __restrict__ n_fb, int fb_cap) {
   __shared__ UnitEntry stage[kWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + warp;
@@ -244,6 +246,14 @@ __global__ void __launch_bounds__(kWarps * 32)
   if (active) {
     float4* od = reinterpret_cast<float4*>(dW_down + static_cast<int64_t>(j) * d + c0);
     float4* oi = reinterpret_cast<float4*>(dW_inT + static_cast<int64_t>(j) * d + c0);
+    if (min(*n_fb, fb_cap) > 0) {
+      // the fallback rows' share was stored first by the tensor cores
+      const float4 d0 = od[0], d1 = od[1], i0 = oi[0], i1 = oi[1];
+      a_down[0] += d0.x; a_down[1] += d0.y; a_down[2] += d0.z; a_down[3] += d0.w;
+      a_down[4] += d1.x; a_down[5] += d1.y; a_down[6] += d1.z; a_down[7] += d1.w;
+      a_in[0] += i0.x; a_in[1] += i0.y; a_in[2] += i0.z; a_in[3] += i0.w;
+      a_in[4] += i1.x; a_in[5] += i1.y; a_in[6] += i1.z; a_in[7] += i1.w;
+    }
     od[0] = make_float4(a_down[0], a_down[1], a_down[2], a_down[3]);
     od[1] = make_float4(a_down[4], a_down[5], a_down[6], a_down[7]);
     oi[0] = make_float4(a_in[0], a_in[1], a_in[2], a_in[3]);
@@ -375,14 +385,30 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                        Lh.tile,   Lh.cap, f,         lambda,      ws.dz_cells, ws.dz_fb,  ws.dz_hl};
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
   }
-  // dX (gather-SpMM for TwELL rows, tensor-core GEMMs for fallback rows) runs
-  // on a second stream while this stream computes the weight gradients; both
-  // only read the SDDMM's dZ.
+  // Second stream: the fallback rows' weight-gradient share (stored into dW
+  // first), then dX (fallback GEMMs + the TwELL rows' gather-SpMM).  This
+  // stream: the unit-major lists, then dw_kernel adds the TwELL share once the
+  // fallback share is in place.
   AuxFork fork(s);
   TW_TRY_RC(fork.status());
+  cudaStream_t a = fork.aux();
+  const bool fb = Lh.fb_cap > 0 && N > 0;
+  if (fb) {
+    {
+      const int grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
+      LaunchScope ls(TWELL_KERNEL_DW, a);
+      fb_operands_kernel<<<grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad);
+    }
+    TW_CHECK_LAUNCH();
+    TW_TRY_RC(launch_gemm_store_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, 1, dW_down, d, Lh.status,
+                                   TWELL_KERNEL_DW, a));
+    // K = (slot, part): the high and low parts of dZ against X twice
+    TW_TRY_RC(launch_gemm_store_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, dW_inT, d, Lh.status,
+                                   TWELL_KERNEL_DW, a));
+  }
+  TW_TRY_RC(fork.aux_to_main());  // dW holds the fallback share before dw_kernel runs
   if (N > 0) {
-    cudaStream_t a = fork.aux();
-    if (Lh.fb_cap > 0) {
+    if (fb) {
       const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
       PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
@@ -430,28 +456,15 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
     dw_kernel<<<dim3((f + kWarps - 1) / kWarps, col_blocks), kWarps * 32, 0, s>>>(
-        f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d, dW_inT, dW_down, db);
+        f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d, dW_inT, dW_down, db, Lh.n_fb,
+        fb ? Lh.fb_cap : 0);
   }
   TW_CHECK_LAUNCH();
-  // ---- the fallback rows' share, on the tensor cores
-  if (Lh.fb_cap > 0 && N > 0) {
-    {
-      const int grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
-      LaunchScope ls(TWELL_KERNEL_DW, s);
-      fb_operands_kernel<<<grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad);
-    }
-    TW_CHECK_LAUNCH();
-    AddEpiParams down{dW_down, d};
-    AddEpiParams in{dW_inT, d};
-    TW_TRY_RC(launch_gemm_add_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, 1, down, Lh.status, TWELL_KERNEL_DW, s));
-    // K = (slot, part): the high and low parts of dZ against X twice
-    TW_TRY_RC(launch_gemm_add_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, in, Lh.status, TWELL_KERNEL_DW, s));
-    {
-      LaunchScope ls(TWELL_KERNEL_DW, s);
-      fb_db_kernel<<<(f + 255) / 256, 256, 0, s>>>(L, ws.dz_fb, db);
-    }
-    TW_CHECK_LAUNCH();
+  if (fb) {
+    LaunchScope ls(TWELL_KERNEL_DW, s);
+    fb_db_kernel<<<(f + 255) / 256, 256, 0, s>>>(L, ws.dz_fb, db);
   }
+  TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.join());
   return TWELL_OK;
 }

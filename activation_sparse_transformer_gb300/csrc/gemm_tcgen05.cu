@@ -10,8 +10,9 @@
 //     "Reshaping math for the GPU": a dense matrix catches the rare dense
 //     tokens).
 //   * DenseEpi: bf16 rows with optional bias and ReLU (dense comparator).
-//   * PartialEpi: fp32 partial sums of one K split (fallback rows'
-//     down-projection).
+//   * PartialEpi: fp32 stores, per K split when the K range is split (the
+//     fallback rows' down-projection, dX and weight-gradient shares).
+//   * GatedPackEpi: the gated (Llama-style) up-projection with the pack.
 //   * SampleEpi: dH = dY . W_down^T kept only at the TwELL pattern, plus the
 //     L1 term's gradient (bayesiansapien note, TL;DR) -- the backward SDDMM.
 //
@@ -420,40 +421,6 @@ struct PartialEpi {
   }
 };
 
-// out[row][col] += acc (fp32): contributions added onto a result another
-// kernel wrote first (the fallback rows' share of the weight gradients).
-struct AddEpi {
-  static constexpr bool kDualB = false;
-  using Params = AddEpiParams;
-  static constexpr uint32_t kSmemBytes = 0;
-
-  template <int BN>
-  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
-                                               int ks, uint8_t*, int) {
-    (void)ks;
-    const bool valid = row < M;
-    float* base = p.out + static_cast<int64_t>(row) * p.ld + col0;
-#pragma unroll 1
-    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
-      if (valid) {
-        float4* dst = reinterpret_cast<float4*>(base + c * 32);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 o = dst[q];
-          o.x += __uint_as_float(r[4 * q]);
-          o.y += __uint_as_float(r[4 * q + 1]);
-          o.z += __uint_as_float(r[4 * q + 2]);
-          o.w += __uint_as_float(r[4 * q + 3]);
-          dst[q] = o;
-        }
-      }
-    }
-  }
-};
-
 struct SampleEpi {
   static constexpr bool kDualB = false;
   using Params = SampleEpiParams;
@@ -830,21 +797,20 @@ int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, cons
                                                    lda);
 }
 
-int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
-                       const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
-  if (M % 128 != 0) return TWELL_ERR_UNSUPPORTED;
-  if (N % 256 == 0)
-    return launch_gemm<256, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
-  if (N % 128 == 0)
-    return launch_gemm<128, AddEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
-  return TWELL_ERR_UNSUPPORTED;
-}
-
 int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t* Bu, int M, int N, int K,
                            const PackEpiParams& p, int32_t* status, cudaStream_t s) {
   if (p.cap > GatedPackEpi::kMaxCap || N % 128 != 0 || 128 % p.tile != 0) return TWELL_ERR_UNSUPPORTED;
   return launch_gemm<256, GatedPackEpi, false, false>(A, Bg, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s,
                                                       nullptr, 1, 0, Bu);
+}
+
+int launch_gemm_store_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
+                         float* out, int64_t ld, int32_t* status, int kernel_id, cudaStream_t s) {
+  if (M % 128 != 0 || N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  PartialEpiParams p{out, ld, 0};
+  if (N % 256 == 0)
+    return launch_gemm<256, PartialEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
+  return launch_gemm<128, PartialEpi, true, true>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s, K_dev, k_mul);
 }
 
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,

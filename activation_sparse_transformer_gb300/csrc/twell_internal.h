@@ -40,6 +40,8 @@ class AuxFork {
   int status() const { return rc_; }
   cudaStream_t aux() const { return aux_; }
   int join();
+  // s waits for everything queued on aux so far (aux continues independently)
+  int aux_to_main();
 
  private:
   cudaStream_t s_;
@@ -92,12 +94,6 @@ struct PartialEpiParams {
   int64_t split_stride;
 };
 
-// out[row][col] += acc, fp32 (row-major, leading dimension ld)
-struct AddEpiParams {
-  float* out;
-  int64_t ld;
-};
-
 // dH = dY . W_down^T sampled at the TwELL pattern (the ReLU mask), plus the
 // L1 gradient: dZ = dH + lambda where h > 0.
 struct SampleEpiParams {
@@ -132,11 +128,12 @@ int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, cons
                                cudaStream_t s, int64_t lda = 0);
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s);
-// out[M][N] += A^T . B with A row-major [K][M] and B row-major [K][N] (both
-// M/N-major); only the first k_mul * (*K_dev) rows of K count, and rows up to
-// the next multiple of 64 past them must be zero in both operands.
-int launch_gemm_add_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
-                       const AddEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+// out[M][N] = A^T . B (fp32 store) with A row-major [K][M] and B row-major
+// [K][N] (both M/N-major); only the first k_mul * (*K_dev) rows of K count,
+// rows up to the next multiple of 64 past them must be zero in both operands,
+// and nothing is written when k_mul * (*K_dev) is 0.
+int launch_gemm_store_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
+                         float* out, int64_t ld, int32_t* status, int kernel_id, cudaStream_t s);
 int choose_fb_ksplit(int K);   // K splits used for the fallback rows' down-projection
 
 // forward helpers (fwd_kernels.cu)

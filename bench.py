@@ -50,7 +50,7 @@ def dist_info():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -65,7 +65,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -303,6 +303,86 @@ def bench_ours(args, rank, world, local):
     return result
 
 
+def bench_next(args):
+    """Forward-only measurements of the next shapes (opt-in, one JSON line each):
+    the gated (Llama-style) layer and the decode-shaped sweep."""
+    import numpy as np
+    import torch
+
+    import activation_sparse_transformer_gb300 as tw
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    tw.load_library()
+    peaks, peak_src = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def dt(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def timed(fn, k):
+        for _ in range(args.warmup):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        for i in range(k):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    cfgs = [synth.CONFIGS["gated"]] + synth.decode_sweep()
+    for cfg in cfgs:
+        inp = synth.make_ffn_inputs(cfg)
+        N, d, f, T, C = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap
+        fb = cfg.fallback_capacity if not cfg.name.startswith("decode") else N
+        X, Wi, b, Wd = dt(inp["X"]), dt(inp["W_inT"]), dt(inp["b"]), dt(inp["W_down"])
+        packed = tw.alloc_packed(N, f, T, C, fb, dev)
+        Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
+        if cfg.gated:
+            Wu = dt(inp["W_uT"])
+            fn = lambda: tw.twell_gated_ffn_fwd(X, Wi, Wu, b, Wd, packed, Y, ws, stream)
+        else:
+            fn = lambda: tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, ws, stream)
+        fn()
+        rc = tw.twell_read_status(packed, stream)
+        if rc != 0:
+            raise RuntimeError(f"{cfg.name}: status {rc}")
+        n_fb = int(packed.n_fb[0].item())
+        nnz = int(packed.counts.to(torch.int64).sum().item())
+        ms = timed(fn, args.steps)
+        if cfg.gated:
+            flops = 2.0 * 2 * N * d * f
+            roof_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+            bound = "tensor (gate and up GEMMs)"
+        else:
+            H = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+            tw.twell_unpack(packed, H)
+            used = int((H.view(torch.int16) & 0x7FFF).ne(0).any(dim=0).sum().item())
+            byts = f * d * 2 + used * d * 2 + 2 * N * d * 2 + packed.values.numel() * 3
+            roof_us = byts / (peaks["hbm_gbs"] * 1e9) * 1e6
+            bound = f"hbm (W_in^T + {used} active W_down rows)"
+            del H
+        print(json.dumps({
+            "metric": f"sparse-FFN forward tokens/s ({cfg.name})", "value": round(N / (ms * 1e-3), 1),
+            "unit": "tokens/s", "ms": round(ms, 4), "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
+            "config": {"workload": cfg.name, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
+                       "sparsity_target": cfg.sparsity, "gated": cfg.gated,
+                       "l2": "flushed between steps (2x L2 write)"},
+            "layer": {"n_fb": n_fb, "twell_entries": nnz},
+            "roofline": {"bound": bound, "time_us": round(roof_us, 2), "frac": round(roof_us / (ms * 1e3), 4),
+                         "peak_source": peak_src},
+        }), flush=True)
+        del X, Wi, b, Wd, packed, Y, ws
+        torch.cuda.empty_cache()
+
+
 def cpu_sample_rows(default):
     return int(os.environ.get("TWELL_CPU_SAMPLE_ROWS", default))
 
@@ -372,11 +452,13 @@ def bench_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next", action="store_true",
+                    help="forward-only lines for the gated layer and the decode sweep instead of the main step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_info()
@@ -384,6 +466,10 @@ def main():
         res = bench_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+    if args.next:
+        if rank == 0:
+            bench_next(args)
         return
     if world > 1:
         import torch
