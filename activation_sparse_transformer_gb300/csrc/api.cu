@@ -75,7 +75,12 @@ AuxFork::AuxFork(cudaStream_t s) : s_(s) {
   std::lock_guard<std::mutex> lk(g_aux_mu);
   AuxState& a = g_aux[dev];
   if (!a.stream) {
-    if (cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking) != cudaSuccess ||
+    // the second stream carries the small fallback-row work next to a large
+    // kernel on the caller's stream: the highest priority lets its CTAs take
+    // SMs as they free up instead of queueing behind the large grid
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&a.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
         cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&a.mid, cudaEventDisableTiming) != cudaSuccess) {

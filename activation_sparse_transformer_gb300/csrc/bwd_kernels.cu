@@ -78,8 +78,10 @@ __device__ __forceinline__ void build_row_masks(const Layout& L, int r0, int r1,
   __syncthreads();
 }
 
+constexpr int kListThreads = 1024;  // the list passes are latency-bound: many cells in flight
+
 // Pass 1: entries per (unit, row block), stored unit-major (blk_count[j][b]).
-__global__ void unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
+__global__ void __launch_bounds__(kListThreads) unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
   extern __shared__ uint32_t mask[];
   const int r0 = blockIdx.x * kBwdRowsPerBlock;
   const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ c
 
 // Pass 2: every entry written at its unit's cursor plus the number of the
 // unit's entries in earlier rows of the block.
-__global__ void unit_fill_kernel(Layout L, int n_blocks, const float* __restrict__ dz_cells,
+__global__ void __launch_bounds__(kListThreads) unit_fill_kernel(Layout L, int n_blocks, const float* __restrict__ dz_cells,
                                  const int32_t* __restrict__ blk_count, const int32_t* __restrict__ col_ptr,
                                  int32_t* __restrict__ col_rows, float* __restrict__ col_h,
                                  float* __restrict__ col_dz) {
@@ -300,14 +302,25 @@ __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, con
   }
 }
 
-// db[j] += sum over fallback slots (ascending) of dZ_fb[slot][j].
-__global__ void fb_db_kernel(Layout L, const float* __restrict__ dz_fb, float* __restrict__ db) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= L.f) return;
+// db[j] += sum over the fallback slots of dZ_fb[slot][j]: a CTA covers 32
+// units, warp w sums slots w, w + 8, ... and the eight partial sums are added
+// in warp order (a fixed order, so the result is deterministic).
+__global__ void __launch_bounds__(256) fb_db_kernel(Layout L, const float* __restrict__ dz_fb, float* __restrict__ db) {
+  __shared__ float part[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 32 + lane;
   const int nfb = min(*L.n_fb, L.fb_cap);
   float s = 0.f;
-  for (int slot = 0; slot < nfb; ++slot) s += dz_fb[static_cast<int64_t>(slot) * L.f + j];
-  db[j] += s;
+  if (j < L.f)
+    for (int slot = warp; slot < nfb; slot += 8) s += dz_fb[static_cast<int64_t>(slot) * L.f + j];
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && j < L.f) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += part[w][lane];
+    db[j] += t;
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -434,7 +447,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   }
   if (ws.n_blocks > 0) {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_hist_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.n_blocks, ws.blk_count);
+    unit_hist_kernel<<<ws.n_blocks, kListThreads, fsm, s>>>(L, ws.n_blocks, ws.blk_count);
   }
   TW_CHECK_LAUNCH();
   {
@@ -449,7 +462,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   if (ws.n_blocks > 0) {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_fill_kernel<<<ws.n_blocks, 256, fsm, s>>>(L, ws.n_blocks, ws.dz_cells, ws.blk_count, ws.col_ptr,
+    unit_fill_kernel<<<ws.n_blocks, kListThreads, fsm, s>>>(L, ws.n_blocks, ws.dz_cells, ws.blk_count, ws.col_ptr,
                                                     ws.col_rows, ws.col_h, ws.col_dz);
   }
   TW_CHECK_LAUNCH();
@@ -462,7 +475,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   if (fb) {
     LaunchScope ls(TWELL_KERNEL_DW, s);
-    fb_db_kernel<<<(f + 255) / 256, 256, 0, s>>>(L, ws.dz_fb, db);
+    fb_db_kernel<<<(f + 31) / 32, 256, 0, s>>>(L, ws.dz_fb, db);
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.join());

@@ -356,6 +356,17 @@ def bench_next(args):
         n_fb = int(packed.n_fb[0].item())
         nnz = int(packed.counts.to(torch.int64).sum().item())
         ms = timed(fn, args.steps)
+        # the same call captured once in a CUDA graph and replayed (no host
+        # launch overhead per kernel): what a decode loop would run
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream(dev)
+            if cfg.gated:
+                tw.twell_gated_ffn_fwd(X, Wi, Wu, b, Wd, packed, Y, ws, cap)
+            else:
+                tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, ws, cap)
+        ms_graph = timed(graph.replay, args.steps)
         if cfg.gated:
             flops = 2.0 * 2 * N * d * f
             roof_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
@@ -370,16 +381,18 @@ def bench_next(args):
             del H
         print(json.dumps({
             "metric": f"sparse-FFN forward tokens/s ({cfg.name})", "value": round(N / (ms * 1e-3), 1),
-            "unit": "tokens/s", "ms": round(ms, 4), "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "unit": "tokens/s", "ms": round(ms, 4), "ms_graph": round(ms_graph, 4),
+            "tokens_per_s_graph": round(N / (ms_graph * 1e-3), 1), "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup,
             "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
             "config": {"workload": cfg.name, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
                        "sparsity_target": cfg.sparsity, "gated": cfg.gated,
                        "l2": "flushed between steps (2x L2 write)"},
             "layer": {"n_fb": n_fb, "twell_entries": nnz},
             "roofline": {"bound": bound, "time_us": round(roof_us, 2), "frac": round(roof_us / (ms * 1e3), 4),
-                         "peak_source": peak_src},
+                         "frac_graph": round(roof_us / (ms_graph * 1e3), 4), "peak_source": peak_src},
         }), flush=True)
-        del X, Wi, b, Wd, packed, Y, ws
+        del X, Wi, b, Wd, packed, Y, ws, graph
         torch.cuda.empty_cache()
 
 
