@@ -262,33 +262,58 @@ int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t str
 }
 
 namespace {
-// Forward workspace: [spill tiles][spill counter][fallback down-projection partials]
+// Forward workspace: [spill tiles][spill counter][fallback down-projection
+// partials] then, for small batches, [up-projection K-split partials][dense H]
+// and [SpMM tile-range partials].
 struct FwdWorkspace {
   size_t spill_off, count_off, part_off, total;
   int32_t spill_cap;
-  int ksplit;
+  int ksplit;                // fallback down-projection K splits
+  bool swap;                 // small batch: swapped-operand up-projection
+  int up_ksplit;
+  size_t up_part_off, h_off;
+  int spmm_nsplit;
+  size_t spmm_part_off;
 };
 
-FwdWorkspace fwd_workspace_layout(int32_t d_model, int32_t d_ff, int32_t tile, int32_t fb_cap) {
+FwdWorkspace fwd_workspace_layout(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t fb_cap) {
   FwdWorkspace w{};
   const int64_t nt = d_ff / tile;
   w.spill_cap = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(fb_cap) * nt, 0xFFFFFF));
-  w.ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
+  // K splits of the fallback rows' down-projection: enough (128 x 128) output
+  // tiles x splits (~256) that few fallback rows still stream W_down on every SM
+  const int fb_tiles = ((fb_cap + 127) / 128) * ((d_model + 127) / 128);
+  const int fb_want = fb_tiles > 0 ? std::max(4, std::min(16, (256 + fb_tiles - 1) / fb_tiles)) : 4;
+  w.ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff, fb_want) : 1;
   w.spill_off = 0;
   w.count_off = align256(sizeof(uint16_t) * static_cast<size_t>(w.spill_cap) * static_cast<size_t>(tile));
   w.part_off = w.count_off + 256;
-  w.total = w.part_off +
-            align256(sizeof(float) * static_cast<size_t>(w.ksplit) * static_cast<size_t>(fb_cap) * d_model);
+  size_t off = w.part_off +
+               align256(sizeof(float) * static_cast<size_t>(w.ksplit) * static_cast<size_t>(fb_cap) * d_model);
+  w.swap = n_rows > 0 && n_rows <= kSwapMaxTokens && d_ff % 128 == 0;
+  w.up_ksplit = 1;
+  if (w.swap) {
+    w.up_ksplit = swap_ksplit(d_model);
+    w.up_part_off = off;
+    off += align256(sizeof(float) * static_cast<size_t>(w.up_ksplit) * n_rows * d_ff);
+    w.h_off = off;
+    off += align256(sizeof(uint16_t) * static_cast<size_t>(n_rows) * d_ff);
+  }
+  w.spmm_nsplit = n_rows > 0 ? spmm_nsplit(n_rows, d_model) : 1;
+  if (w.spmm_nsplit > 1) {
+    w.spmm_part_off = off;
+    off += align256(sizeof(float) * static_cast<size_t>(w.spmm_nsplit) * n_rows * d_model);
+  }
+  w.total = off;
   return w;
 }
 }  // namespace
 
 size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
                                  int32_t fb_cap) {
-  (void)n_rows;
   (void)cap;
-  if (d_model <= 0 || d_ff <= 0 || tile <= 0 || fb_cap < 0) return 0;
-  return fwd_workspace_layout(d_model, d_ff, tile, fb_cap).total;
+  if (n_rows < 0 || d_model <= 0 || d_ff <= 0 || tile <= 0 || fb_cap < 0) return 0;
+  return fwd_workspace_layout(n_rows, d_model, d_ff, tile, fb_cap).total;
 }
 
 }  // extern "C"
@@ -311,7 +336,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   TW_TRY(check_dense(W_down));
   TW_TRY(check_dense(Y));
   if (W_uT && 128 % H->tile != 0) return TWELL_ERR_UNSUPPORTED;
-  const FwdWorkspace w = fwd_workspace_layout(d_model, d_ff, H->tile, H->fb_cap);
+  const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
   if (n_rows == 0) return TWELL_OK;
@@ -320,23 +345,41 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   uint16_t* spill = reinterpret_cast<uint16_t*>(ws + w.spill_off);
   int32_t* spill_count = reinterpret_cast<int32_t*>(ws + w.count_off);
   float* part = reinterpret_cast<float*>(ws + w.part_off);
+  float* spmm_part = w.spmm_nsplit > 1 ? reinterpret_cast<float*>(ws + w.spmm_part_off) : nullptr;
+  uint16_t* Hd = w.swap ? reinterpret_cast<uint16_t*>(ws + w.h_off) : nullptr;
   TW_TRY(reset_words(H, s));
-  TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
-  PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
-                   d_ff / H->tile, H->tile, H->cap};
-  if (W_uT)
-    TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
-  else
-    TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
+  const bool swap = w.swap && !W_uT;
+  if (swap) {
+    // small batch: Z^T = W_in^T . X^T with the hidden units on the 128-row
+    // MMA side and K split so the weight stream covers every SM; the partial
+    // sums are added, biased and packed by a CUDA-core pass that also keeps
+    // the dense h for the fallback copy
+    float* up_part = reinterpret_cast<float*>(ws + w.up_part_off);
+    PartialTEpiParams tp{up_part, d_ff, static_cast<int64_t>(n_rows) * d_ff, n_rows};
+    TW_TRY(launch_gemm_swap_partial(W_inT, X, d_ff, n_rows, d_model, w.up_ksplit, tp, H->status,
+                                    TWELL_KERNEL_UP_PACK, s));
+    TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, s));
+  } else {
+    TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
+    PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
+                     d_ff / H->tile, H->tile, H->cap};
+    if (W_uT)
+      TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
+    else
+      TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
+  }
   TW_TRY(launch_route(*H, s));
   {
-    // the dense-fallback rows (assembly + tensor-core down-projection) run on
-    // a second stream while the gather-SpMM handles the TwELL rows
+    // the dense-fallback rows (assembly or copy + tensor-core down-projection)
+    // run on a second stream while the gather-SpMM handles the TwELL rows
     AuxFork fork(s);
     TW_TRY(fork.status());
-    TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
+    if (swap)
+      TW_TRY(launch_fb_copy(Hd, d_ff, *H, fork.aux()));
+    else
+      TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
     TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
-    TW_TRY(launch_spmm(*H, W_down, d_model, Y, s));
+    TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, s));
     TW_TRY(fork.join());
   }
   return TWELL_OK;

@@ -44,12 +44,13 @@ constexpr int kEpiThreads = 256;
 
 template <int BN>
 struct GemmCfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr uint32_t kABytes = kBM * kBK * 2;
   static constexpr uint32_t kBBytes = BN * kBK * 2;
+  // narrow (swapped-operand) tiles stream A: as many stages as ~192 KB holds
+  static constexpr int kStages = BN == 256 ? 4 : BN == 128 ? 6 : static_cast<int>(196608u / (kABytes + kBBytes));
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
   static constexpr uint32_t kPipeBytes = kStages * (kABytes + kBBytes);
-  static constexpr uint32_t kBarBytes = 256;
+  static constexpr uint32_t kBarBytes = 512;  // barriers, TMEM address, abort flag, per-stage parity
 };
 
 struct GemmArgs {
@@ -421,6 +422,35 @@ struct PartialEpi {
   }
 };
 
+// Swapped operands (small batches): accumulator rows are hidden units, the BN
+// columns are tokens; each epilogue half stores BN/2 token columns of fp32
+// partial sums, token-major so a warp's 32 units form one 128-byte run.
+struct PartialTEpi {
+  static constexpr bool kDualB = false;
+  using Params = PartialTEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int ks, uint8_t*, int) {
+    static_assert(BN % 16 == 0 && BN <= 64, "narrow tiles only");
+    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + row;
+#pragma unroll
+    for (int c = 0; c < BN / 2; c += 8) {
+      uint32_t r[8];
+      tmem_ld8(taddr + half * (BN / 2) + c, r);
+      tmem_ld_wait();
+      if (row < M) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int tok = col0 + half * (BN / 2) + c + i;
+          if (tok < p.n_tok) base[static_cast<int64_t>(tok) * p.ld] = __uint_as_float(r[i]);
+        }
+      }
+    }
+  }
+};
+
 struct SampleEpi {
   static constexpr bool kDualB = false;
   using Params = SampleEpiParams;
@@ -504,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args, const typename Epi::Params ep) {
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
+  static_assert(2 * S * 8 + 4 * 8 + 8 + 8 + S * 4 <= static_cast<int>(Cfg::kBarBytes), "barrier region");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -702,7 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
-                const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0, const uint16_t* B2 = nullptr) {
+                const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0, const uint16_t* B2 = nullptr,
+                int b_rows = 0) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
@@ -729,8 +761,9 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
                         kBK);
   } else {
-    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, kBK,
-                        BN);
+    // b_rows < N: the rows past b_rows are read as zeros (TMA fill)
+    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(b_rows > 0 ? b_rows : N),
+                        static_cast<uint64_t>(K) * 2, kBK, BN);
   }
   if (rc) return rc;
   if (!Epi::kDualB) tb2 = tb;
@@ -778,15 +811,28 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
   return TWELL_ERR_UNSUPPORTED;
 }
 
-int choose_fb_ksplit(int K) {
+int choose_fb_ksplit(int K, int max_split) {
   const int num_k = (K + kBK - 1) / kBK;
-  int ks = std::min(4, num_k);
+  int ks = std::max(1, std::min(max_split, num_k));
   while (ks > 1) {
     const int per = (num_k + ks - 1) / ks;
     if (per * (ks - 1) < num_k) break;
     --ks;
   }
   return ks;
+}
+
+int swap_ksplit(int K) { return choose_fb_ksplit(K, 16); }
+
+int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_tok, int K, int ksplit,
+                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
+  if (n_tok <= 0) return TWELL_OK;
+  if (n_tok > kSwapMaxTokens || M % kBM != 0) return TWELL_ERR_UNSUPPORTED;
+  if (n_tok <= 16)
+    return launch_gemm<16, PartialTEpi, false, false>(W, X, M, nullptr, 16, K, ksplit, p, status, kernel_id, s,
+                                                      nullptr, 1, 0, nullptr, n_tok);
+  return launch_gemm<32, PartialTEpi, false, false>(W, X, M, nullptr, 32, K, ksplit, p, status, kernel_id, s, nullptr,
+                                                    1, 0, nullptr, n_tok);
 }
 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,

@@ -43,19 +43,10 @@ __device__ __forceinline__ uint16_t half_word(const uint32_t (&w)[4], int k) {
   return static_cast<uint16_t>((k & 1) ? (w[k / 2] >> 16) : (w[k / 2] & 0xFFFFu));
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
-    pack_cells_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int segs = (L.f + 255) / 256;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= static_cast<int64_t>(L.N) * segs) return;  // whole warp leaves together
-  const int row = static_cast<int>(gw / segs);
-  const int seg = static_cast<int>(gw % segs);
-  const int col = seg * 256 + lane * 8;
-  const bool in = col < L.f;
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (in) v = __ldg(reinterpret_cast<const uint4*>(H + static_cast<int64_t>(row) * ldh + col));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Compaction of 8 consecutive columns [col, col + 8) of one row per lane (a
+// warp covers 256 columns); w holds the 8 bf16 values.  Called by all lanes.
+__device__ __forceinline__ void pack_lane8(const Layout& L, int row, int col, bool in, const uint32_t (&w)[4]) {
+  const int lane = threadIdx.x & 31;
   uint32_t nzmask = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k)
@@ -92,6 +83,59 @@ __global__ void __launch_bounds__(kWarps * 32)
     L.counts[cell] = static_cast<uint8_t>(stored);
     if (total > C) L.row_fb[row] = 1;
   }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    pack_cells_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int segs = (L.f + 255) / 256;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (gw >= static_cast<int64_t>(L.N) * segs) return;  // whole warp leaves together
+  const int row = static_cast<int>(gw / segs);
+  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
+  const bool in = col < L.f;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (in) v = __ldg(reinterpret_cast<const uint4*>(H + static_cast<int64_t>(row) * ldh + col));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  pack_lane8(L, row, col, in, w);
+}
+
+// Small-batch variant: z = sum of the K-split partial sums (split order) +
+// b, h = bf16(z) where z > 2^-134 (the smallest z whose bf16 rounding is not
+// zero), else +0; h is also stored densely in H for the fallback copy.
+__global__ void __launch_bounds__(kWarps * 32)
+    pack_partials_kernel(Layout L, const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ b,
+                         uint16_t* __restrict__ H) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int segs = (L.f + 255) / 256;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (gw >= static_cast<int64_t>(L.N) * segs) return;
+  const int row = static_cast<int>(gw / segs);
+  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
+  const bool in = col < L.f;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (in) {
+    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int64_t split = static_cast<int64_t>(L.N) * L.f;
+    const float* p = part + static_cast<int64_t>(row) * L.f + col;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float4 a = *reinterpret_cast<const float4*>(p + ks * split);
+      const float4 c = *reinterpret_cast<const float4*>(p + ks * split + 4);
+      z[0] += a.x; z[1] += a.y; z[2] += a.z; z[3] += a.w;
+      z[4] += c.x; z[5] += c.y; z[6] += c.z; z[7] += c.w;
+    }
+    const uint4 bq = __ldg(reinterpret_cast<const uint4*>(b + col));
+    const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
+    const float thr = __uint_as_float(0x00008000u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float zb = z[k] + ((k & 1) ? bf16_hi(bw[k / 2]) : bf16_lo(bw[k / 2]));
+      const uint32_t h = zb > thr ? float_to_bf16_bits(zb) : 0u;
+      w[k / 2] |= (k & 1) ? (h << 16) : h;
+    }
+    *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * L.f + col) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  pack_lane8(L, row, col, in, w);
 }
 
 // Fallback rows: copy the dense row, clear the row's cells.
@@ -155,6 +199,16 @@ int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStre
   if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
   LaunchScope ls(TWELL_KERNEL_PACK, s);
   pack_cells_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint16_t* H, const twell_t& L,
+                         cudaStream_t s) {
+  const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
+  if (blocks <= 0) return TWELL_OK;
+  if (blocks > 0x7FFFFFFF || L.d_ff % 8 != 0) return TWELL_ERR_UNSUPPORTED;
+  LaunchScope ls(TWELL_KERNEL_PACK, s);
+  pack_partials_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), part, ksplit, b, H);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

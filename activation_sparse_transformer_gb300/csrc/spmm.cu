@@ -17,6 +17,11 @@
 // fp32 registers.  Each output sums its terms in ascending hidden-unit order.
 // Fallback rows are skipped: their rows of the output belong to the dense
 // fallback path, which may run at the same time on another stream.
+//
+// Small batches have too few (row, 256-column) warps to fill the GPU, so the
+// row's tiles are cut into gridDim.z consecutive ranges (each warp flattens
+// and streams only its range); each range's fp32 sums go to a partial buffer
+// and spmm_reduce_kernel adds the ranges in order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,6 +41,7 @@ struct SpmmArgs {
   const uint8_t* counts;  // [N][nt]
   const int32_t* row_fb;  // [N]: rows >= 0 are fallback rows, left to the fallback path
   uint16_t* out;          // [N][d] bf16
+  float* part;            // [gridDim.z][N][d] fp32 when the tiles are split into ranges, else null
   int N, d, nt, T, C;
   int32_t* status;
 };
@@ -97,11 +103,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   const VT* vals = static_cast<const VT*>(a.values);
   const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
 
+  // ---- this warp's tiles: all of them, or one of gridDim.z consecutive ranges
+  int t_beg = 0, t_end = a.nt;
+  if (gridDim.z > 1) {
+    const int per = (a.nt + gridDim.z - 1) / gridDim.z;
+    t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
+    t_end = min(a.nt, t_beg + per);
+  }
+
   // ---- flatten: tiles in order, 32 per round
   int total = 0;
-  for (int t0 = 0; t0 < a.nt; t0 += 32) {
+  for (int t0 = t_beg; t0 < t_end; t0 += 32) {
     const int t = t0 + lane;
-    const int cnt = t < a.nt ? a.counts[cell0 + t] : 0;
+    const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -135,6 +149,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       const RowEntry<VT> en = list[e];
       en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
     }
+    if (a.part) {
+      float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(blockIdx.z) * a.N + row) * a.d + c0);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      return;
+    }
     uint32_t p[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -144,8 +164,31 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   }
 }
 
+// Y[row] = bf16(sum over the tile ranges, in order, of part[z][row]) for TwELL rows.
+__global__ void __launch_bounds__(256)
+    spmm_reduce_kernel(const float* __restrict__ part, int nsplit, const int32_t* __restrict__ row_fb, int N, int d,
+                       uint16_t* __restrict__ out) {
+  const int64_t i8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (i8 >= static_cast<int64_t>(N) * d) return;
+  const int row = static_cast<int>(i8 / d);
+  if (row_fb[row] >= 0) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int z = 0; z < nsplit; ++z) {
+    const float4* src = reinterpret_cast<const float4*>(part + z * static_cast<int64_t>(N) * d + i8);
+    const float4 x = src[0], y = src[1];
+    acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+    acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+  }
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
+           (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
+  *reinterpret_cast<uint4*>(out + i8) = make_uint4(p[0], p[1], p[2], p[3]);
+}
+
 template <typename VT>
-int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaStream_t s) {
+int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kernel_id, cudaStream_t s) {
   if (a.N <= 0) return TWELL_OK;
   if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   if (a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;  // hidden unit fits the entry's 16 bits
@@ -161,25 +204,47 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaSt
       return TWELL_ERR_CUDA;
     attr[dev] = true;
   }
-  dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256);
+  if (nsplit < 1 || nsplit > 65535 || (nsplit > 1 && !a.part)) return TWELL_ERR_INVALID_ARG;
+  dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
+  SpmmArgs args = a;
+  if (nsplit == 1) args.part = nullptr;
   {
     LaunchScope ls(kernel_id, s);
-    kern<<<grid, kWarps * 32, smem, s>>>(a, W, max_entries);
+    kern<<<grid, kWarps * 32, smem, s>>>(args, W, max_entries);
   }
-  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  if (nsplit > 1) {
+    const int64_t vec = static_cast<int64_t>(a.N) * a.d / 8;
+    LaunchScope ls(kernel_id, s);
+    spmm_reduce_kernel<<<static_cast<unsigned>((vec + 255) / 256), 256, 0, s>>>(a.part, nsplit, a.row_fb, a.N, a.d,
+                                                                               a.out);
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  }
+  return TWELL_OK;
 }
 
 }  // namespace
 
-int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s) {
-  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
-  return launch_spmm_rows<uint16_t>(a, W_down, TWELL_KERNEL_SPMM, s);
+// Tile ranges per row so that a small batch (at most kSwapMaxTokens rows)
+// still launches ~4096 warps (at most 16 ranges); larger batches are not split.
+int spmm_nsplit(int n_rows, int d_model) {
+  const int64_t warps = static_cast<int64_t>(n_rows) * ((d_model + 255) / 256);
+  if (warps <= 0 || n_rows > kSwapMaxTokens) return 1;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, (4096 + warps - 1) / warps)));
+}
+
+int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
+                cudaStream_t s) {
+  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, part, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap,
+             L.status};
+  return launch_spmm_rows<uint16_t>(a, W_down, nsplit, TWELL_KERNEL_SPMM, s);
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s) {
-  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
-  return launch_spmm_rows<float>(a, W, kernel_id, s);
+  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap,
+             L.status};
+  return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
 }
 
 }  // namespace twell

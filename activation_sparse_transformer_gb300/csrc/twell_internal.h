@@ -94,6 +94,16 @@ struct PartialEpiParams {
   int64_t split_stride;
 };
 
+// fp32 partial sums of one K split with the operands swapped (accumulator rows
+// are hidden units, columns are tokens): part[ks * split_stride + token * ld + unit],
+// tokens from n_tok on are not stored.
+struct PartialTEpiParams {
+  float* part;
+  int64_t ld;
+  int64_t split_stride;
+  int32_t n_tok;
+};
+
 // dH = dY . W_down^T sampled at the TwELL pattern (the ReLU mask), plus the
 // L1 gradient: dZ = dH + lambda where h > 0.
 struct SampleEpiParams {
@@ -134,13 +144,25 @@ int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K
 // and nothing is written when k_mul * (*K_dev) is 0.
 int launch_gemm_store_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,
                          float* out, int64_t ld, int32_t* status, int kernel_id, cudaStream_t s);
-int choose_fb_ksplit(int K);   // K splits used for the fallback rows' down-projection
+int choose_fb_ksplit(int K, int max_split = 4);   // K splits used for the fallback rows' down-projection
+// Small-batch up-projection with the operands swapped: Z^T = W . X^T as
+// part[ks][token][unit] fp32 partial sums over ksplit K ranges.  W is [M][K]
+// row-major (M hidden units), X is [n_tok][K] row-major with n_tok <= kSwapMaxTokens.
+constexpr int kSwapMaxTokens = 32;
+int swap_ksplit(int K);
+int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_tok, int K, int ksplit,
+                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 
 // forward helpers (fwd_kernels.cu)
 int launch_route(const twell_t& L, cudaStream_t s);
 int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* spill_count, int32_t spill_cap,
                        cudaStream_t s);
-int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, cudaStream_t s);
+// Y = H . W_down for the TwELL rows.  With nsplit > 1 each row's tiles are
+// cut into nsplit consecutive ranges whose fp32 partial sums go to part
+// ([nsplit][N][d_model]) and are added in range order (small batches).
+int spmm_nsplit(int n_rows, int d_model);
+int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
+                cudaStream_t s);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
@@ -152,6 +174,11 @@ int launch_fb_down(const twell_t& L, const uint16_t* W_down, int d_model, uint16
 // standalone pack / unpack (pack_kernels.cu)
 int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);
 int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);
+// h = bf16(relu(sum over ksplit of part[ks][token][unit] + b[unit])) for every
+// token, packed like launch_pack_cells (overflowing rows flagged) and also
+// written densely to H [n_rows][d_ff] for the fallback copy.
+int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint16_t* H, const twell_t& L,
+                         cudaStream_t s);
 int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 
 // backward (bwd_kernels.cu)

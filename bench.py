@@ -205,10 +205,13 @@ def bench_ours(args, rank, world, local):
     clocks.start()
     launches0 = tw.twell_launch_count()
     t_wall = time.perf_counter()
-    step_ms = timed(step, args.steps, profile=True)
+    step_ms = timed(step, args.steps)
     wall = time.perf_counter() - t_wall
     launches = tw.twell_launch_count() - launches0
     clk = clocks.stop()
+    # per-kernel breakdown from a separate pass with an event pair around every
+    # launch (kept out of the timed steps above)
+    timed(step, min(args.steps, 20), profile=True)
     per_kernel = {}
     for name in tw.KERNELS:
         n, ms = tw.twell_profile_read(name)
@@ -336,6 +339,8 @@ def bench_next(args):
         return statistics.median(a.elapsed_time(b) for a, b in ev)
 
     cfgs = [synth.CONFIGS["gated"]] + synth.decode_sweep()
+    if args.only:
+        cfgs = [c for c in cfgs if c.name in args.only.split(",")]
     for cfg in cfgs:
         inp = synth.make_ffn_inputs(cfg)
         N, d, f, T, C = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap
@@ -356,6 +361,15 @@ def bench_next(args):
         n_fb = int(packed.n_fb[0].item())
         nnz = int(packed.counts.to(torch.int64).sum().item())
         ms = timed(fn, args.steps)
+        tw.twell_profile_reset()
+        tw.twell_profile_enable(True)
+        timed(fn, min(args.steps, 20))
+        tw.twell_profile_enable(False)
+        kernels = {}
+        for name in tw.KERNELS:
+            n_l, k_ms = tw.twell_profile_read(name)
+            if n_l:
+                kernels[name] = {"launches": n_l, "avg_us": round(1000.0 * k_ms / n_l, 2)}
         # the same call captured once in a CUDA graph and replayed (no host
         # launch overhead per kernel): what a decode loop would run
         graph = torch.cuda.CUDAGraph()
@@ -389,6 +403,7 @@ def bench_next(args):
                        "sparsity_target": cfg.sparsity, "gated": cfg.gated,
                        "l2": "flushed between steps (2x L2 write)"},
             "layer": {"n_fb": n_fb, "twell_entries": nnz},
+            "kernels": kernels,
             "roofline": {"bound": bound, "time_us": round(roof_us, 2), "frac": round(roof_us / (ms * 1e3), 4),
                          "frac_graph": round(roof_us / (ms_graph * 1e3), 4), "peak_source": peak_src},
         }), flush=True)
@@ -470,6 +485,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="with --next: comma-separated workload names to run (default: all)")
     ap.add_argument("--next", action="store_true",
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
     args = ap.parse_args()

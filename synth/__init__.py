@@ -167,7 +167,9 @@ def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None) -> dict:
             forced = np.sort(rng.choice(n, size=n_forced, replace=False))
             target[forced] = cfg.forced_activity
         active = np.maximum(1, np.rint(target * f)).astype(np.int64)
-        s = _row_scales(u, b, active)
+        # the scales act on this batch's own pre-activations (not the calibration batch's)
+        u_rows = u if not cfg.calib_rows else bf16_bits_to_f32(x0) @ bf16_bits_to_f32(w_in_t).T
+        s = _row_scales(u_rows, b, active)
         x = f32_to_bf16_bits((bf16_bits_to_f32(x0) * s[:, None]).astype(np.float32))
     else:
         x = x0
