@@ -822,7 +822,7 @@ int choose_fb_ksplit(int K, int max_split) {
   return ks;
 }
 
-int swap_ksplit(int K) { return choose_fb_ksplit(K, 16); }
+int swap_ksplit(int K) { return choose_fb_ksplit(K, 8); }
 
 int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_tok, int K, int ksplit,
                              const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {

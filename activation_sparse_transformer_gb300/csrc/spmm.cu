@@ -164,27 +164,28 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   }
 }
 
-// Y[row] = bf16(sum over the tile ranges, in order, of part[z][row]) for TwELL rows.
+// Y[row] = bf16(sum over the tile ranges, in order, of part[z][row]) for
+// TwELL rows; a thread owns 4 columns (more threads in flight for the few
+// rows of a small batch).
 __global__ void __launch_bounds__(256)
     spmm_reduce_kernel(const float* __restrict__ part, int nsplit, const int32_t* __restrict__ row_fb, int N, int d,
                        uint16_t* __restrict__ out) {
-  const int64_t i8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (i8 >= static_cast<int64_t>(N) * d) return;
-  const int row = static_cast<int>(i8 / d);
+  const int64_t i4 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= static_cast<int64_t>(N) * d) return;
+  const int row = static_cast<int>(i4 / d);
   if (row_fb[row] >= 0) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t stride = static_cast<int64_t>(N) * d;
+#pragma unroll 8
   for (int z = 0; z < nsplit; ++z) {
-    const float4* src = reinterpret_cast<const float4*>(part + z * static_cast<int64_t>(N) * d + i8);
-    const float4 x = src[0], y = src[1];
-    acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
-    acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+    const float4 x = *reinterpret_cast<const float4*>(part + z * stride + i4);
+    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
   }
-  uint32_t p[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
-           (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
-  *reinterpret_cast<uint4*>(out + i8) = make_uint4(p[0], p[1], p[2], p[3]);
+  const uint32_t lo = static_cast<uint32_t>(float_to_bf16_bits(acc.x)) |
+                      (static_cast<uint32_t>(float_to_bf16_bits(acc.y)) << 16);
+  const uint32_t hi = static_cast<uint32_t>(float_to_bf16_bits(acc.z)) |
+                      (static_cast<uint32_t>(float_to_bf16_bits(acc.w)) << 16);
+  *reinterpret_cast<uint2*>(out + i4) = make_uint2(lo, hi);
 }
 
 template <typename VT>
@@ -214,7 +215,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   }
   if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
   if (nsplit > 1) {
-    const int64_t vec = static_cast<int64_t>(a.N) * a.d / 8;
+    const int64_t vec = static_cast<int64_t>(a.N) * a.d / 4;
     LaunchScope ls(kernel_id, s);
     spmm_reduce_kernel<<<static_cast<unsigned>((vec + 255) / 256), 256, 0, s>>>(a.part, nsplit, a.row_fb, a.N, a.d,
                                                                                a.out);
