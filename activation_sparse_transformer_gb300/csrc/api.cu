@@ -271,7 +271,7 @@ struct FwdWorkspace {
   int ksplit;                // fallback down-projection K splits
   bool swap;                 // small batch: swapped-operand up-projection
   int up_ksplit;
-  size_t up_part_off, h_off;
+  size_t up_part_off, h_off, arrivals_off;
   int spmm_nsplit;
   size_t spmm_part_off;
 };
@@ -300,6 +300,11 @@ FwdWorkspace fwd_workspace_layout(int32_t n_rows, int32_t d_model, int32_t d_ff,
     off += align256(sizeof(uint16_t) * static_cast<size_t>(n_rows) * d_ff);
   }
   w.spmm_nsplit = n_rows > 0 ? spmm_nsplit(n_rows, d_model) : 1;
+  if (w.swap || w.spmm_nsplit > 1) {
+    // arrival counters: [0] the pack pass, [64, 64 + kSpmmMaxArrivals) the SpMM ranges
+    w.arrivals_off = off;
+    off += align256(sizeof(int32_t) * (64 + kSpmmMaxArrivals));
+  }
   if (w.spmm_nsplit > 1) {
     w.spmm_part_off = off;
     off += align256(sizeof(float) * static_cast<size_t>(w.spmm_nsplit) * n_rows * d_model);
@@ -347,8 +352,15 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   float* part = reinterpret_cast<float*>(ws + w.part_off);
   float* spmm_part = w.spmm_nsplit > 1 ? reinterpret_cast<float*>(ws + w.spmm_part_off) : nullptr;
   uint16_t* Hd = w.swap ? reinterpret_cast<uint16_t*>(ws + w.h_off) : nullptr;
-  TW_TRY(reset_words(H, s));
   const bool swap = w.swap && !W_uT;
+  int32_t* arrivals = (w.swap || w.spmm_nsplit > 1) ? reinterpret_cast<int32_t*>(ws + w.arrivals_off) : nullptr;
+  if (swap) {
+    // the up-projection's CTA 0 zeroes row_fb and the arrival counters
+    TW_CUDA(cudaMemsetAsync(H->status, 0, sizeof(int32_t), s));
+  } else {
+    TW_TRY(reset_words(H, s));
+    if (arrivals) TW_CUDA(cudaMemsetAsync(arrivals, 0, sizeof(int32_t) * (64 + kSpmmMaxArrivals), s));
+  }
   if (swap) {
     // small batch: Z^T = W_in^T . X^T with the hidden units on the 128-row
     // MMA side and K split so the weight stream covers every SM; the partial
@@ -357,8 +369,9 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     float* up_part = reinterpret_cast<float*>(ws + w.up_part_off);
     PartialTEpiParams tp{up_part, d_ff, static_cast<int64_t>(n_rows) * d_ff, n_rows};
     TW_TRY(launch_gemm_swap_partial(W_inT, X, d_ff, n_rows, d_model, w.up_ksplit, tp, H->status,
-                                    TWELL_KERNEL_UP_PACK, s));
-    TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, s));
+                                    TWELL_KERNEL_UP_PACK, s, H->row_fb, n_rows, arrivals, 64 + kSpmmMaxArrivals));
+    // the last CTA of the pack pass also routes the rows
+    TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, arrivals, s));
   } else {
     TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
     PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
@@ -367,8 +380,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
     else
       TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
+    TW_TRY(launch_route(*H, s));
   }
-  TW_TRY(launch_route(*H, s));
   {
     // the dense-fallback rows (assembly or copy + tensor-core down-projection)
     // run on a second stream while the gather-SpMM handles the TwELL rows
@@ -379,7 +392,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     else
       TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
     TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
-    TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, s));
+    TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr, s));
     TW_TRY(fork.join());
   }
   return TWELL_OK;

@@ -64,6 +64,12 @@ struct GemmArgs {
   int k_mul;
   int32_t* status;
   uint64_t wait_limit_ns;
+  // words that CTA 0 sets to zero for the kernels that follow on the stream
+  // (saves separate memset launches on short latency-bound paths)
+  int32_t* zero0;
+  int n_zero0;
+  int32_t* zero1;
+  int n_zero1;
 };
 
 // Row i of a 32-column TMEM chunk, picked with a select tree (no local memory).
@@ -563,6 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = num_k > 0 ? num_m * num_n * args.ksplit : 0;
   const int k_per = (num_k + args.ksplit - 1) / args.ksplit;
 
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < args.n_zero0; i += blockDim.x) args.zero0[i] = 0;
+    for (int i = threadIdx.x; i < args.n_zero1; i += blockDim.x) args.zero1[i] = 0;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -734,7 +744,8 @@ template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K, int ksplit,
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
                 const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0, const uint16_t* B2 = nullptr,
-                int b_rows = 0) {
+                int b_rows = 0, int32_t* zero0 = nullptr, int n_zero0 = 0, int32_t* zero1 = nullptr,
+                int n_zero1 = 0) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
@@ -779,7 +790,8 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   }
   const int units = ((M + kBM - 1) / kBM) * (N / (Epi::kDualB ? BN / 2 : BN)) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
-  GemmArgs args{M, M_dev, N, K, ksplit, K_dev, k_mul, status, kWaitLimitNs};
+  GemmArgs args{M,      M_dev,        N,     K,       ksplit, K_dev, k_mul, status, kWaitLimitNs,
+                zero0,  zero0 ? n_zero0 : 0, zero1, zero1 ? n_zero1 : 0};
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kThreads, smem, s>>>(ta, tb, tb2, args, p);
@@ -825,14 +837,15 @@ int choose_fb_ksplit(int K, int max_split) {
 int swap_ksplit(int K) { return choose_fb_ksplit(K, 8); }
 
 int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_tok, int K, int ksplit,
-                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
+                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s,
+                             int32_t* zero0, int n_zero0, int32_t* zero1, int n_zero1) {
   if (n_tok <= 0) return TWELL_OK;
-  if (n_tok > kSwapMaxTokens || M % kBM != 0) return TWELL_ERR_UNSUPPORTED;
+  if (n_tok > kSwapMaxTokens || M % kBM != 0 || K <= 0) return TWELL_ERR_UNSUPPORTED;
   if (n_tok <= 16)
     return launch_gemm<16, PartialTEpi, false, false>(W, X, M, nullptr, 16, K, ksplit, p, status, kernel_id, s,
-                                                      nullptr, 1, 0, nullptr, n_tok);
+                                                      nullptr, 1, 0, nullptr, n_tok, zero0, n_zero0, zero1, n_zero1);
   return launch_gemm<32, PartialTEpi, false, false>(W, X, M, nullptr, 32, K, ksplit, p, status, kernel_id, s, nullptr,
-                                                    1, 0, nullptr, n_tok);
+                                                    1, 0, nullptr, n_tok, zero0, n_zero0, zero1, n_zero1);
 }
 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,

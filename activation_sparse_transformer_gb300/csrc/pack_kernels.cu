@@ -100,43 +100,89 @@ __global__ void __launch_bounds__(kWarps * 32)
   pack_lane8(L, row, col, in, w);
 }
 
+// Routing of a small batch (at most 32 rows) by one CTA: the result of
+// route_kernel (fallback rows numbered in ascending row order, rows past
+// fb_cap left with empty cells, n_fb, the overflow status).
+__device__ void route_small(const Layout& L) {
+  __shared__ int slot_s[32];
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    const bool fl = r < L.N && __ldcg(&L.row_fb[r]) != 0;
+    const unsigned m = __ballot_sync(0xffffffffu, fl);
+    const int slot = __popc(m & ((1u << r) - 1u));
+    if (r < L.N) {
+      L.row_fb[r] = fl ? slot : -1;
+      if (fl && slot < L.fb_cap) L.fb_rows[slot] = r;
+    }
+    slot_s[r] = fl ? slot : -1;
+    if (r == 0) {
+      *L.n_fb = __popc(m);
+      if (__popc(m) > L.fb_cap) report_error(L.status, TWELL_ERR_FALLBACK_OVERFLOW);
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < L.N && r < 32; ++r) {
+    if (slot_s[r] < L.fb_cap) continue;  // TwELL row (-1) or stored fallback row
+    const int64_t cell0 = static_cast<int64_t>(r) * L.nt;
+    for (int c = threadIdx.x; c < L.nt; c += blockDim.x) L.counts[cell0 + c] = 0;
+    for (int c = threadIdx.x; c < L.nt * L.C; c += blockDim.x) {
+      L.values[cell0 * L.C + c] = 0;
+      L.idx[cell0 * L.C + c] = 0;
+    }
+  }
+}
+
 // Small-batch variant: z = sum of the K-split partial sums (split order) +
 // b, h = bf16(z) where z > 2^-134 (the smallest z whose bf16 rounding is not
-// zero), else +0; h is also stored densely in H for the fallback copy.
+// zero), else +0; h is also stored densely in H for the fallback copy.  With
+// an arrival counter (zeroed, at most 32 rows) the CTA that finishes last
+// also routes the rows, so no separate routing launch is needed.
 __global__ void __launch_bounds__(kWarps * 32)
     pack_partials_kernel(Layout L, const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ b,
-                         uint16_t* __restrict__ H) {
+                         uint16_t* __restrict__ H, int32_t* arrivals) {
+  __shared__ int last_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int segs = (L.f + 255) / 256;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= static_cast<int64_t>(L.N) * segs) return;
-  const int row = static_cast<int>(gw / segs);
-  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
-  const bool in = col < L.f;
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  if (in) {
-    float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const int64_t split = static_cast<int64_t>(L.N) * L.f;
-    const float* p = part + static_cast<int64_t>(row) * L.f + col;
+  if (gw < static_cast<int64_t>(L.N) * segs) {  // whole warps
+    const int row = static_cast<int>(gw / segs);
+    const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
+    const bool in = col < L.f;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (in) {
+      float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const int64_t split = static_cast<int64_t>(L.N) * L.f;
+      const float* p = part + static_cast<int64_t>(row) * L.f + col;
 #pragma unroll 4
-    for (int ks = 0; ks < ksplit; ++ks) {
-      const float4 a = *reinterpret_cast<const float4*>(p + ks * split);
-      const float4 c = *reinterpret_cast<const float4*>(p + ks * split + 4);
-      z[0] += a.x; z[1] += a.y; z[2] += a.z; z[3] += a.w;
-      z[4] += c.x; z[5] += c.y; z[6] += c.z; z[7] += c.w;
-    }
-    const uint4 bq = __ldg(reinterpret_cast<const uint4*>(b + col));
-    const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
-    const float thr = __uint_as_float(0x00008000u);
+      for (int ks = 0; ks < ksplit; ++ks) {
+        const float4 a = *reinterpret_cast<const float4*>(p + ks * split);
+        const float4 c = *reinterpret_cast<const float4*>(p + ks * split + 4);
+        z[0] += a.x; z[1] += a.y; z[2] += a.z; z[3] += a.w;
+        z[4] += c.x; z[5] += c.y; z[6] += c.z; z[7] += c.w;
+      }
+      const uint4 bq = __ldg(reinterpret_cast<const uint4*>(b + col));
+      const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
+      const float thr = __uint_as_float(0x00008000u);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float zb = z[k] + ((k & 1) ? bf16_hi(bw[k / 2]) : bf16_lo(bw[k / 2]));
-      const uint32_t h = zb > thr ? float_to_bf16_bits(zb) : 0u;
-      w[k / 2] |= (k & 1) ? (h << 16) : h;
+      for (int k = 0; k < 8; ++k) {
+        const float zb = z[k] + ((k & 1) ? bf16_hi(bw[k / 2]) : bf16_lo(bw[k / 2]));
+        const uint32_t h = zb > thr ? float_to_bf16_bits(zb) : 0u;
+        w[k / 2] |= (k & 1) ? (h << 16) : h;
+      }
+      *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * L.f + col) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * L.f + col) = make_uint4(w[0], w[1], w[2], w[3]);
+    pack_lane8(L, row, col, in, w);
   }
-  pack_lane8(L, row, col, in, w);
+  if (!arrivals) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last_s = atomicAdd(arrivals, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  route_small(L);
 }
 
 // Fallback rows: copy the dense row, clear the row's cells.
@@ -204,12 +250,13 @@ int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStre
 }
 
 int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint16_t* H, const twell_t& L,
-                         cudaStream_t s) {
+                         int32_t* arrivals, cudaStream_t s) {
   const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
   if (blocks <= 0) return TWELL_OK;
   if (blocks > 0x7FFFFFFF || L.d_ff % 8 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (arrivals && L.n_rows > 32) return TWELL_ERR_UNSUPPORTED;
   LaunchScope ls(TWELL_KERNEL_PACK, s);
-  pack_partials_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), part, ksplit, b, H);
+  pack_partials_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), part, ksplit, b, H, arrivals);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

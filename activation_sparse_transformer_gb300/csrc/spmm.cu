@@ -20,8 +20,9 @@
 //
 // Small batches have too few (row, 256-column) warps to fill the GPU, so the
 // row's tiles are cut into gridDim.z consecutive ranges (each warp flattens
-// and streams only its range); each range's fp32 sums go to a partial buffer
-// and spmm_reduce_kernel adds the ranges in order.
+// and streams only its range); each range's fp32 sums go to a partial buffer,
+// and the last CTA to finish among the ranges of a (row block, column block)
+// adds them in range order (an arrival counter, no waiting).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -34,6 +35,7 @@ namespace {
 
 constexpr int kWarps = 8;  // rows per CTA
 constexpr int kU = 8;      // W row loads in flight per lane
+constexpr int kMaxDynSmem = 224 * 1024;  // entry lists; the rest of the 227 KB holds the static words
 
 struct SpmmArgs {
   const void* values;     // [N][nt][C] VT
@@ -42,6 +44,7 @@ struct SpmmArgs {
   const int32_t* row_fb;  // [N]: rows >= 0 are fallback rows, left to the fallback path
   uint16_t* out;          // [N][d] bf16
   float* part;            // [gridDim.z][N][d] fp32 when the tiles are split into ranges, else null
+  int32_t* arrivals;      // [gridDim.x][gridDim.y] zeroed counters when the tiles are split
   int N, d, nt, T, C;
   int32_t* status;
 };
@@ -88,104 +91,113 @@ struct RowEntry<float> {
   __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const { fma8(acc, v, wr); }
 };
 
+__device__ __forceinline__ uint4 pack8_bf16(const float (&acc)[8]) {
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
+           (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
+  return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
 // max_entries = n_tiles * C bounds the entries a row can store.
 template <typename VT>
 __global__ void __launch_bounds__(kWarps * 32, 3)
     spmm_row_kernel(const SpmmArgs a, const uint16_t* __restrict__ W, int max_entries) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int last_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw) + warp * max_entries;
   const int row = blockIdx.x * kWarps + warp;
-  if (row >= a.N) return;
-  if (a.row_fb[row] >= 0) return;  // written by the fallback path, which may run concurrently
+  // fallback rows are written by the fallback path, which may run concurrently
+  const bool work = row < a.N && a.row_fb[row] < 0;
   const int c0 = blockIdx.y * 256 + lane * 8;
-  const bool active = c0 < a.d;
-  const VT* vals = static_cast<const VT*>(a.values);
-  const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
-
-  // ---- this warp's tiles: all of them, or one of gridDim.z consecutive ranges
-  int t_beg = 0, t_end = a.nt;
-  if (gridDim.z > 1) {
-    const int per = (a.nt + gridDim.z - 1) / gridDim.z;
-    t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
-    t_end = min(a.nt, t_beg + per);
-  }
-
-  // ---- flatten: tiles in order, 32 per round
-  int total = 0;
-  for (int t0 = t_beg; t0 < t_end; t0 += 32) {
-    const int t = t0 + lane;
-    const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
-    }
-    const int base = total + incl - cnt;
-    const int64_t cell = cell0 + t;
-    for (int s = 0; s < cnt; ++s) list[base + s] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s], vals[cell * a.C + s]);
-    total += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  __syncwarp();
-
-  // ---- stream the named W rows, kU loads in flight
+  const bool active = work && c0 < a.d;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (active) {
-    const uint16_t* wcol = W + c0;
-    int e = 0;
-    for (; e + kU <= total; e += kU) {
-      uint4 w[kU];
-      RowEntry<VT> en[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        en[u] = list[e + u];
-        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
-    }
-    for (; e < total; ++e) {
-      const RowEntry<VT> en = list[e];
-      en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
-    }
-    if (a.part) {
-      float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(blockIdx.z) * a.N + row) * a.d + c0);
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      return;
-    }
-    uint32_t p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      p[i] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i])) |
-             (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * i + 1])) << 16);
-    *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = make_uint4(p[0], p[1], p[2], p[3]);
-  }
-}
 
-// Y[row] = bf16(sum over the tile ranges, in order, of part[z][row]) for
-// TwELL rows; a thread owns 4 columns (more threads in flight for the few
-// rows of a small batch).
-__global__ void __launch_bounds__(256)
-    spmm_reduce_kernel(const float* __restrict__ part, int nsplit, const int32_t* __restrict__ row_fb, int N, int d,
-                       uint16_t* __restrict__ out) {
-  const int64_t i4 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
-  if (i4 >= static_cast<int64_t>(N) * d) return;
-  const int row = static_cast<int>(i4 / d);
-  if (row_fb[row] >= 0) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t stride = static_cast<int64_t>(N) * d;
-#pragma unroll 8
-  for (int z = 0; z < nsplit; ++z) {
-    const float4 x = *reinterpret_cast<const float4*>(part + z * stride + i4);
-    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+  if (work) {
+    const VT* vals = static_cast<const VT*>(a.values);
+    const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+
+    // ---- this warp's tiles: all of them, or one of gridDim.z consecutive ranges
+    int t_beg = 0, t_end = a.nt;
+    if (gridDim.z > 1) {
+      const int per = (a.nt + gridDim.z - 1) / gridDim.z;
+      t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
+      t_end = min(a.nt, t_beg + per);
+    }
+
+    // ---- flatten: tiles in order, 32 per round
+    int total = 0;
+    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+      const int t = t0 + lane;
+      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      const int base = total + incl - cnt;
+      const int64_t cell = cell0 + t;
+      for (int s = 0; s < cnt; ++s)
+        list[base + s] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s], vals[cell * a.C + s]);
+      total += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncwarp();
+
+    // ---- stream the named W rows, kU loads in flight
+    if (active) {
+      const uint16_t* wcol = W + c0;
+      int e = 0;
+      for (; e + kU <= total; e += kU) {
+        uint4 w[kU];
+        RowEntry<VT> en[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          en[u] = list[e + u];
+          w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
+      }
+      for (; e < total; ++e) {
+        const RowEntry<VT> en = list[e];
+        en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+      }
+    }
   }
-  const uint32_t lo = static_cast<uint32_t>(float_to_bf16_bits(acc.x)) |
-                      (static_cast<uint32_t>(float_to_bf16_bits(acc.y)) << 16);
-  const uint32_t hi = static_cast<uint32_t>(float_to_bf16_bits(acc.z)) |
-                      (static_cast<uint32_t>(float_to_bf16_bits(acc.w)) << 16);
-  *reinterpret_cast<uint2*>(out + i4) = make_uint2(lo, hi);
+  if (gridDim.z == 1) {
+    if (active) *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
+    return;
+  }
+
+  // ---- tile ranges: store this range's sums; the CTA that finishes last among
+  // the gridDim.z ranges of this (row block, column block) adds them in range
+  // order and writes Y (no waiting: the others have already left)
+  if (active) {
+    float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(blockIdx.z) * a.N + row) * a.d + c0);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int done = atomicAdd(a.arrivals + blockIdx.x * gridDim.y + blockIdx.y, 1);
+    last_s = done == static_cast<int>(gridDim.z) - 1;
+  }
+  __syncthreads();
+  if (!last_s || !active) return;
+  __threadfence();
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int z = 0; z < static_cast<int>(gridDim.z); ++z) {
+    const float4* src = reinterpret_cast<const float4*>(a.part + (static_cast<int64_t>(z) * a.N + row) * a.d + c0);
+    const float4 x = __ldcg(src), y = __ldcg(src + 1);
+    sum[0] += x.x; sum[1] += x.y; sum[2] += x.z; sum[3] += x.w;
+    sum[4] += y.x; sum[5] += y.y; sum[6] += y.z; sum[7] += y.w;
+  }
+  *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(sum);
 }
 
 template <typename VT>
@@ -195,33 +207,24 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   if (a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;  // hidden unit fits the entry's 16 bits
   const int max_entries = a.nt * a.C;
   const size_t smem = static_cast<size_t>(kWarps) * max_entries * sizeof(RowEntry<VT>);
-  if (smem > 227 * 1024) return TWELL_ERR_UNSUPPORTED;
+  if (smem > kMaxDynSmem) return TWELL_ERR_UNSUPPORTED;
   auto kern = spmm_row_kernel<VT>;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess)
       return TWELL_ERR_CUDA;
     attr[dev] = true;
   }
-  if (nsplit < 1 || nsplit > 65535 || (nsplit > 1 && !a.part)) return TWELL_ERR_INVALID_ARG;
+  if (nsplit < 1 || nsplit > 64 || (nsplit > 1 && (!a.part || !a.arrivals))) return TWELL_ERR_INVALID_ARG;
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
-  SpmmArgs args = a;
-  if (nsplit == 1) args.part = nullptr;
+  if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
   {
     LaunchScope ls(kernel_id, s);
-    kern<<<grid, kWarps * 32, smem, s>>>(args, W, max_entries);
+    kern<<<grid, kWarps * 32, smem, s>>>(a, W, max_entries);
   }
-  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
-  if (nsplit > 1) {
-    const int64_t vec = static_cast<int64_t>(a.N) * a.d / 4;
-    LaunchScope ls(kernel_id, s);
-    spmm_reduce_kernel<<<static_cast<unsigned>((vec + 255) / 256), 256, 0, s>>>(a.part, nsplit, a.row_fb, a.N, a.d,
-                                                                               a.out);
-    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
-  }
-  return TWELL_OK;
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
 }  // namespace
@@ -235,16 +238,16 @@ int spmm_nsplit(int n_rows, int d_model) {
 }
 
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                cudaStream_t s) {
-  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, part, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap,
-             L.status};
+                int32_t* arrivals, cudaStream_t s) {
+  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, part, arrivals, L.n_rows, d_model, L.d_ff / L.tile, L.tile,
+             L.cap, L.status};
   return launch_spmm_rows<uint16_t>(a, W_down, nsplit, TWELL_KERNEL_SPMM, s);
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s) {
-  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap,
-             L.status};
+  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, nullptr, L.n_rows, d_model, L.d_ff / L.tile, L.tile,
+             L.cap, L.status};
   return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
 }
 

@@ -150,8 +150,11 @@ int choose_fb_ksplit(int K, int max_split = 4);   // K splits used for the fallb
 // row-major (M hidden units), X is [n_tok][K] row-major with n_tok <= kSwapMaxTokens.
 constexpr int kSwapMaxTokens = 32;
 int swap_ksplit(int K);
+// CTA 0 also sets n_zero0 words at zero0 and n_zero1 at zero1 to zero (state
+// of the kernels that follow on the stream).
 int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_tok, int K, int ksplit,
-                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+                             const PartialTEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s,
+                             int32_t* zero0 = nullptr, int n_zero0 = 0, int32_t* zero1 = nullptr, int n_zero1 = 0);
 
 // forward helpers (fwd_kernels.cu)
 int launch_route(const twell_t& L, cudaStream_t s);
@@ -159,10 +162,12 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* s
                        cudaStream_t s);
 // Y = H . W_down for the TwELL rows.  With nsplit > 1 each row's tiles are
 // cut into nsplit consecutive ranges whose fp32 partial sums go to part
-// ([nsplit][N][d_model]) and are added in range order (small batches).
+// ([nsplit][N][d_model]) and are added in range order (small batches); the
+// arrival counters (kSpmmMaxArrivals int32) must be zero on entry.
+constexpr int kSpmmMaxArrivals = 1024;
 int spmm_nsplit(int n_rows, int d_model);
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                cudaStream_t s);
+                int32_t* arrivals, cudaStream_t s);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
@@ -176,9 +181,11 @@ int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStre
 int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s);
 // h = bf16(relu(sum over ksplit of part[ks][token][unit] + b[unit])) for every
 // token, packed like launch_pack_cells (overflowing rows flagged) and also
-// written densely to H [n_rows][d_ff] for the fallback copy.
+// written densely to H [n_rows][d_ff] for the fallback copy.  With an arrival
+// counter (one int32 of workspace, zero on entry; n_rows <= 32) the rows are
+// also routed, as launch_route would.
 int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint16_t* H, const twell_t& L,
-                         cudaStream_t s);
+                         int32_t* arrivals, cudaStream_t s);
 int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 
 // backward (bwd_kernels.cu)
