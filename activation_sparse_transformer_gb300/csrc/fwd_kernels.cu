@@ -113,39 +113,44 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
   }
 }
 
-// One CTA per fallback slot (grid-stride), a warp per tile: the dense tile
-// comes from the spill buffer when the cell overflowed, else it is rebuilt
-// from the cell's entries; then the cell becomes empty (count 0, padding).
+// A warp per (fallback slot, tile), grid-stride over all of them: the dense
+// tile comes from the spill buffer when the cell overflowed, else it is
+// rebuilt from the cell's entries; then the cell becomes empty (count 0,
+// padding).  Every (slot, tile) is independent, so the few fallback rows still
+// spread over the whole GPU.
 __global__ void __launch_bounds__(256)
     fb_assemble_kernel(Layout L, const uint16_t* __restrict__ spill, int32_t spill_cap) {
   const int nfb = min(*L.n_fb, L.fb_cap);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int vec = L.T / 8;  // 16-byte vectors per tile
-  for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
+  const int64_t items = static_cast<int64_t>(nfb) * L.nt;
+  const int64_t gw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t gws = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t it = gw0; it < items; it += gws) {
+    const int slot = static_cast<int>(it / L.nt), t = static_cast<int>(it % L.nt);
     const int row = L.fb_rows[slot];
     uint16_t* out_row = L.fb_dense + static_cast<int64_t>(slot) * L.f;
-    for (int t = warp; t < L.nt; t += 8) {
-      const int64_t cell = static_cast<int64_t>(row) * L.nt + t;
-      const int cnt = L.counts[cell];
-      uint4* dst = reinterpret_cast<uint4*>(out_row + static_cast<int64_t>(t) * L.T);
-      if (cnt == kSpilledCell) {
-        const uint32_t s24 = static_cast<uint32_t>(L.values[cell * L.C]) |
-                             (static_cast<uint32_t>(L.idx[cell * L.C]) << 16);
-        const bool have = s24 < static_cast<uint32_t>(spill_cap);
-        const uint4* src = reinterpret_cast<const uint4*>(spill + static_cast<int64_t>(s24) * L.T);
-        for (int q = lane; q < vec; q += 32) dst[q] = have ? src[q] : make_uint4(0, 0, 0, 0);
-      } else {
-        for (int q = lane; q < vec; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        if (lane < cnt) out_row[static_cast<int64_t>(t) * L.T + L.idx[cell * L.C + lane]] = L.values[cell * L.C + lane];
-      }
+    const int64_t cell = static_cast<int64_t>(row) * L.nt + t;
+    const int cnt = L.counts[cell];
+    uint4* dst = reinterpret_cast<uint4*>(out_row + static_cast<int64_t>(t) * L.T);
+    if (cnt == kSpilledCell) {
+      const uint32_t s24 = static_cast<uint32_t>(L.values[cell * L.C]) |
+                           (static_cast<uint32_t>(L.idx[cell * L.C]) << 16);
+      const bool have = s24 < static_cast<uint32_t>(spill_cap);
+      const uint4* src = reinterpret_cast<const uint4*>(spill + static_cast<int64_t>(s24) * L.T);
+      for (int q = lane; q < vec; q += 32) dst[q] = have ? src[q] : make_uint4(0, 0, 0, 0);
+    } else {
+      for (int q = lane; q < vec; q += 32) dst[q] = make_uint4(0, 0, 0, 0);
       __syncwarp();
-      if (lane == 0) L.counts[cell] = 0;
-      for (int q = lane; q < L.C; q += 32) {
-        L.values[cell * L.C + q] = 0;
-        L.idx[cell * L.C + q] = 0;
-      }
+      if (lane < cnt) out_row[static_cast<int64_t>(t) * L.T + L.idx[cell * L.C + lane]] = L.values[cell * L.C + lane];
     }
+    __syncwarp();
+    if (lane == 0) L.counts[cell] = 0;
+    for (int q = lane; q < L.C; q += 32) {
+      L.values[cell * L.C + q] = 0;
+      L.idx[cell * L.C + q] = 0;
+    }
+    __syncwarp();
   }
 }
 
@@ -189,7 +194,8 @@ int launch_route(const twell_t& L, cudaStream_t s) {
 int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* /*spill_count*/,
                        int32_t spill_cap, cudaStream_t s) {
   if (L.fb_cap <= 0) return TWELL_OK;
-  const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
+  const int64_t warps = static_cast<int64_t>(L.fb_cap) * (L.d_ff / L.tile);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((warps + 7) / 8, 4 * sm_count())));
   LaunchScope ls(TWELL_KERNEL_FB_ASSEMBLE, s);
   fb_assemble_kernel<<<grid, 256, 0, s>>>(flat(L), spill, spill_cap);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;

@@ -402,28 +402,34 @@ struct DenseEpi {
   }
 };
 
+// fp32 tile store.  Each warp turns its 32 rows x 32 columns around in shared
+// memory (33-word rows: no bank conflicts either way) so that every store
+// instruction writes one full 128-byte row segment.
 struct PartialEpi {
   static constexpr bool kDualB = false;
   using Params = PartialEpiParams;
-  static constexpr uint32_t kSmemBytes = 0;
+  static constexpr int kPitch = 33;
+  static constexpr uint32_t kSmemBytes = (kEpiThreads / 32) * 32 * kPitch * 4;
 
   template <int BN>
   static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
-                                               int ks, uint8_t*, int) {
-    const bool valid = row < M;
-    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + static_cast<int64_t>(row) * p.ld + col0;
+                                               int ks, uint8_t* smem, int et) {
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;  // first row of this warp's 32
+    float* st = reinterpret_cast<float*>(smem) + (et >> 5) * 32 * kPitch;
+    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + col0 + lane;
 #pragma unroll 1
     for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
-      if (valid) {
-        float4* dst = reinterpret_cast<float4*>(base + c * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-      }
+      for (int i = 0; i < 32; ++i) st[lane * kPitch + i] = __uint_as_float(r[i]);
+      __syncwarp();
+#pragma unroll 4
+      for (int rr = 0; rr < 32; ++rr)
+        if (row0 + rr < M) base[static_cast<int64_t>(row0 + rr) * p.ld + c * 32] = st[rr * kPitch + lane];
+      __syncwarp();
     }
   }
 };
