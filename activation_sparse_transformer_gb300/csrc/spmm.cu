@@ -9,7 +9,8 @@
 // a token block buys almost no reuse unless the block holds thousands of
 // tokens (far more accumulators than an SM has registers).  The kernel is
 // therefore built for memory-level parallelism instead: a warp owns one token
-// row and 256 output columns.  It first flattens the row's stored entries
+// row and 256 output columns at a time (a persistent grid, warps striding over
+// the (row, column block) items).  It first flattens the row's stored entries
 // (tile-major, slots ascending, so hidden units ascend) into its shared-memory
 // list -- counts of 32 tiles per round, a warp prefix sum, each lane
 // expanding its own cell -- then streams the named W rows with coalesced
@@ -100,7 +101,64 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&acc)[8]) {
   return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
+// Sum of one row's stored entries in tiles [t_beg, t_end) times the W rows
+// they name, for this lane's 8 columns starting at c0 (the whole warp calls it
+// for one row; inactive lanes only help flatten).
+template <typename VT>
+__device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t* __restrict__ W, RowEntry<VT>* list,
+                                              int lane, int row, int c0, bool active, int t_beg, int t_end,
+                                              float (&acc)[8]) {
+  const VT* vals = static_cast<const VT*>(a.values);
+  const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+
+  // ---- flatten: tiles in order, 32 per round
+  int total = 0;
+  for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+    const int t = t0 + lane;
+    const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const int base = total + incl - cnt;
+    const int64_t cell = cell0 + t;
+    for (int s = 0; s < cnt; ++s)
+      list[base + s] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s], vals[cell * a.C + s]);
+    total += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+
+  // ---- stream the named W rows, kU loads in flight
+  if (active) {
+    const uint16_t* wcol = W + c0;
+    int e = 0;
+    for (; e + kU <= total; e += kU) {
+      uint4 w[kU];
+      RowEntry<VT> en[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        en[u] = list[e + u];
+        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
+    }
+    for (; e < total; ++e) {
+      const RowEntry<VT> en = list[e];
+      en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+    }
+  }
+  __syncwarp();  // the list is rewritten by the warp's next item
+}
+
 // max_entries = n_tiles * C bounds the entries a row can store.
+//
+// Whole rows (gridDim.z == 1): a persistent grid whose warps walk the (row,
+// 256-column block) items with a fixed stride, so a warp that drew short rows
+// takes the next item instead of idling until its CTA's longest row ends; the
+// 8 warps of a CTA start on the 8 column blocks of one row.
 template <typename VT>
 __global__ void __launch_bounds__(kWarps * 32, 3)
     spmm_row_kernel(const SpmmArgs a, const uint16_t* __restrict__ W, int max_entries) {
@@ -108,68 +166,34 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   __shared__ int last_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw) + warp * max_entries;
+
+  if (gridDim.z == 1) {
+    const int cbs = (a.d + 255) / 256;
+    const int64_t items = static_cast<int64_t>(a.N) * cbs;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp; it < items;
+         it += static_cast<int64_t>(gridDim.x) * kWarps) {
+      const int row = static_cast<int>(it / cbs);
+      if (a.row_fb[row] >= 0) continue;  // written by the fallback path, which may run concurrently
+      const int c0 = static_cast<int>(it % cbs) * 256 + lane * 8;
+      const bool active = c0 < a.d;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      row_block_sum<VT>(a, W, list, lane, row, c0, active, 0, a.nt, acc);
+      if (active) *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
+    }
+    return;
+  }
+
   const int row = blockIdx.x * kWarps + warp;
-  // fallback rows are written by the fallback path, which may run concurrently
   const bool work = row < a.N && a.row_fb[row] < 0;
   const int c0 = blockIdx.y * 256 + lane * 8;
   const bool active = work && c0 < a.d;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-
   if (work) {
-    const VT* vals = static_cast<const VT*>(a.values);
-    const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
-
-    // ---- this warp's tiles: all of them, or one of gridDim.z consecutive ranges
-    int t_beg = 0, t_end = a.nt;
-    if (gridDim.z > 1) {
-      const int per = (a.nt + gridDim.z - 1) / gridDim.z;
-      t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
-      t_end = min(a.nt, t_beg + per);
-    }
-
-    // ---- flatten: tiles in order, 32 per round
-    int total = 0;
-    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
-      const int t = t0 + lane;
-      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += x;
-      }
-      const int base = total + incl - cnt;
-      const int64_t cell = cell0 + t;
-      for (int s = 0; s < cnt; ++s)
-        list[base + s] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s], vals[cell * a.C + s]);
-      total += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    __syncwarp();
-
-    // ---- stream the named W rows, kU loads in flight
-    if (active) {
-      const uint16_t* wcol = W + c0;
-      int e = 0;
-      for (; e + kU <= total; e += kU) {
-        uint4 w[kU];
-        RowEntry<VT> en[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          en[u] = list[e + u];
-          w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
-      }
-      for (; e < total; ++e) {
-        const RowEntry<VT> en = list[e];
-        en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
-      }
-    }
-  }
-  if (gridDim.z == 1) {
-    if (active) *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
-    return;
+    // this warp's range of tiles, one of gridDim.z consecutive ranges
+    const int per = (a.nt + gridDim.z - 1) / gridDim.z;
+    const int t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
+    const int t_end = min(a.nt, t_beg + per);
+    row_block_sum<VT>(a, W, list, lane, row, c0, active, t_beg, t_end, acc);
   }
 
   // ---- tile ranges: store this range's sums; the CTA that finishes last among
@@ -220,6 +244,13 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   if (nsplit < 1 || nsplit > 64 || (nsplit > 1 && (!a.part || !a.arrivals))) return TWELL_ERR_INVALID_ARG;
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
+  if (nsplit == 1) {
+    // persistent: three CTAs per SM (the register limit), warps stride over the items
+    const int64_t items = static_cast<int64_t>(a.N) * ((a.d + 255) / 256);
+    grid = dim3(static_cast<unsigned>(std::max<int64_t>(
+                    1, std::min<int64_t>((items + kWarps - 1) / kWarps, 3 * static_cast<int64_t>(sm_count())))),
+                1, 1);
+  }
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kWarps * 32, smem, s>>>(a, W, max_entries);
