@@ -302,17 +302,20 @@ __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, con
   }
 }
 
-// db[j] += sum over the fallback slots of dZ_fb[slot][j]: a CTA covers 32
-// units, warp w sums slots w, w + 8, ... and the eight partial sums are added
-// in warp order (a fixed order, so the result is deterministic).
-__global__ void __launch_bounds__(256) fb_db_kernel(Layout L, const float* __restrict__ dz_fb, float* __restrict__ db) {
+// db[j] += sum over the fallback slots of dZ[slot][j] (= high + low part): a
+// CTA covers 32 units, warp w sums slots w, w + 8, ... and the eight partial
+// sums are added in warp order (a fixed order, so the result is deterministic).
+__global__ void __launch_bounds__(256) fb_db_kernel(Layout L, const uint16_t* __restrict__ dz_hl,
+                                                    float* __restrict__ db) {
   __shared__ float part[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * 32 + lane;
   const int nfb = min(*L.n_fb, L.fb_cap);
   float s = 0.f;
   if (j < L.f)
-    for (int slot = warp; slot < nfb; slot += 8) s += dz_fb[static_cast<int64_t>(slot) * L.f + j];
+    for (int slot = warp; slot < nfb; slot += 8)
+      s += bf16_bits_to_float(dz_hl[static_cast<int64_t>(2 * slot) * L.f + j]) +
+           bf16_bits_to_float(dz_hl[static_cast<int64_t>(2 * slot + 1) * L.f + j]);
   part[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && j < L.f) {
@@ -343,12 +346,11 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t padf = static_cast<size_t>(fb_pad) * d_ff;
   const size_t padd = static_cast<size_t>(fb_pad) * d_model;
   const size_t o_dzc = take(sizeof(float) * cells);
-  const size_t o_dzf = take(sizeof(float) * static_cast<size_t>(fb_cap) * d_ff);
   const size_t o_hl = take(sizeof(uint16_t) * 2 * padf);
   const size_t o_hfb = take(sizeof(uint16_t) * padf);
   const size_t o_dyg = take(sizeof(uint16_t) * padd);
   const size_t o_xg = take(sizeof(uint16_t) * 2 * padd);
-  const size_t o_part = take(sizeof(float) * 2 * ksplit * static_cast<size_t>(fb_cap) * d_model);
+  const size_t o_part = take(sizeof(float) * ksplit * static_cast<size_t>(fb_cap) * d_model);
   const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
   const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
   const size_t o_rows = take(sizeof(int32_t) * cells);
@@ -357,7 +359,6 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   if (ws && base) {
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
-    ws->dz_fb = reinterpret_cast<float*>(b + o_dzf);
     ws->dz_hl = reinterpret_cast<uint16_t*>(b + o_hl);
     ws->hfb = reinterpret_cast<uint16_t*>(b + o_hfb);
     ws->dyg = reinterpret_cast<uint16_t*>(b + o_dyg);
@@ -394,8 +395,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const int col_blocks = (d + 255) / 256;
   if (N > 0) {
     // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
-    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb,   Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
-                       Lh.tile,   Lh.cap, f,         lambda,      ws.dz_cells, ws.dz_fb,  ws.dz_hl};
+    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
+                       Lh.tile,   Lh.cap, f,         lambda,    ws.dz_cells, ws.dz_hl};
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
   }
   // Second stream: the fallback rows' weight-gradient share (stored into dW
@@ -422,15 +423,12 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_TRY_RC(fork.aux_to_main());  // dW holds the fallback share before dw_kernel runs
   if (N > 0) {
     if (fb) {
-      const int64_t split = static_cast<int64_t>(ws.ksplit) * Lh.fb_cap * d;
-      PartialEpiParams hi{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
-      PartialEpiParams lo{ws.part + split, d, static_cast<int64_t>(Lh.fb_cap) * d};
-      // the high and low parts are every other row of dz_hl
-      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, hi, Lh.status,
-                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f)));
-      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl + f, W_inT, Lh.fb_cap, Lh.n_fb, d, f, ws.ksplit, lo, Lh.status,
-                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f)));
-      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, 2 * ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
+      // one GEMM over K = 2 d_ff: row s of dz_hl viewed with stride 2 d_ff is
+      // [high_s | low_s], and both halves meet the same W_in^T rows (K wraps)
+      PartialEpiParams pp{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
+      TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl, W_inT, Lh.fb_cap, Lh.n_fb, d, 2 * f, ws.ksplit, pp, Lh.status,
+                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f), f));
+      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
     }
     TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, a));
   }
@@ -475,7 +473,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   if (fb) {
     LaunchScope ls(TWELL_KERNEL_DW, s);
-    fb_db_kernel<<<(f + 31) / 32, 256, 0, s>>>(L, ws.dz_fb, db);
+    fb_db_kernel<<<(f + 31) / 32, 256, 0, s>>>(L, ws.dz_hl, db);
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.join());

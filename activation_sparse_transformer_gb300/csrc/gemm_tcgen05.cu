@@ -70,6 +70,7 @@ struct GemmArgs {
   int n_zero0;
   int32_t* zero1;
   int n_zero1;
+  int b_k_wrap;  // N-major B: K row coordinate taken modulo this (0 = no wrap), a multiple of 64
 };
 
 // Row i of a 32-column TMEM chunk, picked with a select tree (no local memory).
@@ -502,8 +503,6 @@ struct SampleEpi {
         uint4 hq[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) hq[q] = hp[q];
-        const int64_t off = static_cast<int64_t>(fb) * p.d_ff + col;
-        float4* dst = reinterpret_cast<float4*>(p.dz_fb + off);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -525,7 +524,6 @@ struct SampleEpi {
               lo[i / 2] = lb;
             }
           }
-          dst[q] = make_float4(o[0], o[1], o[2], o[3]);
         }
         uint4* dh = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
         uint4* dl = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
@@ -637,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B is [K][N]: BN/64 boxes of 64 N-columns x 64 K-rows, 8 KB apart
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q)
-              tma_load_2d(sB + stage * Cfg::kBBytes + q * 8192, &tmB, &full[stage], n_blk * BN + q * 64, kb * kBK);
+              tma_load_2d(sB + stage * Cfg::kBBytes + q * 8192, &tmB, &full[stage], n_blk * BN + q * 64,
+                          args.b_k_wrap ? (kb * kBK) % args.b_k_wrap : kb * kBK);
           } else {
             tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, &full[stage], kb * kBK, n_blk * BN);
           }
@@ -751,7 +750,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
                 const typename Epi::Params& p, int32_t* status, int kernel_id, cudaStream_t s,
                 const int32_t* K_dev = nullptr, int k_mul = 1, int64_t lda = 0, const uint16_t* B2 = nullptr,
                 int b_rows = 0, int32_t* zero0 = nullptr, int n_zero0 = 0, int32_t* zero1 = nullptr,
-                int n_zero1 = 0) {
+                int n_zero1 = 0, int b_k_wrap = 0) {
   using Cfg = GemmCfg<BN>;
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
@@ -775,8 +774,9 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
     rc = encode_tmap_2d(&tb2, B2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2,
                         kBK, BN / 2);
   } else if (kBNMajor) {
-    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(N) * 2, 64,
-                        kBK);
+    if (b_k_wrap % kBK != 0 || b_k_wrap < 0) return TWELL_ERR_UNSUPPORTED;
+    rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(N), static_cast<uint64_t>(b_k_wrap ? b_k_wrap : K),
+                        static_cast<uint64_t>(N) * 2, 64, kBK);
   } else {
     // b_rows < N: the rows past b_rows are read as zeros (TMA fill)
     rc = encode_tmap_2d(&tb, B, static_cast<uint64_t>(K), static_cast<uint64_t>(b_rows > 0 ? b_rows : N),
@@ -797,7 +797,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   const int units = ((M + kBM - 1) / kBM) * (N / (Epi::kDualB ? BN / 2 : BN)) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
   GemmArgs args{M,      M_dev,        N,     K,       ksplit, K_dev, k_mul, status, kWaitLimitNs,
-                zero0,  zero0 ? n_zero0 : 0, zero1, zero1 ? n_zero1 : 0};
+                zero0,  zero0 ? n_zero0 : 0, zero1, zero1 ? n_zero1 : 0, b_k_wrap};
   {
     LaunchScope ls(kernel_id, s);
     kern<<<grid, kThreads, smem, s>>>(ta, tb, tb2, args, p);
@@ -856,10 +856,10 @@ int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_
 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
-                               cudaStream_t s, int64_t lda) {
+                               cudaStream_t s, int64_t lda, int b_k_wrap) {
   if (N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   return launch_gemm<128, PartialEpi, false, true>(A, B, M, M_dev, N, K, ksplit, p, status, kernel_id, s, nullptr, 1,
-                                                   lda);
+                                                   lda, nullptr, 0, nullptr, 0, nullptr, 0, b_k_wrap);
 }
 
 int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t* Bu, int M, int N, int K,

@@ -116,10 +116,9 @@ struct SampleEpiParams {
   int32_t n_tiles, tile, cap, d_ff;
   float lambda;
   float* dz_cells;          // [M][n_tiles][C] fp32, stored slots only
-  float* dz_fb;             // [fb_cap][d_ff] fp32, dense (0 where h == 0)
-  uint16_t* dz_hl;          // [2 * fb_pad][d_ff] bf16: row 2s = bf16(dz_fb[s]) (high part),
-                            // row 2s+1 = bf16(dz_fb[s] - high) (low part); high + low carry
-                            // dz to ~2^-17 relative
+  uint16_t* dz_hl;          // [2 * fb_pad][d_ff] bf16 for the fallback rows' dense dZ (0 where h == 0):
+                            // row 2s = bf16(dz) (high part), row 2s+1 = bf16(dz - high) (low
+                            // part); high + low carry dz to ~2^-17 relative
 };
 
 // C[M, N] = A[M, K] . B^T with A row-major [M][K] (K-major).  B is row-major
@@ -133,9 +132,11 @@ int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t
                            const PackEpiParams& p, int32_t* status, cudaStream_t s);
 int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int M, const int32_t* M_dev, int N,
                       int K, const DenseEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
+// b_k_wrap > 0: B holds b_k_wrap rows of K and row k of the product's K is
+// B's row k mod b_k_wrap (the same B against the high and low parts of A).
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
-                               cudaStream_t s, int64_t lda = 0);
+                               cudaStream_t s, int64_t lda = 0, int b_k_wrap = 0);
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s);
 // out[M][N] = A^T . B (fp32 store) with A row-major [K][M] and B row-major
@@ -191,13 +192,13 @@ int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
 // backward (bwd_kernels.cu)
 struct BwdWorkspace {
   float* dz_cells;        // [N][n_tiles][C] fp32: dZ at the stored TwELL entries
-  float* dz_fb;           // [fb_cap][d_ff] fp32: dZ of the fallback rows (0 off the pattern)
-  uint16_t* dz_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of dz_fb, interleaved by row
+  uint16_t* dz_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of the fallback rows' dZ
+                          // (0 off the pattern), interleaved by row
   uint16_t* hfb;          // [fb_pad][d_ff] fallback rows of H (zero past n_fb)
   uint16_t* dyg;          // [fb_pad][d_model] dY of the fallback rows (zero past n_fb)
   uint16_t* xg2;          // [2 * fb_pad][d_model] X of the fallback rows, each row twice
   int32_t fb_pad;         // fb_cap rounded up to 64
-  float* part;            // [2 * ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
+  float* part;            // [ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
   int32_t ksplit;
   int32_t* blk_count;     // [n_blocks][d_ff] entries per (row block, hidden unit), then offsets
   int32_t* col_ptr;       // [d_ff + 1] start of each hidden unit's entry list

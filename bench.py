@@ -61,6 +61,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.power = []
 
     def start(self):
         try:
@@ -87,7 +88,7 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -98,9 +99,14 @@ class ClockSampler:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[3]))
+            except ValueError:
+                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        self.power = pw
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
@@ -155,8 +161,11 @@ def bench_ours(args, rank, world, local):
     dWi = torch.empty((f, d), dtype=torch.float32, device=dev)
     dWd = torch.empty((f, d), dtype=torch.float32, device=dev)
     db = torch.empty((f,), dtype=torch.float32, device=dev)
-    wsf = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(tw.bwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
+    # one workspace serves the forward and the backward (nothing in the
+    # forward's outlives its call)
+    ws_bytes = max(tw.fwd_workspace_bytes(N, d, f, T, C, fb), tw.bwd_workspace_bytes(N, d, f, T, C, fb))
+    wsf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    wsb = wsf
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -233,6 +242,38 @@ def bench_ours(args, rank, world, local):
     dense_ms = timed(dense, max(3, args.steps // 2))
     del Hbuf
 
+    # energy per token: board power (nvidia-smi, this GPU) sampled over a
+    # back-to-back loop of at least ~0.6 s of each call (warm L2, no flush
+    # writes in the loop, so the flush's own energy is not counted)
+    def energy(fn, ms_each):
+        iters = max(50, int(600.0 / max(ms_each, 1e-3)))
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        smp = ClockSampler(local)
+        smp.start()
+        time.sleep(0.1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        smp.stop()
+        loop_ms = e0.elapsed_time(e1)
+        pw = smp.power[2:-1] if len(smp.power) > 4 else smp.power
+        if not pw:
+            return None
+        watts = statistics.median(pw)
+        return {"j_per_token": watts * loop_ms * 1e-3 / (iters * N), "power_w": round(watts, 1),
+                "ms_per_call": round(loop_ms / iters, 4), "samples": len(pw)}
+
+    en_step = energy(step, statistics.median(step_ms))
+    en_fwd = energy(fwd, statistics.median(fwd_ms))
+    Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+    en_dense = energy(dense, statistics.median(dense_ms))
+    del Hbuf
+
     # end to end through the C ABI with host buffers (pinned), copies timed
     hX = torch.from_numpy(base["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hdY = torch.from_numpy(dY_np.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -278,6 +319,8 @@ def bench_ours(args, rank, world, local):
         if note:
             roof["traffic_note"] = note
     fwd_m = med(fwd_ms)
+    packed_bytes = (packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel() + packed.row_fb.numel() * 4
+                    + packed.fb_rows.numel() * 4 + packed.fb_dense.numel() * 2)
     roof_fwd_us = max(flops_up / (peaks["bf16_tflops"] * 1e12),
                       (N * d * 2 * 2 + f * d * 2 * 2 + N * (f // T) * (3 * C + 1)) / (peaks["hbm_gbs"] * 1e9)) * 1e6
     result = {
@@ -302,6 +345,18 @@ def bench_ours(args, rank, world, local):
         "gpu_launches": int(launches),
         "clocks": clk,
         "timed_wall_s": round(wall, 3),
+        "energy": {"fwd_bwd_step": en_step, "fwd": en_fwd, "dense_fwd": en_dense,
+                   "how": "median nvidia-smi power.draw of this GPU over a back-to-back loop (>= 0.6 s, warm L2) "
+                          "x loop time / tokens; the GPU sits in a shared machine"},
+        "memory": {
+            "saved_for_backward_bytes": {"twell": int(packed_bytes), "dense_bf16_h": N * f * 2},
+            "twell_step_bytes": int(packed_bytes + wsf.numel()),
+            "dense_step_lower_bound_bytes": N * f * 2 * 2,
+            "note": "caller-allocated device buffers of one fwd+bwd beyond inputs, weights, outputs and "
+                    "gradients: TwELL H (values, idx, counts, row maps, fallback rows) + the one workspace "
+                    "both calls share, "
+                    "against a dense step that keeps bf16 H and materialises a bf16 dZ",
+        },
     }
     return result
 

@@ -121,7 +121,9 @@ TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_st
  * has its dense h kept by the up-projection, so the fallback rows of fb_dense
  * hold exactly the h the GEMM produced.
  * workspace: device, >= twell_fwd_workspace_bytes(...) bytes (always > 0),
- * 256-byte aligned; its contents need no initialisation. */
+ * 256-byte aligned; its contents need no initialisation and nothing in it is
+ * needed once the call's work on the stream has finished, so one buffer can
+ * serve this call and a later twell_ffn_bwd on the same stream. */
 TWELL_API int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
                   const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
                   const twell_t* H, uint16_t* Y, void* workspace, size_t workspace_bytes,
@@ -180,7 +182,8 @@ TWELL_API size_t twell_ffn_fwd_noalloc_max_scratch(void);
  *   dW_down [d_ff][d_model] fp32        dW_down[j] = sum_n h[n][j] dY[n]
  *   db      [d_ff] fp32                 db[j] = sum_n dZ[n][j]
  * dH is only formed at H's non-zeros (SDDMM).  Deterministic: no atomics.
- * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned. */
+ * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned
+ * (it may be the forward call's workspace, see twell_ffn_fwd). */
 TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                   const twell_t* H, int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
                   float* dW_inT, float* dW_down, float* db, void* workspace,
