@@ -52,6 +52,12 @@ def _configure(lib):
     lib.oracle_grad_weights.argtypes = [P, P, P, P, ctypes.c_float, I, I, I, P, I, P, P, P]
     lib.oracle_check_format.restype = I
     lib.oracle_check_format.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
+    lib.oracle_pack_tiles.restype = I
+    lib.oracle_pack_tiles.argtypes = [P, I, I, I, I, I, P, P, P, P, P]
+    lib.oracle_unpack_tiles.argtypes = [P, P, P, P, I, I, I, I, P]
+    lib.oracle_down_packed_tiles.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+    lib.oracle_check_format_tiles.restype = I
+    lib.oracle_check_format_tiles.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
     return lib
 
 
@@ -142,10 +148,34 @@ def pack(H, T: int, C: int, fb_cap: int) -> dict:
     return out
 
 
+def pack_tiles(H, T: int, C: int, pool_cap: int) -> dict:
+    """Scalar-loop packer of the tile-granular hybrid: tiles with more than C
+    non-zeros are kept densely in a pool (slots in (row, tile) order)."""
+    H = _c(H, np.uint16)
+    N, f = H.shape
+    nt = f // T
+    out = {
+        "values": np.empty((N, nt, C), dtype=np.uint16),
+        "idx": np.empty((N, nt, C), dtype=np.uint8),
+        "counts": np.empty((N, nt), dtype=np.uint8),
+        "row_fb": np.empty((N,), dtype=np.int32),
+        "pool": np.zeros((pool_cap, T), dtype=np.uint16),
+    }
+    n = _load().oracle_pack_tiles(_p(H), N, f, T, C, pool_cap, _p(out["values"]), _p(out["idx"]),
+                                  _p(out["counts"]), _p(out["row_fb"]), _p(out["pool"]))
+    out["n_fb"] = int(n)
+    out["T"], out["C"], out["pool_cap"], out["hybrid"] = T, C, pool_cap, "tiles"
+    return out
+
+
 def unpack(packed: dict, f: int) -> np.ndarray:
     v, i, c = packed["values"], packed["idx"], packed["counts"]
     N = c.shape[0]
     H = np.empty((N, f), dtype=np.uint16)
+    if packed.get("hybrid") == "tiles":
+        _load().oracle_unpack_tiles(_p(_c(v, np.uint16)), _p(_c(i, np.uint8)), _p(_c(c, np.uint8)),
+                                    _p(_c(packed["pool"], np.uint16)), N, f, packed["T"], packed["C"], _p(H))
+        return H
     _load().oracle_unpack(_p(_c(v, np.uint16)), _p(_c(i, np.uint8)), _p(_c(c, np.uint8)),
                           _p(_c(packed["row_fb"], np.int32)), _p(_c(packed["fb_dense"], np.uint16)),
                           N, f, packed["T"], packed["C"], _p(H))
@@ -166,6 +196,11 @@ def down_packed(packed: dict, W_down) -> np.ndarray:
     f, d = W_down.shape
     N = packed["counts"].shape[0]
     Y = np.empty((N, d), dtype=np.float32)
+    if packed.get("hybrid") == "tiles":
+        _load().oracle_down_packed_tiles(_p(_c(packed["values"], np.uint16)), _p(_c(packed["idx"], np.uint8)),
+                                         _p(_c(packed["counts"], np.uint8)), _p(_c(packed["pool"], np.uint16)),
+                                         _p(W_down), N, f, d, packed["T"], packed["C"], _p(Y))
+        return Y
     _load().oracle_down_packed(_p(_c(packed["values"], np.uint16)), _p(_c(packed["idx"], np.uint8)),
                                _p(_c(packed["counts"], np.uint8)), _p(_c(packed["row_fb"], np.int32)),
                                _p(_c(packed["fb_dense"], np.uint16)), _p(W_down), N, f, d,
@@ -211,15 +246,26 @@ def grad_weights(X, W_down, H, dY, lam: float, cols=None):
 def check_format(packed: dict, f: int) -> int:
     """0 when the packed layer satisfies the TwELL format invariants, else a rule code."""
     N = packed["counts"].shape[0]
+    if packed.get("hybrid") == "tiles":
+        return int(_load().oracle_check_format_tiles(
+            _p(_c(packed["values"], np.uint16)), _p(_c(packed["idx"], np.uint8)),
+            _p(_c(packed["counts"], np.uint8)), _p(_c(packed["row_fb"], np.int32)),
+            _p(_c(packed["pool"], np.uint16)), int(packed["n_fb"]), N, f, packed["T"], packed["C"],
+            packed["pool_cap"]))
     return int(_load().oracle_check_format(
         _p(_c(packed["values"], np.uint16)), _p(_c(packed["idx"], np.uint8)), _p(_c(packed["counts"], np.uint8)),
         _p(_c(packed["row_fb"], np.int32)), _p(_c(packed["fb_rows"], np.int32)), int(packed["n_fb"]),
         N, f, packed["T"], packed["C"], packed["fb_cap"]))
 
 
-def forward(X, W_inT, b, W_down, T: int, C: int, fb_cap: int, rows=None) -> dict:
-    """Whole forward for the selected rows: z, h, packed h, Y (fp32) and bf16(Y)."""
+def forward(X, W_inT, b, W_down, T: int, C: int, fb_cap: int, rows=None, hybrid: str = "rows") -> dict:
+    """Whole forward for the selected rows: z, h, packed h, Y (fp32) and bf16(Y).
+    hybrid="tiles" packs with the tile-granular hybrid, a pool of
+    fb_cap * (d_ff / T) dense tiles."""
     Z, H = hidden(X, W_inT, b, rows)
-    packed = pack(H, T, C, fb_cap)
+    if hybrid == "tiles":
+        packed = pack_tiles(H, T, C, fb_cap * (H.shape[1] // T))
+    else:
+        packed = pack(H, T, C, fb_cap)
     Y = down_packed(packed, W_down)
     return {"Z": Z, "H": H, "packed": packed, "Y": Y, "Y_bf16": round_bf16(Y)}

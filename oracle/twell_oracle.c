@@ -33,6 +33,9 @@
  *   slots in ascending row order; non-zero means bf16(h) != 0 after rounding;
  *   bias added in fp32 before the ReLU; no down-projection bias; the L1 term is
  *   lambda * sum |h| so its gradient is lambda wherever h > 0.
+ *   The tile-granular hybrid (a variant the pages do not spell out) keeps an
+ *   over-full tile densely in a pool, slots in (row, tile) order, the slot
+ *   number in the cell's first entry and the count set to 255.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -174,6 +177,116 @@ EXPORT void oracle_unpack(const uint16_t* values, const uint8_t* idx, const uint
     for (int32_t t = 0; t < nt; ++t) {
       int64_t cell = (int64_t)n * nt + t;
       for (int32_t s = 0; s < counts[cell]; ++s) h[(int64_t)t * T + idx[cell * C + s]] = values[cell * C + s];
+    }
+  }
+}
+
+/* Tile-granular hybrid (a variant of the paper's Figure 1 as the bayesiansapien
+ * note describes it: the hybrid splits between TwELL and a dense store; here
+ * the unit of the split is one (row, tile) cell instead of a whole row).  A
+ * tile whose non-zero count exceeds C is kept densely: its T values go to the
+ * next slot of the tile pool (slots numbered in ascending (row, tile) order),
+ * the cell's count is 255 and the slot number sits in the cell's first entry
+ * (value = low 16 bits, index = bits 16..23; the other C - 1 slots are
+ * padding).  Tiles with at most C non-zeros are packed as in oracle_pack.  No
+ * row is routed whole: row_fb is -1 everywhere.  Returns the number of dense
+ * tiles, which may exceed pool_cap; dense tiles past the capacity are not
+ * stored and their cells stay empty (count 0).  Needs C >= 1. */
+EXPORT int32_t oracle_pack_tiles(const uint16_t* H, int32_t N, int32_t f, int32_t T, int32_t C, int32_t pool_cap,
+                                 uint16_t* values, uint8_t* idx, uint8_t* counts, int32_t* row_fb,
+                                 uint16_t* pool) {
+  const int32_t nt = f / T;
+  int32_t n_dense = 0;
+  for (int32_t n = 0; n < N; ++n) {
+    const uint16_t* h = H + (int64_t)n * f;
+    row_fb[n] = -1;
+    for (int32_t t = 0; t < nt; ++t) {
+      int64_t cell = (int64_t)n * nt + t;
+      int32_t cnt = 0;
+      for (int32_t s = 0; s < C; ++s) {
+        values[cell * C + s] = 0;
+        idx[cell * C + s] = 0;
+      }
+      for (int32_t i = 0; i < T; ++i) {
+        uint16_t v = h[(int64_t)t * T + i];
+        if (bf16_to_f32(v) != 0.0f) {
+          if (cnt < C) {
+            values[cell * C + cnt] = v;
+            idx[cell * C + cnt] = (uint8_t)i;
+          }
+          cnt += 1;
+        }
+      }
+      if (cnt > C) {
+        /* dense tile: the entries written above become padding again */
+        for (int32_t s = 0; s < C; ++s) {
+          values[cell * C + s] = 0;
+          idx[cell * C + s] = 0;
+        }
+      } else {
+        counts[cell] = (uint8_t)cnt;
+        continue;
+      }
+      if (n_dense < pool_cap) {
+        counts[cell] = 255;
+        values[cell * C] = (uint16_t)(n_dense & 0xFFFF);
+        idx[cell * C] = (uint8_t)((n_dense >> 16) & 0xFF);
+        memcpy(pool + (int64_t)n_dense * T, h + (int64_t)t * T, sizeof(uint16_t) * (size_t)T);
+      } else {
+        counts[cell] = 0;
+      }
+      n_dense += 1;
+    }
+  }
+  return n_dense;
+}
+
+/* Tile-granular hybrid -> dense: zero H, write the stored entries, copy each
+ * dense tile from its pool slot. */
+EXPORT void oracle_unpack_tiles(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
+                                const uint16_t* pool, int32_t N, int32_t f, int32_t T, int32_t C, uint16_t* H) {
+  const int32_t nt = f / T;
+  for (int32_t n = 0; n < N; ++n) {
+    uint16_t* h = H + (int64_t)n * f;
+    memset(h, 0, sizeof(uint16_t) * (size_t)f);
+    for (int32_t t = 0; t < nt; ++t) {
+      int64_t cell = (int64_t)n * nt + t;
+      if (counts[cell] == 255) {
+        int64_t slot = (int64_t)values[cell * C] | ((int64_t)idx[cell * C] << 16);
+        memcpy(h + (int64_t)t * T, pool + slot * T, sizeof(uint16_t) * (size_t)T);
+        continue;
+      }
+      for (int32_t s = 0; s < counts[cell]; ++s) h[(int64_t)t * T + idx[cell * C + s]] = values[cell * C + s];
+    }
+  }
+}
+
+/* Y from the tile-granular hybrid: stored entries of each tile, or the dense
+ * tile's non-zeros walked in column order, so j ascends as in oracle_down_dense. */
+EXPORT void oracle_down_packed_tiles(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
+                                     const uint16_t* pool, const uint16_t* W_down, int32_t N, int32_t f, int32_t d,
+                                     int32_t T, int32_t C, float* Y) {
+  const int32_t nt = f / T;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t n = 0; n < N; ++n) {
+    float* y = Y + (int64_t)n * d;
+    for (int32_t c = 0; c < d; ++c) {
+      float acc = 0.0f;
+      for (int32_t t = 0; t < nt; ++t) {
+        int64_t cell = (int64_t)n * nt + t;
+        if (counts[cell] == 255) {
+          const uint16_t* tile = pool + ((int64_t)values[cell * C] | ((int64_t)idx[cell * C] << 16)) * T;
+          for (int32_t i = 0; i < T; ++i)
+            if (bf16_to_f32(tile[i]) != 0.0f)
+              acc += bf16_to_f32(tile[i]) * bf16_to_f32(W_down[((int64_t)t * T + i) * d + c]);
+          continue;
+        }
+        for (int32_t s = 0; s < counts[cell]; ++s) {
+          int32_t j = t * T + idx[cell * C + s];
+          acc += bf16_to_f32(values[cell * C + s]) * bf16_to_f32(W_down[(int64_t)j * d + c]);
+        }
+      }
+      y[c] = acc;
     }
   }
 }
@@ -337,5 +450,53 @@ EXPORT int32_t oracle_check_format(const uint16_t* values, const uint8_t* idx, c
   for (int32_t s = 1; s < n_fb && s < fb_cap; ++s)
     if (fb_rows[s] <= fb_rows[s - 1]) return 8;
   if (seen_fb != n_fb) return 9;
+  return 0;
+}
+
+/* Format invariants of the tile-granular hybrid.  Returns 0 when all hold,
+ * else a code naming the first violated rule:
+ *   1 count above C (and not 255)      3 index >= T
+ *   4 indices not strictly increasing  5 stored value equal to zero
+ *   6 padding slot not (+0.0, 0)       7 row_fb not -1
+ *  10 dense tiles not numbered 0, 1, 2, ... in (row, tile) order
+ *  11 number of dense tiles != min(n_dense, pool_cap)
+ *  12 a dense tile with at most C non-zeros */
+EXPORT int32_t oracle_check_format_tiles(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
+                                         const int32_t* row_fb, const uint16_t* pool, int32_t n_dense, int32_t N,
+                                         int32_t f, int32_t T, int32_t C, int32_t pool_cap) {
+  const int32_t nt = f / T;
+  int32_t next = 0;
+  for (int32_t n = 0; n < N; ++n) {
+    if (row_fb[n] != -1) return 7;
+    for (int32_t t = 0; t < nt; ++t) {
+      int64_t cell = (int64_t)n * nt + t;
+      int32_t cnt = counts[cell];
+      if (cnt == 255) {
+        int32_t slot = (int32_t)values[cell * C] | ((int32_t)idx[cell * C] << 16);
+        if (slot != next || slot >= pool_cap) return 10;
+        int32_t nz = 0;
+        for (int32_t i = 0; i < T; ++i)
+          if (bf16_to_f32(pool[(int64_t)slot * T + i]) != 0.0f) nz += 1;
+        if (nz <= C) return 12;
+        for (int32_t s = 1; s < C; ++s)
+          if (values[cell * C + s] != 0 || idx[cell * C + s] != 0) return 6;
+        next += 1;
+        continue;
+      }
+      if (cnt > C) return 1;
+      for (int32_t s = 0; s < C; ++s) {
+        uint16_t v = values[cell * C + s];
+        uint8_t i = idx[cell * C + s];
+        if (s < cnt) {
+          if (i >= T) return 3;
+          if (s > 0 && i <= idx[cell * C + s - 1]) return 4;
+          if (bf16_to_f32(v) == 0.0f) return 5;
+        } else if (v != 0 || i != 0) {
+          return 6;
+        }
+      }
+    }
+  }
+  if (next != (n_dense < pool_cap ? n_dense : pool_cap)) return 11;
   return 0;
 }

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_tiles as tile_pins
 
 MUTATIONS = [
     ("bias dropped", "float z = acc + bf16_to_f32(b[j]);", "float z = acc;",
@@ -40,6 +41,12 @@ MUTATIONS = [
      pins.test_backward_single_active_unit_rank_one),
     ("rounding ties away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;",
      "if (rest >= 0x8000u) keep += 1u;", pins.test_bf16_rounding_hand_cases),
+    ("tile slots out of order", "values[cell * C] = (uint16_t)(n_dense & 0xFFFF);",
+     "values[cell * C] = (uint16_t)((n_dense ^ 1) & 0xFFFF);", tile_pins.test_tiles_hand_example),
+    ("dense-tile rule >= C", "if (cnt > C) {\n        /* dense tile", "if (cnt >= C) {\n        /* dense tile",
+     lambda: tile_pins.test_tiles_brute_force_all_patterns(3)),
+    ("dense tiles left out of Y", "acc += bf16_to_f32(tile[i]) * bf16_to_f32(W_down[((int64_t)t * T + i) * d + c]);",
+     "acc += 0.0f;", tile_pins.test_tiles_packed_product_equals_dense_bitwise),
 ]
 
 
