@@ -37,7 +37,7 @@ class TwellError(RuntimeError):
 class twell_t(ctypes.Structure):
     _fields_ = [
         ("n_rows", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("tile", ctypes.c_int32),
-        ("cap", ctypes.c_int32), ("fb_cap", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("cap", ctypes.c_int32), ("fb_cap", ctypes.c_int32), ("hybrid", ctypes.c_int32),
         ("values", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("counts", ctypes.c_void_p),
         ("row_fb", ctypes.c_void_p), ("fb_rows", ctypes.c_void_p), ("fb_dense", ctypes.c_void_p),
         ("n_fb", ctypes.c_void_p), ("status", ctypes.c_void_p),
@@ -122,15 +122,22 @@ class Packed:
     tile: int
     cap: int
     fb_cap: int
+    hybrid: int = 0   # HYBRID_ROWS or HYBRID_TILES
 
     def struct(self) -> twell_t:
         p = lambda t: t.data_ptr() if t is not None and t.numel() else None
-        return twell_t(self.n_rows, self.d_ff, self.tile, self.cap, self.fb_cap, 0,
+        return twell_t(self.n_rows, self.d_ff, self.tile, self.cap, self.fb_cap, self.hybrid,
                        p(self.values), p(self.idx), p(self.counts), p(self.row_fb), p(self.fb_rows),
                        p(self.fb_dense), p(self.n_fb), p(self.status))
 
 
-def alloc_packed(n_rows: int, d_ff: int, tile: int, cap: int, fb_cap: int, device="cuda") -> Packed:
+HYBRID_ROWS, HYBRID_TILES, DENSE_TILE = 0, 1, 255
+
+
+def alloc_packed(n_rows: int, d_ff: int, tile: int, cap: int, fb_cap: int, device="cuda",
+                 hybrid: int = HYBRID_ROWS) -> Packed:
+    """Buffers of a packed layer.  With hybrid=HYBRID_TILES, fb_dense is the pool
+    of fb_cap * d_ff / tile dense tiles."""
     import torch
     nt = d_ff // tile
     kw = dict(device=device)
@@ -143,7 +150,7 @@ def alloc_packed(n_rows: int, d_ff: int, tile: int, cap: int, fb_cap: int, devic
         fb_dense=torch.empty((max(fb_cap, 1), d_ff), dtype=torch.bfloat16, **kw),
         n_fb=torch.zeros((4,), dtype=torch.int32, **kw),
         status=torch.zeros((4,), dtype=torch.int32, **kw),
-        n_rows=n_rows, d_ff=d_ff, tile=tile, cap=cap, fb_cap=fb_cap,
+        n_rows=n_rows, d_ff=d_ff, tile=tile, cap=cap, fb_cap=fb_cap, hybrid=hybrid,
     )
 
 

@@ -197,12 +197,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int check_layout(const twell_t* L) {
   if (!L) return TWELL_ERR_INVALID_ARG;
-  if (L->n_rows < 0 || L->d_ff <= 0 || L->fb_cap < 0 || L->reserved != 0) return TWELL_ERR_INVALID_ARG;
+  if (L->n_rows < 0 || L->d_ff <= 0 || L->fb_cap < 0) return TWELL_ERR_INVALID_ARG;
+  if (L->hybrid != TWELL_HYBRID_ROWS && L->hybrid != TWELL_HYBRID_TILES) return TWELL_ERR_INVALID_ARG;
   const int T = L->tile;
   if (T != 32 && T != 64 && T != 128 && T != 256) return TWELL_ERR_INVALID_ARG;
   if (L->cap < 1 || L->cap > T || L->cap > 32) return TWELL_ERR_INVALID_ARG;
   if (L->d_ff % T != 0) return TWELL_ERR_INVALID_ARG;
   if (L->d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  // tile pool slots are 24-bit
+  if (L->hybrid == TWELL_HYBRID_TILES && static_cast<int64_t>(L->fb_cap) * (L->d_ff / T) > 0xFFFFFF)
+    return TWELL_ERR_UNSUPPORTED;
   if (!L->n_fb || !L->status) return TWELL_ERR_INVALID_ARG;
   if (L->n_rows > 0 && (!L->values || !L->idx || !L->counts || !L->row_fb)) return TWELL_ERR_INVALID_ARG;
   if (L->fb_cap > 0 && (!L->fb_rows || !L->fb_dense)) return TWELL_ERR_INVALID_ARG;
@@ -249,6 +253,11 @@ int twell_pack(const uint16_t* H, int64_t ldh, const twell_t* out, twell_stream_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   TW_TRY(reset_words(out, s));
   TW_TRY(launch_pack_cells(H, ldh, *out, s));
+  if (out->hybrid == TWELL_HYBRID_TILES) {
+    TW_TRY(launch_tile_count(*out, s));
+    TW_TRY(launch_route(*out, s));
+    return launch_tile_assign(*out, H, ldh, nullptr, 0, s);
+  }
   TW_TRY(launch_route(*out, s));
   TW_TRY(launch_fb_copy(H, ldh, *out, s));
   return TWELL_OK;
@@ -341,6 +350,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   TW_TRY(check_dense(W_down));
   TW_TRY(check_dense(Y));
   if (W_uT && 128 % H->tile != 0) return TWELL_ERR_UNSUPPORTED;
+  const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
+  if (tiles && (W_uT || (n_rows > 0 && n_rows <= kSwapMaxTokens))) return TWELL_ERR_UNSUPPORTED;
   const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
@@ -380,6 +391,14 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
     else
       TW_TRY(launch_gemm_pack(X, W_inT, n_rows, d_ff, d_model, pp, H->status, s));
+    if (tiles) {
+      // tile-granular hybrid: the spilled over-full tiles become the pool's
+      // dense tiles in (row, tile) order, and the SpMM reads them there
+      TW_TRY(launch_tile_count(*H, s));
+      TW_TRY(launch_route(*H, s));
+      TW_TRY(launch_tile_assign(*H, nullptr, 0, spill, w.spill_cap, s));
+      return launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr, s);
+    }
     TW_TRY(launch_route(*H, s));
   }
   {
@@ -426,6 +445,7 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
   TW_TRY(check_layout(H));
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (H->hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
   TW_TRY(check_dense(W_down));
@@ -473,7 +493,10 @@ int twell_read_status(const twell_t* layout, twell_stream_t stream) {
   if (cudaMemcpy(&st, layout->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return TWELL_ERR_CUDA;
   if (cudaMemcpy(&nfb, layout->n_fb, sizeof nfb, cudaMemcpyDeviceToHost) != cudaSuccess) return TWELL_ERR_CUDA;
   if (st != 0) return st;
-  if (nfb > layout->fb_cap) return TWELL_ERR_FALLBACK_OVERFLOW;
+  const int64_t cap = layout->hybrid == TWELL_HYBRID_TILES && layout->tile > 0
+                          ? static_cast<int64_t>(layout->fb_cap) * (layout->d_ff / layout->tile)
+                          : layout->fb_cap;
+  if (nfb > cap) return TWELL_ERR_FALLBACK_OVERFLOW;
   return TWELL_OK;
 }
 

@@ -22,7 +22,7 @@ namespace {
 
 // Flat copy of the layout for kernel parameters.
 struct Layout {
-  int32_t N, f, T, C, fb_cap, nt;
+  int32_t N, f, T, C, fb_cap, nt, hybrid;
   uint16_t* values;
   uint8_t* idx;
   uint8_t* counts;
@@ -34,31 +34,37 @@ struct Layout {
 };
 
 Layout flat(const twell_t& L) {
-  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.values, L.idx,
+  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.hybrid, L.values, L.idx,
                 L.counts, L.row_fb, L.fb_rows, L.fb_dense, L.n_fb, L.status};
 }
 
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteRows = 8;  // rows per thread per pass
 
-// row_fb holds 0/1 overflow flags on entry and -1 / fallback slot on exit.
-// One CTA: an exclusive block scan of the flags gives every fallback row its
-// slot in ascending row order, so the result is deterministic.
+// Rows variant: row_fb holds 0/1 overflow flags on entry and -1 / fallback
+// slot on exit.  Tiles variant: row_fb holds each row's number of dense tiles
+// on entry and, on exit, the pool slot of the row's first dense tile (-1 for
+// rows without one); n_fb counts the dense tiles.  One CTA: an exclusive
+// block scan gives the slots in ascending row order, so the result is
+// deterministic.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
   __shared__ int warp_tot[kRouteThreads / 32];
   __shared__ int base_s;
+  const bool tiles = L.hybrid == TWELL_HYBRID_TILES;
+  const int64_t cap = tiles ? static_cast<int64_t>(L.fb_cap) * L.nt : L.fb_cap;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) base_s = 0;
   __syncthreads();
   for (int start = 0; start < L.N; start += kRouteThreads * kRouteRows) {
     const int r0 = start + tid * kRouteRows;
-    int flags = 0, local = 0;
+    int cnt[kRouteRows];
+    int local = 0;
 #pragma unroll
     for (int i = 0; i < kRouteRows; ++i) {
       const int r = r0 + i;
-      const int fl = (r < L.N && L.row_fb[r] != 0) ? 1 : 0;
-      flags |= fl << i;
-      local += fl;
+      const int v = r < L.N ? L.row_fb[r] : 0;
+      cnt[i] = tiles ? v : (v != 0 ? 1 : 0);
+      local += cnt[i];
     }
     int incl = local;
 #pragma unroll
@@ -84,7 +90,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
     for (int i = 0; i < kRouteRows; ++i) {
       const int r = r0 + i;
       if (r >= L.N) break;
-      if ((flags >> i) & 1) {
+      if (tiles) {
+        L.row_fb[r] = cnt[i] > 0 ? slot : -1;
+      } else if (cnt[i]) {
         L.row_fb[r] = slot;
         if (slot < L.fb_cap) {
           L.fb_rows[slot] = r;
@@ -98,10 +106,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
             L.idx[cell0 * L.C + c] = 0;
           }
         }
-        ++slot;
       } else {
         L.row_fb[r] = -1;
       }
+      slot += cnt[i];
     }
     __syncthreads();
     if (tid == kRouteThreads - 1) base_s = slot;
@@ -109,7 +117,78 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
   }
   if (tid == 0) {
     *L.n_fb = base_s;
-    if (base_s > L.fb_cap) report_error(L.status, TWELL_ERR_FALLBACK_OVERFLOW);
+    if (base_s > cap) report_error(L.status, TWELL_ERR_FALLBACK_OVERFLOW);
+  }
+}
+
+// Tiles variant, before routing: a row flagged by the pack (row_fb != 0) gets
+// its number of dense tiles (cells marked 255).  A warp per row, grid-stride.
+__global__ void __launch_bounds__(256) tile_count_kernel(Layout L) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t gws = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = gw0; r < L.N; r += gws) {
+    if (L.row_fb[r] == 0) continue;
+    int n = 0;
+    for (int t0 = 0; t0 < L.nt; t0 += 32) {
+      const int t = t0 + lane;
+      const bool dense = t < L.nt && L.counts[r * L.nt + t] == TWELL_DENSE_TILE;
+      n += __popc(__ballot_sync(0xffffffffu, dense));
+    }
+    if (lane == 0) L.row_fb[r] = n;
+  }
+}
+
+// Tiles variant, after routing: each dense tile of a row takes the next pool
+// slot (row_fb = the row's first slot) in tile order; its T values are copied
+// into the pool from the dense H (standalone pack) or from the spill buffer
+// the up-projection wrote (fused forward, spill index in the cell's first
+// entry), and the cell's first entry becomes the pool slot.  A dense tile past
+// the pool's capacity leaves an empty cell.  row_fb ends at -1 for every row.
+__global__ void __launch_bounds__(256)
+    tile_assign_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh, const uint16_t* __restrict__ spill,
+                       int32_t spill_cap) {
+  const int lane = threadIdx.x & 31;
+  const int64_t cap = static_cast<int64_t>(L.fb_cap) * L.nt;
+  const int vec = L.T / 8;  // 16-byte vectors per tile
+  const int64_t gw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t gws = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = gw0; r < L.N; r += gws) {
+    const int base = L.row_fb[r];
+    if (base < 0) continue;
+    int64_t slot = base;
+    for (int t0 = 0; t0 < L.nt; t0 += 32) {
+      const int tl = t0 + lane;
+      unsigned m = __ballot_sync(0xffffffffu, tl < L.nt && L.counts[r * L.nt + tl] == TWELL_DENSE_TILE);
+      while (m) {
+        const int t = t0 + __ffs(m) - 1;
+        m &= m - 1;
+        const int64_t cell = r * L.nt + t;
+        if (slot < cap) {
+          uint4* dst = reinterpret_cast<uint4*>(L.fb_dense + slot * L.T);
+          if (spill) {
+            const uint32_t s24 = static_cast<uint32_t>(L.values[cell * L.C]) |
+                                 (static_cast<uint32_t>(L.idx[cell * L.C]) << 16);
+            const bool have = s24 < static_cast<uint32_t>(spill_cap);
+            const uint4* src = reinterpret_cast<const uint4*>(spill + static_cast<int64_t>(s24) * L.T);
+            for (int q = lane; q < vec; q += 32) dst[q] = have ? src[q] : make_uint4(0, 0, 0, 0);
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(H + r * ldh + static_cast<int64_t>(t) * L.T);
+            for (int q = lane; q < vec; q += 32) dst[q] = src[q];
+          }
+        }
+        __syncwarp();  // the spill index is read before the cell is rewritten
+        const bool keep = slot < cap;
+        for (int q = lane; q < L.C; q += 32) {
+          L.values[cell * L.C + q] = (keep && q == 0) ? static_cast<uint16_t>(slot & 0xFFFF) : 0;
+          L.idx[cell * L.C + q] = (keep && q == 0) ? static_cast<uint8_t>((slot >> 16) & 0xFF) : 0;
+        }
+        if (lane == 0 && !keep) L.counts[cell] = 0;
+        __syncwarp();
+        ++slot;
+      }
+    }
+    if (lane == 0) L.row_fb[r] = -1;
   }
 }
 
@@ -184,6 +263,23 @@ __global__ void fb_reduce_kernel(Layout L, const float* __restrict__ part, int k
 }
 
 }  // namespace
+
+int launch_tile_count(const twell_t& L, cudaStream_t s) {
+  if (L.n_rows <= 0) return TWELL_OK;
+  const int grid = std::max(1, std::min((L.n_rows + 7) / 8, 4 * sm_count()));
+  LaunchScope ls(TWELL_KERNEL_ROUTE, s);
+  tile_count_kernel<<<grid, 256, 0, s>>>(flat(L));
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_tile_assign(const twell_t& L, const uint16_t* H, int64_t ldh, const uint16_t* spill, int32_t spill_cap,
+                       cudaStream_t s) {
+  if (L.n_rows <= 0) return TWELL_OK;
+  const int grid = std::max(1, std::min((L.n_rows + 7) / 8, 4 * sm_count()));
+  LaunchScope ls(TWELL_KERNEL_FB_ASSEMBLE, s);
+  tile_assign_kernel<<<grid, 256, 0, s>>>(flat(L), H, ldh, spill, spill_cap);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
 
 int launch_route(const twell_t& L, cudaStream_t s) {
   LaunchScope ls(TWELL_KERNEL_ROUTE, s);

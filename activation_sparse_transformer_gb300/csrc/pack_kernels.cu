@@ -21,7 +21,7 @@ namespace twell {
 namespace {
 
 struct Layout {
-  int32_t N, f, T, C, fb_cap, nt;
+  int32_t N, f, T, C, fb_cap, nt, hybrid;
   uint16_t* values;
   uint8_t* idx;
   uint8_t* counts;
@@ -33,7 +33,7 @@ struct Layout {
 };
 
 Layout flat(const twell_t& L) {
-  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.values, L.idx,
+  return Layout{L.n_rows, L.d_ff, L.tile, L.cap, L.fb_cap, L.d_ff / L.tile, L.hybrid, L.values, L.idx,
                 L.counts, L.row_fb, L.fb_rows, L.fb_dense, L.n_fb, L.status};
 }
 
@@ -63,24 +63,29 @@ __device__ __forceinline__ void pack_lane8(const Layout& L, int row, int col, bo
   if (!in) return;
   const int C = L.C;
   const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
+  // tile-granular hybrid: an over-full tile becomes a dense tile (its pool
+  // slot is written into the cell once all rows are counted)
+  const bool dense = L.hybrid == TWELL_HYBRID_TILES && total > C;
   int slot = incl - local;
+  if (!dense) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if ((nzmask >> k) & 1u) {
-      if (slot < C) {
-        L.values[cell * C + slot] = half_word(w, k);
-        L.idx[cell * C + slot] = static_cast<uint8_t>(gl * 8 + k);
+    for (int k = 0; k < 8; ++k) {
+      if ((nzmask >> k) & 1u) {
+        if (slot < C) {
+          L.values[cell * C + slot] = half_word(w, k);
+          L.idx[cell * C + slot] = static_cast<uint8_t>(gl * 8 + k);
+        }
+        ++slot;
       }
-      ++slot;
     }
   }
-  const int stored = total < C ? total : C;
+  const int stored = dense ? 0 : (total < C ? total : C);
   for (int s = stored + gl; s < C; s += G) {
     L.values[cell * C + s] = 0;
     L.idx[cell * C + s] = 0;
   }
   if (gl == 0) {
-    L.counts[cell] = static_cast<uint8_t>(stored);
+    L.counts[cell] = dense ? static_cast<uint8_t>(TWELL_DENSE_TILE) : static_cast<uint8_t>(stored);
     if (total > C) L.row_fb[row] = 1;
   }
 }
@@ -215,6 +220,11 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int fb = L.row_fb[row];
   if (fb >= 0) {
     out = *reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f + col);
+  } else if (L.hybrid == TWELL_HYBRID_TILES && L.counts[static_cast<int64_t>(row) * L.nt + col / L.T] ==
+                                                    TWELL_DENSE_TILE) {
+    const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
+    const int64_t slot = static_cast<int64_t>(L.values[cell * L.C]) | (static_cast<int64_t>(L.idx[cell * L.C]) << 16);
+    out = *reinterpret_cast<const uint4*>(L.fb_dense + slot * L.T + col % L.T);
   } else {
     const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
     const int lo = col % L.T;

@@ -46,6 +46,7 @@ struct SpmmArgs {
   uint16_t* out;          // [N][d] bf16
   float* part;            // [gridDim.z][N][d] fp32 when the tiles are split into ranges, else null
   int32_t* arrivals;      // [gridDim.x][gridDim.y] zeroed counters when the tiles are split
+  const uint16_t* pool;   // tile-granular hybrid: the pool of dense tiles, else null
   int N, d, nt, T, C;
   int32_t* status;
 };
@@ -101,6 +102,35 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&acc)[8]) {
   return make_uint4(p[0], p[1], p[2], p[3]);
 }
 
+template <typename VT>
+__device__ __forceinline__ VT from_bf16(uint16_t v);
+template <>
+__device__ __forceinline__ uint16_t from_bf16<uint16_t>(uint16_t v) { return v; }
+template <>
+__device__ __forceinline__ float from_bf16<float>(uint16_t v) { return bf16_bits_to_float(v); }
+
+// acc += sum over list[0, total) of value x (W row j)[c0, c0 + 8), kU rows in flight.
+template <typename VT>
+__device__ __forceinline__ void stream_list(const SpmmArgs& a, const uint16_t* __restrict__ wcol,
+                                            const RowEntry<VT>* list, int total, float (&acc)[8]) {
+  int e = 0;
+  for (; e + kU <= total; e += kU) {
+    uint4 w[kU];
+    RowEntry<VT> en[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      en[u] = list[e + u];
+      w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
+  }
+  for (; e < total; ++e) {
+    const RowEntry<VT> en = list[e];
+    en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+  }
+}
+
 // Sum of one row's stored entries in tiles [t_beg, t_end) times the W rows
 // they name, for this lane's 8 columns starting at c0 (the whole warp calls it
 // for one row; inactive lanes only help flatten).
@@ -111,11 +141,12 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
   const VT* vals = static_cast<const VT*>(a.values);
   const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
 
-  // ---- flatten: tiles in order, 32 per round
+  // ---- flatten: tiles in order, 32 per round (dense tiles come after)
   int total = 0;
   for (int t0 = t_beg; t0 < t_end; t0 += 32) {
     const int t = t0 + lane;
-    const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+    const int cnt_raw = t < t_end ? a.counts[cell0 + t] : 0;
+    const int cnt = (a.pool && cnt_raw == TWELL_DENSE_TILE) ? 0 : cnt_raw;
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -131,23 +162,32 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
   __syncwarp();
 
   // ---- stream the named W rows, kU loads in flight
-  if (active) {
-    const uint16_t* wcol = W + c0;
-    int e = 0;
-    for (; e + kU <= total; e += kU) {
-      uint4 w[kU];
-      RowEntry<VT> en[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        en[u] = list[e + u];
-        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+  if (active) stream_list<VT>(a, W + c0, list, total, acc);
+
+  // ---- tile-granular hybrid: each dense tile's non-zeros, gathered the same way
+  if (a.pool) {
+    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+      const int tl = t0 + lane;
+      unsigned m = __ballot_sync(0xffffffffu, tl < t_end && a.counts[cell0 + tl] == TWELL_DENSE_TILE);
+      while (m) {
+        const int t = t0 + __ffs(m) - 1;
+        m &= m - 1;
+        const int64_t cell = cell0 + t;
+        const int64_t slot = static_cast<int64_t>(static_cast<const uint16_t*>(a.values)[cell * a.C]) |
+                             (static_cast<int64_t>(a.idx[cell * a.C]) << 16);
+        const uint16_t* tile = a.pool + slot * a.T;
+        __syncwarp();  // the list is free again
+        int n = 0;
+        for (int i0 = 0; i0 < a.T; i0 += 32) {
+          const uint16_t v = tile[i0 + lane];
+          const bool nz = (v & 0x7FFFu) != 0;
+          const unsigned b = __ballot_sync(0xffffffffu, nz);
+          if (nz) list[n + __popc(b & ((1u << lane) - 1u))] = RowEntry<VT>::make(t * a.T + i0 + lane, from_bf16<VT>(v));
+          n += __popc(b);
+        }
+        __syncwarp();
+        if (active) stream_list<VT>(a, W + c0, list, n, acc);
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
-    }
-    for (; e < total; ++e) {
-      const RowEntry<VT> en = list[e];
-      en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
     }
   }
   __syncwarp();  // the list is rewritten by the warp's next item
@@ -229,7 +269,8 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   if (a.N <= 0) return TWELL_OK;
   if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   if (a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;  // hidden unit fits the entry's 16 bits
-  const int max_entries = a.nt * a.C;
+  // a dense tile's non-zeros pass through the same list
+  const int max_entries = a.pool ? std::max(a.nt * a.C, a.T) : a.nt * a.C;
   const size_t smem = static_cast<size_t>(kWarps) * max_entries * sizeof(RowEntry<VT>);
   if (smem > kMaxDynSmem) return TWELL_ERR_UNSUPPORTED;
   auto kern = spmm_row_kernel<VT>;
@@ -270,15 +311,27 @@ int spmm_nsplit(int n_rows, int d_model) {
 
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
                 int32_t* arrivals, cudaStream_t s) {
-  SpmmArgs a{L.values, L.idx, L.counts, L.row_fb, Y, part, arrivals, L.n_rows, d_model, L.d_ff / L.tile, L.tile,
-             L.cap, L.status};
+  SpmmArgs a{L.values,
+             L.idx,
+             L.counts,
+             L.row_fb,
+             Y,
+             part,
+             arrivals,
+             L.hybrid == TWELL_HYBRID_TILES ? L.fb_dense : nullptr,
+             L.n_rows,
+             d_model,
+             L.d_ff / L.tile,
+             L.tile,
+             L.cap,
+             L.status};
   return launch_spmm_rows<uint16_t>(a, W_down, nsplit, TWELL_KERNEL_SPMM, s);
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int kernel_id, cudaStream_t s) {
-  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, nullptr, L.n_rows, d_model, L.d_ff / L.tile, L.tile,
-             L.cap, L.status};
+  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, nullptr, nullptr, L.n_rows, d_model, L.d_ff / L.tile,
+             L.tile, L.cap, L.status};
   return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
 }
 

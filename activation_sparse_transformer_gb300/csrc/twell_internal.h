@@ -159,6 +159,12 @@ int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_
 
 // forward helpers (fwd_kernels.cu)
 int launch_route(const twell_t& L, cudaStream_t s);
+// tile-granular hybrid: dense tiles per flagged row (before launch_route), then
+// pool slots, pool copies (from H, or from the spill buffer when H is null)
+// and the cells' slot numbers (after it)
+int launch_tile_count(const twell_t& L, cudaStream_t s);
+int launch_tile_assign(const twell_t& L, const uint16_t* H, int64_t ldh, const uint16_t* spill, int32_t spill_cap,
+                       cudaStream_t s);
 int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* spill_count, int32_t spill_cap,
                        cudaStream_t s);
 // Y = H . W_down for the TwELL rows.  With nsplit > 1 each row's tiles are

@@ -45,6 +45,22 @@
  *     take slots 0, 1, ... in ascending row order.
  *   - Unused slots are padding: value +0.0 (0x0000), index 0.
  *   - "Non-zero" means the bf16 value compares unequal to zero.
+ *
+ * Tile-granular variant (twell_t.hybrid = TWELL_HYBRID_TILES; the pages'
+ * Figure 1, as the bayesiansapien note describes it, shows hybrids that split
+ * between formats; this one splits per (row, tile) instead of per row):
+ *   - A tile with more than C non-zeros is a dense tile: its T values live in
+ *     the next slot of a tile pool, fb_dense viewed as [fb_cap * n_tiles][T],
+ *     slots numbered 0, 1, ... in ascending (row, tile) order.  Its cell has
+ *     count 255 (TWELL_DENSE_TILE), the slot number in its first entry (value =
+ *     low 16 bits, index = bits 16..23) and padding in the others.
+ *   - No row is routed whole: row_fb is -1 for every row, fb_rows is unused,
+ *     *n_fb counts dense tiles (may exceed fb_cap * n_tiles; tiles past the
+ *     pool are not stored, their cells are left empty, and the status word
+ *     reports TWELL_ERR_FALLBACK_OVERFLOW).
+ *   - Supported by twell_pack, twell_unpack and twell_ffn_fwd (n_rows > 32);
+ *     the backward, the gated forward and the small-batch forward return
+ *     TWELL_ERR_UNSUPPORTED for it.
  */
 #ifndef TWELL_H
 #define TWELL_H
@@ -76,6 +92,12 @@ enum {
   TWELL_ERR_NO_DEVICE = -8           /* no sm_103a device current */
 };
 
+enum {
+  TWELL_HYBRID_ROWS = 0,   /* a row with an over-full tile goes whole to fb_dense */
+  TWELL_HYBRID_TILES = 1,  /* only the over-full tiles go, to a pool of dense tiles */
+  TWELL_DENSE_TILE = 255   /* cell count of a dense tile (tile-granular variant) */
+};
+
 /* A packed activation matrix H [n_rows][d_ff].  The struct itself lives in
  * host memory and is read during the call; every pointer in it is a device
  * pointer to caller-owned memory of the stated size. */
@@ -85,14 +107,15 @@ typedef struct twell_t {
   int32_t tile;       /* T */
   int32_t cap;        /* C */
   int32_t fb_cap;     /* rows the dense fallback can hold (>= 0) */
-  int32_t reserved;   /* must be 0 */
+  int32_t hybrid;     /* TWELL_HYBRID_ROWS (0) or TWELL_HYBRID_TILES */
   uint16_t* values;   /* [N][f/T][C] bf16 */
   uint8_t* idx;       /* [N][f/T][C] tile-local index */
-  uint8_t* counts;    /* [N][f/T] non-zeros stored in the cell (0 for fallback rows) */
+  uint8_t* counts;    /* [N][f/T] non-zeros stored in the cell (0 for fallback rows;
+                         TWELL_DENSE_TILE for a dense tile of the tile-granular variant) */
   int32_t* row_fb;    /* [N] -1 = TwELL row, else slot in fb_dense */
-  int32_t* fb_rows;   /* [fb_cap] row of each fallback slot, ascending */
-  uint16_t* fb_dense; /* [fb_cap][f] bf16 dense rows */
-  int32_t* n_fb;      /* device scalar: number of fallback rows found (may exceed fb_cap) */
+  int32_t* fb_rows;   /* [fb_cap] row of each fallback slot, ascending (rows variant) */
+  uint16_t* fb_dense; /* [fb_cap][f] bf16 dense rows, or the pool of fb_cap * f / T dense tiles */
+  int32_t* n_fb;      /* device scalar: fallback rows (or dense tiles) found; may exceed the capacity */
   int32_t* status;    /* device scalar: 0 or a TWELL_ERR_* code set by a kernel */
 } twell_t;
 
@@ -201,7 +224,9 @@ TWELL_API int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, cons
                         uint16_t* Hbuf, uint16_t* Y, twell_stream_t stream);
 
 /* Synchronises `stream`, then returns *layout->status if non-zero, else
- * TWELL_ERR_FALLBACK_OVERFLOW when *layout->n_fb > fb_cap, else TWELL_OK. */
+ * TWELL_ERR_FALLBACK_OVERFLOW when *layout->n_fb exceeds the capacity (fb_cap
+ * rows, or fb_cap * d_ff / tile dense tiles for the tile-granular variant),
+ * else TWELL_OK. */
 TWELL_API int twell_read_status(const twell_t* layout, twell_stream_t stream);
 
 /* Static string for a TWELL_* code. */
