@@ -393,7 +393,11 @@ def bench_next(args):
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev)
 
-    cfgs = [synth.CONFIGS["gated"]] + synth.decode_sweep()
+    import dataclasses
+    # the 1B forward with row-granular and tile-granular fallback, same inputs
+    cfgs = ([synth.CONFIGS["gated"]] + synth.decode_sweep() +
+            [dataclasses.replace(synth.CONFIGS["1b"], name="1b_rows"),
+             dataclasses.replace(synth.CONFIGS["1b"], name="1b_tiles")])
     if args.only:
         cfgs = [c for c in cfgs if c.name in args.only.split(",")]
     for cfg in cfgs:
@@ -401,7 +405,8 @@ def bench_next(args):
         N, d, f, T, C = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap
         fb = cfg.fallback_capacity if not cfg.name.startswith("decode") else N
         X, Wi, b, Wd = dt(inp["X"]), dt(inp["W_inT"]), dt(inp["b"]), dt(inp["W_down"])
-        packed = tw.alloc_packed(N, f, T, C, fb, dev)
+        hybrid = tw.HYBRID_TILES if cfg.name.endswith("_tiles") else tw.HYBRID_ROWS
+        packed = tw.alloc_packed(N, f, T, C, fb, dev, hybrid=hybrid)
         Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
         if cfg.gated:
@@ -414,7 +419,8 @@ def bench_next(args):
         if rc != 0:
             raise RuntimeError(f"{cfg.name}: status {rc}")
         n_fb = int(packed.n_fb[0].item())
-        nnz = int(packed.counts.to(torch.int64).sum().item())
+        cnts = packed.counts.to(torch.int64)
+        nnz = int(cnts[cnts != tw.DENSE_TILE].sum().item())   # entries stored in TwELL cells
         ms = timed(fn, args.steps)
         tw.twell_profile_reset()
         tw.twell_profile_enable(True)
@@ -440,6 +446,9 @@ def bench_next(args):
             flops = 2.0 * 2 * N * d * f
             roof_us = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
             bound = "tensor (gate and up GEMMs)"
+        elif cfg.name.startswith("1b"):
+            roof_us = 2.0 * N * d * f / (peaks["bf16_tflops"] * 1e12) * 1e6
+            bound = "tensor (up GEMM)"
         else:
             H = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
             tw.twell_unpack(packed, H)
@@ -457,7 +466,9 @@ def bench_next(args):
             "config": {"workload": cfg.name, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
                        "sparsity_target": cfg.sparsity, "gated": cfg.gated,
                        "l2": "flushed between steps (2x L2 write)"},
-            "layer": {"n_fb": n_fb, "twell_entries": nnz},
+            "layer": {"n_fb": n_fb, "twell_entries": nnz,
+                      "hybrid": "tiles" if hybrid == tw.HYBRID_TILES else "rows",
+                      "fallback_bytes": n_fb * (T if hybrid == tw.HYBRID_TILES else f) * 2},
             "kernels": kernels,
             "roofline": {"bound": bound, "time_us": round(roof_us, 2), "frac": round(roof_us / (ms * 1e3), 4),
                          "frac_graph": round(roof_us / (ms_graph * 1e3), 4), "peak_source": peak_src},
