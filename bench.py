@@ -268,11 +268,13 @@ def bench_ours(args, rank, world, local):
         return {"j_per_token": watts * loop_ms * 1e-3 / (iters * N), "power_w": round(watts, 1),
                 "ms_per_call": round(loop_ms / iters, 4), "samples": len(pw)}
 
-    en_step = energy(step, statistics.median(step_ms))
-    en_fwd = energy(fwd, statistics.median(fwd_ms))
-    Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
-    en_dense = energy(dense, statistics.median(dense_ms))
-    del Hbuf
+    en_step = en_fwd = en_dense = None
+    if not args.no_energy:
+        en_step = energy(step, statistics.median(step_ms))
+        en_fwd = energy(fwd, statistics.median(fwd_ms))
+        Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+        en_dense = energy(dense, statistics.median(dense_ms))
+        del Hbuf
 
     # end to end through the C ABI with host buffers (pinned): every step
     # uploads its X and dY and downloads its Y and dX inside the timed loop.
@@ -595,6 +597,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-energy", action="store_true",
+                    help="skip the energy loops (e.g. to keep an ncu launch list to the timed steps)")
     ap.add_argument("--only", default="",
                     help="with --next: comma-separated workload names to run (default: all)")
     ap.add_argument("--next", action="store_true",
