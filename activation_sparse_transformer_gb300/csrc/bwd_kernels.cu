@@ -48,17 +48,6 @@ Layout flat(const twell_t& L) {
 constexpr int kWarps = 8;
 constexpr int kU = 4;  // rows in flight per lane in dw_kernel
 
-__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
-  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
-  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
-  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
-  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
-  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
-  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
-  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
-  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
-}
-
 // Unit-major regrouping of the TwELL entries.  A CTA owns a block of
 // kBwdRowsPerBlock (= 32) rows.  For every hidden unit it builds a 32-bit mask
 // with bit r set when row r of the block stores that unit (a unit appears at
@@ -115,16 +104,23 @@ __global__ void unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_bl
 }
 
 // Exclusive scan of the per-unit totals: col_ptr[j] = start, col_ptr[f] = all.
+// One CTA; each thread takes 8 consecutive units per pass (8192 per pass).
 __global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ col_ptr, int f) {
   __shared__ int warp_tot[32];
   __shared__ int base_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) base_s = 0;
   __syncthreads();
-  for (int start = 0; start < f; start += 1024) {
-    const int j = start + tid;
-    const int v = j < f ? col_ptr[j] : 0;
-    int incl = v;
+  for (int start = 0; start < f; start += 1024 * 8) {
+    const int j0 = start + tid * 8;
+    int v[8];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = j0 + i < f ? col_ptr[j0 + i] : 0;
+      local += v[i];
+    }
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, incl, o);
@@ -143,10 +139,14 @@ __global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ c
       warp_tot[lane] = wi - w;
     }
     __syncthreads();
-    const int excl = base_s + warp_tot[warp] + incl - v;
-    if (j < f) col_ptr[j] = excl;
+    int run = base_s + warp_tot[warp] + incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (j0 + i < f) col_ptr[j0 + i] = run;
+      run += v[i];
+    }
     __syncthreads();
-    if (tid == 1023) base_s = excl + v;
+    if (tid == 1023) base_s = run;
     __syncthreads();
   }
   if (tid == 0) col_ptr[f] = base_s;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         gb += en[u].dz;
         if (active) {
           fma8_bf16(a_down, static_cast<uint16_t>(en[u].h_bits), g[u]);
-          fma8(a_in, en[u].dz, x[u]);
+          fma8_f32x2(a_in, en[u].dz, x[u]);
         }
       }
     }
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (active) {
         fma8_bf16(a_down, static_cast<uint16_t>(en.h_bits),
                   __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en.row) * d + c0)));
-        fma8(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
+        fma8_f32x2(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
       }
     }
     __syncwarp();
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(256) fb_db_kernel(Layout L, const uint16_t* __
   const int nfb = min(*L.n_fb, L.fb_cap);
   float s = 0.f;
   if (j < L.f)
+#pragma unroll 4
     for (int slot = warp; slot < nfb; slot += 8)
       s += bf16_bits_to_float(dz_hl[static_cast<int64_t>(2 * slot) * L.f + j]) +
            bf16_bits_to_float(dz_hl[static_cast<int64_t>(2 * slot + 1) * L.f + j]);

@@ -213,6 +213,25 @@ __device__ __forceinline__ void fma8_bf16(float (&acc)[8], uint16_t v, const uin
       : "h"(v), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
 }
 
+// acc[0..7] += v * w's 8 bf16 (widened exactly to fp32), two fp32 lanes per
+// instruction (fma.rn.f32x2: each lane one fused multiply-add, rounded to
+// nearest, the same result as fmaf per element).
+__device__ __forceinline__ void fma8_f32x2(float (&acc)[8], float v, const uint4& w) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t lo = ws[q] << 16, hi = ws[q] & 0xFFFF0000u;
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "mov.b64 c, {%4, %4};\n\t"
+        "fma.rn.f32x2 a, c, b, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(acc[2 * q]), "+f"(acc[2 * q + 1])
+        : "r"(lo), "r"(hi), "f"(v));
+  }
+}
+
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   __nv_bfloat16 b = __float2bfloat16_rn(x);
   return *reinterpret_cast<uint16_t*>(&b);

@@ -58,17 +58,6 @@ __device__ __forceinline__ float as_f32<uint16_t>(uint16_t v) { return bf16_bits
 template <>
 __device__ __forceinline__ float as_f32<float>(float v) { return v; }
 
-__device__ __forceinline__ void fma8(float (&acc)[8], float v, const uint4& w) {
-  acc[0] = fmaf(v, bf16_lo(w.x), acc[0]);
-  acc[1] = fmaf(v, bf16_hi(w.x), acc[1]);
-  acc[2] = fmaf(v, bf16_lo(w.y), acc[2]);
-  acc[3] = fmaf(v, bf16_hi(w.y), acc[3]);
-  acc[4] = fmaf(v, bf16_lo(w.z), acc[4]);
-  acc[5] = fmaf(v, bf16_hi(w.z), acc[5]);
-  acc[6] = fmaf(v, bf16_lo(w.w), acc[6]);
-  acc[7] = fmaf(v, bf16_hi(w.w), acc[7]);
-}
-
 // Entry of the per-warp list.  bf16 values: one word, hidden unit j in the low
 // 16 bits and the value's bits in the high 16.  fp32 values: (j, value).
 template <typename VT>
@@ -90,7 +79,7 @@ struct RowEntry<float> {
   float v;
   static __device__ __forceinline__ RowEntry make(int j, float val) { return RowEntry{j, val}; }
   __device__ __forceinline__ int j() const { return jj; }
-  __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const { fma8(acc, v, wr); }
+  __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const { fma8_f32x2(acc, v, wr); }
 };
 
 __device__ __forceinline__ uint4 pack8_bf16(const float (&acc)[8]) {
