@@ -25,6 +25,7 @@ EXPORTED = [
     "twell_bwd_workspace_bytes", "twell_dense_ffn_fwd", "twell_read_status", "twell_status_string",
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
+    "twell_selftest_wait_timeout",
 ]
 
 
@@ -74,6 +75,7 @@ def load_library() -> ctypes.CDLL:
         "twell_ffn_fwd_noalloc": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P]),
         "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
         "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
+        "twell_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -225,6 +227,13 @@ def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
 def twell_read_status(packed: Packed, stream=None) -> int:
     st = packed.struct()
     return int(load_library().twell_read_status(ctypes.byref(st), _stream(stream)))
+
+
+def twell_selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:
+    """Run the pipelines' bounded wait on a barrier nothing arrives on; status
+    (a device int32 tensor) becomes TWELL_ERR_WAIT_TIMEOUT once limit_ns pass."""
+    _check(load_library().twell_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)),
+           "twell_selftest_wait_timeout")
 
 
 def twell_launch_count() -> int:

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtwell.so")
-SOURCES = ["api.cu", "gemm_tcgen05.cu", "fwd_kernels.cu", "pack_kernels.cu", "bwd_kernels.cu", "spmm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_tcgen05.cu", "fwd_kernels.cu", "pack_kernels.cu", "bwd_kernels.cu", "spmm.cu", "noalloc.cu",
+           "selftest.cu"]
 HEADERS = ["sm103.cuh", "twell_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -229,6 +229,14 @@ TWELL_API int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, cons
  * else TWELL_OK. */
 TWELL_API int twell_read_status(const twell_t* layout, twell_stream_t stream);
 
+/* Self-test of the failure detection (no counterpart on the pages): launches
+ * one small kernel that runs the pipelines' bounded mbarrier wait on a barrier
+ * nothing arrives on; after limit_ns of GPU time the wait gives up and
+ * *status (device int32) is set to TWELL_ERR_WAIT_TIMEOUT, exactly as a
+ * stalled GEMM or SpMM pipeline would report, and the kernel returns.
+ * 0 < limit_ns <= 10 s.  Asynchronous on `stream`. */
+TWELL_API int twell_selftest_wait_timeout(int32_t* status, uint64_t limit_ns, twell_stream_t stream);
+
 /* Static string for a TWELL_* code. */
 TWELL_API const char* twell_status_string(int code);
 

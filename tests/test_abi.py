@@ -62,6 +62,15 @@ def test_host_argument_checks_without_gpu(lib):
     # d_ff not a multiple of 128 (but of T)
     bad = tw.twell_t(16, 960, 64, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
     assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -3
+    # unknown hybrid variant; tile pool too large for 24-bit slots
+    bad = tw.twell_t(16, 1024, 64, 8, 4, 7, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -1
+    bad = tw.twell_t(16, 1024, 64, 8, 1 << 21, tw.HYBRID_TILES, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000,
+                     0x7000, 0x8000)
+    assert lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(bad), None) == -3
+    # the wait self-test checks its arguments on the host
+    assert lib.twell_selftest_wait_timeout(None, 1000, None) == -1
+    assert lib.twell_selftest_wait_timeout(ctypes.c_void_p(0x10000), 0, None) == -1
     # a well-formed call reaches the device check and stops there on a CPU-only host
     rc = lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(L), None)
     try:
