@@ -253,6 +253,71 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(sum);
 }
 
+// Whole rows, row-granular hybrid: a CTA per row at a time (persistent,
+// stride gridDim.x).  Every 256-column block of a row gathers the same W rows,
+// so the CTA flattens the row's entries once -- warp w expands tiles
+// [w * tpw, (w + 1) * tpw), a CTA prefix over the warps' totals places them
+// in ascending hidden-unit order -- and its 8 warps then stream column blocks
+// w, w + 8, ... from that one shared list.
+template <typename VT>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+    spmm_rowcta_kernel(const SpmmArgs a, const uint16_t* __restrict__ W) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int warp_tot[kWarps + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw);
+  const VT* vals = static_cast<const VT*>(a.values);
+  const int cbs = (a.d + 255) / 256;
+  const int tpw = (a.nt + kWarps - 1) / kWarps;
+  for (int row = blockIdx.x; row < a.N; row += gridDim.x) {
+    // fallback rows are written by the fallback path, which may run concurrently
+    if (a.row_fb[row] >= 0) continue;  // uniform over the CTA
+    const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+    const int t_beg = min(a.nt, warp * tpw), t_end = min(a.nt, t_beg + tpw);
+    // this warp's tiles: counts, warp prefix (rounds of 32 tiles)
+    int wtotal = 0;
+    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+      const int t = t0 + lane;
+      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+      wtotal += __reduce_add_sync(0xffffffffu, cnt);
+    }
+    if (lane == 0) warp_tot[warp] = wtotal;
+    __syncthreads();
+    int base = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = warp_tot[w];
+      base += w < warp ? v : 0;
+      total += v;
+    }
+    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+      const int t = t0 + lane;
+      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      const int64_t cell = cell0 + t;
+      const int pos = base + incl - cnt;
+      for (int s2 = 0; s2 < cnt; ++s2)
+        list[pos + s2] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s2], vals[cell * a.C + s2]);
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    __syncthreads();
+    for (int cb = warp; cb < cbs; cb += kWarps) {
+      const int c0 = cb * 256 + lane * 8;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (c0 < a.d) {
+        stream_list<VT>(a, W + c0, list, total, acc);
+        *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
+      }
+    }
+    __syncthreads();  // the list and warp totals are rewritten for the next row
+  }
+}
+
 template <typename VT>
 int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kernel_id, cudaStream_t s) {
   if (a.N <= 0) return TWELL_OK;
@@ -274,6 +339,24 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   if (nsplit < 1 || nsplit > 64 || (nsplit > 1 && (!a.part || !a.arrivals))) return TWELL_ERR_INVALID_ARG;
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
+  if (nsplit == 1 && !a.pool) {
+    // a CTA per row: one shared flatten for all column blocks; persistent, three
+    // CTAs per SM (the register limit)
+    auto rk = spmm_rowcta_kernel<VT>;
+    const size_t rsmem = static_cast<size_t>(a.nt) * a.C * sizeof(RowEntry<VT>);
+    static bool rattr[64] = {};
+    if (dev < 64 && !rattr[dev]) {
+      if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess)
+        return TWELL_ERR_CUDA;
+      rattr[dev] = true;
+    }
+    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 3 * static_cast<int64_t>(sm_count()))));
+    {
+      LaunchScope ls(kernel_id, s);
+      rk<<<rgrid, kWarps * 32, rsmem, s>>>(a, W);
+    }
+    return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+  }
   if (nsplit == 1) {
     // persistent: three CTAs per SM (the register limit), warps stride over the items
     const int64_t items = static_cast<int64_t>(a.N) * ((a.d + 255) / 256);
