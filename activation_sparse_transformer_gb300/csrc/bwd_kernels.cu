@@ -11,12 +11,12 @@
 //             GEMM of dZ (as bf16 high + low parts) with W_in^T read N-major
 //   unit lists  the TwELL entries regrouped by hidden unit, rows ascending,
 //             built deterministically (block histograms, scans, ordered fill)
-//   dw_kernel dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] = sum_n dZ[n][j] X[n],
+//   dw_unitcta_kernel  dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] = sum_n dZ[n][j] X[n],
 //             db[j] = sum_n dZ[n][j] over the TwELL entries
 //   fallback  the dense fallback rows' share of dW_down and dW_in^T stored
 //             first by tcgen05 GEMMs with both operands M/N-major (H_fb^T .
 //             dY_fb and dZ_fb^T . X_fb, dZ as high + low bf16 parts) on the
-//             second stream; dw_kernel adds the TwELL share on top; a column
+//             second stream; dw_unitcta_kernel adds the TwELL share on top; a column
 //             sum adds the fallback share of db
 // No atomics on outputs, so every result is deterministic.
 #include <cuda_runtime.h>
@@ -46,7 +46,7 @@ Layout flat(const twell_t& L) {
 }
 
 constexpr int kWarps = 8;
-constexpr int kU = 4;  // rows in flight per lane in dw_kernel
+constexpr int kU = 4;  // entries in flight per lane in dw_unitcta_kernel (2 rows each)
 
 // Unit-major regrouping of the TwELL entries.  A CTA owns a block of
 // kBwdRowsPerBlock (= 32) rows.  For every hidden unit it builds a 32-bit mask
@@ -178,11 +178,9 @@ __global__ void __launch_bounds__(kListThreads) unit_fill_kernel(Layout L, int n
   }
 }
 
-// Warp per hidden unit j and 256 columns: TwELL entries in ascending row.
-// The warp stages 32 entries at a time (row, h, dZ) in its shared-memory
-// slot with one coalesced load per lane, then walks them with kU rows of dY
-// and X in flight per lane.  h is exactly a bf16 value, so the dW_down update
-// uses the mixed bf16 x bf16 + fp32 fma.
+// One staged entry of a hidden unit's list (row, h, dZ); rows ascend.  h is
+// exactly a bf16 value, so the dW_down update uses the mixed bf16 x bf16 +
+// fp32 fma; the dW_in^T update multiplies the fp32 dZ by X two lanes at a time.
 struct UnitEntry {
   int32_t row;
   uint32_t h_bits;  // bf16 bits of h in the low half
@@ -190,78 +188,89 @@ struct UnitEntry {
   float pad;
 };
 
-__global__ void __launch_bounds__(kWarps * 32)
-    dw_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
-              const float* __restrict__ col_h, const float* __restrict__ col_dz, const uint16_t* __restrict__ X,
-              const uint16_t* __restrict__ dY, int d, float* __restrict__ dW_inT, float* __restrict__ dW_down,
-              float* __restrict__ db, const int32_t* __restrict__ n_fb, int fb_cap) {
-  __shared__ UnitEntry stage[kWarps][32];
+// A CTA per hidden unit at a time (persistent, stride gridDim.x): the unit's
+// entries are staged once per 256 into shared memory by the whole CTA, and
+// warp w accumulates column blocks w, w + 8, ... from them (the same entries
+// serve every column block, so they are read from global memory once).
+constexpr int kDwChunk = kWarps * 32;
+
+__global__ void __launch_bounds__(kWarps * 32, 3)
+    dw_unitcta_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
+                      const float* __restrict__ col_h, const float* __restrict__ col_dz,
+                      const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
+                      float* __restrict__ dW_inT, float* __restrict__ dW_down, float* __restrict__ db,
+                      const int32_t* __restrict__ n_fb, int fb_cap) {
+  __shared__ UnitEntry stage[kDwChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * kWarps + warp;
-  if (j >= f) return;
-  const int c0 = blockIdx.y * 256 + lane * 8;
-  const bool active = c0 < d;
-  float a_down[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float gb = 0.f;
-  const int e0 = col_ptr[j], e1 = col_ptr[j + 1];
-  UnitEntry* st = stage[warp];
-  for (int b = e0; b < e1; b += 32) {
-    const int m = min(32, e1 - b);
-    if (lane < m) {
-      const float h = col_h[b + lane];
-      st[lane] = UnitEntry{col_rows[b + lane], static_cast<uint32_t>(__float_as_uint(h) >> 16), col_dz[b + lane], 0.f};
-    }
-    __syncwarp();
-    int e = 0;
-    for (; e + kU <= m; e += kU) {
-      uint4 g[kU], x[kU];
-      UnitEntry en[kU];
+  const bool have_fb = min(*n_fb, fb_cap) > 0;
+  const int cbs = (d + 255) / 256;
+  for (int j = blockIdx.x; j < f; j += gridDim.x) {
+    const int e0 = col_ptr[j], e1 = col_ptr[j + 1];
+    for (int cb0 = 0; cb0 < cbs; cb0 += kWarps) {
+      const int c0 = (cb0 + warp) * 256 + lane * 8;
+      const bool active = cb0 + warp < cbs && c0 < d;
+      float a_down[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float gb = 0.f;
+      for (int b = e0; b < e1; b += kDwChunk) {
+        const int m = min(kDwChunk, e1 - b);
+        __syncthreads();  // the previous chunk has been consumed
+        if (static_cast<int>(threadIdx.x) < m) {
+          const int q = b + threadIdx.x;
+          stage[threadIdx.x] = UnitEntry{col_rows[q], static_cast<uint32_t>(__float_as_uint(col_h[q]) >> 16),
+                                         col_dz[q], 0.f};
+        }
+        __syncthreads();
+        int e = 0;
+        for (; e + kU <= m; e += kU) {
+          uint4 g[kU], x[kU];
+          UnitEntry en[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        en[u] = st[e + u];
-        if (active) {
-          g[u] = __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en[u].row) * d + c0));
-          x[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en[u].row) * d + c0));
+          for (int u = 0; u < kU; ++u) {
+            en[u] = stage[e + u];
+            if (active) {
+              g[u] = __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en[u].row) * d + c0));
+              x[u] = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en[u].row) * d + c0));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            gb += en[u].dz;
+            if (active) {
+              fma8_bf16(a_down, static_cast<uint16_t>(en[u].h_bits), g[u]);
+              fma8_f32x2(a_in, en[u].dz, x[u]);
+            }
+          }
+        }
+        for (; e < m; ++e) {
+          const UnitEntry en = stage[e];
+          gb += en.dz;
+          if (active) {
+            fma8_bf16(a_down, static_cast<uint16_t>(en.h_bits),
+                      __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en.row) * d + c0)));
+            fma8_f32x2(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
+          }
         }
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        gb += en[u].dz;
-        if (active) {
-          fma8_bf16(a_down, static_cast<uint16_t>(en[u].h_bits), g[u]);
-          fma8_f32x2(a_in, en[u].dz, x[u]);
-        }
-      }
-    }
-    for (; e < m; ++e) {
-      const UnitEntry en = st[e];
-      gb += en.dz;
       if (active) {
-        fma8_bf16(a_down, static_cast<uint16_t>(en.h_bits),
-                  __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en.row) * d + c0)));
-        fma8_f32x2(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
+        float4* od = reinterpret_cast<float4*>(dW_down + static_cast<int64_t>(j) * d + c0);
+        float4* oi = reinterpret_cast<float4*>(dW_inT + static_cast<int64_t>(j) * d + c0);
+        if (have_fb) {
+          // the fallback rows' share was stored first by the tensor cores
+          const float4 d0 = od[0], d1 = od[1], i0 = oi[0], i1 = oi[1];
+          a_down[0] += d0.x; a_down[1] += d0.y; a_down[2] += d0.z; a_down[3] += d0.w;
+          a_down[4] += d1.x; a_down[5] += d1.y; a_down[6] += d1.z; a_down[7] += d1.w;
+          a_in[0] += i0.x; a_in[1] += i0.y; a_in[2] += i0.z; a_in[3] += i0.w;
+          a_in[4] += i1.x; a_in[5] += i1.y; a_in[6] += i1.z; a_in[7] += i1.w;
+        }
+        od[0] = make_float4(a_down[0], a_down[1], a_down[2], a_down[3]);
+        od[1] = make_float4(a_down[4], a_down[5], a_down[6], a_down[7]);
+        oi[0] = make_float4(a_in[0], a_in[1], a_in[2], a_in[3]);
+        oi[1] = make_float4(a_in[4], a_in[5], a_in[6], a_in[7]);
       }
+      if (cb0 == 0 && threadIdx.x == 0) db[j] = gb;
     }
-    __syncwarp();
   }
-  if (active) {
-    float4* od = reinterpret_cast<float4*>(dW_down + static_cast<int64_t>(j) * d + c0);
-    float4* oi = reinterpret_cast<float4*>(dW_inT + static_cast<int64_t>(j) * d + c0);
-    if (min(*n_fb, fb_cap) > 0) {
-      // the fallback rows' share was stored first by the tensor cores
-      const float4 d0 = od[0], d1 = od[1], i0 = oi[0], i1 = oi[1];
-      a_down[0] += d0.x; a_down[1] += d0.y; a_down[2] += d0.z; a_down[3] += d0.w;
-      a_down[4] += d1.x; a_down[5] += d1.y; a_down[6] += d1.z; a_down[7] += d1.w;
-      a_in[0] += i0.x; a_in[1] += i0.y; a_in[2] += i0.z; a_in[3] += i0.w;
-      a_in[4] += i1.x; a_in[5] += i1.y; a_in[6] += i1.z; a_in[7] += i1.w;
-    }
-    od[0] = make_float4(a_down[0], a_down[1], a_down[2], a_down[3]);
-    od[1] = make_float4(a_down[4], a_down[5], a_down[6], a_down[7]);
-    oi[0] = make_float4(a_in[0], a_in[1], a_in[2], a_in[3]);
-    oi[1] = make_float4(a_in[4], a_in[5], a_in[6], a_in[7]);
-  }
-  if (blockIdx.y == 0 && lane == 0) db[j] = gb;
 }
 
 // Operands of the fallback rows' weight-gradient GEMMs, K = fallback slot:
@@ -393,7 +402,6 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const Layout L = flat(Lh);
   const int f = Lh.d_ff;
   const int N = Lh.n_rows;
-  const int col_blocks = (d + 255) / 256;
   if (N > 0) {
     // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
     SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
@@ -402,7 +410,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   }
   // Second stream: the fallback rows' weight-gradient share (stored into dW
   // first), then dX (fallback GEMMs + the TwELL rows' gather-SpMM).  This
-  // stream: the unit-major lists, then dw_kernel adds the TwELL share once the
+  // stream: the unit-major lists, then dw_unitcta_kernel adds the TwELL share once the
   // fallback share is in place.
   AuxFork fork(s);
   TW_TRY_RC(fork.status());
@@ -421,7 +429,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     TW_TRY_RC(launch_gemm_store_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, dW_inT, d, Lh.status,
                                    TWELL_KERNEL_DW, a));
   }
-  TW_TRY_RC(fork.aux_to_main());  // dW holds the fallback share before dw_kernel runs
+  TW_TRY_RC(fork.aux_to_main());  // dW holds the fallback share before dw_unitcta_kernel runs
   if (N > 0) {
     if (fb) {
       // one GEMM over K = 2 d_ff: row s of dz_hl viewed with stride 2 d_ff is
@@ -467,9 +475,9 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
-    dw_kernel<<<dim3((f + kWarps - 1) / kWarps, col_blocks), kWarps * 32, 0, s>>>(
-        f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d, dW_inT, dW_down, db, Lh.n_fb,
-        fb ? Lh.fb_cap : 0);
+    const int grid = std::max(1, std::min(f, 3 * sm_count()));
+    dw_unitcta_kernel<<<grid, kWarps * 32, 0, s>>>(f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d,
+                                                   dW_inT, dW_down, db, Lh.n_fb, fb ? Lh.fb_cap : 0);
   }
   TW_CHECK_LAUNCH();
   if (fb) {
