@@ -404,32 +404,41 @@ struct DenseEpi {
 };
 
 // fp32 tile store.  Each warp turns its 32 rows x 32 columns around in shared
-// memory (33-word rows: no bank conflicts either way) so that every store
-// instruction writes one full 128-byte row segment.
+// memory so that its stores write whole 128-byte row segments, four rows per
+// 16-byte-per-lane instruction.  The 16-byte chunks of a staged row are
+// XOR-swizzled by the row (chunk k of row r sits at k ^ (r & 7)), so both the
+// row-wise writes and the column-wise reads are free of bank conflicts.
 struct PartialEpi {
   static constexpr bool kDualB = false;
   using Params = PartialEpiParams;
-  static constexpr int kPitch = 33;
-  static constexpr uint32_t kSmemBytes = (kEpiThreads / 32) * 32 * kPitch * 4;
+  static constexpr uint32_t kSmemBytes = (kEpiThreads / 32) * 32 * 32 * 4;
 
   template <int BN>
   static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
                                                int ks, uint8_t* smem, int et) {
     const int lane = threadIdx.x & 31;
     const int row0 = row - lane;  // first row of this warp's 32
-    float* st = reinterpret_cast<float*>(smem) + (et >> 5) * 32 * kPitch;
-    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + col0 + lane;
+    float* st = reinterpret_cast<float*>(smem) + (et >> 5) * 32 * 32;
+    float* base = p.part + static_cast<int64_t>(ks) * p.split_stride + col0;
+    const int k_rd = lane & 7;         // 16-byte chunk this lane reads / stores
+    const int r_rd = lane >> 3;        // row within each group of four
 #pragma unroll 1
     for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
       uint32_t r[32];
       tmem_ld32(taddr + c * 32, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) st[lane * kPitch + i] = __uint_as_float(r[i]);
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(st + lane * 32 + 4 * (k ^ (lane & 7))) =
+            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
       __syncwarp();
-#pragma unroll 4
-      for (int rr = 0; rr < 32; ++rr)
-        if (row0 + rr < M) base[static_cast<int64_t>(row0 + rr) * p.ld + c * 32] = st[rr * kPitch + lane];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int rr = 4 * g + r_rd;
+        const uint4 v = *reinterpret_cast<const uint4*>(st + rr * 32 + 4 * (k_rd ^ (rr & 7)));
+        if (row0 + rr < M)
+          *reinterpret_cast<uint4*>(base + static_cast<int64_t>(row0 + rr) * p.ld + c * 32 + 4 * k_rd) = v;
+      }
       __syncwarp();
     }
   }
