@@ -69,38 +69,47 @@ __device__ __forceinline__ void build_row_masks(const Layout& L, int r0, int r1,
 
 constexpr int kListThreads = 1024;  // the list passes are latency-bound: many cells in flight
 
-// Pass 1: entries per (unit, row block), stored unit-major (blk_count[j][b]).
+// Pass 1: entries per (unit, row block), stored block-major (blk_count[b][j]:
+// each CTA writes one contiguous row of f counts).
 __global__ void __launch_bounds__(kListThreads) unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
   extern __shared__ uint32_t mask[];
   const int r0 = blockIdx.x * kBwdRowsPerBlock;
   const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
   build_row_masks(L, r0, r1, mask);
   for (int j = threadIdx.x; j < L.f; j += blockDim.x)
-    blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] = __popc(mask[j]);
+    blk_count[static_cast<int64_t>(blockIdx.x) * L.f + j] = __popc(mask[j]);
 }
 
-// Warp per unit: exclusive scan over its row blocks (in place); the total goes
-// to col_ptr[j].
-__global__ void unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f,
-                                       int32_t* __restrict__ col_ptr) {
+// Exclusive scan over the row blocks of each unit, in place; the unit's total
+// goes to col_ptr[j].  A CTA takes 32 units (lane = unit, so every access is a
+// 128-byte row segment of blk_count[b][j]); warp w scans a contiguous range of
+// blocks and the eight warps' totals are combined in warp order.
+__global__ void __launch_bounds__(256) unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f,
+                                                              int32_t* __restrict__ col_ptr) {
+  __shared__ int tot[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (j >= f) return;
-  int32_t* p = blk_count + static_cast<int64_t>(j) * n_blocks;
-  int run = 0;
-  for (int b0 = 0; b0 < n_blocks; b0 += 32) {
-    const int b = b0 + lane;
-    const int c = b < n_blocks ? p[b] : 0;
-    int incl = c;
+  const int j = blockIdx.x * 32 + lane;
+  const bool in = j < f;
+  const int per = (n_blocks + 7) / 8;
+  const int b0 = min(n_blocks, warp * per), b1 = min(n_blocks, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += in ? blk_count[static_cast<int64_t>(b) * f + j] : 0;
+  tot[warp][lane] = sum;
+  __syncthreads();
+  int run = 0, all = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
-    }
-    if (b < n_blocks) p[b] = run + incl - c;
-    run += __shfl_sync(0xffffffffu, incl, 31);
+  for (int w = 0; w < 8; ++w) {
+    run += w < warp ? tot[w][lane] : 0;
+    all += tot[w][lane];
   }
-  if (lane == 0) col_ptr[j] = run;
+  if (!in) return;
+  for (int b = b0; b < b1; ++b) {
+    int32_t* q = blk_count + static_cast<int64_t>(b) * f + j;
+    const int c = *q;
+    *q = run;
+    run += c;
+  }
+  if (warp == 0) col_ptr[j] = all;
 }
 
 // Exclusive scan of the per-unit totals: col_ptr[j] = start, col_ptr[f] = all.
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kListThreads) unit_fill_kernel(Layout L, int n
     const int r = i / L.nt;
     for (int s = 0; s < cnt; ++s) {
       const int j = t * L.T + L.idx[cell * L.C + s];
-      const int pos = col_ptr[j] + blk_count[static_cast<int64_t>(j) * n_blocks + blockIdx.x] +
+      const int pos = col_ptr[j] + blk_count[static_cast<int64_t>(blockIdx.x) * L.f + j] +
                       __popc(mask[j] & ((1u << r) - 1u));
       col_rows[pos] = r0 + r;
       col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + s]);
@@ -459,7 +468,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_block_scan_kernel<<<(f + 7) / 8, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
+    unit_block_scan_kernel<<<(f + 31) / 32, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
   }
   TW_CHECK_LAUNCH();
   {
