@@ -2,10 +2,14 @@
 """Throughput of the TwELL activation-sparse FFN layer on one GB300.
 
 One step = the whole layer: twell_ffn_fwd (tensor-core up-projection with the
-fused bias/ReLU/TwELL-pack epilogue, hybrid routing, dense-fallback recompute,
-gather-SpMM down-projection) followed by twell_ffn_bwd (SDDMM with the L1
-term, dX gather, unit-major weight gradients), on the 1B-model FFN shape
-N=4096, d_model=2048, d_ff=8192, T=128, C=8 with synthetic seeded inputs.
+fused bias/ReLU/TwELL-pack epilogue, hybrid routing, dense fallback rows on the
+tensor cores, gather-SpMM down-projection) followed by twell_ffn_bwd (SDDMM
+with the L1 term, dX gather, unit-major weight gradients), on the 1B-model FFN
+shape N=4096, d_model=2048, d_ff=8192, T=128, C=8 with synthetic seeded inputs.
+
+With N GPUs (torchrun, one rank per GPU) every rank runs its own batch of the
+same shape (weak scaling, no data-path collective); the job's time per step is
+the slowest rank's and `value` counts the tokens of all ranks.
 
 Prints one JSON line.  `value` is tokens/s of the step with inputs resident in
 HBM (L2 flushed between steps by writing a 2x-L2 buffer); `e2e` is the same
@@ -40,6 +44,28 @@ def load_peaks():
             d = json.load(fh)
         return d, "measured"
     return dict(PEAKS_FALLBACK), "fallback"
+
+
+def rank_config(cfg, rank: int):
+    """Weak scaling: every rank draws its own batch of the same shape (seed
+    shifted by 1000 x rank); rank 0 keeps the configuration's own seed."""
+    import synth
+    return cfg if rank == 0 else synth.FFNConfig(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
+
+
+def max_over_ranks(values, world: int, device):
+    """Element-wise maximum over the ranks: the slowest rank sets the job's time."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world: int, n_rows: int, ms: float) -> float:
+    """Tokens per second of the whole job: every rank's batch, the slowest rank's time."""
+    return world * n_rows / (ms * 1e-3)
 
 
 def dist_info():
@@ -142,11 +168,8 @@ def bench_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     tw.load_library()
     cfg = synth.CONFIGS[args.config]
-    base = synth.make_ffn_inputs(cfg)
     # every rank draws its own batch (weak scaling: per-GPU work is fixed)
-    if rank:
-        shifted = synth.FFNConfig(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
-        base = synth.make_ffn_inputs(shifted)
+    base = synth.make_ffn_inputs(rank_config(cfg, rank))
     N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
     lam = cfg.l1_lambda or 1e-4
     dY_np = synth.make_grad_output(N, d, seed=cfg.seed + 77 + rank)
@@ -338,13 +361,7 @@ def bench_ours(args, rank, world, local):
     def med(v):
         return statistics.median(v)
 
-    ms = med(step_ms)
-    if world > 1:
-        t = torch.tensor([ms, med(e2e_ms)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_m = float(t[0]), float(t[1])
-    else:
-        e2e_m = med(e2e_ms)
+    ms, e2e_m = max_over_ranks([med(step_ms), med(e2e_ms)], world, dev)
 
     peaks, peak_src = load_peaks()
     flops_up = 2.0 * N * d * f
@@ -367,7 +384,7 @@ def bench_ours(args, rank, world, local):
     roof_fwd_us = max(flops_up / (peaks["bf16_tflops"] * 1e12),
                       (N * d * 2 * 2 + f * d * 2 * 2 + N * (f // T) * (3 * C + 1)) / (peaks["hbm_gbs"] * 1e9)) * 1e6
     result = {
-        "metric": METRIC, "value": round(world * N / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(job_throughput(world, N, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
         "config": {"workload": WORKLOAD, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
@@ -383,7 +400,7 @@ def bench_ours(args, rank, world, local):
                   "packed_h_bytes": int(packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel()
                                         + fb * f * 2),
                   "dense_h_bytes": N * f * 2},
-        "e2e": {"value": round(world * N / (e2e_m * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(job_throughput(world, N, e2e_m), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_m, 4),
                 "how": "through the C ABI; each step uploads X, dY from pinned host memory and downloads Y, "
                        "dX, on two copy streams one step ahead / behind the compute; 4 rotating device buffer "
