@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 // in ascending hidden-unit order -- and its 8 warps then stream column blocks
 // w, w + 8, ... from that one shared list.
 template <typename VT>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+__global__ void __launch_bounds__(kWarps * 32, 4)
     spmm_rowcta_kernel(const SpmmArgs a, const uint16_t* __restrict__ W) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_tot[kWarps + 1];
@@ -350,7 +350,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
         return TWELL_ERR_CUDA;
       rattr[dev] = true;
     }
-    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 3 * static_cast<int64_t>(sm_count()))));
+    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 4 * static_cast<int64_t>(sm_count()))));
     {
       LaunchScope ls(kernel_id, s);
       rk<<<rgrid, kWarps * 32, rsmem, s>>>(a, W);
