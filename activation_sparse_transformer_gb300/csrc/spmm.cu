@@ -7,23 +7,26 @@
 //
 // At ~1% density a W row is used by ~1% of the tokens, so staging W slabs for
 // a token block buys almost no reuse unless the block holds thousands of
-// tokens (far more accumulators than an SM has registers).  The kernel is
-// therefore built for memory-level parallelism instead: a warp owns one token
-// row and 256 output columns at a time (a persistent grid, warps striding over
-// the (row, column block) items).  It first flattens the row's stored entries
-// (tile-major, slots ascending, so hidden units ascend) into its shared-memory
-// list -- counts of 32 tiles per round, a warp prefix sum, each lane
-// expanding its own cell -- then streams the named W rows with coalesced
-// 16-byte loads, kU independent loads in flight per lane, and accumulates in
-// fp32 registers.  Each output sums its terms in ascending hidden-unit order.
-// Fallback rows are skipped: their rows of the output belong to the dense
-// fallback path, which may run at the same time on another stream.
+// tokens (far more accumulators than an SM has registers).  The kernels are
+// therefore built for memory-level parallelism instead.  The main one
+// (spmm_rowcta_kernel) gives a CTA one token row at a time (a persistent grid,
+// four CTAs per SM): the CTA flattens the row's stored entries (tile-major,
+// slots ascending, so hidden units ascend) into one shared-memory list, and
+// its eight warps stream the named W rows for 256-column blocks w, w + 8, ...
+// with coalesced 16-byte loads, kU independent loads in flight per lane,
+// accumulating in fp32 registers.  Each output sums its terms in ascending
+// hidden-unit order.  Fallback rows are skipped: their rows of the output
+// belong to the dense fallback path, which may run at the same time on
+// another stream.
 //
-// Small batches have too few (row, 256-column) warps to fill the GPU, so the
-// row's tiles are cut into gridDim.z consecutive ranges (each warp flattens
-// and streams only its range); each range's fp32 sums go to a partial buffer,
-// and the last CTA to finish among the ranges of a (row block, column block)
-// adds them in range order (an arrival counter, no waiting).
+// spmm_row_kernel, a warp per (row, 256-column block), serves the two other
+// cases.  The tile-granular hybrid: after a row's TwELL entries it gathers the
+// non-zeros of the row's dense tiles from the tile pool.  Small batches: too
+// few rows to fill the GPU, so the row's tiles are cut into gridDim.z
+// consecutive ranges (each warp flattens and streams only its range); each
+// range's fp32 sums go to a partial buffer, and the last CTA to finish among
+// the ranges of a (row block, column block) adds them in range order (an
+// arrival counter, no waiting).
 #include <cuda_runtime.h>
 
 #include <algorithm>
