@@ -580,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int K = args.K_dev ? min(args.K, max(0, *args.K_dev) * args.k_mul) : args.K;
   const int num_k = (K + kBK - 1) / kBK;
   const int num_units = num_k > 0 ? num_m * num_n * args.ksplit : 0;
-  const int k_per = (num_k + args.ksplit - 1) / args.ksplit;
+  // K split ks covers k-blocks [ks * num_k / ksplit, (ks + 1) * num_k / ksplit):
+  // balanced, every split non-empty when ksplit <= num_k
 
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < args.n_zero0; i += blockDim.x) args.zero0[i] = 0;
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const int m_blk = u % num_m, rest = u / num_m;
         const int n_blk = rest % num_n, ks = rest / num_n;
-        const int kb0 = ks * k_per, kb1 = min(num_k, kb0 + k_per);
+        const int kb0 = ks * num_k / args.ksplit, kb1 = (ks + 1) * num_k / args.ksplit;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, limit, abort)) {
             ok = false;
@@ -679,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const int ks = (u / num_m) / num_n;
-        const int kb0 = ks * k_per, kb1 = min(num_k, kb0 + k_per);
+        const int kb0 = ks * num_k / args.ksplit, kb1 = (ks + 1) * num_k / args.ksplit;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, limit, abort)) {
           ok = false;
           break;
@@ -764,8 +765,7 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   if (M <= 0 || N <= 0 || K <= 0) return TWELL_OK;
   const int num_k = (K + kBK - 1) / kBK;
   if (ksplit < 1 || ksplit > num_k) return TWELL_ERR_UNSUPPORTED;
-  const int k_per = (num_k + ksplit - 1) / ksplit;
-  if (k_per * (ksplit - 1) >= num_k) return TWELL_ERR_UNSUPPORTED;  // every split must own a K block
+  if (K_dev && ksplit > 1) return TWELL_ERR_UNSUPPORTED;  // a device-side K could leave a split empty
   CUtensorMap ta, tb, tb2;
   int rc;
   if (kANMajor)
@@ -840,13 +840,7 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
 
 int choose_fb_ksplit(int K, int max_split) {
   const int num_k = (K + kBK - 1) / kBK;
-  int ks = std::max(1, std::min(max_split, num_k));
-  while (ks > 1) {
-    const int per = (num_k + ks - 1) / ks;
-    if (per * (ks - 1) < num_k) break;
-    --ks;
-  }
-  return ks;
+  return std::max(1, std::min(max_split, num_k));
 }
 
 int swap_ksplit(int K) { return choose_fb_ksplit(K, 8); }
