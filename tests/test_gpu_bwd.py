@@ -98,3 +98,26 @@ def test_bwd_1b_full_size_sampled(tw):
     assert_close(dWi[cols], rWi, "dW_inT")
     assert_close(dWd[cols], rWd, "dW_down")
     assert_close(db[cols], rdb, "db")
+
+
+def test_train_shape_full_size_sampled(tw):
+    """The training configuration (N = 8192, 1% forced-dense rows, lambda 1e-4)
+    in the launch configuration the bench times, checked on sampled rows and
+    hidden units plus fallback rows."""
+    import torch
+    cfg = synth.CONFIGS["train"]
+    inp = synth.make_ffn_inputs(cfg)
+    dY = inp["dY"]
+    lam = cfg.l1_lambda
+    H, dX, dWi, dWd, db = run(tw, torch, cfg, inp, dY, lam)
+    rng = np.random.default_rng(9)
+    rows = np.sort(rng.choice(cfg.n_rows, size=128, replace=False)).astype(np.int32)
+    fbrows = np.nonzero(oracle.pack(H, cfg.tile, cfg.cap, cfg.fallback_capacity)["row_fb"] >= 0)[0][:8]
+    rows = np.unique(np.concatenate([rows, fbrows])).astype(np.int32)
+    _, dZ = oracle.grad_hidden(dY, inp["W_down"], H[rows], lam, rows=rows)
+    assert_close(dX[rows], oracle.grad_input(dZ, inp["W_inT"]), "dX")
+    cols = np.sort(rng.choice(cfg.d_ff, size=48, replace=False)).astype(np.int32)
+    rWi, rWd, rdb = oracle.grad_weights(inp["X"], inp["W_down"], H, dY, lam, cols=cols)
+    assert_close(dWi[cols], rWi, "dW_inT")
+    assert_close(dWd[cols], rWd, "dW_down")
+    assert_close(db[cols], rdb, "db")
