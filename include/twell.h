@@ -142,7 +142,12 @@ TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_st
  * h = bf16(z) where z = X.W_in + b > 0 (fp32 accumulation), else +0; Y is the
  * fp32 sum over h's non-zeros rounded once to bf16.  A tile that overflows C
  * has its dense h kept by the up-projection, so the fallback rows of fb_dense
- * hold exactly the h the GEMM produced.
+ * hold exactly the h the GEMM produced.  Batches of at most 32 rows (decode)
+ * take a path built for them: the up-projection with the hidden units on the
+ * 128-row MMA side and K split over the SMs (its fp32 partial sums added in
+ * split order), and the down-projection with each row's tiles cut into ranges
+ * added in order; results agree with the large-batch path up to fp32
+ * summation order (bit for bit on inputs whose partial sums are exact).
  * workspace: device, >= twell_fwd_workspace_bytes(...) bytes (always > 0),
  * 256-byte aligned; its contents need no initialisation and nothing in it is
  * needed once the call's work on the stream has finished, so one buffer can
