@@ -54,13 +54,6 @@ struct SpmmArgs {
   int32_t* status;
 };
 
-template <typename VT>
-__device__ __forceinline__ float as_f32(VT v);
-template <>
-__device__ __forceinline__ float as_f32<uint16_t>(uint16_t v) { return bf16_bits_to_float(v); }
-template <>
-__device__ __forceinline__ float as_f32<float>(float v) { return v; }
-
 // Entry of the per-warp list.  bf16 values: one word, hidden unit j in the low
 // 16 bits and the value's bits in the high 16.  fp32 values: (j, value).
 template <typename VT>
