@@ -105,14 +105,21 @@ int AuxFork::join() {
   return rc_;
 }
 
-int AuxFork::aux_to_main() {
+int AuxFork::mark_aux() {
   if (joined_ || rc_ != 0) return rc_;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lk(g_aux_mu);
-  AuxState& a = g_aux[dev];
-  if (cudaEventRecord(a.mid, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, a.mid, 0) != cudaSuccess)
-    rc_ = TWELL_ERR_CUDA;
+  if (cudaEventRecord(g_aux[dev].mid, aux_) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
+  return rc_;
+}
+
+int AuxFork::main_wait_mark() {
+  if (joined_ || rc_ != 0) return rc_;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_aux_mu);
+  if (cudaStreamWaitEvent(s_, g_aux[dev].mid, 0) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
   return rc_;
 }
 
@@ -364,6 +371,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   float* spmm_part = w.spmm_nsplit > 1 ? reinterpret_cast<float*>(ws + w.spmm_part_off) : nullptr;
   uint16_t* Hd = w.swap ? reinterpret_cast<uint16_t*>(ws + w.h_off) : nullptr;
   const bool swap = w.swap && !W_uT;
+  int32_t* row_counter = swap ? nullptr : spill_count + 1;  // the gather's row counter, zeroed with the count
   int32_t* arrivals = (w.swap || w.spmm_nsplit > 1) ? reinterpret_cast<int32_t*>(ws + w.arrivals_off) : nullptr;
   if (swap) {
     // the up-projection's CTA 0 zeroes row_fb and the arrival counters
@@ -384,7 +392,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     // the last CTA of the pack pass also routes the rows
     TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, arrivals, s));
   } else {
-    TW_CUDA(cudaMemsetAsync(spill_count, 0, sizeof(int32_t), s));
+    TW_CUDA(cudaMemsetAsync(spill_count, 0, 2 * sizeof(int32_t), s));
     PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
                      d_ff / H->tile, H->tile, H->cap};
     if (W_uT)
@@ -397,7 +405,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       TW_TRY(launch_tile_count(*H, s));
       TW_TRY(launch_route(*H, s));
       TW_TRY(launch_tile_assign(*H, nullptr, 0, spill, w.spill_cap, s));
-      return launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr, s);
+      return launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
+                         row_counter, s);
     }
     TW_TRY(launch_route(*H, s));
   }
@@ -411,7 +420,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     else
       TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
     TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
-    TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr, s));
+    TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
+                       row_counter, s));
     TW_TRY(fork.join());
   }
   return TWELL_OK;

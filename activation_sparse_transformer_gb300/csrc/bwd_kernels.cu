@@ -375,6 +375,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t o_rows = take(sizeof(int32_t) * cells);
   const size_t o_h = take(sizeof(float) * cells);
   const size_t o_dz = take(sizeof(float) * cells);
+  const size_t o_cnt = take(sizeof(int32_t));
   if (ws && base) {
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
@@ -391,6 +392,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->col_h = reinterpret_cast<float*>(b + o_h);
     ws->col_dz = reinterpret_cast<float*>(b + o_dz);
     ws->n_blocks = n_blocks;
+    ws->row_counter = reinterpret_cast<int32_t*>(b + o_cnt);
   }
   return off;
 }
@@ -415,12 +417,13 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
     SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
                        Lh.tile,   Lh.cap, f,         lambda,    ws.dz_cells, ws.dz_hl};
-    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s));
+    // its CTA 0 also zeroes the dX gather's row counter
+    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
   }
   // Second stream: the fallback rows' weight-gradient share (stored into dW
   // first), then dX (fallback GEMMs + the TwELL rows' gather-SpMM).  This
-  // stream: the unit-major lists, then dw_unitcta_kernel adds the TwELL share once the
-  // fallback share is in place.
+  // stream: the unit-major lists (independent of the fallback share), then
+  // dw_unitcta_kernel adds the TwELL share once the fallback share is in place.
   AuxFork fork(s);
   TW_TRY_RC(fork.status());
   cudaStream_t a = fork.aux();
@@ -438,7 +441,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     TW_TRY_RC(launch_gemm_store_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, dW_inT, d, Lh.status,
                                    TWELL_KERNEL_DW, a));
   }
-  TW_TRY_RC(fork.aux_to_main());  // dW holds the fallback share before dw_unitcta_kernel runs
+  TW_TRY_RC(fork.mark_aux());  // dW holds the fallback share from here on
   if (N > 0) {
     if (fb) {
       // one GEMM over K = 2 d_ff: row s of dz_hl viewed with stride 2 d_ff is
@@ -448,7 +451,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                                            TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f), f));
       TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
     }
-    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, TWELL_KERNEL_DX, a));
+    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit
   const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
@@ -482,6 +485,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                                                     ws.col_rows, ws.col_h, ws.col_dz);
   }
   TW_CHECK_LAUNCH();
+  TW_TRY_RC(fork.main_wait_mark());  // the fallback share is in dW before the TwELL share is added
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
     const int grid = std::max(1, std::min(f, 3 * sm_count()));

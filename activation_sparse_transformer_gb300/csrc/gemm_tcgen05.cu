@@ -882,11 +882,14 @@ int launch_gemm_store_mn(const uint16_t* A, const uint16_t* B, int M, int N, int
 }
 
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
-                       int32_t* status, cudaStream_t s) {
+                       int32_t* status, cudaStream_t s, int32_t* zero, int n_zero) {
+  const int nz = zero ? n_zero : 0;
   if (N % 256 == 0)
-    return launch_gemm<256, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
+    return launch_gemm<256, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s,
+                                                     nullptr, 1, 0, nullptr, 0, zero, nz);
   if (N % 128 == 0)
-    return launch_gemm<128, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s);
+    return launch_gemm<128, SampleEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_SDDMM, s,
+                                                     nullptr, 1, 0, nullptr, 0, zero, nz);
   return TWELL_ERR_UNSUPPORTED;
 }
 

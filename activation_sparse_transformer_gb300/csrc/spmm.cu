@@ -50,6 +50,7 @@ struct SpmmArgs {
   float* part;            // [gridDim.z][N][d] fp32 when the tiles are split into ranges, else null
   int32_t* arrivals;      // [gridDim.x][gridDim.y] zeroed counters when the tiles are split
   const uint16_t* pool;   // tile-granular hybrid: the pool of dense tiles, else null
+  int32_t* row_counter;   // zeroed word: rows handed out past the first gridDim.x, else null (fixed stride)
   int N, d, nt, T, C;
   int32_t* status;
 };
@@ -249,68 +250,82 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(sum);
 }
 
-// Whole rows, row-granular hybrid: a CTA per row at a time (persistent,
-// stride gridDim.x).  Every 256-column block of a row gathers the same W rows,
-// so the CTA flattens the row's entries once -- warp w expands tiles
-// [w * tpw, (w + 1) * tpw), a CTA prefix over the warps' totals places them
-// in ascending hidden-unit order -- and its 8 warps then stream column blocks
-// w, w + 8, ... from that one shared list.
+// Whole rows, row-granular hybrid: a CTA per row at a time (persistent).
+// Every 256-column block of a row gathers the same W rows, so the CTA
+// flattens the row's entries once -- warp w expands tiles [w * tpw, (w + 1) *
+// tpw), a CTA prefix over the warps' totals places them in ascending
+// hidden-unit order -- and its 8 warps then stream column blocks w, w + 8, ...
+// from that one shared list.  Rows are handed out dynamically (a CTA starts on
+// row blockIdx.x and takes the next unclaimed row from a counter), so a CTA
+// that drew long rows does not hold up the launch; the claim for the next row
+// is issued when a row starts, so its latency hides under the row's loads.
 template <typename VT>
 __global__ void __launch_bounds__(kWarps * 32, 4)
     spmm_rowcta_kernel(const SpmmArgs a, const uint16_t* __restrict__ W) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_tot[kWarps + 1];
+  __shared__ int next_row_s[2];  // by iteration parity: a skipped row has no barrier before the next write
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw);
   const VT* vals = static_cast<const VT*>(a.values);
   const int cbs = (a.d + 255) / 256;
   const int tpw = (a.nt + kWarps - 1) / kWarps;
-  for (int row = blockIdx.x; row < a.N; row += gridDim.x) {
+  for (int row = blockIdx.x, it = 0; row < a.N; it ^= 1) {
+    int claim = 0;
+    if (threadIdx.x == 0)
+      claim = a.row_counter ? static_cast<int>(gridDim.x) + atomicAdd(a.row_counter, 1) : row + gridDim.x;
     // fallback rows are written by the fallback path, which may run concurrently
-    if (a.row_fb[row] >= 0) continue;  // uniform over the CTA
-    const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
-    const int t_beg = min(a.nt, warp * tpw), t_end = min(a.nt, t_beg + tpw);
-    // this warp's tiles: counts, warp prefix (rounds of 32 tiles)
-    int wtotal = 0;
-    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
-      const int t = t0 + lane;
-      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
-      wtotal += __reduce_add_sync(0xffffffffu, cnt);
-    }
-    if (lane == 0) warp_tot[warp] = wtotal;
-    __syncthreads();
-    int base = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int v = warp_tot[w];
-      base += w < warp ? v : 0;
-      total += v;
-    }
-    for (int t0 = t_beg; t0 < t_end; t0 += 32) {
-      const int t = t0 + lane;
-      const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += x;
+    if (a.row_fb[row] < 0) {  // uniform over the CTA
+      const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+      const int t_beg = min(a.nt, warp * tpw), t_end = min(a.nt, t_beg + tpw);
+      // this warp's tiles: counts, warp prefix (rounds of 32 tiles)
+      int wtotal = 0;
+      for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+        const int t = t0 + lane;
+        const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+        wtotal += __reduce_add_sync(0xffffffffu, cnt);
       }
-      const int64_t cell = cell0 + t;
-      const int pos = base + incl - cnt;
-      for (int s2 = 0; s2 < cnt; ++s2)
-        list[pos + s2] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s2], vals[cell * a.C + s2]);
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    __syncthreads();
-    for (int cb = warp; cb < cbs; cb += kWarps) {
-      const int c0 = cb * 256 + lane * 8;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (c0 < a.d) {
-        stream_list<VT>(a, W + c0, list, total, acc);
-        *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
+      if (lane == 0) warp_tot[warp] = wtotal;
+      __syncthreads();
+      int base = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int v = warp_tot[w];
+        base += w < warp ? v : 0;
+        total += v;
       }
+      for (int t0 = t_beg; t0 < t_end; t0 += 32) {
+        const int t = t0 + lane;
+        const int cnt = t < t_end ? a.counts[cell0 + t] : 0;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += x;
+        }
+        const int64_t cell = cell0 + t;
+        const int pos = base + incl - cnt;
+        for (int s2 = 0; s2 < cnt; ++s2)
+          list[pos + s2] = RowEntry<VT>::make(t * a.T + a.idx[cell * a.C + s2], vals[cell * a.C + s2]);
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncthreads();
+      // the claim has had the flatten's loads to arrive; publishing it here
+      // keeps it out of the streaming loop's registers
+      if (threadIdx.x == 0) next_row_s[it] = claim;
+      for (int cb = warp; cb < cbs; cb += kWarps) {
+        const int c0 = cb * 256 + lane * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (c0 < a.d) {
+          stream_list<VT>(a, W + c0, list, total, acc);
+          *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
+        }
+      }
+    } else if (threadIdx.x == 0) {
+      next_row_s[it] = claim;
     }
     __syncthreads();  // the list and warp totals are rewritten for the next row
+    row = next_row_s[it];
   }
 }
 
@@ -378,7 +393,7 @@ int spmm_nsplit(int n_rows, int d_model) {
 }
 
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                int32_t* arrivals, cudaStream_t s) {
+                int32_t* arrivals, int32_t* row_counter, cudaStream_t s) {
   SpmmArgs a{L.values,
              L.idx,
              L.counts,
@@ -387,6 +402,7 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
              part,
              arrivals,
              L.hybrid == TWELL_HYBRID_TILES ? L.fb_dense : nullptr,
+             row_counter,
              L.n_rows,
              d_model,
              L.d_ff / L.tile,
@@ -397,9 +413,9 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
-                    int kernel_id, cudaStream_t s) {
-  SpmmArgs a{vals, L.idx, L.counts, L.row_fb, out, nullptr, nullptr, nullptr, L.n_rows, d_model, L.d_ff / L.tile,
-             L.tile, L.cap, L.status};
+                    int32_t* row_counter, int kernel_id, cudaStream_t s) {
+  SpmmArgs a{vals,     L.idx,   L.counts, L.row_fb,         out,    nullptr, nullptr, nullptr, row_counter,
+             L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
   return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
 }
 

@@ -40,8 +40,11 @@ class AuxFork {
   int status() const { return rc_; }
   cudaStream_t aux() const { return aux_; }
   int join();
-  // s waits for everything queued on aux so far (aux continues independently)
-  int aux_to_main();
+  // mark_aux records the point reached by the work queued on aux so far;
+  // main_wait_mark makes s wait for that point (aux continues independently),
+  // so s can queue independent work in between
+  int mark_aux();
+  int main_wait_mark();
 
  private:
   cudaStream_t s_;
@@ -137,8 +140,9 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
                                cudaStream_t s, int64_t lda = 0, int b_k_wrap = 0);
+// zero[0, n_zero) (int32), when given, is zeroed by the GEMM's CTA 0.
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
-                       int32_t* status, cudaStream_t s);
+                       int32_t* status, cudaStream_t s, int32_t* zero = nullptr, int n_zero = 0);
 // out[M][N] = A^T . B (fp32 store) with A row-major [K][M] and B row-major
 // [K][N] (both M/N-major); only the first k_mul * (*K_dev) rows of K count,
 // rows up to the next multiple of 64 past them must be zero in both operands,
@@ -170,13 +174,15 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* s
 // Y = H . W_down for the TwELL rows.  With nsplit > 1 each row's tiles are
 // cut into nsplit consecutive ranges whose fp32 partial sums go to part
 // ([nsplit][N][d_model]) and are added in range order (small batches); the
-// arrival counters (kSpmmMaxArrivals int32) must be zero on entry.
+// arrival counters (kSpmmMaxArrivals int32) must be zero on entry.  Whole
+// rows are handed out through row_counter (one int32, zero on entry) when it
+// is given, else by a fixed stride.
 constexpr int kSpmmMaxArrivals = 1024;
 int spmm_nsplit(int n_rows, int d_model);
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                int32_t* arrivals, cudaStream_t s);
+                int32_t* arrivals, int32_t* row_counter, cudaStream_t s);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
-                    int kernel_id, cudaStream_t s);
+                    int32_t* row_counter, int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
 int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_model, uint16_t* out, int kernel_id,
                      cudaStream_t s);
@@ -212,6 +218,7 @@ struct BwdWorkspace {
   float* col_h;           // [capacity] h of each entry
   float* col_dz;          // [capacity] dZ of each entry
   int32_t n_blocks;       // row blocks of kBwdRowsPerBlock rows
+  int32_t* row_counter;   // [1] the dX gather's row counter (zeroed by the SDDMM GEMM)
 };
 constexpr int kBwdRowsPerBlock = 32;  // one bit per row in the unit-list row masks
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,

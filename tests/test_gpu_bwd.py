@@ -43,14 +43,17 @@ def run(tw, torch, cfg, inp, dY, lam):
     return from_dev_bits(H), from_dev_f32(dX), dWi.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,N,T,C,lam", [("pr1", 256, 64, 8, 1e-4), ("ragged", 301, 128, 8, 1e-2),
-                                              ("t32", 160, 32, 4, 0.0)])
-def test_bwd_matches_oracle(tw, name, N, T, C, lam):
+@pytest.mark.parametrize("name,N,d,T,C,lam", [("pr1", 256, 256, 64, 8, 1e-4), ("ragged", 301, 256, 128, 8, 1e-2),
+                                                ("t32", 160, 256, 32, 4, 0.0),
+                                                # dX through the bulk-copy ring (2048 and 4096 columns)
+                                                ("wide", 300, 2048, 128, 8, 1e-4),
+                                                ("wide16", 200, 4096, 64, 16, 1e-3)])
+def test_bwd_matches_oracle(tw, name, N, d, T, C, lam):
     import torch
-    cfg = synth.FFNConfig(name, N, 256, 1024, T, C, seed=N + 7, row_spread="lognormal", forced_frac_rows=0.03,
+    cfg = synth.FFNConfig(name, N, d, 1024, T, C, seed=N + 7, row_spread="lognormal", forced_frac_rows=0.03,
                           fb_cap=N // 4)
     inp = synth.make_ffn_inputs(cfg)
-    dY = synth.make_grad_output(N, 256, seed=N)
+    dY = synth.make_grad_output(N, d, seed=N)
     H, dX, dWi, dWd, db = run(tw, torch, cfg, inp, dY, lam)
     _, dZ = oracle.grad_hidden(dY, inp["W_down"], H, lam)
     assert_close(dX, oracle.grad_input(dZ, inp["W_inT"]), "dX")
