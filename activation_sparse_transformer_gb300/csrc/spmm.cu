@@ -10,7 +10,7 @@
 // tokens (far more accumulators than an SM has registers).  The kernels are
 // therefore built for memory-level parallelism instead.  The main one
 // (spmm_rowcta_kernel) gives a CTA one token row at a time (a persistent grid,
-// four CTAs per SM): the CTA flattens the row's stored entries (tile-major,
+// four CTAs per SM, rows handed out from a counter): the CTA flattens the row's stored entries (tile-major,
 // slots ascending, so hidden units ascend) into one shared-memory list, and
 // its eight warps stream the named W rows for 256-column blocks w, w + 8, ...
 // with coalesced 16-byte loads, kU independent loads in flight per lane,
@@ -351,7 +351,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
   if (nsplit == 1 && !a.pool) {
-    // a CTA per row: one shared flatten for all column blocks; persistent, three
+    // a CTA per row: one shared flatten for all column blocks; persistent, four
     // CTAs per SM (the register limit)
     auto rk = spmm_rowcta_kernel<VT>;
     const size_t rsmem = static_cast<size_t>(a.nt) * a.C * sizeof(RowEntry<VT>);
