@@ -63,6 +63,40 @@ def test_bwd_matches_oracle(tw, name, N, d, T, C, lam):
     assert_close(db, rdb, "db")
 
 
+def test_repeat_calls_bit_identical(tw):
+    # one workspace shared by forward and backward, each called twice: the
+    # gathers hand out rows from counters that every call re-zeroes, and each
+    # output is summed by one thread in a fixed order, so repeated calls give
+    # the same bits
+    import torch
+    cfg = synth.FFNConfig("rep", 300, 2048, 1024, 128, 8, seed=41, row_spread="lognormal", forced_frac_rows=0.03,
+                          fb_cap=64)
+    inp = synth.make_ffn_inputs(cfg)
+    N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    dY = to_dev(synth.make_grad_output(N, d, seed=5), torch)
+    ws = torch.full((max(tw.fwd_workspace_bytes(N, d, f, T, C, fb), tw.bwd_workspace_bytes(N, d, f, T, C, fb)),),
+                    0x5A, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(2):
+        p = tw.alloc_packed(N, f, T, C, fb, dev)
+        Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+        tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws)
+        assert tw.twell_read_status(p) == 0
+        assert int(p.n_fb[0].item()) > 0
+        dX = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+        dWi = torch.empty((f, d), dtype=torch.float32, device=dev)
+        dWd = torch.empty((f, d), dtype=torch.float32, device=dev)
+        db = torch.empty((f,), dtype=torch.float32, device=dev)
+        tw.twell_ffn_bwd(X, Wi, Wd, p, dY, 1e-4, dX, dWi, dWd, db, ws)
+        torch.cuda.synchronize()
+        outs.append([from_dev_bits(Y), from_dev_bits(dX), dWi.cpu().numpy().view(np.uint32),
+                     dWd.cpu().numpy().view(np.uint32), db.cpu().numpy().view(np.uint32)])
+    for a, c in zip(*outs):
+        assert np.array_equal(a, c)
+
+
 def test_bwd_zero_upstream_closed_form(tw):
     # dY = 0: dZ = lambda exactly on the pattern, so db = lambda * active count,
     # dW_down = 0 and dX = lambda * sum of active W_in^T rows (integer weights:

@@ -141,6 +141,39 @@ def test_fwd_1b_full_size_sampled(tw):
     assert set(inp["forced_rows"].tolist()) <= set(np.nonzero(ref["row_fb"] >= 0)[0].tolist())
 
 
+def test_fwd_every_row_fallback(tw):
+    # C = 1 at ~20% activity: every row overflows, so no row reaches the gather
+    # and Y comes whole from the dense-fallback path (integer layer: exact)
+    import torch
+    N, d, f, T, C = 160, 256, 1024, 64, 1
+    inp = synth.make_integer_inputs(N, d, f, seed=12, sparsity=0.8)
+    ref = oracle.forward(inp["X"], inp["W_inT"], inp["b"], inp["W_down"], T, C, N)
+    assert ref["packed"]["n_fb"] == N
+    assert np.abs(ref["Y"]).max() < 2 ** 24
+    p, Y, rc = run_fwd(tw, torch, inp, T, C, N)
+    assert rc == 0, tw.status_string(rc)
+    check_packing_of(p, ref["H"], T, C, N)
+    assert np.array_equal(from_dev_bits(Y), ref["Y_bf16"])
+
+
+def test_fwd_rows_without_entries(tw):
+    # rows whose input is zero have z = b <= 0 everywhere: no stored entry, a
+    # zero Y row written by the gather (integer layer: exact)
+    import torch
+    N, d, f, T, C = 200, 256, 1024, 64, 8
+    inp = synth.make_integer_inputs(N, d, f, seed=13, sparsity=0.97)
+    empty = np.unique(np.concatenate([np.arange(0, 50), np.arange(50, N, 3)]))
+    inp["X"][empty] = 0
+    ref = oracle.forward(inp["X"], inp["W_inT"], inp["b"], inp["W_down"], T, C, N)
+    assert not ref["H"][empty].any()
+    p, Y, rc = run_fwd(tw, torch, inp, T, C, N)
+    assert rc == 0, tw.status_string(rc)
+    check_packing_of(p, ref["H"], T, C, N)
+    Yg = from_dev_bits(Y)
+    assert np.array_equal(Yg, ref["Y_bf16"])
+    assert not Yg[empty].any()
+
+
 def test_fwd_fallback_overflow_status(tw):
     import torch
     cfg = synth.FFNConfig("t", 256, 256, 1024, 64, 8, seed=3, row_spread="lognormal", forced_frac_rows=0.1,
