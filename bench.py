@@ -260,6 +260,18 @@ def bench_ours(args, rank, world, local):
     # the same calls back to back without the L2 scrub (warm L2: the weights stay resident)
     warm_step_ms = timed(step, min(args.steps, 50), warm=True)
     warm_fwd_ms = timed(fwd, min(args.steps, 50), warm=True)
+    # the same fwd + bwd calls captured once in a CUDA graph and replayed: the
+    # same kernels on the same buffers, without the host launch path between them
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream(dev)
+        tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, wsf, cap)
+        tw.twell_ffn_bwd(X, Wi, Wd, packed, dY, lam, dX, dWi, dWd, db, wsb, cap)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    graph_step_ms = timed(graph.replay, args.steps)
     Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
 
     def dense():
@@ -397,6 +409,10 @@ def bench_ours(args, rank, world, local):
         "roofline": roof,
         "fwd": {"tokens_per_s": round(world * N / (fwd_m * 1e-3), 1), "ms": round(fwd_m, 4),
                 "roofline_us": round(roof_fwd_us, 2), "roofline_frac": round(roof_fwd_us / (fwd_m * 1e3), 4)},
+        "graph": {"ms_per_step": round(med(graph_step_ms), 4),
+                  "tokens_per_s": round(job_throughput(world, N, med(graph_step_ms)), 1),
+                  "note": "the same fwd + bwd calls captured once in a CUDA graph and replayed, L2 flushed "
+                          "between replays"},
         "warm_l2": {"ms_per_step": round(med(warm_step_ms), 4), "fwd_ms": round(med(warm_fwd_ms), 4),
                     "tokens_per_s": round(job_throughput(world, N, med(warm_step_ms)), 1),
                     "note": "no L2 scrub between calls; the headline value scrubs L2 (cold)"},
