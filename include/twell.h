@@ -209,7 +209,10 @@ TWELL_API size_t twell_ffn_fwd_noalloc_max_scratch(void);
  *   dW_inT  [d_ff][d_model] fp32        dW_inT[j] = sum_n dZ[n][j] X[n]
  *   dW_down [d_ff][d_model] fp32        dW_down[j] = sum_n h[n][j] dY[n]
  *   db      [d_ff] fp32                 db[j] = sum_n dZ[n][j]
- * dH is only formed at H's non-zeros (SDDMM).  Deterministic: no atomics.
+ * dH is only formed at H's non-zeros (SDDMM).  Deterministic: every output
+ * element is summed by one thread in a fixed order (no atomics on outputs;
+ * rows are handed to CTAs through an atomic counter, which changes only who
+ * computes a row, not how).
  * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned
  * (it may be the forward call's workspace, see twell_ffn_fwd). */
 TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
