@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const int64_t split = static_cast<int64_t>(L.N) * L.f;
       const float* p = part + static_cast<int64_t>(row) * L.f + col;
-#pragma unroll 4
+#pragma unroll 8
       for (int ks = 0; ks < ksplit; ++ks) {
         const float4 a = *reinterpret_cast<const float4*>(p + ks * split);
         const float4 c = *reinterpret_cast<const float4*>(p + ks * split + 4);

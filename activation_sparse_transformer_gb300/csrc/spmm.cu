@@ -348,6 +348,22 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
     attr[dev] = true;
   }
   if (nsplit < 1 || nsplit > 64 || (nsplit > 1 && (!a.part || !a.arrivals))) return TWELL_ERR_INVALID_ARG;
+  if (nsplit > 1) {
+    // no more tile ranges than fit in one wave of resident CTAs: a second wave
+    // would repeat the whole latency chain of this short launch
+    static int resident[64] = {};
+    static size_t resident_smem[64] = {};
+    if (dev < 64 && (resident[dev] == 0 || resident_smem[dev] != smem)) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess)
+        return TWELL_ERR_CUDA;
+      resident[dev] = std::max(1, per_sm) * sm_count();
+      resident_smem[dev] = smem;
+    }
+    const int64_t per_split = static_cast<int64_t>((a.N + kWarps - 1) / kWarps) * ((a.d + 255) / 256);
+    const int fit = static_cast<int>(std::max<int64_t>(1, (dev < 64 ? resident[dev] : sm_count()) / per_split));
+    nsplit = std::min(nsplit, fit);
+  }
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
   if (nsplit == 1 && !a.pool) {
