@@ -24,6 +24,7 @@ EXPORTED = [
     "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",
     "twell_bwd_workspace_bytes", "twell_dense_ffn_fwd", "twell_read_status", "twell_status_string",
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
+    "twell_profile_timeline",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
     "twell_selftest_wait_timeout",
 ]
@@ -72,6 +73,9 @@ def load_library() -> ctypes.CDLL:
         "twell_profile_enable": (ctypes.c_int, [ctypes.c_int]),
         "twell_profile_reset": (ctypes.c_int, []),
         "twell_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]),
+        "twell_profile_timeline": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                                  ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_double)]),
         "twell_ffn_fwd_noalloc": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P]),
         "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
         "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
@@ -246,6 +250,20 @@ def twell_profile_enable(on: bool) -> None:
 
 def twell_profile_reset() -> None:
     _check(load_library().twell_profile_reset(), "twell_profile_reset")
+
+
+def twell_profile_timeline(max_entries: int = 4096) -> list:
+    """Recorded launches in order: dicts with kernel (name), stream, start_ms,
+    end_ms (device times relative to the first recorded launch)."""
+    k = (ctypes.c_int32 * max_entries)()
+    st = (ctypes.c_uint64 * max_entries)()
+    a = (ctypes.c_double * max_entries)()
+    b = (ctypes.c_double * max_entries)()
+    n = load_library().twell_profile_timeline(max_entries, k, st, a, b)
+    _check(min(n, 0), "twell_profile_timeline")
+    names = {v: name for name, v in KERNELS.items()}
+    return [{"kernel": names.get(k[i], str(k[i])), "stream": int(st[i]), "start_ms": a[i], "end_ms": b[i]}
+            for i in range(n)]
 
 
 def twell_profile_read(kernel) -> tuple:

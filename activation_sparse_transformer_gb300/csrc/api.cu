@@ -18,6 +18,7 @@ namespace {
 struct Pending {
   int kernel;
   cudaEvent_t start, stop;
+  cudaStream_t stream;
 };
 std::mutex g_mu;
 int64_t g_launches = 0;
@@ -53,7 +54,7 @@ LaunchScope::~LaunchScope() {
   std::lock_guard<std::mutex> lk(g_mu);
   cudaEvent_t stop = take_event();
   cudaEventRecord(stop, stream_);
-  g_pending.push_back(Pending{kernel_, start_, stop});
+  g_pending.push_back(Pending{kernel_, start_, stop, stream_});
 }
 
 // ---------------------------------------------------------------- aux stream
@@ -549,6 +550,25 @@ int twell_profile_reset(void) {
     g_prof_ms[k] = 0.0;
   }
   return TWELL_OK;
+}
+
+int twell_profile_timeline(int max, int32_t* kernel, uint64_t* stream, double* start_ms, double* end_ms) {
+  if (max < 0 || (max > 0 && (!kernel || !stream || !start_ms || !end_ms))) return TWELL_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TWELL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const int n = static_cast<int>(std::min<size_t>(static_cast<size_t>(max), g_pending.size()));
+  for (int i = 0; i < n; ++i) {
+    const Pending& p = g_pending[i];
+    float a = 0.f, b = 0.f;
+    if (cudaEventElapsedTime(&a, g_pending[0].start, p.start) != cudaSuccess ||
+        cudaEventElapsedTime(&b, g_pending[0].start, p.stop) != cudaSuccess)
+      return TWELL_ERR_CUDA;
+    kernel[i] = p.kernel;
+    stream[i] = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(p.stream));
+    start_ms[i] = a;
+    end_ms[i] = b;
+  }
+  return n;
 }
 
 int twell_profile_read(int kernel, int64_t* launches, double* total_ms) {

@@ -48,144 +48,97 @@ Layout flat(const twell_t& L) {
 constexpr int kWarps = 8;
 constexpr int kU = 4;  // entries in flight per lane in dw_unitcta_kernel (2 rows each)
 
-// Unit-major regrouping of the TwELL entries.  A CTA owns a block of
-// kBwdRowsPerBlock (= 32) rows.  For every hidden unit it builds a 32-bit mask
-// with bit r set when row r of the block stores that unit (a unit appears at
-// most once per row), so popc(mask) counts the unit's entries in the block and
-// cursor + popc(mask & ((1 << r) - 1)) is the place of row r's entry: rows
-// ascending, no atomics on the output, every cell processed in parallel.
-__device__ __forceinline__ void build_row_masks(const Layout& L, int r0, int r1, uint32_t* mask) {
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x) mask[j] = 0;
+// Unit-major regrouping of the TwELL entries, one launch: a CTA per tile t
+// builds the lists of the tile's T hidden units (every unit of a tile lives in
+// the same column of cells, so the tile's bookkeeping stays in shared memory)
+// into the tile's own region of the entry arrays, [t * N * C, (t + 1) * N * C).
+// Warp w owns a contiguous range of 32-row blocks.  Pass 1 counts each unit's
+// entries per warp; scans over the warps and then over the units give every
+// (warp, unit) its start.  Pass 2 walks each warp's blocks in order: a 32-bit
+// mask per unit (bit = row of the block) places row r's entry at the unit's
+// start + the warp's running cursor + popc(mask below r).  Rows ascend within
+// every unit, nothing is atomic on the output, and the result is a pure
+// function of the pattern.
+constexpr int kListWarps = 32;
+
+__global__ void __launch_bounds__(kListWarps * 32)
+    unit_lists_kernel(Layout L, const float* __restrict__ dz_cells, int32_t* __restrict__ col_beg,
+                      int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
+                      float* __restrict__ col_dz) {
+  extern __shared__ int32_t lsm[];
+  const int T = L.T, t = blockIdx.x;
+  int32_t* wcur = lsm;                                            // [kListWarps][T]: counts, then cursors
+  uint32_t* wmask = reinterpret_cast<uint32_t*>(lsm + kListWarps * T);  // [kListWarps][T]
+  int32_t* ustart = lsm + 2 * kListWarps * T;                     // [T]
+  __shared__ int scan_tot[kListWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nblk = (L.N + 31) / 32;
+  const int per = (nblk + kListWarps - 1) / kListWarps;
+  const int b0 = min(nblk, warp * per), b1 = min(nblk, b0 + per);
+  for (int i = tid; i < kListWarps * T; i += blockDim.x) wcur[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < (r1 - r0) * L.nt; i += blockDim.x) {
-    const int64_t cell = static_cast<int64_t>(r0) * L.nt + i;
-    const int cnt = L.counts[cell];
-    const int t = i % L.nt;
-    const uint32_t bit = 1u << (i / L.nt);
-    for (int s = 0; s < cnt; ++s) atomicOr(&mask[t * L.T + L.idx[cell * L.C + s]], bit);
+  // ---- pass 1: entries per (warp, unit)
+  for (int blk = b0; blk < b1; ++blk) {
+    const int r = blk * 32 + lane;
+    if (r < L.N) {
+      const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
+      const int cnt = L.counts[cell];
+      for (int sl = 0; sl < cnt; ++sl) atomicAdd(&wcur[warp * T + L.idx[cell * L.C + sl]], 1);
+    }
   }
   __syncthreads();
-}
-
-constexpr int kListThreads = 1024;  // the list passes are latency-bound: many cells in flight
-
-// Pass 1: entries per (unit, row block), stored block-major (blk_count[b][j]:
-// each CTA writes one contiguous row of f counts).
-__global__ void __launch_bounds__(kListThreads) unit_hist_kernel(Layout L, int n_blocks, int32_t* __restrict__ blk_count) {
-  extern __shared__ uint32_t mask[];
-  const int r0 = blockIdx.x * kBwdRowsPerBlock;
-  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
-  build_row_masks(L, r0, r1, mask);
-  for (int j = threadIdx.x; j < L.f; j += blockDim.x)
-    blk_count[static_cast<int64_t>(blockIdx.x) * L.f + j] = __popc(mask[j]);
-}
-
-// Exclusive scan over the row blocks of each unit, in place; the unit's total
-// goes to col_ptr[j].  A CTA takes 32 units (lane = unit, so every access is a
-// 128-byte row segment of blk_count[b][j]); warp w scans a contiguous range of
-// blocks and the eight warps' totals are combined in warp order.
-__global__ void __launch_bounds__(256) unit_block_scan_kernel(int32_t* __restrict__ blk_count, int n_blocks, int f,
-                                                              int32_t* __restrict__ col_ptr) {
-  __shared__ int tot[8][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * 32 + lane;
-  const bool in = j < f;
-  const int per = (n_blocks + 7) / 8;
-  const int b0 = min(n_blocks, warp * per), b1 = min(n_blocks, b0 + per);
-  int sum = 0;
-  for (int b = b0; b < b1; ++b) sum += in ? blk_count[static_cast<int64_t>(b) * f + j] : 0;
-  tot[warp][lane] = sum;
+  // ---- scans: over the warps per unit (counts -> exclusive starts), then over the units
+  int total = 0;
+  if (tid < T) {
+    for (int w = 0; w < kListWarps; ++w) {
+      const int c = wcur[w * T + tid];
+      wcur[w * T + tid] = total;
+      total += c;
+    }
+  }
+  int incl = total;  // threads past T hold 0
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) scan_tot[warp] = incl;
   __syncthreads();
-  int run = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    run += w < warp ? tot[w][lane] : 0;
-    all += tot[w][lane];
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += scan_tot[w];
+  const int64_t base = static_cast<int64_t>(t) * L.N * L.C;
+  if (tid < T) {
+    const int start = before + incl - total;
+    ustart[tid] = start;
+    col_beg[t * T + tid] = static_cast<int32_t>(base + start);
+    col_end[t * T + tid] = static_cast<int32_t>(base + start + total);
   }
-  if (!in) return;
-  for (int b = b0; b < b1; ++b) {
-    int32_t* q = blk_count + static_cast<int64_t>(b) * f + j;
-    const int c = *q;
-    *q = run;
-    run += c;
-  }
-  if (warp == 0) col_ptr[j] = all;
-}
-
-// Exclusive scan of the per-unit totals: col_ptr[j] = start, col_ptr[f] = all.
-// One CTA; each thread takes 8 consecutive units per pass (8192 per pass).
-__global__ void __launch_bounds__(1024) unit_scan_kernel(int32_t* __restrict__ col_ptr, int f) {
-  __shared__ int warp_tot[32];
-  __shared__ int base_s;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) base_s = 0;
   __syncthreads();
-  for (int start = 0; start < f; start += 1024 * 8) {
-    const int j0 = start + tid * 8;
-    int v[8];
-    int local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[i] = j0 + i < f ? col_ptr[j0 + i] : 0;
-      local += v[i];
+  // ---- pass 2: place every entry, blocks of each warp in ascending order
+  uint32_t* m = wmask + warp * T;
+  int32_t* cur = wcur + warp * T;
+  for (int blk = b0; blk < b1; ++blk) {
+    for (int u = lane; u < T; u += 32) m[u] = 0;
+    __syncwarp();
+    const int r = blk * 32 + lane;
+    const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
+    const int cnt = r < L.N ? L.counts[cell] : 0;
+    for (int sl = 0; sl < cnt; ++sl) atomicOr(&m[L.idx[cell * L.C + sl]], 1u << lane);
+    __syncwarp();
+    for (int sl = 0; sl < cnt; ++sl) {
+      const int u = L.idx[cell * L.C + sl];
+      const int64_t pos = base + ustart[u] + cur[u] + __popc(m[u] & ((1u << lane) - 1u));
+      col_rows[pos] = r;
+      col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + sl]);
+      col_dz[pos] = dz_cells[cell * L.C + sl];
     }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int w = warp_tot[lane];
-      int wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += x;
-      }
-      warp_tot[lane] = wi - w;
-    }
-    __syncthreads();
-    int run = base_s + warp_tot[warp] + incl - local;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (j0 + i < f) col_ptr[j0 + i] = run;
-      run += v[i];
-    }
-    __syncthreads();
-    if (tid == 1023) base_s = run;
-    __syncthreads();
+    __syncwarp();
+    for (int u = lane; u < T; u += 32) cur[u] += __popc(m[u]);
+    __syncwarp();
   }
-  if (tid == 0) col_ptr[f] = base_s;
 }
 
-// Pass 2: every entry written at its unit's cursor plus the number of the
-// unit's entries in earlier rows of the block.
-__global__ void __launch_bounds__(kListThreads) unit_fill_kernel(Layout L, int n_blocks, const float* __restrict__ dz_cells,
-                                 const int32_t* __restrict__ blk_count, const int32_t* __restrict__ col_ptr,
-                                 int32_t* __restrict__ col_rows, float* __restrict__ col_h,
-                                 float* __restrict__ col_dz) {
-  extern __shared__ uint32_t mask[];
-  const int r0 = blockIdx.x * kBwdRowsPerBlock;
-  const int r1 = min(L.N, r0 + kBwdRowsPerBlock);
-  build_row_masks(L, r0, r1, mask);
-  for (int i = threadIdx.x; i < (r1 - r0) * L.nt; i += blockDim.x) {
-    const int64_t cell = static_cast<int64_t>(r0) * L.nt + i;
-    const int cnt = L.counts[cell];
-    const int t = i % L.nt;
-    const int r = i / L.nt;
-    for (int s = 0; s < cnt; ++s) {
-      const int j = t * L.T + L.idx[cell * L.C + s];
-      const int pos = col_ptr[j] + blk_count[static_cast<int64_t>(blockIdx.x) * L.f + j] +
-                      __popc(mask[j] & ((1u << r) - 1u));
-      col_rows[pos] = r0 + r;
-      col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + s]);
-      col_dz[pos] = dz_cells[cell * L.C + s];
-    }
-  }
-}
+size_t unit_lists_smem(int T) { return sizeof(int32_t) * (2 * static_cast<size_t>(kListWarps) * T + T); }
 
 // One staged entry of a hidden unit's list (row, h, dZ); rows ascend.  h is
 // exactly a bf16 value, so the dW_down update uses the mixed bf16 x bf16 +
@@ -204,7 +157,8 @@ struct UnitEntry {
 constexpr int kDwChunk = kWarps * 32;
 
 __global__ void __launch_bounds__(kWarps * 32, 3)
-    dw_unitcta_kernel(int f, const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ col_rows,
+    dw_unitcta_kernel(int f, const int32_t* __restrict__ col_beg, const int32_t* __restrict__ col_end,
+                      const int32_t* __restrict__ col_rows,
                       const float* __restrict__ col_h, const float* __restrict__ col_dz,
                       const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
                       float* __restrict__ dW_inT, float* __restrict__ dW_down, float* __restrict__ db,
@@ -214,7 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   const bool have_fb = min(*n_fb, fb_cap) > 0;
   const int cbs = (d + 255) / 256;
   for (int j = blockIdx.x; j < f; j += gridDim.x) {
-    const int e0 = col_ptr[j], e1 = col_ptr[j + 1];
+    const int e0 = col_beg[j], e1 = col_end[j];
     for (int cb0 = 0; cb0 < cbs; cb0 += kWarps) {
       const int c0 = (cb0 + warp) * 256 + lane * 8;
       const bool active = cb0 + warp < cbs && c0 < d;
@@ -353,7 +307,6 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
                             void* base) {
   const int nt = d_ff / T;
   const int64_t cells = static_cast<int64_t>(N) * nt * C;
-  const int n_blocks = (N + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
   const int ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
   const int fb_pad = (fb_cap + 63) & ~63;
   size_t off = 0;
@@ -370,8 +323,8 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t o_dyg = take(sizeof(uint16_t) * padd);
   const size_t o_xg = take(sizeof(uint16_t) * 2 * padd);
   const size_t o_part = take(sizeof(float) * ksplit * static_cast<size_t>(fb_cap) * d_model);
-  const size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(n_blocks) * d_ff);
-  const size_t o_ptr = take(sizeof(int32_t) * (static_cast<size_t>(d_ff) + 1));
+  const size_t o_beg = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
+  const size_t o_end = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
   const size_t o_rows = take(sizeof(int32_t) * cells);
   const size_t o_h = take(sizeof(float) * cells);
   const size_t o_dz = take(sizeof(float) * cells);
@@ -386,12 +339,11 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->fb_pad = fb_pad;
     ws->part = reinterpret_cast<float*>(b + o_part);
     ws->ksplit = ksplit;
-    ws->blk_count = reinterpret_cast<int32_t*>(b + o_blk);
-    ws->col_ptr = reinterpret_cast<int32_t*>(b + o_ptr);
+    ws->col_beg = reinterpret_cast<int32_t*>(b + o_beg);
+    ws->col_end = reinterpret_cast<int32_t*>(b + o_end);
     ws->col_rows = reinterpret_cast<int32_t*>(b + o_rows);
     ws->col_h = reinterpret_cast<float*>(b + o_h);
     ws->col_dz = reinterpret_cast<float*>(b + o_dz);
-    ws->n_blocks = n_blocks;
     ws->row_counter = reinterpret_cast<int32_t*>(b + o_cnt);
   }
   return off;
@@ -453,43 +405,29 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     }
     TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
   }
-  // ---- weight gradients: TwELL entries regrouped by hidden unit
-  const size_t fsm = sizeof(int32_t) * static_cast<size_t>(f);
+  // ---- weight gradients: TwELL entries regrouped by hidden unit (a CTA per tile)
+  const size_t lsm = unit_lists_smem(Lh.tile);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(unit_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
-        cudaFuncSetAttribute(unit_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+    if (cudaFuncSetAttribute(unit_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(unit_lists_smem(256))) != cudaSuccess)
       return TWELL_ERR_CUDA;
     attr[dev] = true;
   }
-  if (ws.n_blocks > 0) {
-    LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_hist_kernel<<<ws.n_blocks, kListThreads, fsm, s>>>(L, ws.n_blocks, ws.blk_count);
-  }
-  TW_CHECK_LAUNCH();
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_block_scan_kernel<<<(f + 31) / 32, 256, 0, s>>>(ws.blk_count, ws.n_blocks, f, ws.col_ptr);
-  }
-  TW_CHECK_LAUNCH();
-  {
-    LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_scan_kernel<<<1, 1024, 0, s>>>(ws.col_ptr, f);
-  }
-  TW_CHECK_LAUNCH();
-  if (ws.n_blocks > 0) {
-    LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_fill_kernel<<<ws.n_blocks, kListThreads, fsm, s>>>(L, ws.n_blocks, ws.dz_cells, ws.blk_count, ws.col_ptr,
-                                                    ws.col_rows, ws.col_h, ws.col_dz);
+    unit_lists_kernel<<<f / Lh.tile, kListWarps * 32, lsm, s>>>(L, ws.dz_cells, ws.col_beg, ws.col_end, ws.col_rows,
+                                                             ws.col_h, ws.col_dz);
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.main_wait_mark());  // the fallback share is in dW before the TwELL share is added
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
     const int grid = std::max(1, std::min(f, 3 * sm_count()));
-    dw_unitcta_kernel<<<grid, kWarps * 32, 0, s>>>(f, ws.col_ptr, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d,
+    dw_unitcta_kernel<<<grid, kWarps * 32, 0, s>>>(f, ws.col_beg, ws.col_end, ws.col_rows, ws.col_h, ws.col_dz, X,
+                                                   dY, d,
                                                    dW_inT, dW_down, db, Lh.n_fb, fb ? Lh.fb_cap : 0);
   }
   TW_CHECK_LAUNCH();

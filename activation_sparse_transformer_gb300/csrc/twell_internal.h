@@ -212,15 +212,13 @@ struct BwdWorkspace {
   int32_t fb_pad;         // fb_cap rounded up to 64
   float* part;            // [ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
   int32_t ksplit;
-  int32_t* blk_count;     // [n_blocks][d_ff] entries per (row block, hidden unit), then offsets
-  int32_t* col_ptr;       // [d_ff + 1] start of each hidden unit's entry list
+  int32_t* col_beg;       // [d_ff] start of each hidden unit's entry list (tile t's lists in [t N C, (t + 1) N C))
+  int32_t* col_end;       // [d_ff] end of each hidden unit's entry list
   int32_t* col_rows;      // [capacity] row of each entry, grouped by unit, rows ascending
   float* col_h;           // [capacity] h of each entry
   float* col_dz;          // [capacity] dZ of each entry
-  int32_t n_blocks;       // row blocks of kBwdRowsPerBlock rows
   int32_t* row_counter;   // [1] the dX gather's row counter (zeroed by the SDDMM GEMM)
 };
-constexpr int kBwdRowsPerBlock = 32;  // one bit per row in the unit-list row masks
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
                             void* base);
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,

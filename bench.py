@@ -215,6 +215,26 @@ def bench_ours(args, rank, world, local):
         step()
     torch.cuda.synchronize()
 
+    if args.timeline:
+        timelines = []
+        for _ in range(3):
+            flush.zero_()
+            torch.cuda.synchronize()
+            tw.twell_profile_reset()
+            tw.twell_profile_enable(True)
+            step()
+            tw.twell_profile_enable(False)
+            timelines.append(tw.twell_profile_timeline())
+            tw.twell_profile_reset()
+        main_stream = int(stream.cuda_stream)
+        for tl in timelines:
+            for e in tl:
+                e["stream"] = "main" if e["stream"] == main_stream else "second"
+                e["start_ms"] = round(e["start_ms"], 4)
+                e["end_ms"] = round(e["end_ms"], 4)
+        return {"timeline": timelines, "config": {"workload": WORKLOAD, "n_rows": N},
+                "note": "one fwd + bwd step, three times; times relative to each step's first launch"}
+
     def timed(fn, k, profile=False, warm=False):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
         if profile:
@@ -670,6 +690,9 @@ def main():
                     help="with --next: comma-separated workload names to run (default: all)")
     ap.add_argument("--next", action="store_true",
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
+    ap.add_argument("--timeline", action="store_true",
+                    help="print the launch timeline of one fwd + bwd step (L2 scrubbed before it) instead of "
+                         "the bench line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_info()
@@ -686,7 +709,9 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl")
     res = bench_ours(args, rank, world, local)
-    if rank == 0:
+    if rank == 0 and args.timeline:
+        print(json.dumps(res), flush=True)
+    elif rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
         print(json.dumps(res), flush=True)

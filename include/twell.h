@@ -276,6 +276,20 @@ TWELL_API int twell_profile_enable(int on);
 TWELL_API int twell_profile_reset(void);
 TWELL_API int twell_profile_read(int kernel, int64_t* launches, double* total_ms);
 
+/* Timeline of the launches recorded while profiling was enabled and not yet
+ * consumed by twell_profile_read or cleared by twell_profile_reset, in launch
+ * order: for entry i, kernel[i] (a TWELL_KERNEL_* id), stream[i] (the
+ * cudaStream_t it ran on, as an integer: the caller's stream or the library's
+ * second stream), and start_ms[i] / end_ms[i], the device times of the event
+ * recorded on that stream just before the launch and just after it, relative
+ * to the first entry's start.  Start marks when the stream reached the launch
+ * (the kernel may still wait for SMs), end when it finished.  Writes at most
+ * `max` entries to the caller's host arrays and returns how many it wrote, or
+ * a negative TWELL_* code.  Synchronises the device; the entries stay
+ * recorded. */
+TWELL_API int twell_profile_timeline(int max, int32_t* kernel, uint64_t* stream, double* start_ms,
+                                     double* end_ms);
+
 #ifdef __cplusplus
 }
 #endif
