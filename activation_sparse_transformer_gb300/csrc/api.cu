@@ -393,12 +393,9 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     // the last CTA of the pack pass also routes the rows
     TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, arrivals, s));
   } else {
-    // spill count, the gather's row counter and the routing ticket, zeroed together
-    TW_CUDA(cudaMemsetAsync(spill_count, 0, 3 * sizeof(int32_t), s));
-    // the row-granular hybrid is routed by the GEMM's last CTA (no routing launch)
-    PackEpiParams pp{b,        H->values,     H->idx,    H->counts,    H->row_fb, spill,
-                     spill_count, w.spill_cap, H->status, d_ff / H->tile, H->tile, H->cap,
-                     tiles ? nullptr : spill_count + 2, n_rows, H->fb_cap, H->fb_rows, H->n_fb};
+    TW_CUDA(cudaMemsetAsync(spill_count, 0, 2 * sizeof(int32_t), s));
+    PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
+                     d_ff / H->tile, H->tile, H->cap};
     if (W_uT)
       TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
     else
@@ -412,6 +409,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       return launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
                          row_counter, s);
     }
+    TW_TRY(launch_route(*H, s));
   }
   {
     // the dense-fallback rows (assembly or copy + tensor-core down-projection)

@@ -29,9 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <type_traits>
 
-#include "route.cuh"
 #include "sm103.cuh"
 #include "twell_internal.h"
 
@@ -549,22 +547,6 @@ struct SampleEpi {
 };
 
 // ------------------------------------------------------------ kernel
-// The pack epilogues' routing tail: every CTA takes a ticket once its tiles
-// are stored; the last one routes the rows, so no routing launch follows.
-__device__ __forceinline__ void route_after_pack(const PackEpiParams& p) {
-  __shared__ int last_s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's row flags before its ticket
-    last_s = atomicAdd(p.route_ticket, 1) == static_cast<int>(gridDim.x) - 1;
-  }
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  route_block<kThreads>(RouteRows{p.n_rows, p.n_tiles, p.cap, p.fb_cap, false, p.values, p.idx, p.counts,
-                                  p.row_flag, p.fb_rows, p.n_fb, p.status});
-}
-
 template <int BN, class Epi, bool kANMajor, bool kBNMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -770,9 +752,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
-  }
-  if constexpr (std::is_same<typename Epi::Params, PackEpiParams>::value) {
-    if (ep.route_ticket) route_after_pack(ep);
   }
 }
 

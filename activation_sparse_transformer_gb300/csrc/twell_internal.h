@@ -81,14 +81,6 @@ struct PackEpiParams {
   int32_t n_tiles;
   int32_t tile;           // T
   int32_t cap;            // C
-  // Routing folded into the GEMM (row-granular hybrid): when route_ticket (an
-  // int32, zero on entry) is given, the CTA that finishes last routes the rows
-  // (row_flag -> row_fb slots, fb_rows, n_fb) as the routing launch would.
-  int32_t* route_ticket;
-  int32_t n_rows;
-  int32_t fb_cap;
-  int32_t* fb_rows;
-  int32_t* n_fb;
 };
 
 struct DenseEpiParams {
