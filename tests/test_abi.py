@@ -71,6 +71,9 @@ def test_host_argument_checks_without_gpu(lib):
     # the wait self-test checks its arguments on the host
     assert lib.twell_selftest_wait_timeout(None, 1000, None) == -1
     assert lib.twell_selftest_wait_timeout(ctypes.c_void_p(0x10000), 0, None) == -1
+    # the launch timeline: a negative count, or entries asked for without the arrays
+    assert lib.twell_profile_timeline(-1, None, None, None, None) == -1
+    assert lib.twell_profile_timeline(4, None, None, None, None) == -1
     # a well-formed call reaches the device check and stops there on a CPU-only host
     rc = lib.twell_pack(ctypes.c_void_p(0x10000), 1024, ctypes.byref(L), None)
     try:
