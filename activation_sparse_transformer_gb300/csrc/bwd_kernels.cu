@@ -60,7 +60,16 @@ constexpr int kU = 4;  // entries in flight per lane in dw_unitcta_kernel (2 row
 // every unit, nothing is atomic on the output, and the result is a pure
 // function of the pattern.
 constexpr int kListWarps = 32;
+constexpr int kListChunk = 4;  // row blocks whose cells a warp loads before using them
 
+// The 8 slot indices (C == 8) or values of one cell, loaded as whole vectors so
+// that a chunk of blocks costs one memory latency, not one per block.
+__device__ __forceinline__ int cell_idx8(uint2 w, int sl) {
+  const uint64_t v = (static_cast<uint64_t>(w.y) << 32) | w.x;
+  return static_cast<int>((v >> (8 * sl)) & 0xFFu);
+}
+
+template <bool kC8>
 __global__ void __launch_bounds__(kListWarps * 32)
     unit_lists_kernel(Layout L, const float* __restrict__ dz_cells, int32_t* __restrict__ col_beg,
                       int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
@@ -77,13 +86,23 @@ __global__ void __launch_bounds__(kListWarps * 32)
   const int b0 = min(nblk, warp * per), b1 = min(nblk, b0 + per);
   for (int i = tid; i < kListWarps * T; i += blockDim.x) wcur[i] = 0;
   __syncthreads();
-  // ---- pass 1: entries per (warp, unit)
-  for (int blk = b0; blk < b1; ++blk) {
-    const int r = blk * 32 + lane;
-    if (r < L.N) {
+  // ---- pass 1: entries per (warp, unit), kListChunk blocks' cells loaded at once
+  for (int c0 = b0; c0 < b1; c0 += kListChunk) {
+    int cnt[kListChunk];
+    uint2 iw[kListChunk];
+#pragma unroll
+    for (int j = 0; j < kListChunk; ++j) {
+      const int r = (c0 + j) * 32 + lane;
+      const bool ok = c0 + j < b1 && r < L.N;
       const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
-      const int cnt = L.counts[cell];
-      for (int sl = 0; sl < cnt; ++sl) atomicAdd(&wcur[warp * T + L.idx[cell * L.C + sl]], 1);
+      cnt[j] = ok ? L.counts[cell] : 0;
+      if (kC8) iw[j] = ok ? *reinterpret_cast<const uint2*>(L.idx + cell * 8) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kListChunk; ++j) {
+      const int64_t cell = static_cast<int64_t>((c0 + j) * 32 + lane) * L.nt + t;
+      for (int sl = 0; sl < cnt[j]; ++sl)
+        atomicAdd(&wcur[warp * T + (kC8 ? cell_idx8(iw[j], sl) : L.idx[cell * L.C + sl])], 1);
     }
   }
   __syncthreads();
@@ -117,24 +136,53 @@ __global__ void __launch_bounds__(kListWarps * 32)
   // ---- pass 2: place every entry, blocks of each warp in ascending order
   uint32_t* m = wmask + warp * T;
   int32_t* cur = wcur + warp * T;
-  for (int blk = b0; blk < b1; ++blk) {
-    for (int u = lane; u < T; u += 32) m[u] = 0;
-    __syncwarp();
-    const int r = blk * 32 + lane;
-    const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
-    const int cnt = r < L.N ? L.counts[cell] : 0;
-    for (int sl = 0; sl < cnt; ++sl) atomicOr(&m[L.idx[cell * L.C + sl]], 1u << lane);
-    __syncwarp();
-    for (int sl = 0; sl < cnt; ++sl) {
-      const int u = L.idx[cell * L.C + sl];
-      const int64_t pos = base + ustart[u] + cur[u] + __popc(m[u] & ((1u << lane) - 1u));
-      col_rows[pos] = r;
-      col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + sl]);
-      col_dz[pos] = dz_cells[cell * L.C + sl];
+  for (int c0 = b0; c0 < b1; c0 += kListChunk) {
+    int cnt[kListChunk];
+    uint2 iw[kListChunk];
+#pragma unroll
+    for (int j = 0; j < kListChunk; ++j) {
+      const int r = (c0 + j) * 32 + lane;
+      const bool ok = c0 + j < b1 && r < L.N;
+      const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
+      cnt[j] = ok ? L.counts[cell] : 0;
+      if (kC8) iw[j] = ok ? *reinterpret_cast<const uint2*>(L.idx + cell * 8) : make_uint2(0u, 0u);
     }
-    __syncwarp();
-    for (int u = lane; u < T; u += 32) cur[u] += __popc(m[u]);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kListChunk; ++j) {
+      if (c0 + j >= b1) break;  // uniform over the warp
+      const int r = (c0 + j) * 32 + lane;
+      const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
+      // the block's values and dZ, requested before the masks are built
+      uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+      float4 dz0 = make_float4(0.f, 0.f, 0.f, 0.f), dz1 = dz0;
+      if (kC8 && cnt[j] > 0) {
+        hv = *reinterpret_cast<const uint4*>(L.values + cell * 8);
+        dz0 = *reinterpret_cast<const float4*>(dz_cells + cell * 8);
+        dz1 = *reinterpret_cast<const float4*>(dz_cells + cell * 8 + 4);
+      }
+      for (int u = lane; u < T; u += 32) m[u] = 0;
+      __syncwarp();
+      for (int sl = 0; sl < cnt[j]; ++sl)
+        atomicOr(&m[kC8 ? cell_idx8(iw[j], sl) : L.idx[cell * L.C + sl]], 1u << lane);
+      __syncwarp();
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+      const float dzs[8] = {dz0.x, dz0.y, dz0.z, dz0.w, dz1.x, dz1.y, dz1.z, dz1.w};
+      for (int sl = 0; sl < cnt[j]; ++sl) {
+        const int u = kC8 ? cell_idx8(iw[j], sl) : L.idx[cell * L.C + sl];
+        const int64_t pos = base + ustart[u] + cur[u] + __popc(m[u] & ((1u << lane) - 1u));
+        col_rows[pos] = r;
+        if (kC8) {
+          col_h[pos] = bf16_bits_to_float(static_cast<uint16_t>(hw[sl >> 1] >> (16 * (sl & 1))));
+          col_dz[pos] = dzs[sl];
+        } else {
+          col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + sl]);
+          col_dz[pos] = dz_cells[cell * L.C + sl];
+        }
+      }
+      __syncwarp();
+      for (int u = lane; u < T; u += 32) cur[u] += __popc(m[u]);
+      __syncwarp();
+    }
   }
 }
 
@@ -411,15 +459,18 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(unit_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(unit_lists_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(unit_lists_smem(256))) != cudaSuccess ||
+        cudaFuncSetAttribute(unit_lists_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(unit_lists_smem(256))) != cudaSuccess)
       return TWELL_ERR_CUDA;
     attr[dev] = true;
   }
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    unit_lists_kernel<<<f / Lh.tile, kListWarps * 32, lsm, s>>>(L, ws.dz_cells, ws.col_beg, ws.col_end, ws.col_rows,
-                                                             ws.col_h, ws.col_dz);
+    auto lk = Lh.cap == 8 ? unit_lists_kernel<true> : unit_lists_kernel<false>;
+    lk<<<f / Lh.tile, kListWarps * 32, lsm, s>>>(L, ws.dz_cells, ws.col_beg, ws.col_end, ws.col_rows, ws.col_h,
+                                               ws.col_dz);
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.main_wait_mark());  // the fallback share is in dW before the TwELL share is added
