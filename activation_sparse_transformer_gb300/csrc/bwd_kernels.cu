@@ -10,7 +10,8 @@
 //             fp32 values for TwELL rows; for fallback rows a split-K tcgen05
 //             GEMM of dZ (as bf16 high + low parts) with W_in^T read N-major
 //   unit lists  the TwELL entries regrouped by hidden unit, rows ascending,
-//             built deterministically (block histograms, scans, ordered fill)
+//             built deterministically in one launch (a CTA per tile of units:
+//             counts, scans and row masks in shared memory)
 //   dw_unitcta_kernel  dW_down[j] = sum_n h[n][j] dY[n], dW_in^T[j] = sum_n dZ[n][j] X[n],
 //             db[j] = sum_n dZ[n][j] over the TwELL entries
 //   fallback  the dense fallback rows' share of dW_down and dW_in^T stored
