@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/twell.h: argument checks,
 // TMA descriptor encoding, the launch sequence of each call, the device
-// status word, launch counting and optional per-kernel event timing.
+// status word, launch counting and optional per-kernel event timing (totals
+// per kernel id and a launch timeline).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
