@@ -45,9 +45,15 @@ def run(tw, torch, cfg, inp, dY, lam):
 
 @pytest.mark.parametrize("name,N,d,T,C,lam", [("pr1", 256, 256, 64, 8, 1e-4), ("ragged", 301, 256, 128, 8, 1e-2),
                                                 ("t32", 160, 256, 32, 4, 0.0),
-                                                # dX through the bulk-copy ring (2048 and 4096 columns)
+                                                # wider rows (2048 and 4096 columns)
                                                 ("wide", 300, 2048, 128, 8, 1e-4),
-                                                ("wide16", 200, 4096, 64, 16, 1e-3)])
+                                                ("wide16", 200, 4096, 64, 16, 1e-3),
+                                                # 256-wide tiles (the unit lists' largest shared-memory
+                                                # case) at C = 8 and 16, and a decode-sized batch whose
+                                                # forward takes the small-batch path
+                                                ("t256c8", 130, 256, 256, 8, 0.0),
+                                                ("t256c16", 200, 512, 256, 16, 1e-3),
+                                                ("small", 16, 256, 64, 8, 1e-4)])
 def test_bwd_matches_oracle(tw, name, N, d, T, C, lam):
     import torch
     cfg = synth.FFNConfig(name, N, d, 1024, T, C, seed=N + 7, row_spread="lognormal", forced_frac_rows=0.03,
