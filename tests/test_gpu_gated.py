@@ -50,7 +50,9 @@ def check_pack(p, H, T, C, fb_cap):
 
 
 @pytest.mark.parametrize("N,d,f,T,C,sp", [(256, 128, 512, 64, 8, 0.95), (200, 128, 1024, 128, 16, 0.97),
-                                          (130, 256, 512, 32, 4, 0.9)])
+                                          (130, 256, 512, 32, 4, 0.9),
+                                          # small batches: one zero-filled M tile, the SpMM split into ranges
+                                          (16, 256, 1024, 64, 8, 0.9), (32, 512, 1024, 128, 16, 0.95)])
 def test_gated_integer_bit_exact(tw, N, d, f, T, C, sp):
     import torch
     inp = synth.make_integer_inputs(N, d, f, seed=N + f, lo=-1, hi=1, sparsity=sp, gated=True)
