@@ -53,7 +53,8 @@ def run(tw, torch, cfg, inp, dY, lam):
                                                 # forward takes the small-batch path
                                                 ("t256c8", 130, 256, 256, 8, 0.0),
                                                 ("t256c16", 200, 512, 256, 16, 1e-3),
-                                                ("small", 16, 256, 64, 8, 1e-4)])
+                                                ("small", 16, 256, 64, 8, 1e-4),
+                                                ("c32", 160, 256, 64, 32, 1e-3)])
 def test_bwd_matches_oracle(tw, name, N, d, T, C, lam):
     import torch
     cfg = synth.FFNConfig(name, N, d, 1024, T, C, seed=N + 7, row_spread="lognormal", forced_frac_rows=0.03,

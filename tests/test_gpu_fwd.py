@@ -73,6 +73,9 @@ INT_CASES = [
     (300, 2048, 1024, 128, 8, 0.97, 5),
     (200, 4096, 1024, 64, 16, 0.95, 6),
     (136, 8192, 512, 128, 8, 0.97, 7),
+    # the largest capacity (C = 32), and C = T, where no tile can overflow
+    (200, 256, 1024, 64, 32, 0.8, 8),
+    (130, 128, 512, 32, 32, 0.5, 9),
 ]
 
 
