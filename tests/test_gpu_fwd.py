@@ -233,3 +233,36 @@ def test_dense_comparator(tw):
     mism = (Hg != 0) != (Hr != 0)
     assert not mism.any() or np.abs(Z[mism]).max() < 1e-3
     assert_close(from_dev_f32(Y), oracle.down_dense(Hr, inp["W_down"]), "dense Y")
+
+
+def test_profile_timeline_of_a_forward(tw):
+    # the launch timeline of one forward: launch order, streams and device times
+    import torch
+    cfg = synth.CONFIGS["pr1"]
+    inp = synth.make_ffn_inputs(cfg)
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
+    p = tw.alloc_packed(N, f, T, C, fb, dev)
+    Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws, stream)
+    torch.cuda.synchronize()
+    tw.twell_profile_reset()
+    tw.twell_profile_enable(True)
+    tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws, stream)
+    tw.twell_profile_enable(False)
+    tl = tw.twell_profile_timeline()
+    tw.twell_profile_reset()
+    assert [e["kernel"] for e in tl] == ["up_pack", "route", "fb_assemble", "fb_down", "fb_down", "spmm"]
+    main = int(stream.cuda_stream)
+    assert [e["stream"] == main for e in tl] == [True, True, False, False, False, True]
+    assert tl[0]["start_ms"] == 0.0
+    for e in tl:
+        assert e["end_ms"] >= e["start_ms"] >= 0.0
+    for s in (True, False):   # launches on one stream run in order
+        seq = [e for e in tl if (e["stream"] == main) == s]
+        assert all(a["end_ms"] <= c["start_ms"] + 1e-6 for a, c in zip(seq, seq[1:]))
+    assert tl[1]["start_ms"] >= tl[0]["end_ms"] - 1e-6          # routing after the up-projection
+    assert tl[2]["start_ms"] >= tl[1]["end_ms"] - 1e-6          # the second stream forks after routing
