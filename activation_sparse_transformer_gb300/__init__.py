@@ -4,6 +4,23 @@ Argument marshalling only: every step of the layer runs in the library's CUDA
 kernels (include/twell.h documents each call).  torch supplies device memory
 and the current stream; bf16 tensors are passed by pointer.  If the library
 has not been built, every call raises -- there is no CPU or eager fallback.
+
+One training step of a layer (X [N, d] bf16; W_inT, W_down [f, d] bf16; b [f]
+bf16; T the tile width, C the per-tile capacity, fb_cap the dense fallback
+rows):
+
+    import activation_sparse_transformer_gb300 as tw
+    H = tw.alloc_packed(N, f, T, C, fb_cap, "cuda")      # the packed activations
+    ws = torch.empty(max(tw.fwd_workspace_bytes(N, d, f, T, C, fb_cap),
+                         tw.bwd_workspace_bytes(N, d, f, T, C, fb_cap)),
+                     dtype=torch.uint8, device="cuda")      # one scratch for both calls
+    tw.twell_ffn_fwd(X, W_inT, b, W_down, H, Y, ws)          # Y [N, d] bf16
+    tw.twell_ffn_bwd(X, W_inT, W_down, H, dY, l1_lambda,     # dX bf16; dW_inT, dW_down,
+                     dX, dW_inT, dW_down, db, ws)           # db fp32
+    assert tw.twell_read_status(H) == 0                      # e.g. fallback overflow
+
+The calls are asynchronous on the current stream and can be captured in a CUDA
+graph; twell_pack / twell_unpack convert between dense bf16 H and the packed form.
 """
 from __future__ import annotations
 
