@@ -587,6 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < args.n_zero0; i += blockDim.x) args.zero0[i] = 0;
     for (int i = threadIdx.x; i < args.n_zero1; i += blockDim.x) args.zero1[i] = 0;
   }
+  // nothing to compute (e.g. no fallback rows this call): leave before setting
+  // up barriers and TMEM (uniform over the CTA and the grid)
+  if (num_units == 0) return;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
