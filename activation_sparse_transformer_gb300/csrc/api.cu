@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <mutex>
 #include <vector>
 
@@ -458,6 +459,8 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   if (H->hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
+  // the unit-major lists address the stored entries with 32-bit positions
+  if (static_cast<int64_t>(H->n_rows) * (H->d_ff / H->tile) * H->cap > INT32_MAX) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
   TW_TRY(check_dense(W_inT));
   TW_TRY(check_dense(W_down));

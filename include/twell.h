@@ -214,7 +214,9 @@ TWELL_API size_t twell_ffn_fwd_noalloc_max_scratch(void);
  * rows are handed to CTAs through an atomic counter, which changes only who
  * computes a row, not how).
  * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned
- * (it may be the forward call's workspace, see twell_ffn_fwd). */
+ * (it may be the forward call's workspace, see twell_ffn_fwd).
+ * TWELL_ERR_UNSUPPORTED for the tile-granular variant and when
+ * n_rows * (d_ff / tile) * cap exceeds 2^31 - 1 (32-bit entry positions). */
 TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                   const twell_t* H, int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
                   float* dW_inT, float* dW_down, float* db, void* workspace,
