@@ -634,7 +634,7 @@ def cpu_baseline(rows=None):
     cfg = synth.CONFIGS["1b"]
     base = synth.make_ffn_inputs(cfg)
     dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
-    rows = rows or cpu_sample_rows(384)
+    rows = rows or cpu_sample_rows(1536)  # ~10-15 s of the oracle on the host cores
     oracle.build()
     t = time.perf_counter()
     oracle_step(base, dY, rows, cfg, cfg.l1_lambda or 1e-4)
