@@ -91,3 +91,16 @@ def test_host_argument_checks_without_gpu(lib):
     assert ws % 256 == 0
     assert tw.fwd_workspace_bytes(4096, 2048, 8192, 128, 8, 0) > 0
     assert tw.bwd_workspace_bytes(4096, 2048, 8192, 128, 8, 512) > 4096 * 64 * 8 * 4
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no CPU or eager fallback: without libtwell.so every call raises
+    import pytest
+
+    import activation_sparse_transformer_gb300 as tw
+    monkeypatch.setattr(tw, "_lib_handle", None)
+    monkeypatch.setattr(tw, "LIB_PATH", str(tmp_path / "libtwell.so"))
+    with pytest.raises(RuntimeError):
+        tw.load_library()
+    with pytest.raises(RuntimeError):
+        tw.fwd_workspace_bytes(16, 128, 256, 64, 8, 4)
