@@ -414,18 +414,23 @@ EXPORT void oracle_grad_weights(const uint16_t* X, const uint16_t* W_down, const
  *   1 count above C in a TwELL row      2 non-zero count in a fallback row
  *   3 index >= T                         4 indices not strictly increasing
  *   5 stored value equal to zero         6 padding slot not (+0.0, 0)
- *   7 row_fb / fb_rows not inverse       8 fb_rows not ascending
+ *   7 row_fb / fb_rows not inverse (a row whose slot is past fb_cap, left
+ *     unstored when the fallback overflowed, has no fb_rows entry)
+ *   8 slots not numbered 0, 1, ... in ascending row order, or fb_rows not
+ *     ascending
  *   9 number of fallback rows != n_fb */
 EXPORT int32_t oracle_check_format(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
                                    const int32_t* row_fb, const int32_t* fb_rows, int32_t n_fb,
                                    int32_t N, int32_t f, int32_t T, int32_t C, int32_t fb_cap) {
   const int32_t nt = f / T;
   int32_t seen_fb = 0;
+  int misnumbered = 0;
   for (int32_t n = 0; n < N; ++n) {
     int is_fb = row_fb[n] >= 0;
     if (is_fb) {
+      if (row_fb[n] != seen_fb) misnumbered = 1;
       seen_fb += 1;
-      if (row_fb[n] >= fb_cap || fb_rows[row_fb[n]] != n) return 7;
+      if (row_fb[n] < fb_cap && fb_rows[row_fb[n]] != n) return 7;
     } else if (row_fb[n] != -1) {
       return 7;
     }
@@ -447,6 +452,7 @@ EXPORT int32_t oracle_check_format(const uint16_t* values, const uint8_t* idx, c
       }
     }
   }
+  if (misnumbered) return 8;
   for (int32_t s = 1; s < n_fb && s < fb_cap; ++s)
     if (fb_rows[s] <= fb_rows[s - 1]) return 8;
   if (seen_fb != n_fb) return 9;

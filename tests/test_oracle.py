@@ -174,6 +174,26 @@ def test_format_checker_catches_each_violation():
     assert mutated(lambda p: p["row_fb"].__setitem__(0, 1)) == 7
     assert mutated(lambda p: p["fb_rows"].__setitem__(slice(0, 2), p["fb_rows"][1::-1].copy())) in (7, 8)
     assert mutated(lambda p: p.__setitem__("n_fb", 1)) == 9
+    # slots must be the rows' ranks: an inverse pair (last fallback row <-> a
+    # free slot) is not enough
+    fbr = [int(r) for r in np.flatnonzero(good["row_fb"] >= 0)]
+    assert len(fbr) >= 2 and {3, 17} <= set(fbr) and good["n_fb"] == len(fbr) < 7
+
+    def renumber(p):
+        p["row_fb"][fbr[-1]] = 7
+        p["fb_rows"][7] = fbr[-1]
+    assert mutated(renumber) == 8
+
+    def swap_slots(p):
+        p["row_fb"][fbr[0]], p["row_fb"][fbr[1]] = 1, 0
+        p["fb_rows"][:2] = [fbr[1], fbr[0]]
+    assert mutated(swap_slots) == 8
+    # an overflowed fallback (rows past fb_cap keep their numbers, unstored) is well formed
+    over = oracle.pack(H, T, C, 1)
+    assert over["n_fb"] == len(fbr) and list(over["row_fb"][fbr]) == list(range(len(fbr)))
+    assert oracle.check_format(over, f) == 0
+    over["fb_rows"][0] = fbr[1]
+    assert oracle.check_format(over, f) == 7
 
 
 # ---------------------------------------------------------------- forward arithmetic
