@@ -35,7 +35,7 @@ LIB_PATH = os.path.join(_PKG, "libtwell.so")
 TWELL_OK = 0
 KERNELS = {
     "up_pack": 0, "route": 1, "fb_assemble": 2, "spmm": 4, "fb_down": 5, "pack": 6,
-    "unpack": 7, "sddmm": 8, "dx": 9, "dw": 10, "dense_gemm": 11, "aux": 12,
+    "check_format": 3, "unpack": 7, "sddmm": 8, "dx": 9, "dw": 10, "dense_gemm": 11, "aux": 12,
 }
 EXPORTED = [
     "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",
@@ -43,7 +43,7 @@ EXPORTED = [
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
     "twell_profile_timeline",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
-    "twell_selftest_wait_timeout",
+    "twell_selftest_wait_timeout", "twell_check_format",
 ]
 
 
@@ -97,6 +97,7 @@ def load_library() -> ctypes.CDLL:
         "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
         "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
         "twell_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
+        "twell_check_format": (ctypes.c_int, [L, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -243,6 +244,14 @@ def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
     f = W_inT.shape[0]
     _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, _ptr(Hbuf),
                                               _ptr(Y), _stream(stream)), "twell_dense_ffn_fwd")
+
+
+def twell_check_format(packed: Packed, violations, stream=None) -> None:
+    """Check the layout's format rules on the device (asynchronous): bit k of
+    the device int32 tensor `violations` is set when rule k is broken."""
+    st = packed.struct()
+    _check(load_library().twell_check_format(ctypes.byref(st), _ptr(violations), _stream(stream)),
+           "twell_check_format")
 
 
 def twell_read_status(packed: Packed, stream=None) -> int:

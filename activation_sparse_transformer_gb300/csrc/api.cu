@@ -280,6 +280,13 @@ int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t str
   return launch_unpack(*in, H, ldh, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int twell_check_format(const twell_t* layout, int32_t* violations, twell_stream_t stream) {
+  if (!layout || !violations) return TWELL_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(violations) % alignof(int32_t) != 0) return TWELL_ERR_MISALIGNED;
+  TW_TRY(check_layout(layout));
+  return launch_check_format(*layout, violations, reinterpret_cast<cudaStream_t>(stream));
+}
+
 namespace {
 // Forward workspace: [spill tiles][spill counter][fallback down-projection
 // partials] then, for small batches, [up-projection K-split partials][dense H]
@@ -526,6 +533,7 @@ const char* twell_status_string(int code) {
     case TWELL_ERR_FALLBACK_OVERFLOW: return "more dense-fallback rows than fb_cap";
     case TWELL_ERR_WAIT_TIMEOUT: return "a bounded pipeline wait on the GPU expired";
     case TWELL_ERR_NO_DEVICE: return "no sm_103a device is current";
+    case TWELL_ERR_BAD_FORMAT: return "packed layout breaks a format rule";
     default: return "unknown status";
   }
 }

@@ -10,6 +10,9 @@
 // fb_copy_kernel: dense rows of fallback rows -> fb_dense, their cells cleared.
 // unpack_kernel: each lane rebuilds 8 output columns from its tile's cell (or
 //   from fb_dense) and writes them with one 16-byte store.
+// check_cells_kernel / check_order_kernel: the format rules of a layout
+//   (cell contents, then the numbering of fallback rows or dense tiles),
+//   reported as a mask of broken rules.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -244,6 +247,140 @@ __global__ void __launch_bounds__(kWarps * 32)
   *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + col) = out;
 }
 
+// ---------------------------------------------------------------- format check
+// Rule numbers of the violation mask (bit k = rule k), as twell.h lists them.
+constexpr int kRuleCount = 1, kRuleFbCell = 2, kRuleIdxRange = 3, kRuleIdxOrder = 4, kRuleZero = 5,
+              kRulePad = 6, kRuleRowMap = 7, kRuleFbOrder = 8, kRuleFbCount = 9, kRuleTileOrder = 10,
+              kRuleTileCount = 11, kRuleTileSparse = 12;
+
+__device__ __forceinline__ bool bf16_is_zero(uint16_t v) { return (v & 0x7FFFu) == 0; }
+
+// OR of every lane's bits, one atomic per warp; all lanes must arrive.
+__device__ __forceinline__ void flag_rules(int32_t* mask, int32_t* status, int bits) {
+  bits = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bits)));
+  if ((threadIdx.x & 31) == 0 && bits) {
+    atomicOr(mask, bits);
+    report_error(status, TWELL_ERR_BAD_FORMAT);
+  }
+}
+
+// One thread per cell (grid-stride): the count, the stored entries, the
+// padding, and for a dense tile the pool tile it names.
+__global__ void __launch_bounds__(256) check_cells_kernel(Layout L, int32_t* mask) {
+  const bool tiles = L.hybrid == TWELL_HYBRID_TILES;
+  const int64_t cells = static_cast<int64_t>(L.N) * L.nt;
+  const int64_t pool = static_cast<int64_t>(L.fb_cap) * L.nt;
+  int bits = 0;
+  for (int64_t cell = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; cell < cells;
+       cell += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int cnt = L.counts[cell];
+    const uint16_t* v = L.values + cell * L.C;
+    const uint8_t* ix = L.idx + cell * L.C;
+    int s_begin = 0, entries = cnt;  // slots [s_begin, entries) hold entries, the rest padding
+    if (tiles && cnt == TWELL_DENSE_TILE) {
+      const int64_t slot = static_cast<int64_t>(v[0]) | (static_cast<int64_t>(ix[0]) << 16);
+      if (slot < pool) {  // a slot past the pool breaks the numbering rule instead
+        const uint16_t* p = L.fb_dense + slot * L.T;
+        int nz = 0;
+        for (int i = 0; i < L.T; ++i) nz += bf16_is_zero(p[i]) ? 0 : 1;
+        if (nz <= L.C) bits |= 1 << kRuleTileSparse;
+      }
+      s_begin = 1;  // slot 0 holds the pool slot
+      entries = 0;
+    } else {
+      if (!tiles && cnt != 0 && L.row_fb[cell / L.nt] >= 0) bits |= 1 << kRuleFbCell;
+      if (cnt > L.C) {
+        bits |= 1 << kRuleCount;
+        continue;  // the slots' meaning is unknown
+      }
+    }
+    for (int s = s_begin; s < L.C; ++s) {
+      const uint16_t vs = v[s];
+      const int is = ix[s];
+      if (s < entries) {
+        if (is >= L.T) bits |= 1 << kRuleIdxRange;
+        if (s > 0 && is <= ix[s - 1]) bits |= 1 << kRuleIdxOrder;
+        if (bf16_is_zero(vs)) bits |= 1 << kRuleZero;
+      } else if (vs != 0 || is != 0) {
+        bits |= 1 << kRulePad;
+      }
+    }
+  }
+  flag_rules(mask, L.status, bits);
+}
+
+// One CTA numbers the fallback rows (rows variant) or the dense tiles (tiles
+// variant) in order with a block-wide exclusive scan, 1024 items per pass,
+// and checks each against the slot it holds; then the totals and fb_rows.
+constexpr int kCheckThreads = 1024;
+
+__global__ void __launch_bounds__(kCheckThreads) check_order_kernel(Layout L, int32_t* mask) {
+  __shared__ int warp_tot[kCheckThreads / 32];
+  __shared__ int64_t base_s;
+  const bool tiles = L.hybrid == TWELL_HYBRID_TILES;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t items = tiles ? static_cast<int64_t>(L.N) * L.nt : L.N;
+  const int64_t pool = static_cast<int64_t>(L.fb_cap) * L.nt;
+  int bits = 0;
+  if (tid == 0) base_s = 0;
+  __syncthreads();
+  for (int64_t i0 = 0; i0 < items; i0 += kCheckThreads) {
+    const int64_t i = i0 + tid;
+    bool marked = false;
+    int64_t slot = -1;
+    if (i < items) {
+      if (tiles) {
+        marked = L.counts[i] == TWELL_DENSE_TILE;
+        if (marked) slot = static_cast<int64_t>(L.values[i * L.C]) | (static_cast<int64_t>(L.idx[i * L.C]) << 16);
+      } else {
+        slot = L.row_fb[i];
+        marked = slot >= 0;
+        if (slot < -1) bits |= 1 << kRuleRowMap;
+      }
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, marked);
+    if (lane == 0) warp_tot[warp] = __popc(ball);
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_tot[lane];
+      int incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      warp_tot[lane] = incl - w;  // exclusive prefix of the warps' counts
+    }
+    __syncthreads();
+    const int64_t base = base_s;
+    const int64_t rank = base + warp_tot[warp] + __popc(ball & ((1u << lane) - 1u));
+    if (marked) {
+      if (tiles) {
+        if (slot != rank || slot >= pool) bits |= 1 << kRuleTileOrder;
+      } else {
+        if (slot != rank) bits |= 1 << kRuleFbOrder;
+        if (slot < L.fb_cap && L.fb_rows[slot] != i) bits |= 1 << kRuleRowMap;
+      }
+    }
+    __syncthreads();
+    if (tid == kCheckThreads - 1) base_s = rank + (marked ? 1 : 0);
+    __syncthreads();
+  }
+  const int64_t marked_total = base_s;
+  const int64_t n_fb = *L.n_fb;
+  if (tiles) {
+    for (int r = tid; r < L.N; r += kCheckThreads)
+      if (L.row_fb[r] != -1) bits |= 1 << kRuleRowMap;
+    if (tid == 0 && marked_total != min(n_fb, pool)) bits |= 1 << kRuleTileCount;
+  } else {
+    const int64_t stored = min(n_fb, static_cast<int64_t>(L.fb_cap));
+    for (int64_t s = 1 + tid; s < stored; s += kCheckThreads)
+      if (L.fb_rows[s] <= L.fb_rows[s - 1]) bits |= 1 << kRuleFbOrder;
+    if (tid == 0 && marked_total != n_fb) bits |= 1 << kRuleFbCount;
+  }
+  flag_rules(mask, L.status, bits);
+}
+
 int64_t warps_needed(const twell_t& L) {
   return static_cast<int64_t>(L.n_rows) * ((L.d_ff + 255) / 256);
 }
@@ -284,6 +421,20 @@ int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s) {
   if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
   LaunchScope ls(TWELL_KERNEL_UNPACK, s);
   unpack_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+int launch_check_format(const twell_t& L, int32_t* violations, cudaStream_t s) {
+  if (cudaMemsetAsync(violations, 0, sizeof(int32_t), s) != cudaSuccess) return TWELL_ERR_CUDA;
+  const int64_t cells = static_cast<int64_t>(L.n_rows) * (L.d_ff / L.tile);
+  if (cells > 0) {
+    const int64_t blocks = std::min<int64_t>((cells + 255) / 256, 8 * static_cast<int64_t>(sm_count()));
+    LaunchScope ls(TWELL_KERNEL_CHECK_FORMAT, s);
+    check_cells_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(flat(L), violations);
+    if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  }
+  LaunchScope ls(TWELL_KERNEL_CHECK_FORMAT, s);
+  check_order_kernel<<<1, kCheckThreads, 0, s>>>(flat(L), violations);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

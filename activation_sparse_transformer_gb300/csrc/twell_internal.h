@@ -200,6 +200,8 @@ int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_
 int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint16_t* H, const twell_t& L,
                          int32_t* arrivals, cudaStream_t s);
 int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s);
+// Format rules of a layout -> *violations (mask, zeroed first); two launches.
+int launch_check_format(const twell_t& L, int32_t* violations, cudaStream_t s);
 
 // backward (bwd_kernels.cu)
 struct BwdWorkspace {

@@ -89,7 +89,8 @@ enum {
   TWELL_ERR_WORKSPACE = -5,          /* workspace missing or too small */
   TWELL_ERR_FALLBACK_OVERFLOW = -6,  /* device: more fallback rows than fb_cap */
   TWELL_ERR_WAIT_TIMEOUT = -7,       /* device: a bounded pipeline wait expired */
-  TWELL_ERR_NO_DEVICE = -8           /* no sm_103a device current */
+  TWELL_ERR_NO_DEVICE = -8,          /* no sm_103a device current */
+  TWELL_ERR_BAD_FORMAT = -9          /* device: twell_check_format found a broken rule */
 };
 
 enum {
@@ -247,6 +248,33 @@ TWELL_API int twell_read_status(const twell_t* layout, twell_stream_t stream);
  * 0 < limit_ns <= 10 s.  Asynchronous on `stream`. */
 TWELL_API int twell_selftest_wait_timeout(int32_t* status, uint64_t limit_ns, twell_stream_t stream);
 
+/* Device check of a packed layout against the format rules at the top of this
+ * file: a debugging aid for layouts built outside twell_pack / twell_ffn_fwd
+ * (the gathers trust stored indices and slot numbers, and read out of bounds
+ * when they are wrong).  Zeroes *violations (device int32, 4-byte aligned),
+ * then sets bit k of it when rule k is broken anywhere in the layout:
+ *    1  a cell count above C (tile variant: and not TWELL_DENSE_TILE)
+ *    2  a fallback row with a non-empty cell (rows variant)
+ *    3  a stored index >= T
+ *    4  stored indices not strictly increasing within a cell
+ *    5  a stored value that compares equal to zero
+ *    6  a padding slot not (+0.0, 0)
+ *    7  rows variant: row_fb below -1, or a fallback row n with slot s < fb_cap
+ *       and fb_rows[s] != n; tile variant: row_fb not -1
+ *    8  fallback slots not 0, 1, ... in ascending row order (rows past fb_cap
+ *       keep their numbers), or fb_rows[0 .. min(n_fb, fb_cap)) not ascending
+ *    9  fallback rows marked in row_fb != *n_fb
+ *   10  dense-tile slots not 0, 1, ... in (row, tile) order, or past the pool
+ *   11  dense tiles marked != min(*n_fb, fb_cap * n_tiles)
+ *   12  a dense tile whose pool tile holds at most C non-zeros
+ * When the mask is non-zero, *status becomes TWELL_ERR_BAD_FORMAT unless it
+ * already holds an error.  Reads the layout's arrays; writes nothing else.
+ * Two launches: one thread per cell, then one CTA that numbers the fallback
+ * rows (or dense tiles) in order -- O(n_rows * n_tiles) work, not a hot path.
+ * A layout straight from twell_pack or twell_ffn_fwd passes, including one
+ * whose fallback overflowed fb_cap. */
+TWELL_API int twell_check_format(const twell_t* layout, int32_t* violations, twell_stream_t stream);
+
 /* Static string for a TWELL_* code. */
 TWELL_API const char* twell_status_string(int code);
 
@@ -262,7 +290,7 @@ enum {
   TWELL_KERNEL_UP_PACK = 0,      /* tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue */
   TWELL_KERNEL_ROUTE = 1,        /* fallback routing scan */
   TWELL_KERNEL_FB_ASSEMBLE = 2,  /* dense fallback rows from spilled tiles + cells */
-  TWELL_KERNEL_RESERVED3 = 3,    /* unused */
+  TWELL_KERNEL_CHECK_FORMAT = 3, /* twell_check_format */
   TWELL_KERNEL_SPMM = 4,         /* TwELL gather-SpMM down-projection */
   TWELL_KERNEL_FB_DOWN = 5,      /* fallback rows' down-projection */
   TWELL_KERNEL_PACK = 6,         /* standalone dense -> TwELL */

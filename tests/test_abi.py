@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     import activation_sparse_transformer_gb300 as tw
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         s = tw.status_string(code)
         assert s and s != "unknown status"
     assert tw.status_string(-100) == "unknown status"
@@ -71,6 +71,11 @@ def test_host_argument_checks_without_gpu(lib):
     # the wait self-test checks its arguments on the host
     assert lib.twell_selftest_wait_timeout(None, 1000, None) == -1
     assert lib.twell_selftest_wait_timeout(ctypes.c_void_p(0x10000), 0, None) == -1
+    # the format check wants an aligned result word
+    assert lib.twell_check_format(None, ctypes.c_void_p(0x10000), None) == -1
+    assert lib.twell_check_format(ctypes.byref(L), None, None) == -1
+    assert lib.twell_check_format(ctypes.byref(L), ctypes.c_void_p(0x10002), None) == -2
+    assert lib.twell_check_format(ctypes.byref(bad), ctypes.c_void_p(0x10000), None) == -3
     # the launch timeline: a negative count, or entries asked for without the arrays
     assert lib.twell_profile_timeline(-1, None, None, None, None) == -1
     assert lib.twell_profile_timeline(4, None, None, None, None) == -1
