@@ -645,6 +645,34 @@ def cpu_baseline(rows=None):
                       f"(plain C fp32 loops, OpenMP over {cores} threads), {el:.1f} s"}
 
 
+def time_pr1_oracle() -> None:
+    """Prints the seconds of one oracle fwd + bwd of the whole small layer
+    (N 256, d_model 256, d_ff 1024, T 64, C 8) as one JSON number."""
+    import oracle
+    import synth
+    cfg = synth.CONFIGS["pr1"]
+    base = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
+    oracle.build()
+    t = time.perf_counter()
+    oracle_step(base, dY, cfg.n_rows, cfg, cfg.l1_lambda or 1e-4)
+    print(json.dumps(time.perf_counter() - t))
+
+
+def cpu_single_thread_pr1():
+    """The oracle on one host thread over the whole small layer, in a fresh
+    process: the OpenMP runtime reads OMP_NUM_THREADS once, when it loads."""
+    import synth
+    n = synth.CONFIGS["pr1"].n_rows
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", "import bench; bench.time_pr1_oracle()"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=600, check=True)
+    el = float(out.stdout.strip().splitlines()[-1])
+    return {"value": round(n / el, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fwd+bwd of the whole small layer (N={n}, d_model=256, d_ff=1024, T=64, C=8), "
+                      f"one thread, {el:.2f} s"}
+
+
 def bench_reference(args, rank, world):
     if rank != 0:
         return None
@@ -714,6 +742,10 @@ def main():
     elif rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
+            try:
+                res["cpu_baseline"]["single_thread_pr1"] = cpu_single_thread_pr1()
+            except (subprocess.SubprocessError, ValueError, IndexError) as exc:
+                res["cpu_baseline"]["single_thread_pr1"] = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -56,3 +56,11 @@ def test_two_gloo_ranks_max_and_distinct_batches():
 def test_single_rank_passthrough():
     assert bench.max_over_ranks([1.5, 2.5], 1, None) == [1.5, 2.5]
     assert bench.rank_config(synth.CONFIGS["1b"], 0) is synth.CONFIGS["1b"]
+
+
+def test_single_thread_oracle_line():
+    """The bench's single-thread CPU figure: the oracle over the whole small
+    layer in a child process limited to one OpenMP thread."""
+    line = bench.cpu_single_thread_pr1()
+    assert line["cores"] == 1 and line["kind"] == "oracle" and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and "one thread" in line["sample"]
