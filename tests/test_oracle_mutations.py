@@ -47,6 +47,14 @@ MUTATIONS = [
      lambda: tile_pins.test_tiles_brute_force_all_patterns(3)),
     ("dense tiles left out of Y", "acc += bf16_to_f32(tile[i]) * bf16_to_f32(W_down[((int64_t)t * T + i) * d + c]);",
      "acc += 0.0f;", tile_pins.test_tiles_packed_product_equals_dense_bitwise),
+    ("checker ignores slot numbers", "if (row_fb[n] != seen_fb) misnumbered = 1;", "",
+     pins.test_format_checker_catches_each_violation),
+    ("checker rejects unstored overflow rows", "if (row_fb[n] < fb_cap && fb_rows[row_fb[n]] != n) return 7;",
+     "if (row_fb[n] >= fb_cap || fb_rows[row_fb[n]] != n) return 7;",
+     pins.test_format_checker_catches_each_violation),
+    ("checker index bound off by one", "if (i >= T) return 3;\n          if (s > 0 && i <= idx[cell * C + s - 1]) return 4;\n          if (bf16_to_f32(v) == 0.0f) return 5;\n        } else if (v != 0 || i != 0) {\n          return 6;\n        }\n      }\n    }\n  }\n  if (misnumbered)",
+     "if (i > T) return 3;\n          if (s > 0 && i <= idx[cell * C + s - 1]) return 4;\n          if (bf16_to_f32(v) == 0.0f) return 5;\n        } else if (v != 0 || i != 0) {\n          return 6;\n        }\n      }\n    }\n  }\n  if (misnumbered)",
+     pins.test_format_checker_catches_each_violation),
 ]
 
 
