@@ -122,6 +122,19 @@ def _stream(stream=None) -> int:
     return int(s.cuda_stream)
 
 
+def _need(t, nbytes: int, name: str) -> None:
+    """Rejects a buffer smaller than the bytes the call reads or writes through
+    it (the C ABI receives only the pointer)."""
+    have = 0 if t is None else t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name}: {have} bytes, the call needs {nbytes}")
+
+
+def _need_dense(t, rows: int, row_elems: int, ld: int, elem_bytes: int, name: str) -> None:
+    """A [rows][ld] buffer of which the first row_elems of every row are used."""
+    _need(t, ((rows - 1) * ld + row_elems) * elem_bytes if rows > 0 else 0, name)
+
+
 def _ptr(t) -> Optional[int]:
     if t is None:
         return None
@@ -149,6 +162,16 @@ class Packed:
     hybrid: int = 0   # HYBRID_ROWS or HYBRID_TILES
 
     def struct(self) -> twell_t:
+        N, nt = self.n_rows, self.d_ff // self.tile
+        cells = N * nt
+        _need(self.values, cells * self.cap * 2, "values")
+        _need(self.idx, cells * self.cap, "idx")
+        _need(self.counts, cells, "counts")
+        _need(self.row_fb, N * 4, "row_fb")
+        _need(self.fb_rows, self.fb_cap * 4, "fb_rows")
+        _need(self.fb_dense, self.fb_cap * self.d_ff * 2, "fb_dense")
+        _need(self.n_fb, 4, "n_fb")
+        _need(self.status, 4, "status")
         p = lambda t: t.data_ptr() if t is not None and t.numel() else None
         return twell_t(self.n_rows, self.d_ff, self.tile, self.cap, self.fb_cap, self.hybrid,
                        p(self.values), p(self.idx), p(self.counts), p(self.row_fb), p(self.fb_rows),
@@ -180,11 +203,13 @@ def alloc_packed(n_rows: int, d_ff: int, tile: int, cap: int, fb_cap: int, devic
 
 def twell_pack(H, packed: Packed, stream=None) -> None:
     """Dense bf16 H [n_rows, >= d_ff] -> TwELL hybrid (asynchronous)."""
+    _need_dense(H, packed.n_rows, packed.d_ff, H.stride(0), 2, "H")
     st = packed.struct()
     _check(load_library().twell_pack(_ptr(H), H.stride(0), ctypes.byref(st), _stream(stream)), "twell_pack")
 
 
 def twell_unpack(packed: Packed, H, stream=None) -> None:
+    _need_dense(H, packed.n_rows, packed.d_ff, H.stride(0), 2, "H")
     st = packed.struct()
     _check(load_library().twell_unpack(ctypes.byref(st), _ptr(H), H.stride(0), _stream(stream)), "twell_unpack")
 
@@ -197,9 +222,17 @@ def bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
     return int(load_library().twell_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
 
 
+def _need_layer(n, d, f, W_inT, b, W_down, Y) -> None:
+    _need(W_inT, f * d * 2, "W_inT")
+    _need(b, f * 2, "b")
+    _need(W_down, f * d * 2, "W_down")
+    _need(Y, n * d * 2, "Y")
+
+
 def twell_ffn_fwd(X, W_inT, b, W_down, packed: Packed, Y, workspace, stream=None) -> None:
     n, d = X.shape
     f = W_inT.shape[0]
+    _need_layer(n, d, f, W_inT, b, W_down, Y)
     st = packed.struct()
     _check(load_library().twell_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, ctypes.byref(st),
                                         _ptr(Y), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -210,6 +243,8 @@ def twell_gated_ffn_fwd(X, W_gT, W_uT, b, W_down, packed: Packed, Y, workspace, 
     """Gated ReLU layer: H = ReLU(X.W_g + b) * (X.W_u) packed in TwELL, Y = H.W_down."""
     n, d = X.shape
     f = W_gT.shape[0]
+    _need_layer(n, d, f, W_gT, b, W_down, Y)
+    _need(W_uT, f * d * 2, "W_uT")
     st = packed.struct()
     _check(load_library().twell_gated_ffn_fwd(_ptr(X), _ptr(W_gT), _ptr(W_uT), _ptr(b), _ptr(W_down), n, d, f,
                                               ctypes.byref(st), _ptr(Y), _ptr(workspace),
@@ -222,6 +257,7 @@ def twell_ffn_fwd_noalloc(X, W_inT, b, W_down, packed: Packed, Y, stream=None) -
     array is used (for callers that cannot allocate device memory)."""
     n, d = X.shape
     f = W_inT.shape[0]
+    _need_layer(n, d, f, W_inT, b, W_down, Y)
     st = packed.struct()
     _check(load_library().twell_ffn_fwd_noalloc(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f,
                                                 ctypes.byref(st), _ptr(Y), _stream(stream)),
@@ -231,6 +267,11 @@ def twell_ffn_fwd_noalloc(X, W_inT, b, W_down, packed: Packed, Y, stream=None) -
 def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW_inT, dW_down, db, workspace,
                   stream=None) -> None:
     d = X.shape[1]
+    n, f = packed.n_rows, packed.d_ff
+    for t, nbytes, name in ((X, n * d * 2, "X"), (W_inT, f * d * 2, "W_inT"), (W_down, f * d * 2, "W_down"),
+                            (dY, n * d * 2, "dY"), (dX, n * d * 2, "dX"), (dW_inT, f * d * 4, "dW_inT"),
+                            (dW_down, f * d * 4, "dW_down"), (db, f * 4, "db")):
+        _need(t, nbytes, name)
     st = packed.struct()
     _check(load_library().twell_ffn_bwd(_ptr(X), _ptr(W_inT), _ptr(W_down), ctypes.byref(st), d, _ptr(dY),
                                         float(l1_lambda), _ptr(dX), _ptr(dW_inT), _ptr(dW_down), _ptr(db),
@@ -242,6 +283,8 @@ def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
     """Dense comparator: Y = ReLU(X.W_in + b).W_down on the same tensor-core GEMM."""
     n, d = X.shape
     f = W_inT.shape[0]
+    _need_layer(n, d, f, W_inT, b, W_down, Y)
+    _need(Hbuf, n * f * 2, "Hbuf")
     _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, _ptr(Hbuf),
                                               _ptr(Y), _stream(stream)), "twell_dense_ffn_fwd")
 
@@ -249,6 +292,7 @@ def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
 def twell_check_format(packed: Packed, violations, stream=None) -> None:
     """Check the layout's format rules on the device (asynchronous): bit k of
     the device int32 tensor `violations` is set when rule k is broken."""
+    _need(violations, 4, "violations")
     st = packed.struct()
     _check(load_library().twell_check_format(ctypes.byref(st), _ptr(violations), _stream(stream)),
            "twell_check_format")

@@ -109,3 +109,36 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         tw.load_library()
     with pytest.raises(RuntimeError):
         tw.fwd_workspace_bytes(16, 128, 256, 64, 8, 4)
+
+
+def test_binding_rejects_short_buffers(lib):
+    """The C ABI receives bare pointers, so the binding refuses a tensor with
+    fewer bytes than the call reads or writes through it; correctly sized CPU
+    tensors are then refused as not on the device (there is no CPU path)."""
+    import torch
+    import activation_sparse_transformer_gb300 as tw
+    N, d, f, T, C = 16, 128, 256, 64, 4
+    bf = dict(dtype=torch.bfloat16)
+    p = tw.alloc_packed(N, f, T, C, 2, "cpu")
+    X, Wi, Wd = torch.empty((N, d), **bf), torch.empty((f, d), **bf), torch.empty((f, d), **bf)
+    b, ws = torch.empty(f, **bf), torch.empty(64, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="^Y: "):
+        tw.twell_ffn_fwd(X, Wi, b, Wd, p, torch.empty((N, d - 8), **bf), ws)
+    with pytest.raises(ValueError, match="^b: "):
+        tw.twell_ffn_fwd(X, Wi, b[: f - 1], Wd, p, torch.empty((N, d), **bf), ws)
+    with pytest.raises(ValueError, match="CUDA"):
+        tw.twell_ffn_fwd(X, Wi, b, Wd, p, torch.empty((N, d), **bf), ws)
+    # a gradient buffer of bf16 where fp32 is written is too short
+    dX, db = torch.empty((N, d), **bf), torch.empty(f, dtype=torch.float32)
+    dWd = torch.empty((f, d), dtype=torch.float32)
+    with pytest.raises(ValueError, match="^dW_inT: "):
+        tw.twell_ffn_bwd(X, Wi, Wd, p, X, 0.0, dX, torch.empty((f, d), **bf), dWd, db, ws)
+    # the packed layout's own buffers
+    short = tw.alloc_packed(N, f, T, C, 2, "cpu")
+    short.values = short.values[: N - 1]
+    with pytest.raises(ValueError, match="^values: "):
+        tw.twell_unpack(short, torch.empty((N, f), **bf))
+    with pytest.raises(ValueError, match="^H: "):
+        tw.twell_pack(torch.empty((N - 1, f), **bf), p)
+    with pytest.raises(ValueError, match="^violations: "):
+        tw.twell_check_format(p, torch.empty(0, dtype=torch.int32))
