@@ -46,11 +46,12 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def rank_config(cfg, rank: int):
-    """Weak scaling: every rank draws its own batch of the same shape (seed
-    shifted by 1000 x rank); rank 0 keeps the configuration's own seed."""
+def rank_inputs(cfg, rank: int) -> dict:
+    """Weak scaling: every rank holds the same layer (the configuration's
+    weights and bias) and its own batch of the same shape (batch seed shifted
+    by 1000 x rank); rank 0 keeps the configuration's own batch."""
     import synth
-    return cfg if rank == 0 else synth.FFNConfig(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
+    return synth.make_ffn_inputs(cfg) if rank == 0 else synth.make_ffn_inputs(cfg, batch_seed=cfg.seed + 1000 * rank)
 
 
 def max_over_ranks(values, world: int, device):
@@ -75,8 +76,29 @@ def dist_info():
     return rank, world, local
 
 
+def allreduce_grads(grads, world: int) -> None:
+    """The data-parallel exchange of a training step: every rank's weight
+    gradients (dW_in^T, dW_down, db) summed over the ranks, in place.  Each
+    rank's batch is its own, so the sum is the gradient of the whole job's
+    batch."""
+    if world <= 1:
+        return
+    import torch
+    for g in grads:
+        torch.distributed.all_reduce(g, op=torch.distributed.ReduceOp.SUM)
+
+
+def relaunch_with_ranks(n: int) -> int:
+    """`bench.py --gpus N` outside torchrun: start N ranks on this node (one per
+    GPU) through torch.distributed.run and return its exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", os.environ.get("MASTER_PORT", "29533"),
+           os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd, env=dict(os.environ, TWELL_BENCH_CHILD="1"))
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
+    """nvidia-smi clocks and throttle reasons of one GPU sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -87,7 +109,6 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
-        self.power = []
 
     def start(self):
         try:
@@ -106,7 +127,7 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -114,7 +135,7 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, mx, pw, reasons = [], [], [], set()
+        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -125,16 +146,105 @@ class ClockSampler:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
-            try:
-                pw.append(float(parts[3]))
-            except ValueError:
-                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
-        self.power = pw
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm) if sm else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class EnergyCounter:
+    """The GPU's cumulative energy counter (NVML total energy consumption, mJ),
+    read through the NVML C library.  Read-only: nothing on the GPU is set."""
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        if self.nvml.nvmlInit_v2() != 0:
+            return
+        self.handle = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            uuid = None
+        rc = -1
+        if uuid:
+            rc = self.nvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid if not uuid.startswith("GPU-") else uuid).encode(),
+                                                     ctypes.byref(self.handle))
+        if rc != 0:
+            rc = self.nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(self.handle))
+        self.ok = rc == 0 and self.read_mj() is not None
+
+    def read_mj(self):
+        import ctypes
+        v = ctypes.c_ulonglong(0)
+        if self.nvml.nvmlDeviceGetTotalEnergyConsumption(self.handle, ctypes.byref(v)) != 0:
+            return None
+        return int(v.value)
+
+
+def kernel_work(N, d, f, T, C, nnz_tw, n_fb):
+    """Algorithmic work of one launch (group) of each kernel of the step at one
+    layer shape: FLOPs for the tensor-core products; for the rest the bytes a
+    kernel must move through HBM at least (every input read once, every output
+    written once), and beside them the bytes its gathers pull from L2 (one
+    d_model-wide bf16 row per stored entry and gathered matrix)."""
+    nt = f // T
+    cells = N * nt
+    packed = cells * C * 2 + cells * C + cells          # values, idx, counts
+    fb_rows = n_fb * f * 2
+    row = d * 2                                          # one gathered bf16 row
+    return {
+        "up_pack": {"bound": "tensor", "flops": 2.0 * N * d * f,
+                    "bytes": N * d * 2 + f * d * 2 + packed + N * d * 2, "l2_gather_bytes": nnz_tw * row,
+                    "what": "tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue, with the TwELL rows' "
+                            "gather-SpMM (Y) in the same persistent kernel"},
+        "spmm": {"bound": "hbm", "bytes": packed + f * d * 2 + N * d * 2, "l2_gather_bytes": nnz_tw * row,
+                 "what": "standalone TwELL gather-SpMM (Y)"},
+        "fb_down": {"bound": "tensor", "flops": 2.0 * n_fb * d * f,
+                    "what": "dense fallback rows' down-projection (split-K tcgen05) + ordered reduction"},
+        "sddmm": {"bound": "tensor", "flops": 2.0 * N * d * f,
+                  "what": "tcgen05 dY.W_down^T with the pattern-sampling + L1 epilogue"},
+        "dx": {"bound": "hbm", "bytes": cells * C * 4 + cells * C + cells + f * d * 2 + N * d * 2,
+               "l2_gather_bytes": nnz_tw * row,
+               "what": "dX gather (fp32 dZ entries x W_in^T rows) + fallback rows' GEMM"},
+        "dw": {"bound": "hbm", "bytes": 2 * N * d * 2 + 2 * f * d * 4 + nnz_tw * 12 + f * 4,
+               "l2_gather_bytes": 2 * nnz_tw * row,
+               "what": "dW_down, dW_in^T (fp32) and db: unit-major walk + fallback rows' store GEMMs"},
+        "pack": {"bound": "hbm", "bytes": N * f * 2 + packed + N * 4 + fb_rows,
+                 "what": "standalone dense -> TwELL (twell_pack)"},
+        "unpack": {"bound": "hbm", "bytes": packed + N * 4 + fb_rows + N * f * 2,
+                   "what": "standalone TwELL -> dense (twell_unpack)"},
+    }
+
+
+def roofline_entry(work, us, peaks, peak_src):
+    """achieved / peak of one kernel group from its algorithmic work per step
+    (or per call) and its CUDA-event time per step (the sum of its launches)."""
+    sec = us * 1e-6
+    if work["bound"] == "tensor":
+        ach = work["flops"] / sec / 1e12
+        e = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": round(ach / peaks["bf16_tflops"], 4),
+             "frac_of_sustained": round(ach / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
+             "algorithmic_per_step": work["flops"], "us_per_step": round(us, 2),
+             "peak_source": f"{peak_src} bf16 dense (cuBLAS burst; frac_of_sustained against the sustained loop)"}
+    else:
+        ach = work["bytes"] / sec / 1e9
+        e = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "frac": round(ach / peaks["hbm_gbs"], 4), "algorithmic_per_step": work["bytes"],
+             "us_per_step": round(us, 2), "peak_source": f"{peak_src} HBM copy bandwidth"}
+    if "l2_gather_bytes" in work:
+        e["l2_gather_bytes"] = work["l2_gather_bytes"]
+        e["l2_gather_tbs"] = round(work["l2_gather_bytes"] / sec / 1e12, 2)
+    e["kernel"] = work["what"]
+    return e
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -169,7 +279,7 @@ def bench_ours(args, rank, world, local):
     tw.load_library()
     cfg = synth.CONFIGS[args.config]
     # every rank draws its own batch (weak scaling: per-GPU work is fixed)
-    base = synth.make_ffn_inputs(rank_config(cfg, rank))
+    base = rank_inputs(cfg, rank)
     N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
     lam = cfg.l1_lambda or 1e-4
     dY_np = synth.make_grad_output(N, d, seed=cfg.seed + 77 + rank)
@@ -196,9 +306,14 @@ def bench_ours(args, rank, world, local):
     def fwd():
         tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, wsf, stream)
 
+    def exchange():
+        # data-parallel training: the one exchange of the step
+        allreduce_grads((dWi, dWd, db), world)
+
     def step():
         fwd()
         tw.twell_ffn_bwd(X, Wi, Wd, packed, dY, lam, dX, dWi, dWd, db, wsb, stream)
+        exchange()
 
     # correctness of the routing on this batch (status word, fallback count)
     step()
@@ -251,6 +366,13 @@ def bench_ours(args, rank, world, local):
             tw.twell_profile_enable(False)
         return [a.elapsed_time(bb) for a, bb in ev]
 
+    def med(v):
+        return statistics.median(v)
+
+    # ---- the timed region: K steps, L2 scrubbed between steps, CUDA events on
+    # the launching stream.  The K-step loop is repeated until the region spans
+    # at least --min-window seconds, so the clock record covers the timed work;
+    # the reported time is the median over repeats of each repeat's median step.
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -258,40 +380,66 @@ def bench_ours(args, rank, world, local):
     clocks.start()
     launches0 = tw.twell_launch_count()
     t_wall = time.perf_counter()
-    step_ms = timed(step, args.steps)
+    rep_ms, reps = [], 0
+    while True:
+        rep_ms.append(med(timed(step, args.steps)))
+        reps += 1
+        if time.perf_counter() - t_wall >= args.min_window or reps >= 1000:
+            break
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
-    launches = tw.twell_launch_count() - launches0
+    launches = (tw.twell_launch_count() - launches0) // reps
     clk = clocks.stop()
+
     # per-kernel breakdown from a separate pass with an event pair around every
-    # launch (kept out of the timed steps above)
-    timed(step, min(args.steps, 20), profile=True)
+    # launch (kept out of the timed steps above); a kernel group may launch
+    # several kernels per step, so its time per step is the sum of its launches
+    prof_steps = min(args.steps, 20)
+    timed(step, prof_steps, profile=True)
     per_kernel = {}
     for name in tw.KERNELS:
         n, ms = tw.twell_profile_read(name)
         if n:
-            per_kernel[name] = {"launches": n, "avg_us": 1000.0 * ms / n, "share": 0.0}
-    tot = sum(v["avg_us"] * v["launches"] for v in per_kernel.values()) or 1.0
+            per_kernel[name] = {"launches_per_step": round(n / prof_steps, 2), "avg_us": 1000.0 * ms / n,
+                                "us_per_step": 1000.0 * ms / prof_steps, "share": 0.0}
+    tot = sum(v["us_per_step"] for v in per_kernel.values()) or 1.0
     for v in per_kernel.values():
-        v["share"] = round(v["avg_us"] * v["launches"] / tot, 4)
+        v["share"] = round(v["us_per_step"] / tot, 4)
         v["avg_us"] = round(v["avg_us"], 2)
+        v["us_per_step"] = round(v["us_per_step"], 2)
 
     # forward alone (the layer's inference path) and the dense comparator
-    fwd_ms = timed(fwd, args.steps)
+    fwd_ms = timed(fwd, max(args.steps, 50))
+    tw.twell_profile_reset()
+    tw.twell_profile_enable(True)
+    timed(fwd, prof_steps)
+    tw.twell_profile_enable(False)
+    fwd_kernels = {}
+    for name in tw.KERNELS:
+        n, ms = tw.twell_profile_read(name)
+        if n:
+            fwd_kernels[name] = {"launches_per_call": round(n / prof_steps, 2),
+                                 "us_per_call": round(1000.0 * ms / prof_steps, 2)}
     # the same calls back to back without the L2 scrub (warm L2: the weights stay resident)
     warm_step_ms = timed(step, min(args.steps, 50), warm=True)
     warm_fwd_ms = timed(fwd, min(args.steps, 50), warm=True)
     # the same fwd + bwd calls captured once in a CUDA graph and replayed: the
     # same kernels on the same buffers, without the host launch path between them
-    graph = torch.cuda.CUDAGraph()
-    torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        cap = torch.cuda.current_stream(dev)
-        tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, wsf, cap)
-        tw.twell_ffn_bwd(X, Wi, Wd, packed, dY, lam, dX, dWi, dWd, db, wsb, cap)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    graph_step_ms = timed(graph.replay, args.steps)
+    graph_step_ms = None
+    if world == 1:
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream(dev)
+            tw.twell_ffn_fwd(X, Wi, b, Wd, packed, Y, wsf, cap)
+            tw.twell_ffn_bwd(X, Wi, Wd, packed, dY, lam, dX, dWi, dWd, db, wsb, cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        graph_step_ms = timed(graph.replay, args.steps)
+        del graph
     Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
 
     def dense():
@@ -299,40 +447,63 @@ def bench_ours(args, rank, world, local):
 
     dense()
     dense_ms = timed(dense, max(3, args.steps // 2))
-    del Hbuf
 
-    # energy per token: board power (nvidia-smi, this GPU) sampled over a
-    # back-to-back loop of at least ~0.6 s of each call (warm L2, no flush
-    # writes in the loop, so the flush's own energy is not counted)
-    def energy(fn, ms_each):
-        iters = max(50, int(600.0 / max(ms_each, 1e-3)))
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        smp = ClockSampler(local)
-        smp.start()
-        time.sleep(0.1)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(iters):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        smp.stop()
-        loop_ms = e0.elapsed_time(e1)
-        pw = smp.power[2:-1] if len(smp.power) > 4 else smp.power
-        if not pw:
-            return None
-        watts = statistics.median(pw)
-        return {"j_per_token": watts * loop_ms * 1e-3 / (iters * N), "power_w": round(watts, 1),
-                "ms_per_call": round(loop_ms / iters, 4), "samples": len(pw)}
+    # ---- the standalone format conversions on the dense H of this layer
+    # (67 MB at the 1B shape): TwELL -> dense, then dense -> TwELL
+    packed2 = tw.alloc_packed(N, f, T, C, fb, dev)
+    tw.twell_unpack(packed, Hbuf, stream)
+    tw.twell_pack(Hbuf, packed2, stream)
+    torch.cuda.synchronize()
+    conv = {}
+    for name, fn in (("unpack", lambda: tw.twell_unpack(packed, Hbuf, stream)),
+                     ("pack", lambda: tw.twell_pack(Hbuf, packed2, stream))):
+        ms_list = timed(fn, max(args.steps, 20))
+        tw.twell_profile_reset()
+        tw.twell_profile_enable(True)
+        timed(fn, prof_steps)
+        tw.twell_profile_enable(False)
+        n_l, k_ms = tw.twell_profile_read(name)
+        conv[name] = {"call_ms": round(med(ms_list), 4), "kernel_us_per_call": round(1000.0 * k_ms / prof_steps, 2),
+                      "launches_per_call": round(n_l / prof_steps, 2)}
+    same = all(torch.equal(getattr(packed, k), getattr(packed2, k)) for k in ("values", "idx", "counts"))
+    del packed2, Hbuf
 
-    en_step = en_fwd = en_dense = None
+    # ---- energy per token: the GPU's cumulative energy counter (NVML, mJ)
+    # differenced over a back-to-back loop of >= 2 s of each call, after a
+    # warm-up loop of ~0.5 s so the power has settled (warm L2, no scrub
+    # writes, so the scrub's own energy is not counted)
+    energy_out = None
     if not args.no_energy:
-        en_step = energy(step, statistics.median(step_ms))
-        en_fwd = energy(fwd, statistics.median(fwd_ms))
+        meter = EnergyCounter(local)
+
+        def energy(fn, ms_each, tokens):
+            if not meter.ok:
+                return None
+            warm_iters = max(20, int(500.0 / max(ms_each, 1e-3)))
+            iters = max(50, int(2000.0 / max(ms_each, 1e-3)))
+            for _ in range(warm_iters):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            j0 = meter.read_mj()
+            e0.record(stream)
+            for _ in range(iters):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            j1 = meter.read_mj()
+            loop_ms = e0.elapsed_time(e1)
+            joules = (j1 - j0) * 1e-3
+            return {"j_per_token": joules / (iters * tokens), "avg_power_w": round(joules / (loop_ms * 1e-3), 1),
+                    "ms_per_call": round(loop_ms / iters, 4), "loop_s": round(loop_ms * 1e-3, 2)}
+
         Hbuf = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
-        en_dense = energy(dense, statistics.median(dense_ms))
+        energy_out = {"fwd_bwd_step": [energy(step, med(rep_ms), N) for _ in range(2)],
+                      "fwd": [energy(fwd, med(fwd_ms), N) for _ in range(2)],
+                      "dense_fwd": [energy(dense, med(dense_ms), N) for _ in range(2)],
+                      "how": "NVML total-energy counter of this GPU differenced over a >= 2 s back-to-back loop "
+                             "after a ~0.5 s warm-up loop (warm L2), / tokens; each measured twice; the GPU "
+                             "sits in a shared machine" if meter.ok else "NVML energy counter unavailable"}
         del Hbuf
 
     # end to end through the C ABI with host buffers (pinned): every step
@@ -376,6 +547,7 @@ def bench_ours(args, rank, world, local):
             stream.wait_event(ev_up[i % SETS])
             tw.twell_ffn_fwd(bs["X"], Wi, b, Wd, packed, bs["Y"], wsf, stream)
             tw.twell_ffn_bwd(bs["X"], Wi, Wd, packed, bs["dY"], lam, bs["dX"], dWi, dWd, db, wsb, stream)
+            exchange()
             ev_done[i % SETS].record(stream)
             used[i % SETS] = True
             with torch.cuda.stream(down_s):
@@ -390,56 +562,74 @@ def bench_ours(args, rank, world, local):
 
     e2e_loop(max(3, args.warmup))
     e2e_m_loop = e2e_loop(args.steps)
-    e2e_ms = [e2e_m_loop]
     h2d = hX.numel() * 2 + hdY.numel() * 2
     d2h = hY.numel() * 2 + hdX.numel() * 2
 
-    def med(v):
-        return statistics.median(v)
+    ms, e2e_m = max_over_ranks([med(rep_ms), e2e_m_loop], world, dev)
 
-    ms, e2e_m = max_over_ranks([med(step_ms), med(e2e_ms)], world, dev)
-
+    # ---- rooflines: every kernel group against its own bound; the dominant
+    # one (the largest share of the step's kernel time) is the headline's
     peaks, peak_src = load_peaks()
-    flops_up = 2.0 * N * d * f
-    up = per_kernel.get("up_pack")
-    roof = None
-    if up:
-        achieved = flops_up / (up["avg_us"] * 1e-6) / 1e12
-        traffic, note = ncu_traffic("up_pack", "1b")
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)",
-                "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), 4),
-                "kernel": "up_pack (tcgen05 GEMM + bias/ReLU/TwELL-pack epilogue)",
-                "algorithmic": "2*N*d_model*d_ff flops per launch"}
-        if note:
-            roof["traffic_note"] = note
+    work = kernel_work(N, d, f, T, C, nnz_tw, n_fb)
+    roofs = {}
+    for name, v in per_kernel.items():
+        if name in work:
+            roofs[name] = roofline_entry(work[name], v["us_per_step"], peaks, peak_src)
+            roofs[name]["share_of_step"] = v["share"]
+    for name in ("pack", "unpack"):
+        roofs[name] = roofline_entry(work[name], conv[name]["kernel_us_per_call"], peaks, peak_src)
+    dominant = max((k for k in roofs if k in per_kernel), key=lambda k: per_kernel[k]["share"], default=None)
+    roof = dict(roofs[dominant]) if dominant else None
+    if roof is not None:
+        roof["name"] = dominant
+        if dominant == "up_pack":
+            traffic, note = ncu_traffic("up_pack", "1b")
+            roof["traffic"] = traffic
+            if note:
+                roof["traffic_note"] = note
+        else:
+            roof["traffic"] = None
     fwd_m = med(fwd_ms)
     packed_bytes = (packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel() + packed.row_fb.numel() * 4
                     + packed.fb_rows.numel() * 4 + packed.fb_dense.numel() * 2)
-    roof_fwd_us = max(flops_up / (peaks["bf16_tflops"] * 1e12),
+    roof_fwd_us = max(2.0 * N * d * f / (peaks["bf16_tflops"] * 1e12),
                       (N * d * 2 * 2 + f * d * 2 * 2 + N * (f // T) * (3 * C + 1)) / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    sm_mhz = clk.get("sm_mhz")
+    clk["time_x_median_mhz"] = round(ms * sm_mhz, 1) if sm_mhz else None
     result = {
         "metric": METRIC, "value": round(job_throughput(world, N, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
         "config": {"workload": WORKLOAD, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
                    "fb_cap": fb, "l1_lambda": lam, "l2": "flushed between steps (2x L2 write)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": (f"data parallel x{world}: each rank its own batch, weight gradients "
+                                   "all-reduced (NCCL sum) inside the step") if world > 1 else "single GPU"},
+        "timed_repeats": {"repeats": reps, "steps_each": args.steps,
+                          "rep_ms_min": round(min(rep_ms), 4), "rep_ms_max": round(max(rep_ms), 4),
+                          "note": "the K-step timed loop repeated until the timed window spans >= "
+                                  f"{args.min_window} s; ms_per_step is the median over repeats"},
         "roofline": roof,
+        "roofline_kernels": roofs,
         "fwd": {"tokens_per_s": round(world * N / (fwd_m * 1e-3), 1), "ms": round(fwd_m, 4),
-                "roofline_us": round(roof_fwd_us, 2), "roofline_frac": round(roof_fwd_us / (fwd_m * 1e3), 4)},
-        "graph": {"ms_per_step": round(med(graph_step_ms), 4),
-                  "tokens_per_s": round(job_throughput(world, N, med(graph_step_ms)), 1),
-                  "note": "the same fwd + bwd calls captured once in a CUDA graph and replayed, L2 flushed "
-                          "between replays"},
+                "roofline_us": round(roof_fwd_us, 2), "roofline_frac": round(roof_fwd_us / (fwd_m * 1e3), 4),
+                "kernels": fwd_kernels,
+                "roofline_note": "max(up-projection FLOPs at the measured bf16 burst peak, X + W_in^T + W_down + "
+                                 "packed H + Y bytes at the measured HBM peak)"},
+        "graph": ({"ms_per_step": round(med(graph_step_ms), 4),
+                   "tokens_per_s": round(job_throughput(world, N, med(graph_step_ms)), 1),
+                   "note": "the same fwd + bwd calls captured once in a CUDA graph and replayed, L2 flushed "
+                           "between replays"} if graph_step_ms else None),
         "warm_l2": {"ms_per_step": round(med(warm_step_ms), 4), "fwd_ms": round(med(warm_fwd_ms), 4),
                     "tokens_per_s": round(job_throughput(world, N, med(warm_step_ms)), 1),
                     "note": "no L2 scrub between calls; the headline value scrubs L2 (cold)"},
         "dense_ffn_fwd": {"tokens_per_s": round(world * N / (med(dense_ms) * 1e-3), 1), "ms": round(med(dense_ms), 4),
                           "note": "same tcgen05 GEMM, no sparsity: reported baseline"},
+        "format_conversion": {**conv, "round_trip_identical": bool(same),
+                              "note": "twell_unpack of this layer's packed H into dense bf16 [N, d_ff], then "
+                                      "twell_pack of that dense H; L2 scrubbed between calls"},
         "kernels": per_kernel,
         "layer": {"n_fb": n_fb, "density": round(density, 5), "sparsity": round(1 - density, 5),
+                  "twell_entries": nnz_tw,
                   "packed_h_bytes": int(packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel()
                                         + fb * f * 2),
                   "dense_h_bytes": N * f * 2},
@@ -451,18 +641,7 @@ def bench_ours(args, rank, world, local):
         "gpu_launches": int(launches),
         "clocks": clk,
         "timed_wall_s": round(wall, 3),
-        "energy": {"fwd_bwd_step": en_step, "fwd": en_fwd, "dense_fwd": en_dense,
-                   "how": "median nvidia-smi power.draw of this GPU over a back-to-back loop (>= 0.6 s, warm L2) "
-                          "x loop time / tokens; the GPU sits in a shared machine"},
-        "memory": {
-            "saved_for_backward_bytes": {"twell": int(packed_bytes), "dense_bf16_h": N * f * 2},
-            "twell_step_bytes": int(packed_bytes + wsf.numel()),
-            "dense_step_lower_bound_bytes": N * f * 2 * 2,
-            "note": "caller-allocated device buffers of one fwd+bwd beyond inputs, weights, outputs and "
-                    "gradients: TwELL H (values, idx, counts, row maps, fallback rows) + the one workspace "
-                    "both calls share, "
-                    "against a dense step that keeps bf16 H and materialises a bf16 dZ",
-        },
+        "energy": energy_out,
     }
     return result
 
@@ -695,10 +874,13 @@ def bench_reference(args, rank, world):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     value = round(rows / s, 3)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * s * cfg.n_rows / rows, 1),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * s, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded, see synth/)",
             "config": {"workload": WORKLOAD, "sample_rows": rows},
+            "step": f"one step = fwd+bwd of the first {rows} tokens of the layer (ms_per_step is its measured "
+                    "median time)",
+            "extrapolated_ms_per_full_batch": round(1000 * s * cfg.n_rows / rows, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step: fwd+bwd of the first {rows} tokens as one batch"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -718,12 +900,18 @@ def main():
                     help="with --next: comma-separated workload names to run (default: all)")
     ap.add_argument("--next", action="store_true",
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
+    ap.add_argument("--min-window", type=float, default=1.0,
+                    help="repeat the K-step timed loop until the timed window spans this many seconds")
     ap.add_argument("--timeline", action="store_true",
                     help="print the launch timeline of one fwd + bwd step (L2 scrubbed before it) instead of "
                          "the bench line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_info()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not os.environ.get("TWELL_BENCH_CHILD"):
+        sys.exit(relaunch_with_ranks(args.gpus))
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: run one rank per GPU")
     if args.impl == "reference":
         res = bench_reference(args, rank, world)
         if res is not None:

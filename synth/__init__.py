@@ -26,6 +26,9 @@ Recipe (one config = one seed, numpy PCG64):
   * gated configs add W_u^T ~ N(0, 1/sqrt(d)); the bias places the gate's quantile.
   * decode configs take the bias from a separate calibration batch (seed + 500)
     of calib_rows tokens, since a quantile over 16 tokens says little.
+  * another batch for the same layer (batch_seed, e.g. a data-parallel rank's):
+    X0 drawn from batch_seed, row activities from batch_seed + 1, row scales
+    against the layer's bias.
 """
 from __future__ import annotations
 
@@ -138,10 +141,25 @@ def _row_scales(u: np.ndarray, b: np.ndarray, active: np.ndarray) -> np.ndarray:
     return scales
 
 
-def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None) -> dict:
-    """Draw one layer's inputs: bf16 bit patterns (uint16) plus calibration facts."""
+def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None, batch_seed: Optional[int] = None) -> dict:
+    """Draw one layer's inputs: bf16 bit patterns (uint16) plus calibration facts.
+
+    With batch_seed, the layer (weights and bias, calibrated on the config's own
+    batch) is the config's, and the returned batch X is drawn afresh from
+    batch_seed by the same recipe: another batch for the same layer, as the
+    ranks of a data-parallel job each hold one."""
     n = cfg.n_rows if rows is None else rows
     d, f = cfg.d_model, cfg.d_ff
+    if batch_seed is not None:
+        layer = make_ffn_inputs(cfg, rows=rows)
+        x0 = f32_to_bf16_bits(np.random.default_rng(batch_seed).standard_normal((n, d), dtype=np.float32))
+        # the batch's activity recipe against the shared layer's bias
+        x = _batch_for_layer(cfg, x0, layer["W_inT"], layer["b"], np.random.default_rng(batch_seed + 1))
+        out = dict(layer)
+        out.update(X=x["X"], X0=x0, target_activity=x["target"], forced_rows=x["forced"])
+        if "dY" in layer:
+            out["dY"] = make_grad_output(n, d, batch_seed + 1000)
+        return out
     rng = np.random.default_rng(cfg.seed)
     x0 = f32_to_bf16_bits(rng.standard_normal((n, d), dtype=np.float32))
     w_in_t = f32_to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32) / np.float32(math.sqrt(d)))
@@ -173,13 +191,36 @@ def make_ffn_inputs(cfg: FFNConfig, rows: Optional[int] = None) -> dict:
         x = f32_to_bf16_bits((bf16_bits_to_f32(x0) * s[:, None]).astype(np.float32))
     else:
         x = x0
-    out = {"X": x, "W_inT": w_in_t, "b": b, "W_down": w_down, "target_activity": target,
+    out = {"X": x, "X0": x0, "W_inT": w_in_t, "b": b, "W_down": w_down, "target_activity": target,
            "forced_rows": forced}
     if w_u_t is not None:
         out["W_uT"] = w_u_t
     if cfg.l1_lambda or cfg.name == "train":
         out["dY"] = make_grad_output(n, d, cfg.seed + 1000)
     return out
+
+
+def _batch_for_layer(cfg: FFNConfig, x0: np.ndarray, w_in_t: np.ndarray, b: np.ndarray, rng) -> dict:
+    """A batch for an existing layer: rows of x0 scaled so that row n fires
+    round(p_n * f) units of the layer (lognormal p_n and forced rows as in
+    make_ffn_inputs), or x0 itself for a uniform-activity config."""
+    n, f = x0.shape[0], w_in_t.shape[0]
+    target = np.full(n, 1.0 - cfg.sparsity)
+    forced = np.zeros(0, dtype=np.int64)
+    if cfg.row_spread != "lognormal":
+        return {"X": x0, "target": target, "forced": forced}
+    sigma = 0.5
+    mu = math.log(1.0 - cfg.sparsity) - sigma * sigma / 2
+    target = np.clip(np.exp(rng.normal(mu, sigma, size=n)), 0.001, 0.1)
+    n_forced = int(round(cfg.forced_frac_rows * n))
+    if n_forced:
+        forced = np.sort(rng.choice(n, size=n_forced, replace=False))
+        target[forced] = cfg.forced_activity
+    active = np.maximum(1, np.rint(target * f)).astype(np.int64)
+    u = bf16_bits_to_f32(x0) @ bf16_bits_to_f32(w_in_t).T
+    s = _row_scales(u, b, active)
+    x = f32_to_bf16_bits((bf16_bits_to_f32(x0) * s[:, None]).astype(np.float32))
+    return {"X": x, "target": target, "forced": forced}
 
 
 def make_grad_output(n: int, d: int, seed: int) -> np.ndarray:
