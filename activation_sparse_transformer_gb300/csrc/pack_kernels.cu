@@ -2,14 +2,17 @@
 // TwELL-to-dense paths", repo-explainer "TwELL: The Packing Format That Fits
 // the Machine"; format per the bayesiansapien note's Figure 1 description).
 //
-// pack_cells_kernel: a warp reads 256 consecutive bf16 of one row with
-//   16-byte loads (8 columns per lane); the T/8 lanes of each tile compact
-//   their non-zeros with a segmented popcount prefix over per-lane 8-bit
-//   masks, write them to the cell in ascending column order, pad the rest,
-//   store the count and flag the row (row_fb = 1) when the tile overflows C.
+// pack_cells_kernel: a warp reads 4 x 256 consecutive bf16 of one row with
+//   16-byte loads (8 columns per lane, all loads issued first); per 256
+//   columns the T/8 lanes of each tile compact their non-zeros with a
+//   segmented popcount prefix into a shared-memory copy of the cells
+//   (ascending column order), which one lane per cell writes out with the
+//   padding, in whole vectors; it stores the count and flags the row
+//   (row_fb = 1) when a tile overflows C.
 // fb_copy_kernel: dense rows of fallback rows -> fb_dense, their cells cleared.
-// unpack_kernel: each lane rebuilds 8 output columns from its tile's cell (or
-//   from fb_dense) and writes them with one 16-byte store.
+// unpack_run_kernel: a warp zero-fills a run of 32 cells of a row with
+//   coalesced 16-byte stores, then each lane writes its cell's entries (or a
+//   fallback row / dense tile is copied whole).
 // check_cells_kernel / check_order_kernel: the format rules of a layout
 //   (cell contents, then the numbering of fallback rows or dense tiles),
 //   reported as a mask of broken rules.
@@ -93,19 +96,122 @@ __device__ __forceinline__ void pack_lane8(const Layout& L, int row, int col, bo
   }
 }
 
+// Dense -> cells.  A warp takes kPackSeg consecutive 256-column segments of
+// one row and requests all of them (16 bytes per lane and segment) before it
+// uses any, so each warp has 2 KB of H in flight.  Per segment, each lane
+// finds the non-zeros of its 8 columns with branch-free bit arithmetic, the
+// T/8 lanes of each tile take a segmented popcount prefix, and the lanes that
+// hold non-zeros write them (in ascending column order) into the warp's
+// staging copy of its cells in shared memory, one area per segment, so a
+// single warp barrier follows all segments.  One lane per cell then writes
+// the cell out: its first count slots from the staging copy and padding in
+// the rest, as 16- and 8-byte vectors when C is a multiple of 8.
+constexpr int kPackSeg = 4;
+constexpr int kPackCells = kPackSeg * (256 / 32);   // the most cells a warp's chunk holds (T = 32)
+constexpr int kPackStage = kPackCells * 32;         // x the largest C
+
+// Non-zero pattern of the 8 bf16 values of one lane: bit 15 / bit 31 of word q
+// is set when value 2q / 2q + 1 is not +-0.
+__device__ __forceinline__ void nonzero_halves(const uint4& v, uint32_t (&t)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) t[q] = ((w[q] & 0x7FFF7FFFu) + 0x7FFF7FFFu) & 0x80008000u;
+}
+
+template <int T>
 __global__ void __launch_bounds__(kWarps * 32)
     pack_cells_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
+  __shared__ __align__(16) uint16_t st_vals[kWarps][kPackStage];
+  __shared__ __align__(16) uint8_t st_idx[kWarps][kPackStage];
+  __shared__ int st_cnt[kWarps][kPackCells];  // entries found per cell (may exceed C)
+  constexpr int G = T / 8;                    // lanes per tile: 4, 8, 16 or 32
+  constexpr int cps = 256 / T;                // cells per segment
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int segs = (L.f + 255) / 256;
+  const int chunk_cols = kPackSeg * 256;
+  const int chunks = (L.f + chunk_cols - 1) / chunk_cols;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= static_cast<int64_t>(L.N) * segs) return;  // whole warp leaves together
-  const int row = static_cast<int>(gw / segs);
-  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
-  const bool in = col < L.f;
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (in) v = __ldg(reinterpret_cast<const uint4*>(H + static_cast<int64_t>(row) * ldh + col));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  pack_lane8(L, row, col, in, w);
+  if (gw >= static_cast<int64_t>(L.N) * chunks) return;  // whole warp leaves together
+  const int row = static_cast<int>(gw / chunks);
+  const int c0 = static_cast<int>(gw % chunks) * chunk_cols;
+  const uint16_t* hrow = H + static_cast<int64_t>(row) * ldh;
+  uint4 v[kPackSeg];
+#pragma unroll
+  for (int sg = 0; sg < kPackSeg; ++sg) {
+    const int col = c0 + sg * 256 + lane * 8;
+    v[sg] = col < L.f ? __ldg(reinterpret_cast<const uint4*>(hrow + col)) : make_uint4(0, 0, 0, 0);
+  }
+  const int C = L.C;
+  const int gl = lane % G;
+  uint16_t* sv = st_vals[warp];
+  uint8_t* si = st_idx[warp];
+  int* sc = st_cnt[warp];
+  const int ncell = min(chunk_cols, L.f - c0) / T;  // cells of this chunk (f % T == 0)
+#pragma unroll
+  for (int sg = 0; sg < kPackSeg; ++sg) {
+    uint32_t t[4];
+    nonzero_halves(v[sg], t);
+    const int local = __popc(t[0]) + __popc(t[1]) + __popc(t[2]) + __popc(t[3]);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (gl >= o) incl += x;
+    }
+    const int cell = sg * cps + lane / G;  // the lane's cell within the chunk
+    if (gl == G - 1 && cell < ncell) sc[cell] = incl;
+    // this lane's non-zeros in ascending column (half h of word q is column
+    // 2q + h), each to the next slot while slots remain: predicated, no branch
+    const uint32_t w[4] = {v[sg].x, v[sg].y, v[sg].z, v[sg].w};
+    uint16_t* cv = sv + cell * C;
+    uint8_t* ci = si + cell * C;
+    int slot = incl - local;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool nz = (t[k >> 1] >> (15 + 16 * (k & 1))) & 1u;
+      if (nz && slot < C) {
+        cv[slot] = static_cast<uint16_t>((w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
+        ci[slot] = static_cast<uint8_t>(gl * 8 + k);
+      }
+      slot += nz ? 1 : 0;
+    }
+  }
+  __syncwarp();
+  // one lane per cell writes it out; rows with an over-full tile are flagged
+  const int64_t gcell0 = static_cast<int64_t>(row) * L.nt + c0 / T;
+  bool over = false;
+  for (int c = lane; c < ncell; c += 32) {
+    const int found = sc[c];
+    over |= found > C;
+    const bool dense = L.hybrid == TWELL_HYBRID_TILES && found > C;
+    const int cnt = dense ? 0 : min(found, C);
+    const int64_t g = gcell0 + c;
+    if ((C & 7) == 0) {
+      for (int q = 0; q < C / 8; ++q) {
+        // keep the first cnt - 8q slots of this 8-slot chunk, pad the rest
+        const int keep = min(max(cnt - 8 * q, 0), 8);
+        const uint4 sv4 = reinterpret_cast<const uint4*>(sv + c * C)[q];
+        const uint2 si2 = reinterpret_cast<const uint2*>(si + c * C)[q];
+        const uint32_t vw[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+        uint32_t vo[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int k0 = 2 * h;
+          vo[h] = (keep > k0 + 1) ? vw[h] : (keep > k0 ? (vw[h] & 0xFFFFu) : 0u);
+        }
+        const uint64_t imask = keep >= 8 ? ~0ull : ((1ull << (8 * keep)) - 1ull);
+        const uint64_t iv = (static_cast<uint64_t>(si2.y) << 32 | si2.x) & imask;
+        reinterpret_cast<uint4*>(L.values + g * C)[q] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+        reinterpret_cast<uint2*>(L.idx + g * C)[q] = make_uint2(static_cast<uint32_t>(iv), static_cast<uint32_t>(iv >> 32));
+      }
+    } else {
+      for (int q = 0; q < C; ++q) {
+        L.values[g * C + q] = q < cnt ? sv[c * C + q] : static_cast<uint16_t>(0);
+        L.idx[g * C + q] = q < cnt ? si[c * C + q] : static_cast<uint8_t>(0);
+      }
+    }
+    L.counts[g] = dense ? static_cast<uint8_t>(TWELL_DENSE_TILE) : static_cast<uint8_t>(cnt);
+  }
+  if (__any_sync(0xffffffffu, over) && lane == 0) L.row_fb[row] = 1;
 }
 
 // Routing of a small batch (at most 32 rows) by one CTA: the result of
@@ -210,41 +316,56 @@ __global__ void fb_copy_kernel(Layout L, const uint16_t* __restrict__ H, int64_t
   }
 }
 
+// Cells -> dense, a warp per run of up to 32 consecutive cells of one row
+// (lane = cell).  The warp first writes the run's columns of H as zeros with
+// coalesced 16-byte stores, then (after a warp barrier that orders those
+// stores before the next ones) each lane writes its cell's few stored
+// entries.  A fallback row's run is copied from fb_dense instead, a dense tile
+// of the tile-granular variant from its pool slot.  Most of H is zero at the
+// layer's sparsity, so the kernel is a stream of 16-byte stores.
 __global__ void __launch_bounds__(kWarps * 32)
-    unpack_kernel(Layout L, uint16_t* __restrict__ H, int64_t ldh) {
+    unpack_run_kernel(Layout L, uint16_t* __restrict__ H, int64_t ldh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int segs = (L.f + 255) / 256;
+  const int runs = (L.nt + 31) / 32;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= static_cast<int64_t>(L.N) * segs) return;
-  const int row = static_cast<int>(gw / segs);
-  const int col = static_cast<int>(gw % segs) * 256 + lane * 8;
-  if (col >= L.f) return;
-  uint4 out;
+  if (gw >= static_cast<int64_t>(L.N) * runs) return;
+  const int row = static_cast<int>(gw / runs);
+  const int t0 = static_cast<int>(gw % runs) * 32;
+  const int nc = min(32, L.nt - t0);
+  const int T = L.T, C = L.C;
+  const int vecs = nc * T / 8;  // 16-byte vectors of the run
+  uint4* hrun = reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + static_cast<int64_t>(t0) * T);
   const int fb = L.row_fb[row];
   if (fb >= 0) {
-    out = *reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f + col);
-  } else if (L.hybrid == TWELL_HYBRID_TILES && L.counts[static_cast<int64_t>(row) * L.nt + col / L.T] ==
-                                                    TWELL_DENSE_TILE) {
-    const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
-    const int64_t slot = static_cast<int64_t>(L.values[cell * L.C]) | (static_cast<int64_t>(L.idx[cell * L.C]) << 16);
-    out = *reinterpret_cast<const uint4*>(L.fb_dense + slot * L.T + col % L.T);
-  } else {
-    const int64_t cell = static_cast<int64_t>(row) * L.nt + col / L.T;
-    const int lo = col % L.T;
-    const int cnt = L.counts[cell];
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    for (int s = 0; s < cnt; ++s) {
-      const int i = static_cast<int>(L.idx[cell * L.C + s]) - lo;
-      if (i >= 0 && i < 8) {
-        const uint32_t val = L.values[cell * L.C + s];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (i == k) w[k / 2] |= (k & 1) ? (val << 16) : val;
-      }
+    if (fb < L.fb_cap) {
+      const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f +
+                                                        static_cast<int64_t>(t0) * T);
+      for (int i = lane; i < vecs; i += 32) hrun[i] = src[i];
+    } else {
+      // a fallback row past the capacity is stored nowhere: zeros
+      for (int i = lane; i < vecs; i += 32) hrun[i] = make_uint4(0, 0, 0, 0);
     }
-    out = make_uint4(w[0], w[1], w[2], w[3]);
+    return;
   }
-  *reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + col) = out;
+  const int64_t cell = static_cast<int64_t>(row) * L.nt + t0 + lane;
+  const int cnt = lane < nc ? L.counts[cell] : 0;
+  for (int i = lane; i < vecs; i += 32) hrun[i] = make_uint4(0, 0, 0, 0);
+  __syncwarp();
+  if (lane >= nc || cnt == 0) return;
+  uint16_t* hcell = H + static_cast<int64_t>(row) * ldh + static_cast<int64_t>(t0 + lane) * T;
+  if (L.hybrid == TWELL_HYBRID_TILES && cnt == TWELL_DENSE_TILE) {
+    const int64_t slot = static_cast<int64_t>(L.values[cell * C]) | (static_cast<int64_t>(L.idx[cell * C]) << 16);
+    if (slot < static_cast<int64_t>(L.fb_cap) * L.nt) {
+      const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + slot * T);
+      for (int i = 0; i < T / 8; ++i) reinterpret_cast<uint4*>(hcell)[i] = src[i];
+    }
+    return;
+  }
+  // (bounded by C and T so that a malformed layout cannot write past the cell)
+  for (int s2 = 0; s2 < min(cnt, C); ++s2) {
+    const int j = L.idx[cell * C + s2];
+    if (j < T) hcell[j] = L.values[cell * C + s2];
+  }
 }
 
 // ---------------------------------------------------------------- format check
@@ -388,11 +509,18 @@ int64_t warps_needed(const twell_t& L) {
 }  // namespace
 
 int launch_pack_cells(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_t s) {
-  const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
+  const int64_t warps = static_cast<int64_t>(L.n_rows) * ((L.d_ff + kPackSeg * 256 - 1) / (kPackSeg * 256));
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks <= 0) return TWELL_OK;
   if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
+  const unsigned g = static_cast<unsigned>(blocks);
   LaunchScope ls(TWELL_KERNEL_PACK, s);
-  pack_cells_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  switch (L.tile) {
+    case 32: pack_cells_kernel<32><<<g, kWarps * 32, 0, s>>>(flat(L), H, ldh); break;
+    case 64: pack_cells_kernel<64><<<g, kWarps * 32, 0, s>>>(flat(L), H, ldh); break;
+    case 128: pack_cells_kernel<128><<<g, kWarps * 32, 0, s>>>(flat(L), H, ldh); break;
+    default: pack_cells_kernel<256><<<g, kWarps * 32, 0, s>>>(flat(L), H, ldh); break;
+  }
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -416,11 +544,13 @@ int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_
 }
 
 int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s) {
-  const int64_t blocks = (warps_needed(L) + kWarps - 1) / kWarps;
-  if (blocks <= 0) return TWELL_OK;
+  if (L.n_rows <= 0) return TWELL_OK;
+  const int nt = L.d_ff / L.tile;
+  const int64_t warps = static_cast<int64_t>(L.n_rows) * ((nt + 31) / 32);
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
   LaunchScope ls(TWELL_KERNEL_UNPACK, s);
-  unpack_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  unpack_run_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -59,6 +59,8 @@ CASES = [
     (96, 512, 32, 4, 0.03, 4),
     (64, 1024, 128, 32, 0.05, 5),      # largest capacity
     (40, 768, 64, 1, 0.01, 6),         # capacity 1
+    (72, 768, 64, 24, 0.25, 7),        # C = 24: cells read as three 8-slot vectors
+    (50, 1280, 256, 8, 0.02, 8),       # d_ff = 5 x 256: a 1024-column chunk and a partial one
 ]
 
 
@@ -131,6 +133,14 @@ def test_pack_fallback_overflow_status(tw):
     assert int(p.n_fb[0].item()) == 16
     # the first fb_cap fallback rows are still stored in order
     _compare(p, ref, 6)
+    # unpacking the overflowed layout: rows past fb_cap are stored nowhere and
+    # come back as zeros, as the oracle's unpack gives them
+    out = torch.full((64, 512), 5.0, dtype=torch.bfloat16, device="cuda")
+    tw.twell_unpack(p, out)
+    torch.cuda.synchronize()
+    want = oracle.unpack(ref, 512)
+    assert not want[ref["row_fb"] >= 6].any()
+    assert np.array_equal(from_dev_bits(out), want)
 
 
 def test_pack_full_size_1b(tw):
