@@ -43,9 +43,9 @@ def _configure(lib):
     lib.oracle_hidden_gated.argtypes = [P, P, P, P, I, I, P, I, P, P]
     lib.oracle_pack.restype = I
     lib.oracle_pack.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P]
-    lib.oracle_unpack.argtypes = [P, P, P, P, P, I, I, I, I, P]
+    lib.oracle_unpack.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
     lib.oracle_down_dense.argtypes = [P, P, I, I, I, P]
-    lib.oracle_down_packed.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
+    lib.oracle_down_packed.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
     lib.oracle_round_bf16.argtypes = [P, ctypes.c_int64, P]
     lib.oracle_grad_hidden.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, P, P]
     lib.oracle_grad_input.argtypes = [P, P, I, I, I, P]
@@ -176,9 +176,10 @@ def unpack(packed: dict, f: int) -> np.ndarray:
         _load().oracle_unpack_tiles(_p(_c(v, np.uint16)), _p(_c(i, np.uint8)), _p(_c(c, np.uint8)),
                                     _p(_c(packed["pool"], np.uint16)), N, f, packed["T"], packed["C"], _p(H))
         return H
+    fbd = _c(packed["fb_dense"], np.uint16)
     _load().oracle_unpack(_p(_c(v, np.uint16)), _p(_c(i, np.uint8)), _p(_c(c, np.uint8)),
-                          _p(_c(packed["row_fb"], np.int32)), _p(_c(packed["fb_dense"], np.uint16)),
-                          N, f, packed["T"], packed["C"], _p(H))
+                          _p(_c(packed["row_fb"], np.int32)), _p(fbd),
+                          N, f, packed["T"], packed["C"], packed.get("fb_cap", fbd.shape[0]), _p(H))
     return H
 
 
@@ -204,7 +205,7 @@ def down_packed(packed: dict, W_down) -> np.ndarray:
     _load().oracle_down_packed(_p(_c(packed["values"], np.uint16)), _p(_c(packed["idx"], np.uint8)),
                                _p(_c(packed["counts"], np.uint8)), _p(_c(packed["row_fb"], np.int32)),
                                _p(_c(packed["fb_dense"], np.uint16)), _p(W_down), N, f, d,
-                               packed["T"], packed["C"], _p(Y))
+                               packed["T"], packed["C"], packed.get("fb_cap", packed["fb_dense"].shape[0]), _p(Y))
     return Y
 
 

@@ -165,12 +165,17 @@ EXPORT int32_t oracle_pack(const uint16_t* H, int32_t N, int32_t f, int32_t T, i
  * fallback rows from fb_dense. */
 EXPORT void oracle_unpack(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
                           const int32_t* row_fb, const uint16_t* fb_dense, int32_t N, int32_t f,
-                          int32_t T, int32_t C, uint16_t* H) {
+                          int32_t T, int32_t C, int32_t fb_cap, uint16_t* H) {
   const int32_t nt = f / T;
   for (int32_t n = 0; n < N; ++n) {
     uint16_t* h = H + (int64_t)n * f;
     if (row_fb[n] >= 0) {
-      memcpy(h, fb_dense + (int64_t)row_fb[n] * f, sizeof(uint16_t) * (size_t)f);
+      /* a fallback row past the capacity is stored nowhere (its cells are
+       * empty too): it comes back as zeros */
+      if (row_fb[n] < fb_cap)
+        memcpy(h, fb_dense + (int64_t)row_fb[n] * f, sizeof(uint16_t) * (size_t)f);
+      else
+        memset(h, 0, sizeof(uint16_t) * (size_t)f);
       continue;
     }
     memset(h, 0, sizeof(uint16_t) * (size_t)f);
@@ -311,7 +316,7 @@ EXPORT void oracle_down_dense(const uint16_t* H, const uint16_t* W_down, int32_t
 EXPORT void oracle_down_packed(const uint16_t* values, const uint8_t* idx, const uint8_t* counts,
                                const int32_t* row_fb, const uint16_t* fb_dense,
                                const uint16_t* W_down, int32_t N, int32_t f, int32_t d, int32_t T,
-                               int32_t C, float* Y) {
+                               int32_t C, int32_t fb_cap, float* Y) {
   const int32_t nt = f / T;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int32_t n = 0; n < N; ++n) {
@@ -319,9 +324,12 @@ EXPORT void oracle_down_packed(const uint16_t* values, const uint8_t* idx, const
     for (int32_t c = 0; c < d; ++c) {
       float acc = 0.0f;
       if (row_fb[n] >= 0) {
-        const uint16_t* h = fb_dense + (int64_t)row_fb[n] * f;
-        for (int32_t j = 0; j < f; ++j)
-          if (bf16_to_f32(h[j]) != 0.0f) acc += bf16_to_f32(h[j]) * bf16_to_f32(W_down[(int64_t)j * d + c]);
+        /* a fallback row past the capacity is stored nowhere: a zero row */
+        if (row_fb[n] < fb_cap) {
+          const uint16_t* h = fb_dense + (int64_t)row_fb[n] * f;
+          for (int32_t j = 0; j < f; ++j)
+            if (bf16_to_f32(h[j]) != 0.0f) acc += bf16_to_f32(h[j]) * bf16_to_f32(W_down[(int64_t)j * d + c]);
+        }
       } else {
         for (int32_t t = 0; t < nt; ++t) {
           int64_t cell = (int64_t)n * nt + t;

@@ -380,3 +380,21 @@ def test_gated_hidden_exact_on_integers():
     got = bf(H)
     assert np.array_equal(got, bf(to_bf(want.astype(np.float32))))
     assert np.all(H[zg <= 0] == 0)
+
+
+def test_overflowed_layout_unpacks_rows_past_capacity_as_zeros():
+    """Reading 15: a fallback row past fb_cap is stored nowhere and its cells
+    are emptied, so unpacking the layout gives a zero row for it, and the packed
+    product gives it a zero output row; the stored rows come back exactly."""
+    H = synth.make_dense_h(40, 256, seed=21, activity=0.01, dense_rows=np.arange(0, 40, 5))
+    p = oracle.pack(H, 64, 8, 3)
+    assert p["n_fb"] >= 6
+    over = np.nonzero(p["row_fb"] >= 3)[0]
+    assert len(over) == p["n_fb"] - 3 and (p["counts"][over] == 0).all()
+    want = H.copy()
+    want[over] = 0
+    assert np.array_equal(oracle.unpack(p, 256), want)
+    W = synth.f32_to_bf16_bits(np.random.default_rng(3).standard_normal((256, 64), dtype=np.float32))
+    Y = oracle.down_packed(p, W)
+    assert not Y[over].any()
+    assert np.array_equal(Y, oracle.down_dense(want, W))
