@@ -43,7 +43,7 @@ EXPORTED = [
     "twell_launch_count", "twell_profile_enable", "twell_profile_reset", "twell_profile_read",
     "twell_profile_timeline",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
-    "twell_selftest_wait_timeout", "twell_check_format",
+    "twell_selftest_wait_timeout", "twell_check_format", "twell_dense_ffn_bwd", "twell_dense_bwd_workspace_bytes",
 ]
 
 
@@ -98,6 +98,8 @@ def load_library() -> ctypes.CDLL:
         "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
         "twell_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "twell_check_format": (ctypes.c_int, [L, P, P]),
+        "twell_dense_ffn_bwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, P, ctypes.c_float, P, P, P, P, P, SZ, P]),
+        "twell_dense_bwd_workspace_bytes": (SZ, [I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -287,6 +289,27 @@ def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:
     _need(Hbuf, n * f * 2, "Hbuf")
     _check(load_library().twell_dense_ffn_fwd(_ptr(X), _ptr(W_inT), _ptr(b), _ptr(W_down), n, d, f, _ptr(Hbuf),
                                               _ptr(Y), _stream(stream)), "twell_dense_ffn_fwd")
+
+
+def dense_bwd_workspace_bytes(n_rows, d_model, d_ff) -> int:
+    return int(load_library().twell_dense_bwd_workspace_bytes(n_rows, d_model, d_ff))
+
+
+def twell_dense_ffn_bwd(X, W_inT, W_down, Hbuf, dY, l1_lambda: float, dX, dW_inT, dW_down, db, workspace,
+                        stream=None) -> None:
+    """Dense comparator's backward: the gradients of twell_ffn_bwd for the layer
+    run densely (Hbuf = the dense forward's H), with no sparsity used."""
+    n, d = X.shape
+    f = W_inT.shape[0]
+    for t, nbytes, name in ((X, n * d * 2, "X"), (W_inT, f * d * 2, "W_inT"), (W_down, f * d * 2, "W_down"),
+                            (Hbuf, n * f * 2, "Hbuf"), (dY, n * d * 2, "dY"), (dX, n * d * 2, "dX"),
+                            (dW_inT, f * d * 4, "dW_inT"), (dW_down, f * d * 4, "dW_down"), (db, f * 4, "db"),
+                            (workspace, dense_bwd_workspace_bytes(n, d, f), "workspace")):
+        _need(t, nbytes, name)
+    _check(load_library().twell_dense_ffn_bwd(_ptr(X), _ptr(W_inT), _ptr(W_down), _ptr(Hbuf), n, d, f, _ptr(dY),
+                                              float(l1_lambda), _ptr(dX), _ptr(dW_inT), _ptr(dW_down), _ptr(db),
+                                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              _stream(stream)), "twell_dense_ffn_bwd")
 
 
 def twell_check_format(packed: Packed, violations, stream=None) -> None:

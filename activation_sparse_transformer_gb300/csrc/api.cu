@@ -507,6 +507,54 @@ int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t
   return TWELL_OK;
 }
 
+size_t twell_dense_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff) {
+  (void)d_model;
+  if (n_rows < 0 || d_ff <= 0) return 0;
+  return align256(sizeof(uint16_t) * static_cast<size_t>(n_rows) * d_ff) +
+         align256(sizeof(float) * static_cast<size_t>(kColsumChunks) * d_ff);
+}
+
+int twell_dense_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const uint16_t* H,
+                        int32_t n_rows, int32_t d_model, int32_t d_ff, const uint16_t* dY, float l1_lambda,
+                        uint16_t* dX, float* dW_inT, float* dW_down, float* db, void* workspace,
+                        size_t workspace_bytes, twell_stream_t stream) {
+  if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
+  if (d_model % 128 != 0 || d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  for (const void* p : {static_cast<const void*>(X), static_cast<const void*>(W_inT),
+                        static_cast<const void*>(W_down), static_cast<const void*>(H), static_cast<const void*>(dY),
+                        static_cast<const void*>(dX), static_cast<const void*>(dW_inT),
+                        static_cast<const void*>(dW_down), static_cast<const void*>(db)})
+    TW_TRY(check_dense(p));
+  const size_t need = twell_dense_bwd_workspace_bytes(n_rows, d_model, d_ff);
+  if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
+  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (n_rows == 0) {
+    // no rows: the weight gradients are zero
+    TW_CUDA(cudaMemsetAsync(dW_inT, 0, sizeof(float) * static_cast<size_t>(d_ff) * d_model, s));
+    TW_CUDA(cudaMemsetAsync(dW_down, 0, sizeof(float) * static_cast<size_t>(d_ff) * d_model, s));
+    TW_CUDA(cudaMemsetAsync(db, 0, sizeof(float) * static_cast<size_t>(d_ff), s));
+    return TWELL_OK;
+  }
+  uint16_t* dZ = static_cast<uint16_t*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         align256(sizeof(uint16_t) * static_cast<size_t>(n_rows) * d_ff));
+  // dZ = (dY . W_down^T + lambda) where h > 0: a dense GEMM with a masking epilogue
+  MaskEpiParams mp{H, dZ, d_ff, l1_lambda};
+  TW_TRY(launch_gemm_mask(dY, W_down, n_rows, d_ff, d_model, mp, nullptr, TWELL_KERNEL_DENSE_GEMM, s));
+  // dX = dZ . W_in (W_in^T read as the N-major B operand)
+  DenseEpiParams xp{nullptr, dX, d_model, 0};
+  TW_TRY(launch_gemm_dense(dZ, W_inT, true, n_rows, nullptr, d_model, d_ff, xp, nullptr, TWELL_KERNEL_DENSE_GEMM,
+                           s));
+  // dW_in^T = dZ^T . X and dW_down = H^T . dY, K = the rows
+  TW_TRY(launch_gemm_store_mn(dZ, X, d_ff, d_model, n_rows, nullptr, 1, dW_inT, d_model, nullptr,
+                              TWELL_KERNEL_DENSE_GEMM, s));
+  TW_TRY(launch_gemm_store_mn(H, dY, d_ff, d_model, n_rows, nullptr, 1, dW_down, d_model, nullptr,
+                              TWELL_KERNEL_DENSE_GEMM, s));
+  return launch_colsum_bf16(dZ, n_rows, d_ff, part, db, TWELL_KERNEL_DENSE_GEMM, s);
+}
+
 int twell_read_status(const twell_t* layout, twell_stream_t stream) {
   if (!layout || !layout->status || !layout->n_fb) return TWELL_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

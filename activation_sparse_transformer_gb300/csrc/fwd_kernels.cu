@@ -262,6 +262,46 @@ __global__ void fb_reduce_kernel(Layout L, const float* __restrict__ part, int k
   }
 }
 
+// Column sums of a bf16 matrix, deterministic: block (column block of 256,
+// row chunk) sums its rows per column in fp32 (warp w takes rows w, w + 8, ...;
+// the 8 warps' sums are added in warp order), then one thread per column adds
+// the chunks' partial sums in chunk order.
+__global__ void __launch_bounds__(256)
+    colsum_part_kernel(const uint16_t* __restrict__ Z, int M, int N, int rows_per_chunk, float* __restrict__ part) {
+  __shared__ float red[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 256 + lane * 8;
+  const int r0 = blockIdx.y * rows_per_chunk, r1 = min(M, r0 + rows_per_chunk);
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c0 < N) {
+#pragma unroll 4
+    for (int r = r0 + warp; r < r1; r += 8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Z + static_cast<int64_t>(r) * N + c0));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] += (k & 1) ? bf16_hi(w[k / 2]) : bf16_lo(w[k / 2]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) red[warp][lane * 8 + k] = a[k];
+  __syncthreads();
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  if (c < N) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += red[w][threadIdx.x];
+    part[static_cast<int64_t>(blockIdx.y) * N + c] = sum;
+  }
+}
+
+__global__ void colsum_final_kernel(const float* __restrict__ part, int chunks, int N, float* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= N) return;
+  float sum = 0.f;
+  for (int k = 0; k < chunks; ++k) sum += part[static_cast<int64_t>(k) * N + c];
+  out[c] = sum;
+}
+
 }  // namespace
 
 int launch_tile_count(const twell_t& L, cudaStream_t s) {
@@ -313,6 +353,24 @@ int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_mode
   const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
   LaunchScope ls(kernel_id, s);
   fb_reduce_kernel<<<grid, 256, 0, s>>>(flat(L), part, nsplit, d_model, out);
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+}  // namespace twell
+
+namespace twell {
+
+int launch_colsum_bf16(const uint16_t* Z, int M, int N, float* part, float* out, int kernel_id, cudaStream_t s) {
+  if (N <= 0) return TWELL_OK;
+  if (N % 8 != 0) return TWELL_ERR_UNSUPPORTED;
+  const int rows_per_chunk = std::max(1, (M + kColsumChunks - 1) / kColsumChunks);
+  {
+    LaunchScope ls(kernel_id, s);
+    colsum_part_kernel<<<dim3((N + 255) / 256, kColsumChunks), 256, 0, s>>>(Z, M, N, rows_per_chunk, part);
+  }
+  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  LaunchScope ls(kernel_id, s);
+  colsum_final_kernel<<<(N + 255) / 256, 256, 0, s>>>(part, kColsumChunks, N, out);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

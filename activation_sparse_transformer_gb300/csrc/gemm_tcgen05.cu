@@ -403,6 +403,45 @@ struct DenseEpi {
   }
 };
 
+// Dense comparator's backward through the ReLU and the L1 term: dZ = acc +
+// lambda where the dense forward's h > 0, else 0, stored as bf16 rows.
+struct MaskEpi {
+  static constexpr bool kDualB = false;
+  using Params = MaskEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int, uint8_t*, int) {
+    const bool valid = row < M;
+#pragma unroll 1
+    for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * 32, r);
+      uint4 hq[4] = {};
+      if (valid) {
+        const uint4* hp = reinterpret_cast<const uint4*>(p.H + static_cast<int64_t>(row) * p.ld + col0 + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hq[q] = hp[q];
+      }
+      tmem_ld_wait();
+      if (!valid) continue;
+      uint32_t packed[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float z0 = bias_at(hq, i) > 0.0f ? __uint_as_float(r[i]) + p.lambda : 0.0f;
+        const float z1 = bias_at(hq, i + 1) > 0.0f ? __uint_as_float(r[i + 1]) + p.lambda : 0.0f;
+        packed[i / 2] = static_cast<uint32_t>(float_to_bf16_bits(z0)) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(z1)) << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row) * p.ld + col0 + c * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    }
+  }
+};
+
 // fp32 tile store.  Each warp turns its 32 rows x 32 columns around in shared
 // memory so that its stores write whole 128-byte row segments, four rows per
 // 16-byte-per-lane instruction.  The 16-byte chunks of a staged row are
@@ -873,6 +912,13 @@ int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t
   if (p.cap > GatedPackEpi::kMaxCap || N % 128 != 0 || 128 % p.tile != 0) return TWELL_ERR_UNSUPPORTED;
   return launch_gemm<256, GatedPackEpi, false, false>(A, Bg, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s,
                                                       nullptr, 1, 0, Bu);
+}
+
+int launch_gemm_mask(const uint16_t* A, const uint16_t* B, int M, int N, int K, const MaskEpiParams& p,
+                     int32_t* status, int kernel_id, cudaStream_t s) {
+  if (N % 256 == 0) return launch_gemm<256, MaskEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s);
+  if (N % 128 == 0) return launch_gemm<128, MaskEpi, false, false>(A, B, M, nullptr, N, K, 1, p, status, kernel_id, s);
+  return TWELL_ERR_UNSUPPORTED;
 }
 
 int launch_gemm_store_mn(const uint16_t* A, const uint16_t* B, int M, int N, int K, const int32_t* K_dev, int k_mul,

@@ -124,6 +124,15 @@ struct SampleEpiParams {
                             // part); high + low carry dz to ~2^-17 relative
 };
 
+// dZ = dH + lambda where h > 0 (else 0) for the dense comparator: dH the
+// accumulator, h from the dense H [M][ld] bf16; out [M][ld] bf16.
+struct MaskEpiParams {
+  const uint16_t* H;
+  uint16_t* out;
+  int64_t ld;
+  float lambda;
+};
+
 // C[M, N] = A[M, K] . B^T with A row-major [M][K] (K-major).  B is row-major
 // [N][K] (K-major) for the pack / dense / sample GEMMs and row-major [K][N]
 // (N-major) for the partial GEMM.  Rows beyond min(M, *M_dev) are not stored.
@@ -140,6 +149,12 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
                                cudaStream_t s, int64_t lda = 0, int b_k_wrap = 0);
+int launch_gemm_mask(const uint16_t* A, const uint16_t* B, int M, int N, int K, const MaskEpiParams& p,
+                     int32_t* status, int kernel_id, cudaStream_t s);
+// db[j] = sum over rows of Z[r][j] (bf16 [M][N], fp32 sums): row-chunk
+// partials [kColsumChunks][N] fp32 in `part`, then their sum in chunk order.
+constexpr int kColsumChunks = 16;
+int launch_colsum_bf16(const uint16_t* Z, int M, int N, float* part, float* out, int kernel_id, cudaStream_t s);
 // zero[0, n_zero) (int32), when given, is zeroed by the GEMM's CTA 0.
 int launch_gemm_sample(const uint16_t* A, const uint16_t* B, int M, int N, int K, const SampleEpiParams& p,
                        int32_t* status, cudaStream_t s, int32_t* zero = nullptr, int n_zero = 0);

@@ -566,6 +566,7 @@ def bench_ours(args, rank, world, local):
     d2h = hY.numel() * 2 + hdX.numel() * 2
 
     ms, e2e_m = max_over_ranks([med(rep_ms), e2e_m_loop], world, dev)
+    del bufs, hX, hdY, hY, hdX
 
     # ---- rooflines: every kernel group against its own bound; the dominant
     # one (the largest share of the step's kernel time) is the headline's
@@ -643,7 +644,105 @@ def bench_ours(args, rank, world, local):
         "timed_wall_s": round(wall, 3),
         "energy": energy_out,
     }
+    if world == 1 and not args.no_memory:
+        result["train_memory"] = bench_train_memory(tw, dev, args)
     return result
+
+
+def bench_train_memory(tw, dev, args):
+    """Peak device memory of one training step (forward + backward) at the
+    training shape, TwELL against the dense comparator, measured with the
+    allocator's peak counter: the inputs, weights and upstream gradient are
+    allocated first and left out; everything the step allocates -- the
+    activations kept for the backward, the workspace, the outputs and the
+    weight gradients -- is counted.  Each step is also timed (L2 scrubbed)."""
+    import numpy as np
+    import torch
+
+    import synth
+    cfg = synth.CONFIGS["train"]
+    inp = synth.make_ffn_inputs(cfg)
+    N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
+    lam = cfg.l1_lambda
+
+    def dt(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    X, Wi, b, Wd, dY = dt(inp["X"]), dt(inp["W_inT"]), dt(inp["b"]), dt(inp["W_down"]), dt(inp["dY"])
+    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
+                        dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def measure(alloc, run):
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        bufs = alloc()
+        run(bufs)
+        torch.cuda.synchronize()
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        for _ in range(3):
+            run(bufs)
+        ms = []
+        for _ in range(max(10, args.steps)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run(bufs)
+            e1.record(stream)
+            ms.append((e0, e1))
+        torch.cuda.synchronize()
+        t = statistics.median(a.elapsed_time(bb) for a, bb in ms)
+        del bufs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        return peak, t
+
+    def grads():
+        return dict(dX=torch.empty((N, d), dtype=torch.bfloat16, device=dev),
+                    dWi=torch.empty((f, d), dtype=torch.float32, device=dev),
+                    dWd=torch.empty((f, d), dtype=torch.float32, device=dev),
+                    db=torch.empty((f,), dtype=torch.float32, device=dev),
+                    Y=torch.empty((N, d), dtype=torch.bfloat16, device=dev))
+
+    def twell_alloc():
+        g = grads()
+        g["H"] = tw.alloc_packed(N, f, T, C, fb, dev)
+        g["ws"] = torch.empty(max(tw.fwd_workspace_bytes(N, d, f, T, C, fb), tw.bwd_workspace_bytes(N, d, f, T, C, fb)),
+                              dtype=torch.uint8, device=dev)
+        return g
+
+    def twell_run(g):
+        tw.twell_ffn_fwd(X, Wi, b, Wd, g["H"], g["Y"], g["ws"], stream)
+        tw.twell_ffn_bwd(X, Wi, Wd, g["H"], dY, lam, g["dX"], g["dWi"], g["dWd"], g["db"], g["ws"], stream)
+
+    def dense_alloc():
+        g = grads()
+        g["H"] = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+        g["ws"] = torch.empty(tw.dense_bwd_workspace_bytes(N, d, f), dtype=torch.uint8, device=dev)
+        return g
+
+    def dense_run(g):
+        tw.twell_dense_ffn_fwd(X, Wi, b, Wd, g["H"], g["Y"], stream)
+        tw.twell_dense_ffn_bwd(X, Wi, Wd, g["H"], dY, lam, g["dX"], g["dWi"], g["dWd"], g["db"], g["ws"], stream)
+
+    tw_peak, tw_ms = measure(twell_alloc, twell_run)
+    de_peak, de_ms = measure(dense_alloc, dense_run)
+    grads_bytes = N * d * 2 * 2 + 2 * f * d * 4 + f * 4
+    return {
+        "workload": "training step fwd+bwd: N=8192 d_model=2048 d_ff=8192 T=128 C=8, lognormal rows, 1% rows at "
+                    "20%, lambda 1e-4",
+        "twell": {"peak_bytes": int(tw_peak), "ms_per_step": round(tw_ms, 4),
+                  "tokens_per_s": round(N / (tw_ms * 1e-3), 1)},
+        "dense": {"peak_bytes": int(de_peak), "ms_per_step": round(de_ms, 4),
+                  "tokens_per_s": round(N / (de_ms * 1e-3), 1)},
+        "peak_ratio": round(tw_peak / de_peak, 4),
+        "activation_and_scratch_bytes": {"twell": int(tw_peak - grads_bytes), "dense": int(de_peak - grads_bytes)},
+        "how": "torch.cuda.max_memory_allocated over one step minus the memory allocated before it; inputs, "
+               "weights and dY allocated before and not counted; Y, dX, dW_in^T, dW_down, db (fp32) counted in "
+               "both (activation_and_scratch_bytes leaves them out)",
+    }
 
 
 def bench_next(args):
@@ -900,6 +999,8 @@ def main():
                     help="with --next: comma-separated workload names to run (default: all)")
     ap.add_argument("--next", action="store_true",
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
+    ap.add_argument("--no-memory", action="store_true",
+                    help="skip the training-shape peak-memory comparison against the dense step")
     ap.add_argument("--min-window", type=float, default=1.0,
                     help="repeat the K-step timed loop until the timed window spans this many seconds")
     ap.add_argument("--timeline", action="store_true",

@@ -130,7 +130,9 @@ TWELL_API int twell_pack(const uint16_t* H, int64_t ldh, const twell_t* out, twe
 
 /* TwELL -> dense (the pages' "TwELL-to-dense" path).
  * H: device, [in->n_rows][ldh] bf16 output, ldh >= d_ff, ldh % 8 == 0.
- * Every element of the first d_ff columns is written (zeros included). */
+ * Every element of the first d_ff columns is written (zeros included).  A
+ * fallback row past fb_cap (an overflowed layout: stored nowhere) comes out
+ * as zeros. */
 TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_stream_t stream);
 
 /* Forward of the layer ("fused MLP execution", repo-explainer page; the
@@ -233,6 +235,27 @@ TWELL_API size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int3
 TWELL_API int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b,
                         const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
                         uint16_t* Hbuf, uint16_t* Y, twell_stream_t stream);
+
+/* Backward of the dense comparator (not part of the method): the gradients
+ * twell_ffn_bwd computes, for the layer run densely by twell_dense_ffn_fwd,
+ * with no sparsity used -- the dense training step the TwELL step is measured
+ * against (run time and peak device memory).
+ *   H       [n_rows][d_ff] bf16, the dense forward's Hbuf (h = ReLU(z), bf16)
+ *   X, W_inT, W_down, dY, and the outputs dX (bf16), dW_inT, dW_down, db
+ *   (fp32) as for twell_ffn_bwd.
+ * dZ = (dY . W_down^T + l1_lambda) where h > 0, else 0, is formed densely on
+ * the tensor cores and kept in bf16 (the dense bf16 layer's own precision);
+ * dX = dZ . W_in, dW_inT = dZ^T . X, dW_down = H^T . dY, db = column sums of dZ
+ * (fixed order: deterministic).
+ * workspace: device, >= twell_dense_bwd_workspace_bytes(...) bytes, 256-byte
+ * aligned (holds dZ, n_rows * d_ff bf16, and the column-sum partials). */
+TWELL_API int twell_dense_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
+                                  const uint16_t* H, int32_t n_rows, int32_t d_model, int32_t d_ff,
+                                  const uint16_t* dY, float l1_lambda, uint16_t* dX, float* dW_inT,
+                                  float* dW_down, float* db, void* workspace, size_t workspace_bytes,
+                                  twell_stream_t stream);
+
+TWELL_API size_t twell_dense_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff);
 
 /* Synchronises `stream`, then returns *layout->status if non-zero, else
  * TWELL_ERR_FALLBACK_OVERFLOW when *layout->n_fb exceeds the capacity (fb_cap
