@@ -7,8 +7,12 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "twell_internal.h"
@@ -61,96 +65,133 @@ LaunchScope::~LaunchScope() {
 
 // ---------------------------------------------------------------- aux stream
 namespace {
-struct AuxState {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, mid = nullptr;
-};
-AuxState g_aux[64];
 std::mutex g_aux_mu;
+// the second stream of each (device, caller stream), created on first use
+std::map<std::pair<int, cudaStream_t>, cudaStream_t> g_aux_streams;
+
+cudaStream_t aux_stream_for(int dev, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_aux_mu);
+  auto it = g_aux_streams.find({dev, s});
+  if (it != g_aux_streams.end()) return it->second;
+  // the second stream carries the small fallback-row work next to a large
+  // kernel on the caller's stream: the highest priority lets its CTAs take
+  // SMs as they free up instead of queueing behind the large grid
+  int least = 0, greatest = 0;
+  cudaStream_t a = nullptr;
+  if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&a, cudaStreamNonBlocking, greatest) != cudaSuccess)
+    return nullptr;
+  g_aux_streams[{dev, s}] = a;
+  return a;
+}
 }  // namespace
 
 AuxFork::AuxFork(cudaStream_t s) : s_(s) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     rc_ = TWELL_ERR_CUDA;
     return;
   }
-  std::lock_guard<std::mutex> lk(g_aux_mu);
-  AuxState& a = g_aux[dev];
-  if (!a.stream) {
-    // the second stream carries the small fallback-row work next to a large
-    // kernel on the caller's stream: the highest priority lets its CTAs take
-    // SMs as they free up instead of queueing behind the large grid
-    int least = 0, greatest = 0;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&a.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&a.mid, cudaEventDisableTiming) != cudaSuccess) {
-      rc_ = TWELL_ERR_CUDA;
-      return;
-    }
+  aux_ = aux_stream_for(dev, s);
+  if (!aux_ || cudaEventCreateWithFlags(&fork_, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&join_, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&mid_, cudaEventDisableTiming) != cudaSuccess) {
+    rc_ = TWELL_ERR_CUDA;
+    return;
   }
-  aux_ = a.stream;
-  if (cudaEventRecord(a.fork, s_) != cudaSuccess || cudaStreamWaitEvent(aux_, a.fork, 0) != cudaSuccess)
+  if (cudaEventRecord(fork_, s_) != cudaSuccess || cudaStreamWaitEvent(aux_, fork_, 0) != cudaSuccess)
     rc_ = TWELL_ERR_CUDA;
 }
 
 int AuxFork::join() {
   if (joined_ || rc_ != 0) return rc_;
   joined_ = true;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lk(g_aux_mu);
-  AuxState& a = g_aux[dev];
-  if (cudaEventRecord(a.join, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, a.join, 0) != cudaSuccess)
+  if (cudaEventRecord(join_, aux_) != cudaSuccess || cudaStreamWaitEvent(s_, join_, 0) != cudaSuccess)
     rc_ = TWELL_ERR_CUDA;
   return rc_;
 }
 
 int AuxFork::mark_aux() {
   if (joined_ || rc_ != 0) return rc_;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lk(g_aux_mu);
-  if (cudaEventRecord(g_aux[dev].mid, aux_) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
+  if (cudaEventRecord(mid_, aux_) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
   return rc_;
 }
 
 int AuxFork::main_wait_mark() {
   if (joined_ || rc_ != 0) return rc_;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lk(g_aux_mu);
-  if (cudaStreamWaitEvent(s_, g_aux[dev].mid, 0) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
+  if (cudaStreamWaitEvent(s_, mid_, 0) != cudaSuccess) rc_ = TWELL_ERR_CUDA;
   return rc_;
 }
 
-AuxFork::~AuxFork() { join(); }
+AuxFork::~AuxFork() {
+  join();
+  // released by the runtime once the recorded work has completed
+  for (cudaEvent_t e : {fork_, join_, mid_})
+    if (e) cudaEventDestroy(e);
+}
+
+// ---------------------------------------------------------------- kernel attributes
+namespace {
+std::mutex g_attr_mu;
+std::set<std::pair<int, const void*>> g_smem_set;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_resident;
+}  // namespace
+
+int set_max_dynamic_smem(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TWELL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_smem_set.count({dev, func})) return TWELL_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  g_smem_set.insert({dev, func});
+  return TWELL_OK;
+}
+
+int resident_ctas_per_sm(const void* func, int block, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  const auto key = std::make_tuple(dev, func, block, smem);
+  auto it = g_resident.find(key);
+  if (it != g_resident.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess) return 0;
+  g_resident[key] = n;
+  return n;
+}
 
 // ---------------------------------------------------------------- device facts
+// Device facts are fixed for the process: cached per device, the caches read
+// and written atomically (two threads that race compute the same value).
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int n = 0;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (n <= 0) n = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
 bool device_is_sm103() {
-  static int cached[64] = {};  // 0 unknown, 1 yes, 2 no
+  static std::atomic<int> cached[64] = {};  // 0 unknown, 1 yes, 2 no
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c == 1;
+  }
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   const bool ok = major == 10 && minor == 3;
-  if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+  if (dev >= 0 && dev < 64) cached[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok;
 }
 

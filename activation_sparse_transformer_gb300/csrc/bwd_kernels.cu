@@ -456,17 +456,11 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit (a CTA per tile)
   const size_t lsm = unit_lists_smem(Lh.tile);
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(unit_lists_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(unit_lists_smem(256))) != cudaSuccess ||
-        cudaFuncSetAttribute(unit_lists_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(unit_lists_smem(256))) != cudaSuccess)
-      return TWELL_ERR_CUDA;
-    attr[dev] = true;
-  }
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(unit_lists_kernel<true>),
+                           static_cast<int>(unit_lists_smem(256))) != TWELL_OK ||
+      set_max_dynamic_smem(reinterpret_cast<const void*>(unit_lists_kernel<false>),
+                           static_cast<int>(unit_lists_smem(256))) != TWELL_OK)
+    return TWELL_ERR_CUDA;
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
     auto lk = Lh.cap == 8 ? unit_lists_kernel<true> : unit_lists_kernel<false>;

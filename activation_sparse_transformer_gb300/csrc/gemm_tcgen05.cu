@@ -837,14 +837,8 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
   if (!Epi::kDualB) tb2 = tb;
   const uint32_t smem = 1024 + Cfg::kPipeBytes + Cfg::kBarBytes + Epi::kSmemBytes;
   auto kern = tc_gemm_kernel<BN, Epi, kANMajor, kBNMajor>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return TWELL_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
+  if (rc) return rc;
   const int units = ((M + kBM - 1) / kBM) * (N / (Epi::kDualB ? BN / 2 : BN)) * ksplit;
   const int grid = std::max(1, std::min(units, sm_count()));
   GemmArgs args{M,      M_dev,        N,     K,       ksplit, K_dev, k_mul, status, kWaitLimitNs,

@@ -339,29 +339,15 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   const size_t smem = static_cast<size_t>(kWarps) * max_entries * sizeof(RowEntry<VT>);
   if (smem > kMaxDynSmem) return TWELL_ERR_UNSUPPORTED;
   auto kern = spmm_row_kernel<VT>;
-  static bool attr[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess)
-      return TWELL_ERR_CUDA;
-    attr[dev] = true;
-  }
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), kMaxDynSmem) != TWELL_OK) return TWELL_ERR_CUDA;
   if (nsplit < 1 || nsplit > 64 || (nsplit > 1 && (!a.part || !a.arrivals))) return TWELL_ERR_INVALID_ARG;
   if (nsplit > 1) {
     // no more tile ranges than fit in one wave of resident CTAs: a second wave
     // would repeat the whole latency chain of this short launch
-    static int resident[64] = {};
-    static size_t resident_smem[64] = {};
-    if (dev < 64 && (resident[dev] == 0 || resident_smem[dev] != smem)) {
-      int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess)
-        return TWELL_ERR_CUDA;
-      resident[dev] = std::max(1, per_sm) * sm_count();
-      resident_smem[dev] = smem;
-    }
+    const int per_sm = resident_ctas_per_sm(reinterpret_cast<const void*>(kern), kWarps * 32, smem);
+    if (per_sm <= 0) return TWELL_ERR_CUDA;
     const int64_t per_split = static_cast<int64_t>((a.N + kWarps - 1) / kWarps) * ((a.d + 255) / 256);
-    const int fit = static_cast<int>(std::max<int64_t>(1, (dev < 64 ? resident[dev] : sm_count()) / per_split));
+    const int fit = static_cast<int>(std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sm_count() / per_split));
     nsplit = std::min(nsplit, fit);
   }
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
@@ -371,12 +357,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
     // CTAs per SM (the register limit)
     auto rk = spmm_rowcta_kernel<VT>;
     const size_t rsmem = static_cast<size_t>(a.nt) * a.C * sizeof(RowEntry<VT>);
-    static bool rattr[64] = {};
-    if (dev < 64 && !rattr[dev]) {
-      if (cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess)
-        return TWELL_ERR_CUDA;
-      rattr[dev] = true;
-    }
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(rk), kMaxDynSmem) != TWELL_OK) return TWELL_ERR_CUDA;
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 4 * static_cast<int64_t>(sm_count()))));
     {
       LaunchScope ls(kernel_id, s);

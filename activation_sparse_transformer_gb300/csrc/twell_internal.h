@@ -30,9 +30,19 @@ class LaunchScope {
 
 int sm_count();                      // SMs of the current device (cached per device)
 
-// A second stream per device for work that can overlap the caller's stream
-// (the dense-fallback path).  fork(): aux waits for everything queued on s so
-// far; join(): s waits for everything queued on aux.  Both are asynchronous.
+// Sets a kernel's dynamic shared-memory limit on the current device once
+// (thread-safe); returns TWELL_OK or TWELL_ERR_CUDA.
+int set_max_dynamic_smem(const void* func, int bytes);
+// Resident CTAs per SM of a kernel at a block size and dynamic shared memory
+// on the current device, cached (thread-safe); 0 when the query fails.
+int resident_ctas_per_sm(const void* func, int block, size_t smem);
+
+// A second stream for work that can overlap the caller's stream s (the
+// dense-fallback path).  Each (device, caller stream) pair has its own second
+// stream, created on first use, so callers on different streams never share
+// one; the fork / join events belong to the call.  fork(): aux waits for
+// everything queued on s so far; join(): s waits for everything queued on
+// aux.  Both are asynchronous.
 class AuxFork {
  public:
   explicit AuxFork(cudaStream_t s);
@@ -49,6 +59,7 @@ class AuxFork {
  private:
   cudaStream_t s_;
   cudaStream_t aux_ = nullptr;
+  cudaEvent_t fork_ = nullptr, join_ = nullptr, mid_ = nullptr;
   int rc_ = 0;
   bool joined_ = false;
 };
