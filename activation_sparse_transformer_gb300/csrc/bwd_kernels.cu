@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kListWarps * 32)
                       int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
                       float* __restrict__ col_dz) {
   extern __shared__ int32_t lsm[];
+  grid_dependency_wait();
   const int T = L.T, t = blockIdx.x;
   int32_t* wcur = lsm;                                            // [kListWarps][T]: counts, then cursors
   uint32_t* wmask = reinterpret_cast<uint32_t*>(lsm + kListWarps * T);  // [kListWarps][T]
@@ -329,6 +330,7 @@ __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, con
 __global__ void __launch_bounds__(256) fb_db_kernel(Layout L, const uint16_t* __restrict__ dz_hl,
                                                     float* __restrict__ db) {
   __shared__ float part[8][32];
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * 32 + lane;
   const int nfb = min(*L.n_fb, L.fb_cap);
@@ -464,8 +466,9 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
     auto lk = Lh.cap == 8 ? unit_lists_kernel<true> : unit_lists_kernel<false>;
-    lk<<<f / Lh.tile, kListWarps * 32, lsm, s>>>(L, ws.dz_cells, ws.col_beg, ws.col_end, ws.col_rows, ws.col_h,
-                                               ws.col_dz);
+    if (launch_pdl(lk, dim3(f / Lh.tile), dim3(kListWarps * 32), lsm, s, L, ws.dz_cells, ws.col_beg, ws.col_end,
+                   ws.col_rows, ws.col_h, ws.col_dz) != cudaSuccess)
+      return TWELL_ERR_CUDA;
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.main_wait_mark());  // the fallback share is in dW before the TwELL share is added
@@ -479,7 +482,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   TW_CHECK_LAUNCH();
   if (fb) {
     LaunchScope ls(TWELL_KERNEL_DW, s);
-    fb_db_kernel<<<(f + 31) / 32, 256, 0, s>>>(L, ws.dz_hl, db);
+    if (launch_pdl(fb_db_kernel, dim3((f + 31) / 32), dim3(256), 0, s, L, ws.dz_hl, db) != cudaSuccess)
+      return TWELL_ERR_CUDA;
   }
   TW_CHECK_LAUNCH();
   TW_TRY_RC(fork.join());

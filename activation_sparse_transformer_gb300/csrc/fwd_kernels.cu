@@ -50,6 +50,7 @@ constexpr int kRouteRows = 8;  // rows per thread per pass
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
   __shared__ int warp_tot[kRouteThreads / 32];
   __shared__ int base_s;
+  grid_dependency_wait();
   const bool tiles = L.hybrid == TWELL_HYBRID_TILES;
   const int64_t cap = tiles ? static_cast<int64_t>(L.fb_cap) * L.nt : L.fb_cap;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(256)
 // spread over the whole GPU.
 __global__ void __launch_bounds__(256)
     fb_assemble_kernel(Layout L, const uint16_t* __restrict__ spill, int32_t spill_cap) {
+  grid_dependency_wait();
   const int nfb = min(*L.n_fb, L.fb_cap);
   const int lane = threadIdx.x & 31;
   const int vec = L.T / 8;  // 16-byte vectors per tile
@@ -245,6 +247,7 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&a)[8]) {
 // Y[fb_rows[r]] = bf16(sum over splits of part[ks][r]), splits in order.
 __global__ void fb_reduce_kernel(Layout L, const float* __restrict__ part, int ksplit, int d,
                                  uint16_t* __restrict__ Y) {
+  grid_dependency_wait();
   const int nfb = min(*L.n_fb, L.fb_cap);
   const int64_t stride = static_cast<int64_t>(L.fb_cap) * d;
   for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
@@ -323,7 +326,7 @@ int launch_tile_assign(const twell_t& L, const uint16_t* H, int64_t ldh, const u
 
 int launch_route(const twell_t& L, cudaStream_t s) {
   LaunchScope ls(TWELL_KERNEL_ROUTE, s);
-  route_kernel<<<1, kRouteThreads, 0, s>>>(flat(L));
+  if (launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, flat(L)) != cudaSuccess) return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -333,7 +336,8 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* /
   const int64_t warps = static_cast<int64_t>(L.fb_cap) * (L.d_ff / L.tile);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((warps + 7) / 8, 4 * sm_count())));
   LaunchScope ls(TWELL_KERNEL_FB_ASSEMBLE, s);
-  fb_assemble_kernel<<<grid, 256, 0, s>>>(flat(L), spill, spill_cap);
+  if (launch_pdl(fb_assemble_kernel, dim3(grid), dim3(256), 0, s, flat(L), spill, spill_cap) != cudaSuccess)
+    return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
@@ -352,7 +356,8 @@ int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_mode
   if (L.fb_cap <= 0) return TWELL_OK;
   const int grid = std::max(1, std::min(L.fb_cap, 2 * sm_count()));
   LaunchScope ls(kernel_id, s);
-  fb_reduce_kernel<<<grid, 256, 0, s>>>(flat(L), part, nsplit, d_model, out);
+  if (launch_pdl(fb_reduce_kernel, dim3(grid), dim3(256), 0, s, flat(L), part, nsplit, d_model, out) != cudaSuccess)
+    return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -593,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   static_assert(2 * S * 8 + 4 * 8 + 8 + 8 + S * 4 <= static_cast<int>(Cfg::kBarBytes), "barrier region");
+  grid_dependency_wait();  // before the first read of device memory (M_dev, K_dev, operands)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -845,7 +846,10 @@ int launch_gemm(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_de
                 zero0,  zero0 ? n_zero0 : 0, zero1, zero1 ? n_zero1 : 0, b_k_wrap};
   {
     LaunchScope ls(kernel_id, s);
-    kern<<<grid, kThreads, smem, s>>>(ta, tb, tb2, args, p);
+    if (launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, ta, tb, tb2, args, p) != cudaSuccess) {
+      cudaGetLastError();
+      return TWELL_ERR_CUDA;
+    }
   }
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

@@ -9,9 +9,13 @@
 // scratch buffer.  This entry point keeps that scratch in a fixed array in
 // device memory that is part of the library image.
 //
-// The array holds the rows of X gathered for the dense-fallback recompute:
-// fb_cap * d_model bf16 values, at most kNoAllocScratchBytes.  Every GPU that
-// loads the library keeps the array until the process exits.
+// The array holds what the caller's workspace holds for twell_ffn_fwd, whose
+// size twell_fwd_workspace_bytes(...) gives: the dense tiles spilled by
+// overflowing cells, the call's counters and overflow flags, the K-split
+// partial sums of the fallback rows' down-projection and, for batches of at
+// most 32 rows, the up-projection's K-split partial sums, a dense copy of h
+// and the gather's tile-range partials.  At most kNoAllocScratchBytes; every
+// GPU that loads the library keeps the array until the process exits.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -20,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB: fb_cap * d_model <= 2 Mi elements
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
 
 static __device__ __align__(256) unsigned char g_fwd_scratch[kNoAllocScratchBytes];
 

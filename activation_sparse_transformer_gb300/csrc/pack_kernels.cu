@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     pack_partials_kernel(Layout L, const float* __restrict__ part, int ksplit, const uint16_t* __restrict__ b,
                          uint16_t* __restrict__ H, int32_t* arrivals) {
   __shared__ int last_s;
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int segs = (L.f + 255) / 256;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
@@ -531,7 +532,9 @@ int launch_pack_partials(const float* part, int ksplit, const uint16_t* b, uint1
   if (blocks > 0x7FFFFFFF || L.d_ff % 8 != 0) return TWELL_ERR_UNSUPPORTED;
   if (arrivals && L.n_rows > 32) return TWELL_ERR_UNSUPPORTED;
   LaunchScope ls(TWELL_KERNEL_PACK, s);
-  pack_partials_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), part, ksplit, b, H, arrivals);
+  if (launch_pdl(pack_partials_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kWarps * 32), 0, s, flat(L), part,
+                 ksplit, b, H, arrivals) != cudaSuccess)
+    return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

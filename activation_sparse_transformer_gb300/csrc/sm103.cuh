@@ -21,6 +21,13 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on its stream is still
+// finishing; this waits until that kernel has completed and its writes are
+// visible.  Every kernel the library may launch that way calls it before its
+// first global memory access (it returns at once for a normal launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Records the first device-side error of a call; later errors keep the first.
 __device__ __forceinline__ void report_error(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

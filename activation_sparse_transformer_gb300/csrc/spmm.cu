@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     spmm_row_kernel(const SpmmArgs a, const uint16_t* __restrict__ W, int max_entries) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int last_s;
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw) + warp * max_entries;
 
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_tot[kWarps + 1];
   __shared__ int next_row_s[2];  // by iteration parity: a skipped row has no barrier before the next write
+  grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   RowEntry<VT>* list = reinterpret_cast<RowEntry<VT>*>(smem_raw);
   const VT* vals = static_cast<const VT*>(a.values);
@@ -361,7 +363,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 4 * static_cast<int64_t>(sm_count()))));
     {
       LaunchScope ls(kernel_id, s);
-      rk<<<rgrid, kWarps * 32, rsmem, s>>>(a, W);
+      if (launch_pdl(rk, dim3(rgrid), dim3(kWarps * 32), rsmem, s, a, W) != cudaSuccess) return TWELL_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
   }
@@ -374,7 +376,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   }
   {
     LaunchScope ls(kernel_id, s);
-    kern<<<grid, kWarps * 32, smem, s>>>(a, W, max_entries);
+    if (launch_pdl(kern, grid, dim3(kWarps * 32), smem, s, a, W, max_entries) != cudaSuccess) return TWELL_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

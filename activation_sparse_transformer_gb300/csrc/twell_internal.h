@@ -30,6 +30,24 @@ class LaunchScope {
 
 int sm_count();                      // SMs of the current device (cached per device)
 
+// Launches a kernel with programmatic stream serialization: the kernel's
+// launch and start overlap the end of the previous kernel on the stream, and
+// the kernel executes grid_dependency_wait() before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Sets a kernel's dynamic shared-memory limit on the current device once
 // (thread-safe); returns TWELL_OK or TWELL_ERR_CUDA.
 int set_max_dynamic_smem(const void* func, int bytes);

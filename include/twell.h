@@ -186,11 +186,14 @@ TWELL_API int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const
  * (twell_ffn_fwd_noalloc_max_scratch() bytes, 4 MiB; every GPU that loads the
  * library holds it until the process exits).  It allocates nothing.
  *   - Sizes: twell_fwd_workspace_bytes(...) must not exceed that maximum
- *     (it grows with fb_cap * d_ff and fb_cap * d_model); otherwise
+ *     (it grows with fb_cap * d_ff and fb_cap * d_model, and for batches of
+ *     at most 32 rows with n_rows * d_ff and n_rows * d_model); otherwise
  *     TWELL_ERR_WORKSPACE is returned and nothing is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the process: after
+ *     cudaDeviceReset (or anything else that destroys the device's primary
+ *     context) the entry point must not be called again on that device.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero): calls that overlap on the GPU,
  *     e.g. on two streams, race on it and must be ordered by the caller.

@@ -68,8 +68,8 @@ INT_CASES = [
     (200, 128, 1152, 128, 8, 0.95, 2),    # ragged N, d_ff % 256 == 128 (128-wide N tiles)
     (130, 128, 512, 32, 4, 0.9, 3),       # K = two 64-wide steps, many overflow rows
     (384, 512, 2048, 256, 16, 0.98, 4),
-    # d_model a multiple of 2048: the gather runs through the shared-memory
-    # ring filled by bulk copies (4, 2 and 1 W rows per stage)
+    # wide rows: each stored entry's W_down row spans 8, 16 and 32 of the
+    # gather's 256-column blocks
     (300, 2048, 1024, 128, 8, 0.97, 5),
     (200, 4096, 1024, 64, 16, 0.95, 6),
     (136, 8192, 512, 128, 8, 0.97, 7),

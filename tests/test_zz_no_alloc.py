@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import synth
-from twell_check import assert_close, from_dev_bits, from_dev_f32, to_dev
+from twell_check import from_dev_bits, from_dev_f32, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +66,8 @@ def test_noalloc_matches_workspace_call_twice(tw):
             assert np.array_equal(got[k], want[k]), (call, k)
         assert np.array_equal(got["fb_rows"][:nfb], want["fb_rows"][:nfb])
         assert np.array_equal(got["fb_dense"][:nfb], want["fb_dense"][:nfb])
-        assert_close(got["Y"], want["Y"], f"Y call {call}")
+        # the same kernels in the same order on the same inputs: the same bits
+        assert np.array_equal(got["Y"], want["Y"]), f"Y call {call}"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(tw):
@@ -76,7 +77,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(tw):
     assert cap == 4 << 20
     cfg, (X, Wi, b, Wd) = _inputs(torch)
     N, d, f, T, C = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap
-    fb_too_many = cap // (d * 2) + 1          # gathered fallback rows no longer fit
+    # a fallback capacity whose spill tiles (fb_cap x d_ff bf16) alone exceed the array
+    fb_too_many = cap // (f * 2) + 1
     assert tw.fwd_workspace_bytes(N, d, f, T, C, fb_too_many) > cap
     p = tw.alloc_packed(N, f, T, C, fb_too_many, torch.device("cuda"))
     Y = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
