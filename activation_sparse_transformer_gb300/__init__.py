@@ -36,6 +36,7 @@ TWELL_OK = 0
 KERNELS = {
     "up_pack": 0, "route": 1, "fb_assemble": 2, "spmm": 4, "fb_down": 5, "pack": 6,
     "check_format": 3, "unpack": 7, "sddmm": 8, "dx": 9, "dw": 10, "dense_gemm": 11, "aux": 12,
+    "dw_fallback": 13, "dx_fallback": 14,
 }
 EXPORTED = [
     "twell_pack", "twell_unpack", "twell_ffn_fwd", "twell_fwd_workspace_bytes", "twell_ffn_bwd",

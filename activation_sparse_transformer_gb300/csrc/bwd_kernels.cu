@@ -434,15 +434,15 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   if (fb) {
     {
       const int grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
-      LaunchScope ls(TWELL_KERNEL_DW, a);
+      LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, a);
       fb_operands_kernel<<<grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad);
     }
     TW_CHECK_LAUNCH();
     TW_TRY_RC(launch_gemm_store_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, 1, dW_down, d, Lh.status,
-                                   TWELL_KERNEL_DW, a));
+                                   TWELL_KERNEL_DW_FALLBACK, a));
     // K = (slot, part): the high and low parts of dZ against X twice
     TW_TRY_RC(launch_gemm_store_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, dW_inT, d, Lh.status,
-                                   TWELL_KERNEL_DW, a));
+                                   TWELL_KERNEL_DW_FALLBACK, a));
   }
   TW_TRY_RC(fork.mark_aux());  // dW holds the fallback share from here on
   if (N > 0) {
@@ -451,8 +451,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
       // [high_s | low_s], and both halves meet the same W_in^T rows (K wraps)
       PartialEpiParams pp{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
       TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl, W_inT, Lh.fb_cap, Lh.n_fb, d, 2 * f, ws.ksplit, pp, Lh.status,
-                                           TWELL_KERNEL_DX, a, 2 * static_cast<int64_t>(f), f));
-      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX, a));
+                                           TWELL_KERNEL_DX_FALLBACK, a, 2 * static_cast<int64_t>(f), f));
+      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX_FALLBACK, a));
     }
     TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
   }
@@ -481,7 +481,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   }
   TW_CHECK_LAUNCH();
   if (fb) {
-    LaunchScope ls(TWELL_KERNEL_DW, s);
+    LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, s);
     if (launch_pdl(fb_db_kernel, dim3((f + 31) / 32), dim3(256), 0, s, L, ws.dz_hl, db) != cudaSuccess)
       return TWELL_ERR_CUDA;
   }

@@ -213,10 +213,17 @@ def kernel_work(N, d, f, T, C, nnz_tw, n_fb):
                   "what": "tcgen05 dY.W_down^T with the pattern-sampling + L1 epilogue"},
         "dx": {"bound": "hbm", "bytes": cells * C * 4 + cells * C + cells + f * d * 2 + N * d * 2,
                "l2_gather_bytes": nnz_tw * row,
-               "what": "dX gather (fp32 dZ entries x W_in^T rows) + fallback rows' GEMM"},
+               "what": "dX gather of the TwELL rows (fp32 dZ entries x W_in^T rows)"},
         "dw": {"bound": "hbm", "bytes": 2 * N * d * 2 + 2 * f * d * 4 + nnz_tw * 12 + f * 4,
                "l2_gather_bytes": 2 * nnz_tw * row,
-               "what": "dW_down, dW_in^T (fp32) and db: unit-major walk + fallback rows' store GEMMs"},
+               "what": "unit-major walk: the TwELL rows' dW_down, dW_in^T (fp32, added to the fallback share "
+                       "stored before it) and db"},
+        "dw_fallback": {"bound": "tensor", "flops": 2.0 * 3 * n_fb * d * f,
+                        "what": "the fallback rows' dW_down and dW_in^T (store GEMMs; dZ as two bf16 parts) "
+                                "and db, on the second stream"},
+        "dx_fallback": {"bound": "tensor", "flops": 2.0 * 2 * n_fb * d * f,
+                        "what": "the fallback rows' dX (split-K GEMM over the two bf16 parts of dZ) and its "
+                                "ordered reduction, on the second stream"},
         "pack": {"bound": "hbm", "bytes": N * f * 2 + packed + N * 4 + fb_rows,
                  "what": "standalone dense -> TwELL (twell_pack)"},
         "unpack": {"bound": "hbm", "bytes": packed + N * 4 + fb_rows + N * f * 2,
@@ -247,22 +254,27 @@ def roofline_entry(work, us, peaks, peak_src):
     return e
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch recorded by an ncu capture, if the kernel source
-    has not changed since (the capture stores the source digest)."""
+def source_digest(name: str) -> str:
+    """First 16 hex digits of the sha256 of a kernel source file (csrc/<name>)."""
     import hashlib
+    with open(os.path.join(ROOT, "activation_sparse_transformer_gb300", "csrc", name), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of a kernel recorded by an ncu capture
+    (profiles/ncu_traffic.txt: kernel, workload, source file, its digest at the
+    capture, bytes, the summary that shows the capture), or None with a note
+    when the kernel's source has changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None, None
-    src = os.path.join(ROOT, "activation_sparse_transformer_gb300", "csrc", "gemm_tcgen05.cu")
-    with open(src, "rb") as fh:
-        digest = hashlib.sha256(fh.read()).hexdigest()[:16]
     with open(path) as fh:
         for line in fh:
             parts = line.split()
-            if len(parts) >= 5 and parts[0] == kernel and parts[1] == workload:
-                if parts[2] == digest:
-                    return float(parts[3]), parts[4]
+            if len(parts) >= 6 and parts[0] == kernel and parts[1] == workload:
+                if source_digest(parts[2]) == parts[3]:
+                    return float(parts[4]), parts[5]
                 return None, "stale: kernel changed since the capture"
     return None, None
 
@@ -581,15 +593,16 @@ def bench_ours(args, rank, world, local):
         roofs[name] = roofline_entry(work[name], conv[name]["kernel_us_per_call"], peaks, peak_src)
     dominant = max((k for k in roofs if k in per_kernel), key=lambda k: per_kernel[k]["share"], default=None)
     roof = dict(roofs[dominant]) if dominant else None
+    for name, r in roofs.items():
+        traffic, note = ncu_traffic(name, args.config)
+        r["traffic"] = traffic
+        if note:
+            r["traffic_note"] = note
     if roof is not None:
         roof["name"] = dominant
-        if dominant == "up_pack":
-            traffic, note = ncu_traffic("up_pack", "1b")
-            roof["traffic"] = traffic
-            if note:
-                roof["traffic_note"] = note
-        else:
-            roof["traffic"] = None
+        roof["traffic"] = roofs[dominant]["traffic"]
+        if "traffic_note" in roofs[dominant]:
+            roof["traffic_note"] = roofs[dominant]["traffic_note"]
     fwd_m = med(fwd_ms)
     packed_bytes = (packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel() + packed.row_fb.numel() * 4
                     + packed.fb_rows.numel() * 4 + packed.fb_dense.numel() * 2)

@@ -322,11 +322,13 @@ enum {
   TWELL_KERNEL_PACK = 6,         /* standalone dense -> TwELL */
   TWELL_KERNEL_UNPACK = 7,       /* TwELL -> dense */
   TWELL_KERNEL_SDDMM = 8,        /* backward: dZ at the pattern */
-  TWELL_KERNEL_DX = 9,           /* backward: dX gather */
-  TWELL_KERNEL_DW = 10,          /* backward: dW_down, dW_inT, db */
+  TWELL_KERNEL_DX = 9,           /* backward: dX gather of the TwELL rows */
+  TWELL_KERNEL_DW = 10,          /* backward: unit-major walk adding the TwELL rows' dW_down, dW_inT, db */
   TWELL_KERNEL_DENSE_GEMM = 11,  /* dense comparator GEMMs */
   TWELL_KERNEL_AUX = 12,         /* small helpers (clears, transposed indexes) */
-  TWELL_KERNEL_COUNT = 13
+  TWELL_KERNEL_DW_FALLBACK = 13, /* backward: the fallback rows' dW_down, dW_inT, db share */
+  TWELL_KERNEL_DX_FALLBACK = 14, /* backward: the fallback rows' dX */
+  TWELL_KERNEL_COUNT = 15
 };
 TWELL_API int twell_profile_enable(int on);
 TWELL_API int twell_profile_reset(void);
