@@ -424,7 +424,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
   }
   // Second stream: the fallback rows' weight-gradient share (stored into dW
-  // first), then dX (fallback GEMMs + the TwELL rows' gather-SpMM).  This
+  // first), then dX (the TwELL rows' gather-SpMM, then the fallback rows' GEMM).  This
   // stream: the unit-major lists (independent of the fallback share), then
   // dw_unitcta_kernel adds the TwELL share once the fallback share is in place.
   AuxFork fork(s);
@@ -446,6 +446,9 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   }
   TW_TRY_RC(fork.mark_aux());  // dW holds the fallback share from here on
   if (N > 0) {
+    // the TwELL rows' dX gather first: it needs only the SDDMM's output and,
+    // queued after the fallback rows' dX, it waited for SMs held by the dW walk
+    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
     if (fb) {
       // one GEMM over K = 2 d_ff: row s of dz_hl viewed with stride 2 d_ff is
       // [high_s | low_s], and both halves meet the same W_in^T rows (K wraps)
@@ -454,7 +457,6 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                                            TWELL_KERNEL_DX_FALLBACK, a, 2 * static_cast<int64_t>(f), f));
       TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX_FALLBACK, a));
     }
-    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit (a CTA per tile)
   const size_t lsm = unit_lists_smem(Lh.tile);
