@@ -33,8 +33,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-FFN tokens/s (TwELL fwd/bwd, 99% sparse) + % of HBM/tensor roofline"
 UNIT = "tokens/s"
-WORKLOAD = "1B-scale FFN fwd+bwd: N=4096 d_model=2048 d_ff=8192 T=128 C=8, lognormal row activity (mean 1%), 2% rows at 20%"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_name(cfg) -> str:
+    """The bench line's workload: what the step is, with its sizes and input recipe."""
+    rows = "lognormal row activity (mean 1%)" if cfg.row_spread == "lognormal" else "uniform row activity"
+    forced = (f", {round(100 * cfg.forced_frac_rows)}% rows at {round(100 * cfg.forced_activity)}%"
+              if cfg.forced_frac_rows else "")
+    lam = f", lambda {cfg.l1_lambda:g}" if cfg.l1_lambda else ""
+    return (f"{'1B-scale' if cfg.name == '1b' else cfg.name} FFN fwd+bwd: N={cfg.n_rows} d_model={cfg.d_model} "
+            f"d_ff={cfg.d_ff} T={cfg.tile} C={cfg.cap}, {rows}{forced}{lam}")
 
 
 def load_peaks():
@@ -201,10 +210,8 @@ def kernel_work(N, d, f, T, C, nnz_tw, n_fb):
     fb_rows = n_fb * f * 2
     row = d * 2                                          # one gathered bf16 row
     return {
-        "up_pack": {"bound": "tensor", "flops": 2.0 * N * d * f,
-                    "bytes": N * d * 2 + f * d * 2 + packed + N * d * 2, "l2_gather_bytes": nnz_tw * row,
-                    "what": "tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue, with the TwELL rows' "
-                            "gather-SpMM (Y) in the same persistent kernel"},
+        "up_pack": {"bound": "tensor", "flops": 2.0 * N * d * f, "bytes": N * d * 2 + f * d * 2 + packed,
+                    "what": "tcgen05 up-projection + bias/ReLU/TwELL-pack epilogue"},
         "spmm": {"bound": "hbm", "bytes": packed + f * d * 2 + N * d * 2, "l2_gather_bytes": nnz_tw * row,
                  "what": "standalone TwELL gather-SpMM (Y)"},
         "fb_down": {"bound": "tensor", "flops": 2.0 * n_fb * d * f,
@@ -359,7 +366,7 @@ def bench_ours(args, rank, world, local):
                 e["stream"] = "main" if e["stream"] == main_stream else "second"
                 e["start_ms"] = round(e["start_ms"], 4)
                 e["end_ms"] = round(e["end_ms"], 4)
-        return {"timeline": timelines, "config": {"workload": WORKLOAD, "n_rows": N},
+        return {"timeline": timelines, "config": {"workload": workload_name(cfg), "n_rows": N},
                 "note": "one fwd + bwd step, three times; times relative to each step's first launch"}
 
     def timed(fn, k, profile=False, warm=False):
@@ -614,7 +621,7 @@ def bench_ours(args, rank, world, local):
         "metric": METRIC, "value": round(job_throughput(world, N, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
-        "config": {"workload": WORKLOAD, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
+        "config": {"workload": workload_name(cfg), "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
                    "fb_cap": fb, "l1_lambda": lam, "l2": "flushed between steps (2x L2 write)",
                    "parallelism": (f"data parallel x{world}: each rank its own batch, weight gradients "
                                    "all-reduced (NCCL sum) inside the step") if world > 1 else "single GPU"},
@@ -922,7 +929,7 @@ def cpu_baseline(rows=None):
 
     import oracle
     import synth
-    cfg = synth.CONFIGS["1b"]
+    cfg = synth.CONFIGS[args.config]
     base = synth.make_ffn_inputs(cfg)
     dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
     rows = rows or cpu_sample_rows(1536)  # ~10-15 s of the oracle on the host cores
@@ -969,7 +976,7 @@ def bench_reference(args, rank, world):
         return None
     import oracle
     import synth
-    cfg = synth.CONFIGS["1b"]
+    cfg = synth.CONFIGS[args.config]
     base = synth.make_ffn_inputs(cfg)
     dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
     lam = cfg.l1_lambda or 1e-4
@@ -989,7 +996,7 @@ def bench_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * s, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded, see synth/)",
-            "config": {"workload": WORKLOAD, "sample_rows": rows},
+            "config": {"workload": workload_name(cfg), "sample_rows": rows},
             "step": f"one step = fwd+bwd of the first {rows} tokens of the layer (ms_per_step is its measured "
                     "median time)",
             "extrapolated_ms_per_full_batch": round(1000 * s * cfg.n_rows / rows, 1),
