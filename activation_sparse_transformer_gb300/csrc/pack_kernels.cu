@@ -10,9 +10,9 @@
 //   padding, in whole vectors; it stores the count and flags the row
 //   (row_fb = 1) when a tile overflows C.
 // fb_copy_kernel: dense rows of fallback rows -> fb_dense, their cells cleared.
-// unpack_run_kernel: a warp zero-fills a run of 32 cells of a row with
-//   coalesced 16-byte stores, then each lane writes its cell's entries (or a
-//   fallback row / dense tile is copied whole).
+// unpack_run_kernel: a warp builds a 2048-column run of a row in shared
+//   memory (zeros, then the cells' entries or dense tiles) and writes it out
+//   with coalesced 16-byte stores (a fallback row is copied whole).
 // check_cells_kernel / check_order_kernel: the format rules of a layout
 //   (cell contents, then the numbering of fallback rows or dense tiles),
 //   reported as a mask of broken rules.
@@ -119,7 +119,7 @@ __device__ __forceinline__ void nonzero_halves(const uint4& v, uint32_t (&t)[4])
 }
 
 template <int T>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 6)
     pack_cells_kernel(Layout L, const uint16_t* __restrict__ H, int64_t ldh) {
   __shared__ __align__(16) uint16_t st_vals[kWarps][kPackStage];
   __shared__ __align__(16) uint8_t st_idx[kWarps][kPackStage];
@@ -160,19 +160,32 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int cell = sg * cps + lane / G;  // the lane's cell within the chunk
     if (gl == G - 1 && cell < ncell) sc[cell] = incl;
     // this lane's non-zeros in ascending column (half h of word q is column
-    // 2q + h), each to the next slot while slots remain: predicated, no branch
-    const uint32_t w[4] = {v[sg].x, v[sg].y, v[sg].z, v[sg].w};
-    uint16_t* cv = sv + cell * C;
-    uint8_t* ci = si + cell * C;
-    int slot = incl - local;
+    // 2q + h), each to the next slot while slots remain.  At the layer's
+    // sparsity most lanes hold none, so only words with a non-zero half are
+    // visited.
+    if (local) {
+      const uint32_t w[4] = {v[sg].x, v[sg].y, v[sg].z, v[sg].w};
+      uint16_t* cv = sv + cell * C;
+      uint8_t* ci = si + cell * C;
+      int slot = incl - local;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const bool nz = (t[k >> 1] >> (15 + 16 * (k & 1))) & 1u;
-      if (nz && slot < C) {
-        cv[slot] = static_cast<uint16_t>((w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
-        ci[slot] = static_cast<uint8_t>(gl * 8 + k);
+      for (int q = 0; q < 4; ++q) {
+        if (t[q] == 0u) continue;
+        if (t[q] & 0x8000u) {
+          if (slot < C) {
+            cv[slot] = static_cast<uint16_t>(w[q] & 0xFFFFu);
+            ci[slot] = static_cast<uint8_t>(gl * 8 + 2 * q);
+          }
+          ++slot;
+        }
+        if (t[q] & 0x80000000u) {
+          if (slot < C) {
+            cv[slot] = static_cast<uint16_t>(w[q] >> 16);
+            ci[slot] = static_cast<uint8_t>(gl * 8 + 2 * q + 1);
+          }
+          ++slot;
+        }
       }
-      slot += nz ? 1 : 0;
     }
   }
   __syncwarp();
@@ -317,55 +330,109 @@ __global__ void fb_copy_kernel(Layout L, const uint16_t* __restrict__ H, int64_t
   }
 }
 
-// Cells -> dense, a warp per run of up to 32 consecutive cells of one row
-// (lane = cell).  The warp first writes the run's columns of H as zeros with
-// coalesced 16-byte stores, then (after a warp barrier that orders those
-// stores before the next ones) each lane writes its cell's few stored
-// entries.  A fallback row's run is copied from fb_dense instead, a dense tile
-// of the tile-granular variant from its pool slot.  Most of H is zero at the
-// layer's sparsity, so the kernel is a stream of 16-byte stores.
-__global__ void __launch_bounds__(kWarps * 32)
+// Cells -> dense.  A warp takes runs of kUnpackCols columns of one row
+// (grid-stride over (row, run)) and builds each run in its own shared-memory
+// buffer: zeros, then every cell's stored entries (or a dense tile of the
+// tile-granular variant, copied from its pool slot), then the run goes out
+// as coalesced 16-byte stores, so every byte of H is written exactly once
+// and no scattered partial-sector writes reach L2.  The row's routing word,
+// each lane's first cell's count and (C a multiple of 8) its first 8 slots
+// are requested together before any of them is used.  A fallback row's run
+// is copied from fb_dense (zeros past fb_cap: such a row is stored nowhere).
+constexpr int kUnpackCols = 2048;  // 4 KB of bf16 per warp
+
+__device__ __forceinline__ uint16_t slot_value8(const uint4& v, int sl) {
+  const uint32_t w = sl < 2 ? v.x : (sl < 4 ? v.y : (sl < 6 ? v.z : v.w));
+  return static_cast<uint16_t>((sl & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+__device__ __forceinline__ int slot_index8(const uint2& v, int sl) {
+  return static_cast<int>(((sl < 4 ? v.x : v.y) >> (8 * (sl & 3))) & 0xFFu);
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 5)
     unpack_run_kernel(Layout L, uint16_t* __restrict__ H, int64_t ldh) {
+  extern __shared__ uint4 urun4[];  // [kWarps][kUnpackCols / 8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int runs = (L.nt + 31) / 32;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (gw >= static_cast<int64_t>(L.N) * runs) return;
-  const int row = static_cast<int>(gw / runs);
-  const int t0 = static_cast<int>(gw % runs) * 32;
-  const int nc = min(32, L.nt - t0);
+  uint4* run4 = urun4 + warp * (kUnpackCols / 8);
+  uint16_t* run = reinterpret_cast<uint16_t*>(run4);
   const int T = L.T, C = L.C;
-  const int vecs = nc * T / 8;  // 16-byte vectors of the run
-  uint4* hrun = reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + static_cast<int64_t>(t0) * T);
-  const int fb = L.row_fb[row];
-  if (fb >= 0) {
-    if (fb < L.fb_cap) {
-      const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f +
-                                                        static_cast<int64_t>(t0) * T);
-      for (int i = lane; i < vecs; i += 32) hrun[i] = src[i];
-    } else {
-      // a fallback row past the capacity is stored nowhere: zeros
-      for (int i = lane; i < vecs; i += 32) hrun[i] = make_uint4(0, 0, 0, 0);
+  const bool c8 = (C & 7) == 0;
+  const bool tiles = L.hybrid == TWELL_HYBRID_TILES;
+  const int runs = (L.f + kUnpackCols - 1) / kUnpackCols;
+  const int64_t total = static_cast<int64_t>(L.N) * runs;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp; gw < total;
+       gw += static_cast<int64_t>(gridDim.x) * kWarps) {
+    const int row = static_cast<int>(gw / runs);
+    const int c0 = static_cast<int>(gw % runs) * kUnpackCols;
+    const int ncol = min(kUnpackCols, L.f - c0);  // a multiple of T (f % T == 0)
+    const int vecs = ncol / 8;
+    const int ncell = ncol / T;
+    const int64_t cell0 = static_cast<int64_t>(row) * L.nt + c0 / T;
+    uint4* hrun = reinterpret_cast<uint4*>(H + static_cast<int64_t>(row) * ldh + c0);
+    const int fb = L.row_fb[row];
+    int cnt0 = 0;
+    uint4 val0 = zero;
+    uint2 idx0 = make_uint2(0u, 0u);
+    if (lane < ncell) {
+      cnt0 = L.counts[cell0 + lane];
+      if (c8) {
+        val0 = *reinterpret_cast<const uint4*>(L.values + (cell0 + lane) * C);
+        idx0 = *reinterpret_cast<const uint2*>(L.idx + (cell0 + lane) * C);
+      }
     }
-    return;
-  }
-  const int64_t cell = static_cast<int64_t>(row) * L.nt + t0 + lane;
-  const int cnt = lane < nc ? L.counts[cell] : 0;
-  for (int i = lane; i < vecs; i += 32) hrun[i] = make_uint4(0, 0, 0, 0);
-  __syncwarp();
-  if (lane >= nc || cnt == 0) return;
-  uint16_t* hcell = H + static_cast<int64_t>(row) * ldh + static_cast<int64_t>(t0 + lane) * T;
-  if (L.hybrid == TWELL_HYBRID_TILES && cnt == TWELL_DENSE_TILE) {
-    const int64_t slot = static_cast<int64_t>(L.values[cell * C]) | (static_cast<int64_t>(L.idx[cell * C]) << 16);
-    if (slot < static_cast<int64_t>(L.fb_cap) * L.nt) {
-      const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + slot * T);
-      for (int i = 0; i < T / 8; ++i) reinterpret_cast<uint4*>(hcell)[i] = src[i];
+    if (fb >= 0) {  // uniform over the warp: the whole row is dense
+      if (fb < L.fb_cap) {
+        const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + static_cast<int64_t>(fb) * L.f + c0);
+        for (int i = lane; i < vecs; i += 32) hrun[i] = src[i];
+      } else {
+        for (int i = lane; i < vecs; i += 32) hrun[i] = zero;
+      }
+      continue;
     }
-    return;
-  }
-  // (bounded by C and T so that a malformed layout cannot write past the cell)
-  for (int s2 = 0; s2 < min(cnt, C); ++s2) {
-    const int j = L.idx[cell * C + s2];
-    if (j < T) hcell[j] = L.values[cell * C + s2];
+    for (int i = lane; i < vecs; i += 32) run4[i] = zero;
+    __syncwarp();
+    for (int c = lane; c < ncell; c += 32) {
+      const int64_t cell = cell0 + c;
+      int cnt = cnt0;
+      uint4 vv = val0;
+      uint2 ii = idx0;
+      if (c != lane) {
+        cnt = L.counts[cell];
+        if (c8 && cnt > 0) {
+          vv = *reinterpret_cast<const uint4*>(L.values + cell * C);
+          ii = *reinterpret_cast<const uint2*>(L.idx + cell * C);
+        }
+      }
+      if (cnt == 0) continue;
+      uint16_t* cr = run + c * T;
+      if (tiles && cnt == TWELL_DENSE_TILE) {
+        const int64_t slot = c8 ? (static_cast<int64_t>(vv.x & 0xFFFFu) | (static_cast<int64_t>(ii.x & 0xFFu) << 16))
+                                : (static_cast<int64_t>(L.values[cell * C]) | (static_cast<int64_t>(L.idx[cell * C]) << 16));
+        if (slot < static_cast<int64_t>(L.fb_cap) * L.nt) {
+          const uint4* src = reinterpret_cast<const uint4*>(L.fb_dense + slot * T);
+          for (int k = 0; k < T / 8; ++k) reinterpret_cast<uint4*>(cr)[k] = src[k];
+        }
+        continue;
+      }
+      // (indices bounded by T so that a malformed layout cannot write past the cell)
+      const int n = min(cnt, C);
+      int sl = 0;
+      if (c8) {
+        for (; sl < min(n, 8); ++sl) {
+          const int j = slot_index8(ii, sl);
+          if (j < T) cr[j] = slot_value8(vv, sl);
+        }
+      }
+      for (; sl < n; ++sl) {
+        const int j = L.idx[cell * C + sl];
+        if (j < T) cr[j] = L.values[cell * C + sl];
+      }
+    }
+    __syncwarp();
+    for (int i = lane; i < vecs; i += 32) hrun[i] = run4[i];
+    __syncwarp();  // every lane has read the run before the buffer is zeroed again
   }
 }
 
@@ -548,12 +615,13 @@ int launch_fb_copy(const uint16_t* H, int64_t ldh, const twell_t& L, cudaStream_
 
 int launch_unpack(const twell_t& L, uint16_t* H, int64_t ldh, cudaStream_t s) {
   if (L.n_rows <= 0) return TWELL_OK;
-  const int nt = L.d_ff / L.tile;
-  const int64_t warps = static_cast<int64_t>(L.n_rows) * ((nt + 31) / 32);
-  const int64_t blocks = (warps + kWarps - 1) / kWarps;
-  if (blocks > 0x7FFFFFFF) return TWELL_ERR_UNSUPPORTED;
+  const int64_t warps = static_cast<int64_t>(L.n_rows) * ((L.d_ff + kUnpackCols - 1) / kUnpackCols);
+  const size_t smem = sizeof(uint16_t) * kWarps * kUnpackCols;
+  const int per_sm = std::max(1, resident_ctas_per_sm(reinterpret_cast<const void*>(unpack_run_kernel),
+                                                      kWarps * 32, smem));
+  const int64_t blocks = std::min<int64_t>((warps + kWarps - 1) / kWarps, static_cast<int64_t>(per_sm) * sm_count());
   LaunchScope ls(TWELL_KERNEL_UNPACK, s);
-  unpack_run_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(flat(L), H, ldh);
+  unpack_run_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, smem, s>>>(flat(L), H, ldh);
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -485,6 +485,18 @@ def bench_ours(args, rank, world, local):
         conv[name] = {"call_ms": round(med(ms_list), 4), "kernel_us_per_call": round(1000.0 * k_ms / prof_steps, 2),
                       "launches_per_call": round(n_l / prof_steps, 2)}
     same = all(torch.equal(getattr(packed, k), getattr(packed2, k)) for k in ("values", "idx", "counts"))
+    # plain torch streams over the same bytes as dense H, under the same scrub:
+    # on this GPU a write-only stream runs at about half the copy bandwidth, so
+    # unpack (67 MB written) is compared with a fill and pack (67 MB read) with
+    # a reduction
+    red = torch.empty((), dtype=torch.float32, device=dev)
+    hwords = Hbuf.view(-1).view(torch.float32)  # finite: pairs of non-negative finite bf16
+    stream_ref = {"write_stream_us": round(1000.0 * med(timed(lambda: Hbuf.zero_(), max(args.steps, 20))), 2),
+                  "read_stream_us": round(1000.0 * med(timed(lambda: torch.amax(hwords, dim=0, out=red),
+                                                             max(args.steps, 20))), 2),
+                  "bytes": int(Hbuf.numel() * Hbuf.element_size())}
+    conv["unpack"]["vs_write_stream"] = round(stream_ref["write_stream_us"] / conv["unpack"]["kernel_us_per_call"], 3)
+    conv["pack"]["vs_read_stream"] = round(stream_ref["read_stream_us"] / conv["pack"]["kernel_us_per_call"], 3)
     del packed2, Hbuf
 
     # ---- energy per token: the GPU's cumulative energy counter (NVML, mJ)
@@ -645,7 +657,10 @@ def bench_ours(args, rank, world, local):
                     "note": "no L2 scrub between calls; the headline value scrubs L2 (cold)"},
         "dense_ffn_fwd": {"tokens_per_s": round(world * N / (med(dense_ms) * 1e-3), 1), "ms": round(med(dense_ms), 4),
                           "note": "same tcgen05 GEMM, no sparsity: reported baseline"},
-        "format_conversion": {**conv, "round_trip_identical": bool(same),
+        "format_conversion": {**conv, "round_trip_identical": bool(same), "torch_streams": {
+            **stream_ref, "how": "torch fill (Hbuf.zero_) and fp32 max-reduction over a dense-H-sized buffer, L2 "
+                                 "scrubbed before each; vs_*_stream = that stream's time / the conversion's kernel "
+                                 "time"},
                               "note": "twell_unpack of this layer's packed H into dense bf16 [N, d_ff], then "
                                       "twell_pack of that dense H; L2 scrubbed between calls"},
         "kernels": per_kernel,
