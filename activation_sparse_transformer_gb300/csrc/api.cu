@@ -287,9 +287,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
     if ((expr) != cudaSuccess) return TWELL_ERR_CUDA;  \
   } while (0)
 
-int reset_words(const twell_t* L, cudaStream_t s) {
+// status = 0 and every row_fb word = `row_fill` repeated in its four bytes
+// (0x00: 0, 0xFF: -1)
+int reset_words(const twell_t* L, cudaStream_t s, int row_fill = 0) {
   TW_CUDA(cudaMemsetAsync(L->status, 0, sizeof(int32_t), s));
-  if (L->n_rows > 0) TW_CUDA(cudaMemsetAsync(L->row_fb, 0, sizeof(int32_t) * static_cast<size_t>(L->n_rows), s));
+  if (L->n_rows > 0)
+    TW_CUDA(cudaMemsetAsync(L->row_fb, row_fill, sizeof(int32_t) * static_cast<size_t>(L->n_rows), s));
   return TWELL_OK;
 }
 
@@ -428,7 +431,9 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     // the up-projection's CTA 0 zeroes row_fb and the arrival counters
     TW_CUDA(cudaMemsetAsync(H->status, 0, sizeof(int32_t), s));
   } else {
-    TW_TRY(reset_words(H, s));
+    // rows not flagged by the up-projection read -1 (the tile-granular
+    // variant counts dense tiles from 0)
+    TW_TRY(reset_words(H, s, tiles ? 0 : 0xFF));
     if (arrivals) TW_CUDA(cudaMemsetAsync(arrivals, 0, sizeof(int32_t) * (64 + kSpmmMaxArrivals), s));
   }
   if (swap) {
@@ -459,17 +464,21 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       return launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
                          row_counter, s);
     }
-    TW_TRY(launch_route(*H, s));
   }
   {
-    // the dense-fallback rows (assembly or copy + tensor-core down-projection)
-    // run on a second stream while the gather-SpMM handles the TwELL rows
+    // the dense-fallback rows (routing, assembly or copy, tensor-core
+    // down-projection) run on a second stream while the gather-SpMM handles
+    // the TwELL rows: it skips every row with row_fb >= 0, which holds for a
+    // flagged row before routing (1) and after it (its slot), so it does not
+    // wait for the routing scan
     AuxFork fork(s);
     TW_TRY(fork.status());
-    if (swap)
+    if (swap) {
       TW_TRY(launch_fb_copy(Hd, d_ff, *H, fork.aux()));
-    else
+    } else {
+      TW_TRY(launch_route(*H, fork.aux(), -1));
       TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
+    }
     TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
     TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
                        row_counter, s));

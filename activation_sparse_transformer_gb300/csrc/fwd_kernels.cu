@@ -41,13 +41,16 @@ Layout flat(const twell_t& L) {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteRows = 8;  // rows per thread per pass
 
-// Rows variant: row_fb holds 0/1 overflow flags on entry and -1 / fallback
-// slot on exit.  Tiles variant: row_fb holds each row's number of dense tiles
+// Rows variant: row_fb holds overflow flags on entry (1 for a flagged row,
+// `empty` for the others: 0 after twell_pack, -1 in the forward) and -1 /
+// fallback slot on exit.  With empty = -1 a reader that only asks "is this a
+// fallback row" (row_fb >= 0) gets the same answer before, during and after
+// routing, so the forward's gather-SpMM need not wait for it.  Tiles variant: row_fb holds each row's number of dense tiles
 // on entry and, on exit, the pool slot of the row's first dense tile (-1 for
 // rows without one); n_fb counts the dense tiles.  One CTA: an exclusive
 // block scan gives the slots in ascending row order, so the result is
 // deterministic.
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int32_t empty) {
   __shared__ int warp_tot[kRouteThreads / 32];
   __shared__ int base_s;
   grid_dependency_wait();
@@ -63,8 +66,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L) {
 #pragma unroll
     for (int i = 0; i < kRouteRows; ++i) {
       const int r = r0 + i;
-      const int v = r < L.N ? L.row_fb[r] : 0;
-      cnt[i] = tiles ? v : (v != 0 ? 1 : 0);
+      const int v = r < L.N ? L.row_fb[r] : (tiles ? 0 : empty);
+      cnt[i] = tiles ? v : (v != empty ? 1 : 0);
       local += cnt[i];
     }
     int incl = local;
@@ -324,9 +327,10 @@ int launch_tile_assign(const twell_t& L, const uint16_t* H, int64_t ldh, const u
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-int launch_route(const twell_t& L, cudaStream_t s) {
+int launch_route(const twell_t& L, cudaStream_t s, int32_t empty) {
   LaunchScope ls(TWELL_KERNEL_ROUTE, s);
-  if (launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, flat(L)) != cudaSuccess) return TWELL_ERR_CUDA;
+  if (launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, flat(L), empty) != cudaSuccess)
+    return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 

@@ -206,7 +206,8 @@ int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_
                              int32_t* zero0 = nullptr, int n_zero0 = 0, int32_t* zero1 = nullptr, int n_zero1 = 0);
 
 // forward helpers (fwd_kernels.cu)
-int launch_route(const twell_t& L, cudaStream_t s);
+// rows variant: row_fb holds 1 for a flagged row and `empty` for the others
+int launch_route(const twell_t& L, cudaStream_t s, int32_t empty = 0);
 // tile-granular hybrid: dense tiles per flagged row (before launch_route), then
 // pool slots, pool copies (from H, or from the spill buffer when H is null)
 // and the cells' slot numbers (after it)

@@ -257,7 +257,8 @@ def test_profile_timeline_of_a_forward(tw):
     tw.twell_profile_reset()
     assert [e["kernel"] for e in tl] == ["up_pack", "route", "fb_assemble", "fb_down", "fb_down", "spmm"]
     main = int(stream.cuda_stream)
-    assert [e["stream"] == main for e in tl] == [True, True, False, False, False, True]
+    # routing and the fallback rows on the second stream, the gather-SpMM on the caller's
+    assert [e["stream"] == main for e in tl] == [True, False, False, False, False, True]
     assert tl[0]["start_ms"] == 0.0
     for e in tl:
         assert e["end_ms"] >= e["start_ms"] >= 0.0
@@ -265,4 +266,5 @@ def test_profile_timeline_of_a_forward(tw):
         seq = [e for e in tl if (e["stream"] == main) == s]
         assert all(a["end_ms"] <= c["start_ms"] + 1e-6 for a, c in zip(seq, seq[1:]))
     assert tl[1]["start_ms"] >= tl[0]["end_ms"] - 1e-6          # routing after the up-projection
-    assert tl[2]["start_ms"] >= tl[1]["end_ms"] - 1e-6          # the second stream forks after routing
+    assert tl[2]["start_ms"] >= tl[1]["end_ms"] - 1e-6          # assembly after routing
+    assert tl[5]["start_ms"] >= tl[0]["end_ms"] - 1e-6          # the SpMM after the up-projection only
