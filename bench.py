@@ -7,9 +7,11 @@ tensor cores, gather-SpMM down-projection) followed by twell_ffn_bwd (SDDMM
 with the L1 term, dX gather, unit-major weight gradients), on the 1B-model FFN
 shape N=4096, d_model=2048, d_ff=8192, T=128, C=8 with synthetic seeded inputs.
 
-With N GPUs (torchrun, one rank per GPU) every rank runs its own batch of the
-same shape (weak scaling, no data-path collective); the job's time per step is
-the slowest rank's and `value` counts the tokens of all ranks.
+With N GPUs (torchrun, one rank per GPU; `--gpus N` starts the ranks itself)
+every rank holds the same layer and runs its own batch of the same shape (weak
+scaling); the step ends with the data-parallel exchange, an all-reduce (sum)
+of dW_in^T, dW_down and db.  The job's time per step is the slowest rank's
+and `value` counts the tokens of all ranks.
 
 Prints one JSON line.  `value` is tokens/s of the step with inputs resident in
 HBM (L2 flushed between steps by writing a 2x-L2 buffer); `e2e` is the same
