@@ -782,9 +782,10 @@ def bench_train_memory(tw, dev, args):
     }
 
 
-def bench_next(args):
-    """Forward-only measurements of the next shapes (opt-in, one JSON line each):
-    the gated (Llama-style) layer and the decode-shaped sweep."""
+def next_shapes(args, steps):
+    """Forward-only measurements of the next shapes, one result dict each (a
+    generator): the gated (Llama-style) layer, the decode-shaped sweep and the
+    1B forward with row- and tile-granular fallback, `steps` timed calls each."""
     import numpy as np
     import torch
 
@@ -859,11 +860,11 @@ def bench_next(args):
         if decode:
             copies = [tuple(t.clone() for t in (X, Wi, b, Wd)) for _ in range(3)]
             rot = [(lambda c=c: tw.twell_ffn_fwd(c[0], c[1], c[2], c[3], packed, Y, ws, stream)) for c in copies]
-        ms_flush = timed(fn, args.steps)
-        ms = timed(fn, args.steps, rotate=rot) if decode else ms_flush
+        ms_flush = timed(fn, steps)
+        ms = timed(fn, steps, rotate=rot) if decode else ms_flush
         tw.twell_profile_reset()
         tw.twell_profile_enable(True)
-        timed(fn, min(args.steps, 20), rotate=rot)
+        timed(fn, min(steps, 20), rotate=rot)
         tw.twell_profile_enable(False)
         kernels = {}
         for name in tw.KERNELS:
@@ -883,7 +884,7 @@ def bench_next(args):
                 else:
                     tw.twell_ffn_fwd(c[0], c[1], c[2], c[3], packed, Y, ws, cap)
             graphs.append(graph)
-        ms_graph = timed(graphs[0].replay, args.steps, rotate=[g.replay for g in graphs] if decode else None)
+        ms_graph = timed(graphs[0].replay, steps, rotate=[g.replay for g in graphs] if decode else None)
         roof_wo_us = None
         if cfg.gated:
             flops = 2.0 * 2 * N * d * f
@@ -902,11 +903,11 @@ def bench_next(args):
             # the layer specification's byte list leaves W_in^T out; reported beside the honest count
             roof_wo_us = (byts - f * d * 2) / (peaks["hbm_gbs"] * 1e9) * 1e6
             del H
-        print(json.dumps({
+        yield {
             "metric": f"sparse-FFN forward tokens/s ({cfg.name})", "value": round(N / (ms * 1e-3), 1),
             "unit": "tokens/s", "ms": round(ms, 4), "ms_graph": round(ms_graph, 4),
             "ms_l2_scrubbed": round(ms_flush, 4),
-            "tokens_per_s_graph": round(N / (ms_graph * 1e-3), 1), "n_gpus": 1, "steps": args.steps,
+            "tokens_per_s_graph": round(N / (ms_graph * 1e-3), 1), "n_gpus": 1, "steps": steps,
             "warmup": args.warmup,
             "dtype": "bf16", "data": "synthetic (seeded, see synth/)",
             "config": {"workload": cfg.name, "n_rows": N, "d_model": d, "d_ff": f, "tile": T, "cap": C,
@@ -920,9 +921,28 @@ def bench_next(args):
             "roofline": {"bound": bound, "time_us": round(roof_us, 2), "frac": round(roof_us / (ms * 1e3), 4),
                          "frac_graph": round(roof_us / (ms_graph * 1e3), 4), "peak_source": peak_src,
                          "time_us_without_w_in": round(roof_wo_us, 2) if roof_wo_us else None},
-        }), flush=True)
+        }
         del X, Wi, b, Wd, packed, Y, ws, graph, graphs, copies, rot
         torch.cuda.empty_cache()
+
+
+def bench_next(args):
+    """`--next`: one JSON line per next shape."""
+    for res in next_shapes(args, args.steps):
+        print(json.dumps(res), flush=True)
+
+
+def next_summary(args, steps=50):
+    """The next shapes in brief, for the main bench line."""
+    out = {}
+    for res in next_shapes(args, steps):
+        r = res["roofline"]
+        out[res["config"]["workload"]] = {"ms": res["ms"], "ms_graph": res["ms_graph"], "roofline_us": r["time_us"],
+                                          "bound": r["bound"], "frac": r["frac"], "frac_graph": r["frac_graph"]}
+    out["how"] = (f"forward only, {steps} timed calls each (median); decode shapes rotate 3 device copies of the "
+                  "weights with no scrub, the others scrub L2; frac_graph = the call replayed as a CUDA graph; "
+                  "full lines with `bench.py --next`")
+    return out
 
 
 def cpu_sample_rows(default):
@@ -941,12 +961,10 @@ def oracle_step(base, dY, rows, cfg, lam):
     oracle.grad_weights(X, base["W_down"], H, dY[:rows], lam)
 
 
-def cpu_baseline(rows=None):
-    import numpy as np
-
+def cpu_baseline(config="1b", rows=None):
     import oracle
     import synth
-    cfg = synth.CONFIGS[args.config]
+    cfg = synth.CONFIGS[config]
     base = synth.make_ffn_inputs(cfg)
     dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=cfg.seed + 77)
     rows = rows or cpu_sample_rows(1536)  # ~10-15 s of the oracle on the host cores
@@ -956,7 +974,7 @@ def cpu_baseline(rows=None):
     el = time.perf_counter() - t
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(rows / el, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fwd+bwd of the first {rows} tokens of the 1B-shape layer as one batch "
+            "sample": f"fwd+bwd of the first {rows} tokens of the {cfg.name} layer as one batch "
                       f"(plain C fp32 loops, OpenMP over {cores} threads), {el:.1f} s"}
 
 
@@ -1038,6 +1056,8 @@ def main():
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
     ap.add_argument("--no-memory", action="store_true",
                     help="skip the training-shape peak-memory comparison against the dense step")
+    ap.add_argument("--no-next", action="store_true",
+                    help="leave the next shapes' summary (gated layer, decode sweep, tile routing) out of the line")
     ap.add_argument("--min-window", type=float, default=1.0,
                     help="repeat the K-step timed loop until the timed window spans this many seconds")
     ap.add_argument("--timeline", action="store_true",
@@ -1067,11 +1087,13 @@ def main():
         print(json.dumps(res), flush=True)
     elif rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline()
+            res["cpu_baseline"] = cpu_baseline(args.config)
             try:
                 res["cpu_baseline"]["single_thread_pr1"] = cpu_single_thread_pr1()
             except (subprocess.SubprocessError, ValueError, IndexError) as exc:
                 res["cpu_baseline"]["single_thread_pr1"] = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+        if not args.no_next and world == 1 and args.config == "1b":
+            res["next_shapes"] = next_summary(args)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -44,3 +44,12 @@ def test_workload_names():
         "1B-scale FFN fwd+bwd: N=4096 d_model=2048 d_ff=8192 T=128 C=8")
     name = bench.workload_name(synth.CONFIGS["train"])
     assert "N=8192" in name and "1% rows at 20%" in name and "lambda 0.0001" in name
+
+
+def test_cpu_baseline_leg_runs():
+    """The bench's CPU leg (the oracle timed on the host cores) on a few rows
+    of the small layer: the same call the bench line makes, run here so a
+    broken leg fails on CPU."""
+    line = bench.cpu_baseline("pr1", rows=16)
+    assert line["kind"] == "oracle" and line["unit"] == bench.UNIT and line["value"] > 0
+    assert line["cores"] >= 1 and "pr1 layer" in line["sample"]
