@@ -474,14 +474,17 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     AuxFork fork(s);
     TW_TRY(fork.status());
     if (swap) {
+      // small batch: the fallback rows' dense h goes to fb_dense (an output of
+      // the layout), and their rows of Y are gathered by the SpMM from the
+      // dense h the pack pass kept, beside the TwELL rows: no fallback GEMM
       TW_TRY(launch_fb_copy(Hd, d_ff, *H, fork.aux()));
     } else {
       TW_TRY(launch_route(*H, fork.aux(), -1));
       TW_TRY(launch_fb_assemble(*H, spill, spill_count, w.spill_cap, fork.aux()));
+      TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
     }
-    TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
     TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
-                       row_counter, s));
+                       row_counter, s, swap ? Hd : nullptr));
     TW_TRY(fork.join());
   }
   return TWELL_OK;

@@ -26,7 +26,9 @@
 // consecutive ranges (each warp flattens and streams only its range); each
 // range's fp32 sums go to a partial buffer, and the last CTA to finish among
 // the ranges of a (row block, column block) adds them in range order (an
-// arrival counter, no waiting).
+// arrival counter, no waiting).  A small batch's fallback rows are gathered
+// here too, from the dense h its pack pass keeps, so no tensor-core fallback
+// GEMM and reduction follow on the second stream.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -53,6 +55,9 @@ struct SpmmArgs {
   int32_t* row_counter;   // zeroed word: rows handed out past the first gridDim.x, else null (fixed stride)
   int N, d, nt, T, C;
   int32_t* status;
+  // small batches: every row's h as dense bf16 [N][nt * T]; the fallback rows
+  // (row_fb >= 0) are then gathered from it here instead of by the fallback path
+  const uint16_t* dense_h;
 };
 
 // Entry of the per-warp list.  bf16 values: one word, hidden unit j in the low
@@ -119,13 +124,38 @@ __device__ __forceinline__ void stream_list(const SpmmArgs& a, const uint16_t* _
 
 // Sum of one row's stored entries in tiles [t_beg, t_end) times the W rows
 // they name, for this lane's 8 columns starting at c0 (the whole warp calls it
-// for one row; inactive lanes only help flatten).
+// for one row; inactive lanes only help flatten).  With dense = true the row
+// is a fallback row of a small batch: its non-zeros come from the dense h
+// (a.dense_h) instead of the cells, in ascending column order, streamed every
+// time the list (max_entries) fills.
 template <typename VT>
 __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t* __restrict__ W, RowEntry<VT>* list,
                                               int lane, int row, int c0, bool active, int t_beg, int t_end,
-                                              float (&acc)[8]) {
+                                              float (&acc)[8], bool dense = false, int max_entries = 0) {
   const VT* vals = static_cast<const VT*>(a.values);
   const int64_t cell0 = static_cast<int64_t>(row) * a.nt;
+
+  if (dense) {
+    const uint16_t* hrow = a.dense_h + static_cast<int64_t>(row) * a.nt * a.T;
+    int n = 0;
+    for (int c = t_beg * a.T; c < t_end * a.T; c += 32) {  // T is a multiple of 32
+      if (n + 32 > max_entries) {
+        __syncwarp();
+        if (active) stream_list<VT>(a, W + c0, list, n, acc);
+        __syncwarp();  // the list is free again
+        n = 0;
+      }
+      const uint16_t v = hrow[c + lane];
+      const bool nz = (v & 0x7FFFu) != 0;
+      const unsigned b = __ballot_sync(0xffffffffu, nz);
+      if (nz) list[n + __popc(b & ((1u << lane) - 1u))] = RowEntry<VT>::make(c + lane, from_bf16<VT>(v));
+      n += __popc(b);
+    }
+    __syncwarp();
+    if (active) stream_list<VT>(a, W + c0, list, n, acc);
+    __syncwarp();  // the list is rewritten by the warp's next item
+    return;
+  }
 
   // ---- flatten: tiles in order, 32 per round (dense tiles come after)
   int total = 0;
@@ -200,18 +230,21 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp; it < items;
          it += static_cast<int64_t>(gridDim.x) * kWarps) {
       const int row = static_cast<int>(it / cbs);
-      if (a.row_fb[row] >= 0) continue;  // written by the fallback path, which may run concurrently
+      const bool fb_row = a.row_fb[row] >= 0;
+      // written by the fallback path, which may run concurrently (unless gathered from dense h here)
+      if (fb_row && !a.dense_h) continue;
       const int c0 = static_cast<int>(it % cbs) * 256 + lane * 8;
       const bool active = c0 < a.d;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      row_block_sum<VT>(a, W, list, lane, row, c0, active, 0, a.nt, acc);
+      row_block_sum<VT>(a, W, list, lane, row, c0, active, 0, a.nt, acc, fb_row, max_entries);
       if (active) *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
     }
     return;
   }
 
   const int row = blockIdx.x * kWarps + warp;
-  const bool work = row < a.N && a.row_fb[row] < 0;
+  const bool fb_row = row < a.N && a.row_fb[row] >= 0;
+  const bool work = row < a.N && (!fb_row || a.dense_h);
   const int c0 = blockIdx.y * 256 + lane * 8;
   const bool active = work && c0 < a.d;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -220,7 +253,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     const int per = (a.nt + gridDim.z - 1) / gridDim.z;
     const int t_beg = min(a.nt, static_cast<int>(blockIdx.z) * per);
     const int t_end = min(a.nt, t_beg + per);
-    row_block_sum<VT>(a, W, list, lane, row, c0, active, t_beg, t_end, acc);
+    row_block_sum<VT>(a, W, list, lane, row, c0, active, t_beg, t_end, acc, fb_row, max_entries);
   }
 
   // ---- tile ranges: store this range's sums; the CTA that finishes last among
@@ -336,8 +369,8 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   if (a.N <= 0) return TWELL_OK;
   if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   if (a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;  // hidden unit fits the entry's 16 bits
-  // a dense tile's non-zeros pass through the same list
-  const int max_entries = a.pool ? std::max(a.nt * a.C, a.T) : a.nt * a.C;
+  // a dense tile's (or a small batch's dense row's) non-zeros pass through the same list
+  const int max_entries = (a.pool || a.dense_h) ? std::max(a.nt * a.C, a.T) : a.nt * a.C;
   const size_t smem = static_cast<size_t>(kWarps) * max_entries * sizeof(RowEntry<VT>);
   if (smem > kMaxDynSmem) return TWELL_ERR_UNSUPPORTED;
   auto kern = spmm_row_kernel<VT>;
@@ -354,7 +387,7 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   }
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
-  if (nsplit == 1 && !a.pool) {
+  if (nsplit == 1 && !a.pool && !a.dense_h) {
     // a CTA per row: one shared flatten for all column blocks; persistent, four
     // CTAs per SM (the register limit)
     auto rk = spmm_rowcta_kernel<VT>;
@@ -392,7 +425,8 @@ int spmm_nsplit(int n_rows, int d_model) {
 }
 
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                int32_t* arrivals, int32_t* row_counter, cudaStream_t s) {
+                int32_t* arrivals, int32_t* row_counter, cudaStream_t s, const uint16_t* dense_h) {
+  if (dense_h && (L.hybrid == TWELL_HYBRID_TILES || L.tile % 32 != 0)) return TWELL_ERR_UNSUPPORTED;
   SpmmArgs a{L.values,
              L.idx,
              L.counts,
@@ -407,14 +441,15 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
              L.d_ff / L.tile,
              L.tile,
              L.cap,
-             L.status};
+             L.status,
+             dense_h};
   return launch_spmm_rows<uint16_t>(a, W_down, nsplit, TWELL_KERNEL_SPMM, s);
 }
 
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int32_t* row_counter, int kernel_id, cudaStream_t s) {
   SpmmArgs a{vals,     L.idx,   L.counts, L.row_fb,         out,    nullptr, nullptr, nullptr, row_counter,
-             L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status};
+             L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status, nullptr};
   return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
 }
 

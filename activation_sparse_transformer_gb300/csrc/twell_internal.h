@@ -225,7 +225,8 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* s
 constexpr int kSpmmMaxArrivals = 1024;
 int spmm_nsplit(int n_rows, int d_model);
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                int32_t* arrivals, int32_t* row_counter, cudaStream_t s);
+                int32_t* arrivals, int32_t* row_counter, cudaStream_t s,
+                const uint16_t* dense_h = nullptr);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int32_t* row_counter, int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
