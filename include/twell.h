@@ -152,8 +152,9 @@ TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_st
  * added in order; results agree with the large-batch path up to fp32
  * summation order (bit for bit on inputs whose partial sums are exact).
  * More fallback rows than fb_cap: the status word reports
- * TWELL_ERR_FALLBACK_OVERFLOW, the rows past fb_cap are stored nowhere (their
- * cells are emptied) and their rows of Y are left unwritten.
+ * TWELL_ERR_FALLBACK_OVERFLOW and the rows past fb_cap are stored nowhere
+ * (their cells are emptied); their rows of Y are left unwritten, except in
+ * the small-batch path, whose gather takes every row's h from its dense copy.
  * workspace: device, >= twell_fwd_workspace_bytes(...) bytes (always > 0),
  * 256-byte aligned; its contents need no initialisation and nothing in it is
  * needed once the call's work on the stream has finished, so one buffer can

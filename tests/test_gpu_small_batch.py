@@ -68,3 +68,23 @@ def test_small_batch_fallback_overflow_status(tw):
     p, Y, rc = run_fwd(tw, torch, inp, 64, 4, 2)
     assert rc == -6
     assert int(p.n_fb[0].item()) > 2
+
+
+def test_small_batch_overflow_rows_keep_their_y(tw):
+    """More fallback rows than fb_cap in a small batch (integer layer, exact
+    sums): the status reports the overflow, the packed layout is the
+    oracle's packing with that capacity (rows past fb_cap stored nowhere, their
+    cells empty), and every row of Y -- those past fb_cap included, which the
+    small-batch gather takes from the dense h -- is the exact product."""
+    import torch
+    N, d, f, T, C, fb_cap = 16, 256, 1024, 64, 4, 2
+    inp = synth.make_integer_inputs(N, d, f, seed=21, sparsity=0.85)
+    full = oracle.forward(inp["X"], inp["W_inT"], inp["b"], inp["W_down"], T, C, N)
+    assert np.abs(full["Y"]).max() < 2 ** 24
+    p, Y, rc = run_fwd(tw, torch, inp, T, C, fb_cap)
+    assert rc == -6, tw.status_string(rc)   # TWELL_ERR_FALLBACK_OVERFLOW
+    ref = check_packing_of(p, full["H"], T, C, fb_cap)
+    assert ref["n_fb"] > fb_cap
+    past = [r for r in range(N) if ref["row_fb"][r] >= fb_cap]
+    assert past and all(not from_dev_bits(p.counts)[r].any() for r in past)
+    assert np.array_equal(from_dev_bits(Y), full["Y_bf16"])
