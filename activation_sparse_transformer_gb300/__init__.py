@@ -45,6 +45,7 @@ EXPORTED = [
     "twell_profile_timeline",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
     "twell_selftest_wait_timeout", "twell_check_format", "twell_dense_ffn_bwd", "twell_dense_bwd_workspace_bytes",
+    "twell_bwd_tiles_workspace_bytes",
 ]
 
 
@@ -84,6 +85,7 @@ def load_library() -> ctypes.CDLL:
         "twell_fwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
         "twell_ffn_bwd": (ctypes.c_int, [P, P, P, L, I32, P, ctypes.c_float, P, P, P, P, P, SZ, P]),
         "twell_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+        "twell_bwd_tiles_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
         "twell_dense_ffn_fwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, P, P, P]),
         "twell_read_status": (ctypes.c_int, [L, P]),
         "twell_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -221,8 +223,11 @@ def fwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
     return int(load_library().twell_fwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
 
 
-def bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
-    return int(load_library().twell_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
+def bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap, hybrid=None) -> int:
+    """Workspace of twell_ffn_bwd; hybrid=HYBRID_TILES for a tile-granular layout."""
+    lib = load_library()
+    fn = lib.twell_bwd_tiles_workspace_bytes if hybrid == HYBRID_TILES else lib.twell_bwd_workspace_bytes
+    return int(fn(n_rows, d_model, d_ff, tile, cap, fb_cap))
 
 
 def _need_layer(n, d, f, W_inT, b, W_down, Y) -> None:

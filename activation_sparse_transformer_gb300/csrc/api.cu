@@ -518,7 +518,7 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
   TW_TRY(check_layout(H));
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
-  if (H->hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
+  const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
   // the unit-major lists address the stored entries with 32-bit positions
   if (static_cast<int64_t>(H->n_rows) * (H->d_ff / H->tile) * H->cap > INT32_MAX) return TWELL_ERR_UNSUPPORTED;
   TW_TRY(check_dense(X));
@@ -529,13 +529,39 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
   TW_TRY(check_dense(dW_inT));
   TW_TRY(check_dense(dW_down));
   TW_TRY(check_dense(db));
-  const size_t need = twell_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  const size_t base = twell_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  const size_t need =
+      tiles ? twell_bwd_tiles_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap) : base;
   if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
   BwdWorkspace ws{};
   bwd_workspace_layout(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap, &ws, workspace);
-  return launch_bwd(X, W_inT, W_down, *H, dY, l1_lambda, dX, dW_inT, dW_down, db, d_model, ws,
-                    reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!tiles)
+    return launch_bwd(X, W_inT, W_down, *H, dY, l1_lambda, dX, dW_inT, dW_down, db, d_model, ws, s);
+  // tile-granular layout: the backward of its row view, in which every row
+  // holding a dense tile is a fallback row with its dense h (the layer's
+  // gradients do not depend on how h is stored)
+  uint8_t* v = static_cast<uint8_t*>(workspace) + base;
+  twell_t V = *H;
+  V.hybrid = TWELL_HYBRID_ROWS;
+  V.row_fb = reinterpret_cast<int32_t*>(v);
+  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H->n_rows, 1)));
+  V.fb_rows = reinterpret_cast<int32_t*>(v);
+  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H->fb_cap, 1)));
+  V.n_fb = reinterpret_cast<int32_t*>(v);
+  v += 256;
+  V.fb_dense = reinterpret_cast<uint16_t*>(v);
+  TW_TRY(launch_tile_row_view(*H, V, s));
+  return launch_bwd(X, W_inT, W_down, V, dY, l1_lambda, dX, dW_inT, dW_down, db, d_model, ws, s, true);
+}
+
+size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
+                                       int32_t fb_cap) {
+  const size_t base = twell_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap);
+  return base + align256(sizeof(int32_t) * static_cast<size_t>(std::max(n_rows, 1))) +
+         align256(sizeof(int32_t) * static_cast<size_t>(std::max(fb_cap, 1))) + 256 +
+         align256(sizeof(uint16_t) * static_cast<size_t>(std::max(fb_cap, 0)) * static_cast<size_t>(d_ff));
 }
 
 int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,

@@ -70,11 +70,14 @@ __device__ __forceinline__ int cell_idx8(uint2 w, int sl) {
   return static_cast<int>((v >> (8 * sl)) & 0xFFu);
 }
 
+// skip_fb (a row view of a tile-granular layout, else null): rows with
+// skip_fb[r] >= 0 are the view's fallback rows, whose cells (which may name
+// dense tiles) take no part in the lists.
 template <bool kC8>
 __global__ void __launch_bounds__(kListWarps * 32)
     unit_lists_kernel(Layout L, const float* __restrict__ dz_cells, int32_t* __restrict__ col_beg,
                       int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
-                      float* __restrict__ col_dz) {
+                      float* __restrict__ col_dz, const int32_t* __restrict__ skip_fb) {
   extern __shared__ int32_t lsm[];
   grid_dependency_wait();
   const int T = L.T, t = blockIdx.x;
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(kListWarps * 32)
 #pragma unroll
     for (int j = 0; j < kListChunk; ++j) {
       const int r = (c0 + j) * 32 + lane;
-      const bool ok = c0 + j < b1 && r < L.N;
+      const bool ok = c0 + j < b1 && r < L.N && (!skip_fb || skip_fb[r] < 0);
       const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
       cnt[j] = ok ? L.counts[cell] : 0;
       if (kC8) iw[j] = ok ? *reinterpret_cast<const uint2*>(L.idx + cell * 8) : make_uint2(0u, 0u);
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kListWarps * 32)
 #pragma unroll
     for (int j = 0; j < kListChunk; ++j) {
       const int r = (c0 + j) * 32 + lane;
-      const bool ok = c0 + j < b1 && r < L.N;
+      const bool ok = c0 + j < b1 && r < L.N && (!skip_fb || skip_fb[r] < 0);
       const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
       cnt[j] = ok ? L.counts[cell] : 0;
       if (kC8) iw[j] = ok ? *reinterpret_cast<const uint2*>(L.idx + cell * 8) : make_uint2(0u, 0u);
@@ -412,7 +415,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
 
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& Lh,
                const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
-               int d, const BwdWorkspace& ws, cudaStream_t s) {
+               int d, const BwdWorkspace& ws, cudaStream_t s, bool row_view) {
   const Layout L = flat(Lh);
   const int f = Lh.d_ff;
   const int N = Lh.n_rows;
@@ -469,7 +472,7 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     LaunchScope ls(TWELL_KERNEL_AUX, s);
     auto lk = Lh.cap == 8 ? unit_lists_kernel<true> : unit_lists_kernel<false>;
     if (launch_pdl(lk, dim3(f / Lh.tile), dim3(kListWarps * 32), lsm, s, L, ws.dz_cells, ws.col_beg, ws.col_end,
-                   ws.col_rows, ws.col_h, ws.col_dz) != cudaSuccess)
+                   ws.col_rows, ws.col_h, ws.col_dz, row_view ? Lh.row_fb : nullptr) != cudaSuccess)
       return TWELL_ERR_CUDA;
   }
   TW_CHECK_LAUNCH();

@@ -50,7 +50,7 @@ constexpr int kRouteRows = 8;  // rows per thread per pass
 // rows without one); n_fb counts the dense tiles.  One CTA: an exclusive
 // block scan gives the slots in ascending row order, so the result is
 // deterministic.
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int32_t empty) {
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int32_t empty, int clear_past) {
   __shared__ int warp_tot[kRouteThreads / 32];
   __shared__ int base_s;
   grid_dependency_wait();
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int32_t 
         L.row_fb[r] = slot;
         if (slot < L.fb_cap) {
           L.fb_rows[slot] = r;
-        } else {
+        } else if (clear_past) {
           // past the capacity (an error the status word reports): the row is
           // not stored anywhere, but its cells still become empty
           const int64_t cell0 = static_cast<int64_t>(r) * L.nt;
@@ -327,9 +327,84 @@ int launch_tile_assign(const twell_t& L, const uint16_t* H, int64_t ldh, const u
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
-int launch_route(const twell_t& L, cudaStream_t s, int32_t empty) {
+int launch_route(const twell_t& L, cudaStream_t s, int32_t empty, bool clear_past) {
   LaunchScope ls(TWELL_KERNEL_ROUTE, s);
-  if (launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, flat(L), empty) != cudaSuccess)
+  if (launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, flat(L), empty, clear_past ? 1 : 0) !=
+      cudaSuccess)
+    return TWELL_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
+}
+
+// ---- row view of a tile-granular layout (the backward's input): a row that
+// holds a dense tile becomes a fallback row of the view, with its dense h
+// assembled from its cells and its pool tiles; its cells are not touched.
+
+// flags[r] = 1 when row r holds a dense tile, else 0.  A warp per row.
+__global__ void __launch_bounds__(256) tile_row_flags_kernel(Layout L, int32_t* __restrict__ flags) {
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gw0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t gws = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = gw0; r < L.N; r += gws) {
+    bool dense = false;
+    for (int t = lane; t < L.nt; t += 32) dense |= L.counts[r * L.nt + t] == TWELL_DENSE_TILE;
+    dense = __any_sync(0xffffffffu, dense);
+    if (lane == 0) flags[r] = dense ? 1 : 0;
+  }
+}
+
+// The dense h of each routed row of the view (slots below min(n_fb, cap)): a
+// CTA per slot zeroes the row, then writes each cell's stored entries or
+// copies its pool tile (indices bounded by T, slots by the pool).
+__global__ void __launch_bounds__(256) tile_rows_assemble_kernel(Layout L, const int32_t* __restrict__ v_rows,
+                                                                 const int32_t* __restrict__ v_n, int v_cap,
+                                                                 uint16_t* __restrict__ dense) {
+  grid_dependency_wait();
+  const int n = min(*v_n, v_cap);
+  const int64_t pool = static_cast<int64_t>(L.fb_cap) * L.nt;
+  for (int slot = blockIdx.x; slot < n; slot += gridDim.x) {
+    const int r = v_rows[slot];
+    uint16_t* out = dense + static_cast<int64_t>(slot) * L.f;
+    for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(out)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    for (int t = threadIdx.x; t < L.nt; t += blockDim.x) {
+      const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
+      const int cnt = L.counts[cell];
+      uint16_t* o = out + static_cast<int64_t>(t) * L.T;
+      if (cnt == TWELL_DENSE_TILE) {
+        const int64_t ps = static_cast<int64_t>(L.values[cell * L.C]) | (static_cast<int64_t>(L.idx[cell * L.C]) << 16);
+        if (ps < pool)
+          for (int k = 0; k < L.T; ++k) o[k] = L.fb_dense[ps * L.T + k];
+      } else {
+        for (int sl = 0; sl < min(cnt, L.C); ++sl) {
+          const int j = L.idx[cell * L.C + sl];
+          if (j < L.T) o[j] = L.values[cell * L.C + sl];
+        }
+      }
+    }
+    __syncthreads();  // the next slot's zeroing comes after these writes
+  }
+}
+
+int launch_tile_row_view(const twell_t& H, const twell_t& V, cudaStream_t s) {
+  if (H.n_rows <= 0) return TWELL_OK;
+  {
+    const int grid = std::max(1, std::min((H.n_rows + 7) / 8, 4 * sm_count()));
+    LaunchScope ls(TWELL_KERNEL_AUX, s);
+    if (launch_pdl(tile_row_flags_kernel, dim3(grid), dim3(256), 0, s, flat(H), V.row_fb) != cudaSuccess)
+      return TWELL_ERR_CUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return TWELL_ERR_CUDA;
+  // slots in ascending row order; a row past the view's capacity is reported
+  // (overflow status) and its cells are left as they are
+  const int rc = launch_route(V, s, 0, false);
+  if (rc != TWELL_OK) return rc;
+  if (V.fb_cap <= 0) return TWELL_OK;
+  const int grid = std::max(1, std::min(V.fb_cap, 2 * sm_count()));
+  LaunchScope ls(TWELL_KERNEL_AUX, s);
+  if (launch_pdl(tile_rows_assemble_kernel, dim3(grid), dim3(256), 0, s, flat(H), V.fb_rows, V.n_fb, V.fb_cap,
+                 V.fb_dense) != cudaSuccess)
     return TWELL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }

@@ -206,8 +206,12 @@ int launch_gemm_swap_partial(const uint16_t* W, const uint16_t* X, int M, int n_
                              int32_t* zero0 = nullptr, int n_zero0 = 0, int32_t* zero1 = nullptr, int n_zero1 = 0);
 
 // forward helpers (fwd_kernels.cu)
-// rows variant: row_fb holds 1 for a flagged row and `empty` for the others
-int launch_route(const twell_t& L, cudaStream_t s, int32_t empty = 0);
+// rows variant: row_fb holds 1 for a flagged row and `empty` for the others;
+// clear_past: a row past fb_cap gets empty cells (else its cells are left)
+int launch_route(const twell_t& L, cudaStream_t s, int32_t empty = 0, bool clear_past = true);
+// the row view V of a tile-granular layout H (V.row_fb, fb_rows, n_fb and
+// fb_dense in the backward's workspace; V.fb_cap rows)
+int launch_tile_row_view(const twell_t& H, const twell_t& V, cudaStream_t s);
 // tile-granular hybrid: dense tiles per flagged row (before launch_route), then
 // pool slots, pool copies (from H, or from the spill buffer when H is null)
 // and the cells' slot numbers (after it)
@@ -271,6 +275,6 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
                             void* base);
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,
                const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
-               int d_model, const BwdWorkspace& ws, cudaStream_t s);
+               int d_model, const BwdWorkspace& ws, cudaStream_t s, bool row_view = false);
 
 }  // namespace twell

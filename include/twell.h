@@ -58,9 +58,9 @@
  *     *n_fb counts dense tiles (may exceed fb_cap * n_tiles; tiles past the
  *     pool are not stored, their cells are left empty, and the status word
  *     reports TWELL_ERR_FALLBACK_OVERFLOW).
- *   - Supported by twell_pack, twell_unpack and twell_ffn_fwd (n_rows > 32);
- *     the backward, the gated forward and the small-batch forward return
- *     TWELL_ERR_UNSUPPORTED for it.
+ *   - Supported by twell_pack, twell_unpack, twell_ffn_fwd (n_rows > 32) and
+ *     twell_ffn_bwd (through a row view, see there); the gated forward and the
+ *     small-batch forward return TWELL_ERR_UNSUPPORTED for it.
  */
 #ifndef TWELL_H
 #define TWELL_H
@@ -224,9 +224,15 @@ TWELL_API size_t twell_ffn_fwd_noalloc_max_scratch(void);
  * rows are handed to CTAs through an atomic counter, which changes only who
  * computes a row, not how).
  * workspace: device, >= twell_bwd_workspace_bytes(...) bytes, 256-byte aligned
- * (it may be the forward call's workspace, see twell_ffn_fwd).
- * TWELL_ERR_UNSUPPORTED for the tile-granular variant and when
- * n_rows * (d_ff / tile) * cap exceeds 2^31 - 1 (32-bit entry positions). */
+ * (it may be the forward call's workspace, see twell_ffn_fwd); for the
+ * tile-granular variant >= twell_bwd_tiles_workspace_bytes(...).
+ * Tile-granular layouts: the gradients are those of the same h, computed on a
+ * row view built in the workspace, in which each row holding a dense tile is a
+ * fallback row (its dense h assembled from its cells and pool tiles; at most
+ * fb_cap such rows, else the status word reports TWELL_ERR_FALLBACK_OVERFLOW
+ * and the rows past fb_cap are left out); the layout itself is not modified.
+ * TWELL_ERR_UNSUPPORTED when n_rows * (d_ff / tile) * cap exceeds 2^31 - 1
+ * (32-bit entry positions). */
 TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
                   const twell_t* H, int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
                   float* dW_inT, float* dW_down, float* db, void* workspace,
@@ -234,6 +240,11 @@ TWELL_API int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint
 
 TWELL_API size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
                                  int32_t cap, int32_t fb_cap);
+
+/* Workspace of twell_ffn_bwd for a tile-granular layout: twell_bwd_workspace_bytes
+ * plus the row view (routing words, fb_cap slots, fb_cap dense rows). */
+TWELL_API size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
+                                                 int32_t cap, int32_t fb_cap);
 
 /* Dense comparator (not part of the method): Y = ReLU(X.W_in + b).W_down with
  * the same tensor-core GEMM and no sparsity.  W_down is [d_ff][d_model] bf16 as

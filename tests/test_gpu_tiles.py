@@ -1,8 +1,10 @@
 """The tile-granular hybrid on the GPU (only over-full tiles leave TwELL, for a
 pool of dense tiles numbered in (row, tile) order) against the oracle:
 standalone pack / unpack bit-exact, the fused forward bit-exact on integer
-layers and within tolerance on random ones, pool overflow reported, and the
-calls that do not take this variant refusing it."""
+layers and within tolerance on random ones, pool overflow reported, the
+backward (through its row view) equal to the row-routed backward of the same
+layer and within tolerance of the oracle, and the calls that do not take this
+variant refusing it."""
 import ctypes
 
 import numpy as np
@@ -155,6 +157,8 @@ def test_fwd_tiles_1b_sampled(tw):
 
 
 def test_tiles_refused_where_not_built(tw):
+    """The gated forward and the small-batch forward refuse the variant; the
+    backward asks for its own workspace size."""
     import torch
     lib = tw.load_library()
     N, d, f, T, C = 64, 128, 256, 64, 4
@@ -169,10 +173,12 @@ def test_tiles_refused_where_not_built(tw):
     dWi = torch.empty((f, d), dtype=torch.float32, device="cuda")
     dWd = torch.empty((f, d), dtype=torch.float32, device="cuda")
     db = torch.empty((f,), dtype=torch.float32, device="cuda")
+    # the backward takes the variant, with the larger workspace its row view needs
     rc = lib.twell_ffn_bwd(X.data_ptr(), Wi.data_ptr(), Wd.data_ptr(), ctypes.byref(st), d, dY.data_ptr(),
                            ctypes.c_float(0.0), dX.data_ptr(), dWi.data_ptr(), dWd.data_ptr(), db.data_ptr(),
-                           ws.data_ptr(), ws.numel(), None)
-    assert rc == -3
+                           ws.data_ptr(), tw.bwd_workspace_bytes(N, d, f, T, C, 8, hybrid=tw.HYBRID_TILES) - 256,
+                           None)
+    assert rc == -5   # TWELL_ERR_WORKSPACE
     Y = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
     rc = lib.twell_gated_ffn_fwd(X.data_ptr(), Wi.data_ptr(), Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), N, d, f,
                                  ctypes.byref(st), Y.data_ptr(), ws.data_ptr(), ws.numel(), None)
@@ -182,3 +188,59 @@ def test_tiles_refused_where_not_built(tw):
     rc = lib.twell_ffn_fwd(X.data_ptr(), Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), 8, d, f, ctypes.byref(ss),
                            Y.data_ptr(), ws.data_ptr(), ws.numel(), None)
     assert rc == -3
+
+
+def _fwd_bwd(tw, torch, inp, dY, lam, T, C, fb_cap, hybrid):
+    dev = torch.device("cuda")
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    N, d = inp["X"].shape
+    f = inp["W_inT"].shape[0]
+    p = tw.alloc_packed(N, f, T, C, fb_cap, dev, hybrid=hybrid)
+    Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb_cap), dtype=torch.uint8, device=dev)
+    tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws)
+    assert tw.twell_read_status(p) == 0
+    H = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+    tw.twell_unpack(p, H)
+    counts = from_dev_bits(p.counts).copy()
+    dX = torch.full((N, d), 5.0, dtype=torch.bfloat16, device=dev)
+    dWi = torch.full((f, d), 5.0, dtype=torch.float32, device=dev)
+    dWd = torch.full((f, d), 5.0, dtype=torch.float32, device=dev)
+    db = torch.full((f,), 5.0, dtype=torch.float32, device=dev)
+    wsb = torch.full((tw.bwd_workspace_bytes(N, d, f, T, C, fb_cap, hybrid=hybrid),), 0x5A, dtype=torch.uint8,
+                     device=dev)
+    tw.twell_ffn_bwd(X, Wi, Wd, p, to_dev(dY, torch), lam, dX, dWi, dWd, db, wsb)
+    assert tw.twell_read_status(p) == 0
+    torch.cuda.synchronize()
+    # the backward leaves the layout as it was
+    assert np.array_equal(from_dev_bits(p.counts), counts)
+    return (from_dev_bits(H), from_dev_bits(dX).copy(), dWi.cpu().numpy(), dWd.cpu().numpy(), db.cpu().numpy(),
+            int(p.n_fb[0].item()))
+
+
+@pytest.mark.parametrize("N,d,f,T,C,lam,seed", [(301, 256, 1024, 64, 8, 1e-3, 1), (200, 512, 2048, 128, 8, 1e-4, 2),
+                                               (160, 256, 1024, 32, 4, 0.0, 3)])
+def test_tiles_backward(tw, N, d, f, T, C, lam, seed):
+    """The tile variant's backward computes the gradients of the same h as
+    the row-routed layer: bit for bit the row-routed backward's outputs (the
+    rows holding a dense tile are exactly the rows routed whole), and within
+    the stated tolerance of the oracle."""
+    import torch
+    cfg = synth.FFNConfig("tb", N, d, f, T, C, seed=seed, row_spread="lognormal", forced_frac_rows=0.04,
+                          l1_lambda=lam)
+    inp = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(N, d, seed=seed + 5)
+    fb = cfg.fallback_capacity
+    rows = _fwd_bwd(tw, torch, inp, dY, lam, T, C, fb, tw.HYBRID_ROWS)
+    tiles = _fwd_bwd(tw, torch, inp, dY, lam, T, C, fb, tw.HYBRID_TILES)
+    assert rows[5] > 0 and tiles[5] > 0          # fallback rows / dense tiles present
+    assert np.array_equal(rows[0], tiles[0])     # the same h
+    for a, b, name in zip(rows[1:5], tiles[1:5], ("dX", "dW_inT", "dW_down", "db")):
+        assert np.array_equal(a, b), name
+    H = tiles[0]
+    _, dZ = oracle.grad_hidden(dY, inp["W_down"], H, lam)
+    assert_close(synth.bf16_bits_to_f32(tiles[1]), oracle.grad_input(dZ, inp["W_inT"]), "dX")
+    rWi, rWd, rdb = oracle.grad_weights(inp["X"], inp["W_down"], H, dY, lam)
+    assert_close(tiles[2], rWi, "dW_inT")
+    assert_close(tiles[3], rWd, "dW_down")
+    assert_close(tiles[4], rdb, "db")
