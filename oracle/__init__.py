@@ -50,6 +50,9 @@ def _configure(lib):
     lib.oracle_grad_hidden.argtypes = [P, P, P, ctypes.c_float, P, I, I, I, P, P]
     lib.oracle_grad_input.argtypes = [P, P, I, I, I, P]
     lib.oracle_grad_weights.argtypes = [P, P, P, P, ctypes.c_float, I, I, I, P, I, P, P, P]
+    lib.oracle_grad_hidden_gated.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, I, I, I, P, P]
+    lib.oracle_grad_input_gated.argtypes = [P, P, P, P, I, I, I, P]
+    lib.oracle_grad_weights_gated.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, I, I, I, P, I, P, P, P, P]
     lib.oracle_check_format.restype = I
     lib.oracle_check_format.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
     lib.oracle_pack_tiles.restype = I
@@ -242,6 +245,41 @@ def grad_weights(X, W_down, H, dY, lam: float, cols=None):
     _load().oracle_grad_weights(_p(X), _p(W_down), _p(H), _p(dY), float(lam), N, d, f, _p(c), len(c),
                                 _p(dWin), _p(dWdown), _p(db))
     return dWin, dWdown, db
+
+
+def grad_hidden_gated(X, W_gT, W_uT, b, dY, W_down, H, lam: float, rows=None):
+    """(dG, dU) of the gated layer for the selected rows; H is the full [N][f]."""
+    X, W_gT, W_uT, b, dY, W_down, H = (_c(a, np.uint16) for a in (X, W_gT, W_uT, b, dY, W_down, H))
+    f, d = W_gT.shape
+    r = _rows(rows, X.shape[0])
+    dG = np.empty((len(r), f), dtype=np.float32)
+    dU = np.empty((len(r), f), dtype=np.float32)
+    _load().oracle_grad_hidden_gated(_p(X), _p(W_gT), _p(W_uT), _p(b), _p(dY), _p(W_down), _p(H), float(lam),
+                                     _p(r), len(r), d, f, _p(dG), _p(dU))
+    return dG, dU
+
+
+def grad_input_gated(dG, dU, W_gT, W_uT) -> np.ndarray:
+    dG, dU = _c(dG, np.float32), _c(dU, np.float32)
+    W_gT, W_uT = _c(W_gT, np.uint16), _c(W_uT, np.uint16)
+    f, d = W_gT.shape
+    n = dG.shape[0]
+    dX = np.empty((n, d), dtype=np.float32)
+    _load().oracle_grad_input_gated(_p(dG), _p(dU), _p(W_gT), _p(W_uT), n, d, f, _p(dX))
+    return dX
+
+
+def grad_weights_gated(X, W_gT, W_uT, b, W_down, H, dY, lam: float, cols=None):
+    """(dW_gT, dW_uT, dW_down, db) of the gated layer for the hidden units `cols`."""
+    X, W_gT, W_uT, b, W_down, H, dY = (_c(a, np.uint16) for a in (X, W_gT, W_uT, b, W_down, H, dY))
+    N, d = X.shape
+    f = W_gT.shape[0]
+    c = _rows(cols, f)
+    out = [np.empty((len(c), d), dtype=np.float32) for _ in range(3)]
+    db = np.empty((len(c),), dtype=np.float32)
+    _load().oracle_grad_weights_gated(_p(X), _p(W_gT), _p(W_uT), _p(b), _p(W_down), _p(H), _p(dY), float(lam),
+                                      N, d, f, _p(c), len(c), _p(out[0]), _p(out[1]), _p(out[2]), _p(db))
+    return out[0], out[1], out[2], db
 
 
 def check_format(packed: dict, f: int) -> int:

@@ -417,6 +417,106 @@ EXPORT void oracle_grad_weights(const uint16_t* X, const uint16_t* W_down, const
   }
 }
 
+/* Backward of the gated layer  L = sum(Y * dY) + lambda * sum|H|  with
+ * Y = H . W_down, H = bf16(g * u) where g = X . W_g + b > 0 (else +0) and
+ * u = X . W_u (the Llama-style layer named "sparse_llama" on the
+ * repo-explainer page, "The Repo's Two Jobs"; L1 on the activations from the
+ * bayesiansapien note, TL;DR).  h's bf16 rounding is passed straight through
+ * and the pattern is h != 0: where h != 0,
+ *   dh = sum_c dY[n][c] * W_down[j][c] (c ascending) + lambda * sign(h),
+ *   dG = dh * u,  dU = dh * g
+ * (g and u recomputed as oracle_hidden_gated computes them); elsewhere dG and
+ * dU are 0 -- including a (n, j) with g > 0 whose product rounds to zero. */
+static void gated_point(const uint16_t* x, const uint16_t* wg, const uint16_t* wu, const uint16_t* bj,
+                        const uint16_t* gy, const uint16_t* wd, uint16_t hbits, float lambda, int32_t d,
+                        float* dg, float* du) {
+  float h = bf16_to_f32(hbits);
+  if (h == 0.0f) {
+    *dg = 0.0f;
+    *du = 0.0f;
+    return;
+  }
+  float g = 0.0f, u = 0.0f, acc = 0.0f;
+  for (int32_t k = 0; k < d; ++k) {
+    g += bf16_to_f32(x[k]) * bf16_to_f32(wg[k]);
+    u += bf16_to_f32(x[k]) * bf16_to_f32(wu[k]);
+  }
+  g += bf16_to_f32(*bj);
+  for (int32_t c = 0; c < d; ++c) acc += bf16_to_f32(gy[c]) * bf16_to_f32(wd[c]);
+  float dh = acc + (h > 0.0f ? lambda : -lambda);
+  *dg = dh * u;
+  *du = dh * g;
+}
+
+/* dG, dU for the selected rows ([n_sel][f] each); H holds the full [N][f]. */
+EXPORT void oracle_grad_hidden_gated(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
+                                     const uint16_t* b, const uint16_t* dY, const uint16_t* W_down,
+                                     const uint16_t* H, float lambda, const int32_t* rows, int32_t n_sel,
+                                     int32_t d, int32_t f, float* dG, float* dU) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t r = 0; r < n_sel; ++r) {
+    int32_t n = rows[r];
+    for (int32_t j = 0; j < f; ++j)
+      gated_point(X + (int64_t)n * d, W_gT + (int64_t)j * d, W_uT + (int64_t)j * d, b + j,
+                  dY + (int64_t)n * d, W_down + (int64_t)j * d, H[(int64_t)n * f + j], lambda, d,
+                  dG + (int64_t)r * f + j, dU + (int64_t)r * f + j);
+  }
+}
+
+/* dX[r][k] = sum_j (dG[r][j] * W_gT[j][k] + dU[r][j] * W_uT[j][k]) (j ascending,
+ * the gate's term then the up term). */
+EXPORT void oracle_grad_input_gated(const float* dG, const float* dU, const uint16_t* W_gT,
+                                    const uint16_t* W_uT, int32_t n_sel, int32_t d, int32_t f, float* dX) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t r = 0; r < n_sel; ++r) {
+    for (int32_t k = 0; k < d; ++k) {
+      float acc = 0.0f;
+      for (int32_t j = 0; j < f; ++j) {
+        acc += dG[(int64_t)r * f + j] * bf16_to_f32(W_gT[(int64_t)j * d + k]);
+        acc += dU[(int64_t)r * f + j] * bf16_to_f32(W_uT[(int64_t)j * d + k]);
+      }
+      dX[(int64_t)r * d + k] = acc;
+    }
+  }
+}
+
+/* Weight gradients of the gated layer for selected hidden units j, summing n
+ * ascending over all N rows (dG, dU recomputed from their definition):
+ *   dW_down[j][c] = sum_n H[n][j] * dY[n][c]
+ *   dW_gT[j][k]   = sum_n dG[n][j] * X[n][k]
+ *   dW_uT[j][k]   = sum_n dU[n][j] * X[n][k]
+ *   db[j]         = sum_n dG[n][j]            (the bias sits on the gate) */
+EXPORT void oracle_grad_weights_gated(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
+                                      const uint16_t* b, const uint16_t* W_down, const uint16_t* H,
+                                      const uint16_t* dY, float lambda, int32_t N, int32_t d, int32_t f,
+                                      const int32_t* cols, int32_t n_cols, float* dW_gT, float* dW_uT,
+                                      float* dW_down, float* db) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t q = 0; q < n_cols; ++q) {
+    int32_t j = cols[q];
+    float* gg = dW_gT + (int64_t)q * d;
+    float* gu = dW_uT + (int64_t)q * d;
+    float* gdown = dW_down + (int64_t)q * d;
+    float gb = 0.0f;
+    for (int32_t k = 0; k < d; ++k) gg[k] = gu[k] = gdown[k] = 0.0f;
+    for (int32_t n = 0; n < N; ++n) {
+      const uint16_t* x = X + (int64_t)n * d;
+      const uint16_t* gy = dY + (int64_t)n * d;
+      float h = bf16_to_f32(H[(int64_t)n * f + j]);
+      float dg, du;
+      gated_point(x, W_gT + (int64_t)j * d, W_uT + (int64_t)j * d, b + j, gy, W_down + (int64_t)j * d,
+                  H[(int64_t)n * f + j], lambda, d, &dg, &du);
+      for (int32_t c = 0; c < d; ++c) gdown[c] += h * bf16_to_f32(gy[c]);
+      for (int32_t k = 0; k < d; ++k) {
+        gg[k] += dg * bf16_to_f32(x[k]);
+        gu[k] += du * bf16_to_f32(x[k]);
+      }
+      gb += dg;
+    }
+    db[q] = gb;
+  }
+}
+
 /* Format invariants of a packed layer (no H needed).  Returns 0 when all hold,
  * else a code naming the first violated rule:
  *   1 count above C in a TwELL row      2 non-zero count in a fallback row

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_gated_bwd as gated_pins
 import test_oracle_tiles as tile_pins
 
 MUTATIONS = [
@@ -39,6 +40,15 @@ MUTATIONS = [
     ("dW_down uses dz", "for (int32_t c = 0; c < d; ++c) gdown[c] += h * bf16_to_f32(g[c]);",
      "for (int32_t c = 0; c < d; ++c) gdown[c] += dz * bf16_to_f32(g[c]);",
      pins.test_backward_single_active_unit_rank_one),
+    ("gated dG built from the gate", "*dg = dh * u;", "*dg = dh * g;", gated_pins.test_gated_backward_matches_autograd),
+    ("gated L1 sign dropped", "float dh = acc + (h > 0.0f ? lambda : -lambda);", "float dh = acc + lambda;",
+     gated_pins.test_gated_backward_zero_upstream_closed_form),
+    ("gated pattern h > 0", "  if (h == 0.0f) {\n    *dg = 0.0f;", "  if (h <= 0.0f) {\n    *dg = 0.0f;",
+     gated_pins.test_gated_backward_matches_autograd),
+    ("gated dX without the up term",
+     "        acc += dU[(int64_t)r * f + j] * bf16_to_f32(W_uT[(int64_t)j * d + k]);\n", "",
+     gated_pins.test_gated_backward_matches_autograd),
+    ("gated db from dU", "      gb += dg;", "      gb += du;", gated_pins.test_gated_backward_matches_autograd),
     ("rounding ties away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;",
      "if (rest >= 0x8000u) keep += 1u;", pins.test_bf16_rounding_hand_cases),
     ("tile slots out of order", "values[cell * C] = (uint16_t)(n_dense & 0xFFFF);",
