@@ -45,7 +45,8 @@ EXPORTED = [
     "twell_profile_timeline",
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
     "twell_selftest_wait_timeout", "twell_check_format", "twell_dense_ffn_bwd", "twell_dense_bwd_workspace_bytes",
-    "twell_bwd_tiles_workspace_bytes",
+    "twell_bwd_tiles_workspace_bytes", "twell_gated_ffn_fwd_train", "twell_gated_ffn_bwd",
+    "twell_gated_bwd_workspace_bytes",
 ]
 
 
@@ -99,6 +100,10 @@ def load_library() -> ctypes.CDLL:
         "twell_ffn_fwd_noalloc": (ctypes.c_int, [P, P, P, P, I32, I32, I32, L, P, P]),
         "twell_ffn_fwd_noalloc_max_scratch": (SZ, []),
         "twell_gated_ffn_fwd": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, SZ, P]),
+        "twell_gated_ffn_fwd_train": (ctypes.c_int, [P, P, P, P, P, I32, I32, I32, L, P, P, P, SZ, P]),
+        "twell_gated_ffn_bwd": (ctypes.c_int, [P, P, P, P, P, L, P, I32, P, ctypes.c_float, P, P, P, P, P, P, SZ,
+                                               P]),
+        "twell_gated_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
         "twell_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "twell_check_format": (ctypes.c_int, [L, P, P]),
         "twell_dense_ffn_bwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, P, ctypes.c_float, P, P, P, P, P, SZ, P]),
@@ -260,6 +265,21 @@ def twell_gated_ffn_fwd(X, W_gT, W_uT, b, W_down, packed: Packed, Y, workspace, 
            "twell_gated_ffn_fwd")
 
 
+def twell_gated_ffn_fwd_train(X, W_gT, W_uT, b, W_down, packed: Packed, Y, gu, workspace, stream=None) -> None:
+    """twell_gated_ffn_fwd that also keeps (g, u) fp32 at every stored slot in gu
+    ([n_rows][d_ff / tile][cap][2] float32), for twell_gated_ffn_bwd."""
+    n, d = X.shape
+    f = W_gT.shape[0]
+    _need_layer(n, d, f, W_gT, b, W_down, Y)
+    _need(W_uT, f * d * 2, "W_uT")
+    _need(gu, n * (f // packed.tile) * packed.cap * 8, "gu")
+    st = packed.struct()
+    _check(load_library().twell_gated_ffn_fwd_train(_ptr(X), _ptr(W_gT), _ptr(W_uT), _ptr(b), _ptr(W_down), n, d,
+                                                    f, ctypes.byref(st), _ptr(Y), _ptr(gu), _ptr(workspace),
+                                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "twell_gated_ffn_fwd_train")
+
+
 def twell_ffn_fwd_noalloc(X, W_inT, b, W_down, packed: Packed, Y, stream=None) -> None:
     """twell_ffn_fwd without a workspace argument: the library's fixed scratch
     array is used (for callers that cannot allocate device memory)."""
@@ -285,6 +305,30 @@ def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW
                                         float(l1_lambda), _ptr(dX), _ptr(dW_inT), _ptr(dW_down), _ptr(db),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)), "twell_ffn_bwd")
+
+
+def gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
+    """Workspace of twell_gated_ffn_bwd."""
+    return int(load_library().twell_gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
+
+
+def twell_gated_ffn_bwd(X, W_gT, W_uT, b, W_down, packed: Packed, gu, dY, l1_lambda: float, dX, dW_gT, dW_uT,
+                        dW_down, db, workspace, stream=None) -> None:
+    """Backward of the gated layer; gu is what twell_gated_ffn_fwd_train kept."""
+    d = X.shape[1]
+    n, f = packed.n_rows, packed.d_ff
+    for t, nbytes, name in ((X, n * d * 2, "X"), (W_gT, f * d * 2, "W_gT"), (W_uT, f * d * 2, "W_uT"),
+                            (b, f * 2, "b"), (W_down, f * d * 2, "W_down"),
+                            (gu, n * (f // packed.tile) * packed.cap * 8, "gu"), (dY, n * d * 2, "dY"),
+                            (dX, n * d * 2, "dX"), (dW_gT, f * d * 4, "dW_gT"), (dW_uT, f * d * 4, "dW_uT"),
+                            (dW_down, f * d * 4, "dW_down"), (db, f * 4, "db")):
+        _need(t, nbytes, name)
+    st = packed.struct()
+    _check(load_library().twell_gated_ffn_bwd(_ptr(X), _ptr(W_gT), _ptr(W_uT), _ptr(b), _ptr(W_down),
+                                              ctypes.byref(st), _ptr(gu), d, _ptr(dY), float(l1_lambda), _ptr(dX),
+                                              _ptr(dW_gT), _ptr(dW_uT), _ptr(dW_down), _ptr(db), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "twell_gated_ffn_bwd")
 
 
 def twell_dense_ffn_fwd(X, W_inT, b, W_down, Hbuf, Y, stream=None) -> None:

@@ -399,7 +399,7 @@ namespace {
 // caller's stream and the dense-fallback rows on a second stream.
 int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, const uint16_t* b,
             const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y,
-            void* workspace, size_t workspace_bytes, twell_stream_t stream) {
+            void* workspace, size_t workspace_bytes, twell_stream_t stream, float* gu = nullptr) {
   TW_TRY(check_layout(H));
   if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
   if (H->n_rows != n_rows || H->d_ff != d_ff) return TWELL_ERR_INVALID_ARG;
@@ -450,7 +450,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   } else {
     TW_CUDA(cudaMemsetAsync(spill_count, 0, 2 * sizeof(int32_t), s));
     PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
-                     d_ff / H->tile, H->tile, H->cap};
+                     d_ff / H->tile, H->tile, H->cap, gu};
     if (W_uT)
       TW_TRY(launch_gemm_gated_pack(X, W_inT, W_uT, n_rows, d_ff, d_model, pp, H->status, s));
     else
@@ -504,6 +504,15 @@ int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t*
                         uint16_t* Y, void* workspace, size_t workspace_bytes, twell_stream_t stream) {
   if (!W_uT) return TWELL_ERR_INVALID_ARG;
   return ffn_fwd(X, W_gT, W_uT, b, W_down, n_rows, d_model, d_ff, H, Y, workspace, workspace_bytes, stream);
+}
+
+int twell_gated_ffn_fwd_train(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT, const uint16_t* b,
+                              const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff,
+                              const twell_t* H, uint16_t* Y, float* gu, void* workspace, size_t workspace_bytes,
+                              twell_stream_t stream) {
+  if (!W_uT || !gu) return TWELL_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(gu) % 16 != 0) return TWELL_ERR_MISALIGNED;
+  return ffn_fwd(X, W_gT, W_uT, b, W_down, n_rows, d_model, d_ff, H, Y, workspace, workspace_bytes, stream, gu);
 }
 
 size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
@@ -562,6 +571,39 @@ size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t 
   return base + align256(sizeof(int32_t) * static_cast<size_t>(std::max(n_rows, 1))) +
          align256(sizeof(int32_t) * static_cast<size_t>(std::max(fb_cap, 1))) + 256 +
          align256(sizeof(uint16_t) * static_cast<size_t>(std::max(fb_cap, 0)) * static_cast<size_t>(d_ff));
+}
+
+size_t twell_gated_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
+                                       int32_t fb_cap) {
+  if (n_rows < 0 || d_ff <= 0 || tile <= 0 || cap <= 0 || fb_cap < 0) return 0;
+  return bwd_workspace_layout(n_rows, d_model, d_ff, tile, cap, fb_cap, nullptr, nullptr, true);
+}
+
+int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT, const uint16_t* b,
+                        const uint16_t* W_down, const twell_t* H, const float* gu, int32_t d_model,
+                        const uint16_t* dY, float l1_lambda, uint16_t* dX, float* dW_gT, float* dW_uT,
+                        float* dW_down, float* db, void* workspace, size_t workspace_bytes,
+                        twell_stream_t stream) {
+  TW_TRY(check_layout(H));
+  if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
+  if (d_model % 128 != 0 || H->d_ff % 128 != 0 || H->hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(H->n_rows) * (H->d_ff / H->tile) * H->cap > INT32_MAX) return TWELL_ERR_UNSUPPORTED;
+  for (const void* p : {static_cast<const void*>(X), static_cast<const void*>(W_gT), static_cast<const void*>(W_uT),
+                        static_cast<const void*>(b), static_cast<const void*>(W_down), static_cast<const void*>(dY),
+                        static_cast<const void*>(dX), static_cast<const void*>(dW_gT),
+                        static_cast<const void*>(dW_uT), static_cast<const void*>(dW_down),
+                        static_cast<const void*>(db)})
+    TW_TRY(check_dense(p));
+  if (!gu) return TWELL_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(gu) % 16 != 0) return TWELL_ERR_MISALIGNED;
+  const size_t need = twell_gated_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
+  BwdWorkspace ws{};
+  bwd_workspace_layout(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap, &ws, workspace, true);
+  GatedBwd g{W_uT, b, gu, dW_uT};
+  return launch_bwd(X, W_gT, W_down, *H, dY, l1_lambda, dX, dW_gT, dW_down, db, d_model, ws,
+                    reinterpret_cast<cudaStream_t>(stream), false, &g);
 }
 
 int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,

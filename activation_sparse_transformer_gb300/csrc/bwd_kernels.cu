@@ -73,11 +73,12 @@ __device__ __forceinline__ int cell_idx8(uint2 w, int sl) {
 // skip_fb (a row view of a tile-granular layout, else null): rows with
 // skip_fb[r] >= 0 are the view's fallback rows, whose cells (which may name
 // dense tiles) take no part in the lists.
-template <bool kC8>
+// kGated: dz_cells holds (dG, dU) pairs per slot; dG goes to col_dz and dU to col_du.
+template <bool kC8, bool kGated>
 __global__ void __launch_bounds__(kListWarps * 32)
     unit_lists_kernel(Layout L, const float* __restrict__ dz_cells, int32_t* __restrict__ col_beg,
                       int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
-                      float* __restrict__ col_dz, const int32_t* __restrict__ skip_fb) {
+                      float* __restrict__ col_dz, const int32_t* __restrict__ skip_fb, float* __restrict__ col_du) {
   extern __shared__ int32_t lsm[];
   grid_dependency_wait();
   const int T = L.T, t = blockIdx.x;
@@ -159,11 +160,19 @@ __global__ void __launch_bounds__(kListWarps * 32)
       const int64_t cell = static_cast<int64_t>(r) * L.nt + t;
       // the block's values and dZ, requested before the masks are built
       uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-      float4 dz0 = make_float4(0.f, 0.f, 0.f, 0.f), dz1 = dz0;
+      float4 dz0 = make_float4(0.f, 0.f, 0.f, 0.f), dz1 = dz0, dz2 = dz0, dz3 = dz0;
       if (kC8 && cnt[j] > 0) {
         hv = *reinterpret_cast<const uint4*>(L.values + cell * 8);
-        dz0 = *reinterpret_cast<const float4*>(dz_cells + cell * 8);
-        dz1 = *reinterpret_cast<const float4*>(dz_cells + cell * 8 + 4);
+        if (kGated) {
+          const float4* q = reinterpret_cast<const float4*>(dz_cells + cell * 16);
+          dz0 = q[0];
+          dz1 = q[1];
+          dz2 = q[2];
+          dz3 = q[3];
+        } else {
+          dz0 = *reinterpret_cast<const float4*>(dz_cells + cell * 8);
+          dz1 = *reinterpret_cast<const float4*>(dz_cells + cell * 8 + 4);
+        }
       }
       for (int u = lane; u < T; u += 32) m[u] = 0;
       __syncwarp();
@@ -171,17 +180,36 @@ __global__ void __launch_bounds__(kListWarps * 32)
         atomicOr(&m[kC8 ? cell_idx8(iw[j], sl) : L.idx[cell * L.C + sl]], 1u << lane);
       __syncwarp();
       const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-      const float dzs[8] = {dz0.x, dz0.y, dz0.z, dz0.w, dz1.x, dz1.y, dz1.z, dz1.w};
+      // slot sl's dZ (kGated: its (dG, dU) pair is dzs[2 sl], dzs[2 sl + 1])
+      float dzs[kGated ? 16 : 8];
+      const float4 dzq[4] = {dz0, dz1, dz2, dz3};
+#pragma unroll
+      for (int q = 0; q < (kGated ? 4 : 2); ++q) {
+        dzs[4 * q] = dzq[q].x;
+        dzs[4 * q + 1] = dzq[q].y;
+        dzs[4 * q + 2] = dzq[q].z;
+        dzs[4 * q + 3] = dzq[q].w;
+      }
       for (int sl = 0; sl < cnt[j]; ++sl) {
         const int u = kC8 ? cell_idx8(iw[j], sl) : L.idx[cell * L.C + sl];
         const int64_t pos = base + ustart[u] + cur[u] + __popc(m[u] & ((1u << lane) - 1u));
         col_rows[pos] = r;
         if (kC8) {
           col_h[pos] = bf16_bits_to_float(static_cast<uint16_t>(hw[sl >> 1] >> (16 * (sl & 1))));
-          col_dz[pos] = dzs[sl];
+          if (kGated) {
+            col_dz[pos] = dzs[2 * sl];
+            col_du[pos] = dzs[2 * sl + 1];
+          } else {
+            col_dz[pos] = dzs[sl];
+          }
         } else {
           col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + sl]);
-          col_dz[pos] = dz_cells[cell * L.C + sl];
+          if (kGated) {
+            col_dz[pos] = dz_cells[(cell * L.C + sl) * 2];
+            col_du[pos] = dz_cells[(cell * L.C + sl) * 2 + 1];
+          } else {
+            col_dz[pos] = dz_cells[cell * L.C + sl];
+          }
         }
       }
       __syncwarp();
@@ -196,11 +224,12 @@ size_t unit_lists_smem(int T) { return sizeof(int32_t) * (2 * static_cast<size_t
 // One staged entry of a hidden unit's list (row, h, dZ); rows ascend.  h is
 // exactly a bf16 value, so the dW_down update uses the mixed bf16 x bf16 +
 // fp32 fma; the dW_in^T update multiplies the fp32 dZ by X two lanes at a time.
+// The gated layer's entries carry (dG, dU) in (dz, du).
 struct UnitEntry {
   int32_t row;
   uint32_t h_bits;  // bf16 bits of h in the low half
   float dz;
-  float pad;
+  float du;
 };
 
 // A CTA per hidden unit at a time (persistent, stride gridDim.x): the unit's
@@ -209,13 +238,17 @@ struct UnitEntry {
 // serve every column block, so they are read from global memory once).
 constexpr int kDwChunk = kWarps * 32;
 
+// kGated: also dW_u^T[j] = sum_n dU[n][j] X[n] from the same X loads (dW_inT
+// is then dW_g^T, summing dG).
+template <bool kGated>
 __global__ void __launch_bounds__(kWarps * 32, 3)
     dw_unitcta_kernel(int f, const int32_t* __restrict__ col_beg, const int32_t* __restrict__ col_end,
                       const int32_t* __restrict__ col_rows,
                       const float* __restrict__ col_h, const float* __restrict__ col_dz,
                       const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
                       float* __restrict__ dW_inT, float* __restrict__ dW_down, float* __restrict__ db,
-                      const int32_t* __restrict__ n_fb, int fb_cap) {
+                      const int32_t* __restrict__ n_fb, int fb_cap, const float* __restrict__ col_du,
+                      float* __restrict__ dW_uT) {
   __shared__ UnitEntry stage[kDwChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool have_fb = min(*n_fb, fb_cap) > 0;
@@ -227,6 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       const bool active = cb0 + warp < cbs && c0 < d;
       float a_down[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       float a_in[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float a_u[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       float gb = 0.f;
       for (int b = e0; b < e1; b += kDwChunk) {
         const int m = min(kDwChunk, e1 - b);
@@ -234,7 +268,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         if (static_cast<int>(threadIdx.x) < m) {
           const int q = b + threadIdx.x;
           stage[threadIdx.x] = UnitEntry{col_rows[q], static_cast<uint32_t>(__float_as_uint(col_h[q]) >> 16),
-                                         col_dz[q], 0.f};
+                                         col_dz[q], kGated ? col_du[q] : 0.f};
         }
         __syncthreads();
         int e = 0;
@@ -255,6 +289,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
             if (active) {
               fma8_bf16(a_down, static_cast<uint16_t>(en[u].h_bits), g[u]);
               fma8_f32x2(a_in, en[u].dz, x[u]);
+              if (kGated) fma8_f32x2(a_u, en[u].du, x[u]);
             }
           }
         }
@@ -264,7 +299,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
           if (active) {
             fma8_bf16(a_down, static_cast<uint16_t>(en.h_bits),
                       __ldg(reinterpret_cast<const uint4*>(dY + static_cast<int64_t>(en.row) * d + c0)));
-            fma8_f32x2(a_in, en.dz, __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0)));
+            const uint4 xr = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(en.row) * d + c0));
+            fma8_f32x2(a_in, en.dz, xr);
+            if (kGated) fma8_f32x2(a_u, en.du, xr);
           }
         }
       }
@@ -283,6 +320,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         od[1] = make_float4(a_down[4], a_down[5], a_down[6], a_down[7]);
         oi[0] = make_float4(a_in[0], a_in[1], a_in[2], a_in[3]);
         oi[1] = make_float4(a_in[4], a_in[5], a_in[6], a_in[7]);
+        if (kGated) {
+          float4* ou = reinterpret_cast<float4*>(dW_uT + static_cast<int64_t>(j) * d + c0);
+          if (have_fb) {
+            const float4 u0 = ou[0], u1 = ou[1];
+            a_u[0] += u0.x; a_u[1] += u0.y; a_u[2] += u0.z; a_u[3] += u0.w;
+            a_u[4] += u1.x; a_u[5] += u1.y; a_u[6] += u1.z; a_u[7] += u1.w;
+          }
+          ou[0] = make_float4(a_u[0], a_u[1], a_u[2], a_u[3]);
+          ou[1] = make_float4(a_u[4], a_u[5], a_u[6], a_u[7]);
+        }
       }
       if (cb0 == 0 && threadIdx.x == 0) db[j] = gb;
     }
@@ -294,10 +341,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 // xg2[2s] = xg2[2s+1] = X[fb_rows[s]] (paired with the high and low parts of
 // dZ, interleaved the same way).  Rows from n_fb (2 n_fb for the paired
 // buffers) up to the next multiple of 64 are zero, as the GEMM's device-side K
-// requires.
+// requires (du_hl, the gated layer's dU parts, is padded like dz_hl).
 __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
                                    uint16_t* __restrict__ hfb, uint16_t* __restrict__ dyg, uint16_t* __restrict__ xg2,
-                                   uint16_t* __restrict__ dz_hl, int fb_pad) {
+                                   uint16_t* __restrict__ dz_hl, int fb_pad, uint16_t* __restrict__ du_hl) {
   const int nfb = min(*L.n_fb, L.fb_cap);
   const int k1 = min(fb_pad, (nfb + 63) & ~63);
   const int k2 = min(2 * fb_pad, (2 * nfb + 63) & ~63);
@@ -323,6 +370,10 @@ __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, con
     if (!real) {
       uint4* a = reinterpret_cast<uint4*>(dz_hl + static_cast<int64_t>(k) * L.f);
       for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) a[i] = z;
+      if (du_hl) {
+        uint4* u = reinterpret_cast<uint4*>(du_hl + static_cast<int64_t>(k) * L.f);
+        for (int i = threadIdx.x; i < L.f / 8; i += blockDim.x) u[i] = z;
+      }
     }
   }
 }
@@ -358,7 +409,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
 
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
-                            void* base) {
+                            void* base, bool gated) {
   const int nt = d_ff / T;
   const int64_t cells = static_cast<int64_t>(N) * nt * C;
   const int ksplit = fb_cap > 0 ? choose_fb_ksplit(d_ff) : 1;
@@ -371,18 +422,22 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   };
   const size_t padf = static_cast<size_t>(fb_pad) * d_ff;
   const size_t padd = static_cast<size_t>(fb_pad) * d_model;
-  const size_t o_dzc = take(sizeof(float) * cells);
+  const int pairs = gated ? 2 : 1;
+  const size_t o_dzc = take(sizeof(float) * cells * pairs);
   const size_t o_hl = take(sizeof(uint16_t) * 2 * padf);
   const size_t o_hfb = take(sizeof(uint16_t) * padf);
   const size_t o_dyg = take(sizeof(uint16_t) * padd);
   const size_t o_xg = take(sizeof(uint16_t) * 2 * padd);
-  const size_t o_part = take(sizeof(float) * ksplit * static_cast<size_t>(fb_cap) * d_model);
+  const size_t o_part = take(sizeof(float) * pairs * ksplit * static_cast<size_t>(fb_cap) * d_model);
   const size_t o_beg = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
   const size_t o_end = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
   const size_t o_rows = take(sizeof(int32_t) * cells);
   const size_t o_h = take(sizeof(float) * cells);
   const size_t o_dz = take(sizeof(float) * cells);
   const size_t o_cnt = take(sizeof(int32_t));
+  const size_t o_duhl = gated ? take(sizeof(uint16_t) * 2 * padf) : 0;
+  const size_t o_gufb = gated ? take(sizeof(float) * 2 * padf) : 0;
+  const size_t o_du = gated ? take(sizeof(float) * cells) : 0;
   if (ws && base) {
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
@@ -399,6 +454,9 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->col_h = reinterpret_cast<float*>(b + o_h);
     ws->col_dz = reinterpret_cast<float*>(b + o_dz);
     ws->row_counter = reinterpret_cast<int32_t*>(b + o_cnt);
+    ws->du_hl = gated ? reinterpret_cast<uint16_t*>(b + o_duhl) : nullptr;
+    ws->gu_fb = gated ? reinterpret_cast<float*>(b + o_gufb) : nullptr;
+    ws->col_du = gated ? reinterpret_cast<float*>(b + o_du) : nullptr;
   }
   return off;
 }
@@ -415,14 +473,30 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
 
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& Lh,
                const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
-               int d, const BwdWorkspace& ws, cudaStream_t s, bool row_view) {
+               int d, const BwdWorkspace& ws, cudaStream_t s, bool row_view, const GatedBwd* gt) {
   const Layout L = flat(Lh);
   const int f = Lh.d_ff;
   const int N = Lh.n_rows;
+  const bool fb = Lh.fb_cap > 0 && N > 0;
+  const int fb_grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
+  if (gt && fb) {
+    // gated: the fallback rows' operands, then their g and u (recomputed on the
+    // tensor cores from the gathered X rows: row s of xg2 read with stride
+    // 2 d_model), which the SDDMM's epilogue needs for dG = dh' u, dU = dh' g
+    {
+      LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, s);
+      fb_operands_kernel<<<fb_grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad, ws.du_hl);
+    }
+    TW_CHECK_LAUNCH();
+    GUEpiParams gp{gt->b, ws.gu_fb, f};
+    TW_TRY_RC(launch_gemm_gu(ws.xg2, 2 * static_cast<int64_t>(d), W_inT, gt->W_uT, Lh.fb_cap, Lh.n_fb, f, d, gp,
+                             Lh.status, TWELL_KERNEL_SDDMM, s));
+  }
   if (N > 0) {
     // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
-    SampleEpiParams sp{Lh.values, Lh.idx, Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap, f / Lh.tile,
-                       Lh.tile,   Lh.cap, f,         lambda,    ws.dz_cells, ws.dz_hl};
+    SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb,  Lh.fb_dense,         Lh.fb_cap,
+                       f / Lh.tile, Lh.tile, Lh.cap,   f,          lambda,              ws.dz_cells,
+                       ws.dz_hl,    gt ? gt->gu : nullptr, gt ? ws.gu_fb : nullptr, gt ? ws.du_hl : nullptr};
     // its CTA 0 also zeroes the dX gather's row counter
     TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
   }
@@ -433,12 +507,10 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   AuxFork fork(s);
   TW_TRY_RC(fork.status());
   cudaStream_t a = fork.aux();
-  const bool fb = Lh.fb_cap > 0 && N > 0;
   if (fb) {
-    {
-      const int grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
+    if (!gt) {
       LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, a);
-      fb_operands_kernel<<<grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad);
+      fb_operands_kernel<<<fb_grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad, nullptr);
     }
     TW_CHECK_LAUNCH();
     TW_TRY_RC(launch_gemm_store_mn(ws.hfb, ws.dyg, f, d, ws.fb_pad, Lh.n_fb, 1, dW_down, d, Lh.status,
@@ -446,33 +518,45 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     // K = (slot, part): the high and low parts of dZ against X twice
     TW_TRY_RC(launch_gemm_store_mn(ws.dz_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, dW_inT, d, Lh.status,
                                    TWELL_KERNEL_DW_FALLBACK, a));
+    if (gt)
+      TW_TRY_RC(launch_gemm_store_mn(ws.du_hl, ws.xg2, f, d, 2 * ws.fb_pad, Lh.n_fb, 2, gt->dW_uT, d, Lh.status,
+                                     TWELL_KERNEL_DW_FALLBACK, a));
   }
   TW_TRY_RC(fork.mark_aux());  // dW holds the fallback share from here on
   if (N > 0) {
     // the TwELL rows' dX gather first: it needs only the SDDMM's output and,
     // queued after the fallback rows' dX, it waited for SMs held by the dW walk
-    TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
+    if (gt)
+      TW_TRY_RC(launch_spmm_f32x2(Lh, ws.dz_cells, W_inT, gt->W_uT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
+    else
+      TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
     if (fb) {
       // one GEMM over K = 2 d_ff: row s of dz_hl viewed with stride 2 d_ff is
-      // [high_s | low_s], and both halves meet the same W_in^T rows (K wraps)
-      PartialEpiParams pp{ws.part, d, static_cast<int64_t>(Lh.fb_cap) * d};
+      // [high_s | low_s], and both halves meet the same W_in^T rows (K wraps);
+      // gated: a second GEMM of dU's parts with W_u^T into the next ksplit splits
+      const int64_t split = static_cast<int64_t>(Lh.fb_cap) * d;
+      PartialEpiParams pp{ws.part, d, split};
       TW_TRY_RC(launch_gemm_partial_nmajor(ws.dz_hl, W_inT, Lh.fb_cap, Lh.n_fb, d, 2 * f, ws.ksplit, pp, Lh.status,
                                            TWELL_KERNEL_DX_FALLBACK, a, 2 * static_cast<int64_t>(f), f));
-      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, ws.ksplit, d, dX, TWELL_KERNEL_DX_FALLBACK, a));
+      if (gt) {
+        PartialEpiParams pu{ws.part + ws.ksplit * split, d, split};
+        TW_TRY_RC(launch_gemm_partial_nmajor(ws.du_hl, gt->W_uT, Lh.fb_cap, Lh.n_fb, d, 2 * f, ws.ksplit, pu,
+                                             Lh.status, TWELL_KERNEL_DX_FALLBACK, a, 2 * static_cast<int64_t>(f), f));
+      }
+      TW_TRY_RC(launch_fb_reduce(Lh, ws.part, gt ? 2 * ws.ksplit : ws.ksplit, d, dX, TWELL_KERNEL_DX_FALLBACK, a));
     }
   }
   // ---- weight gradients: TwELL entries regrouped by hidden unit (a CTA per tile)
   const size_t lsm = unit_lists_smem(Lh.tile);
-  if (set_max_dynamic_smem(reinterpret_cast<const void*>(unit_lists_kernel<true>),
-                           static_cast<int>(unit_lists_smem(256))) != TWELL_OK ||
-      set_max_dynamic_smem(reinterpret_cast<const void*>(unit_lists_kernel<false>),
-                           static_cast<int>(unit_lists_smem(256))) != TWELL_OK)
+  auto lk = Lh.cap == 8 ? (gt ? unit_lists_kernel<true, true> : unit_lists_kernel<true, false>)
+                        : (gt ? unit_lists_kernel<false, true> : unit_lists_kernel<false, false>);
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(lk), static_cast<int>(unit_lists_smem(256))) != TWELL_OK)
     return TWELL_ERR_CUDA;
   {
     LaunchScope ls(TWELL_KERNEL_AUX, s);
-    auto lk = Lh.cap == 8 ? unit_lists_kernel<true> : unit_lists_kernel<false>;
     if (launch_pdl(lk, dim3(f / Lh.tile), dim3(kListWarps * 32), lsm, s, L, ws.dz_cells, ws.col_beg, ws.col_end,
-                   ws.col_rows, ws.col_h, ws.col_dz, row_view ? Lh.row_fb : nullptr) != cudaSuccess)
+                   ws.col_rows, ws.col_h, ws.col_dz, row_view ? Lh.row_fb : nullptr,
+                   gt ? ws.col_du : nullptr) != cudaSuccess)
       return TWELL_ERR_CUDA;
   }
   TW_CHECK_LAUNCH();
@@ -480,9 +564,10 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   {
     LaunchScope ls(TWELL_KERNEL_DW, s);
     const int grid = std::max(1, std::min(f, 3 * sm_count()));
-    dw_unitcta_kernel<<<grid, kWarps * 32, 0, s>>>(f, ws.col_beg, ws.col_end, ws.col_rows, ws.col_h, ws.col_dz, X,
-                                                   dY, d,
-                                                   dW_inT, dW_down, db, Lh.n_fb, fb ? Lh.fb_cap : 0);
+    auto wk = gt ? dw_unitcta_kernel<true> : dw_unitcta_kernel<false>;
+    wk<<<grid, kWarps * 32, 0, s>>>(f, ws.col_beg, ws.col_end, ws.col_rows, ws.col_h, ws.col_dz, X, dY, d, dW_inT,
+                                   dW_down, db, Lh.n_fb, fb ? Lh.fb_cap : 0, gt ? ws.col_du : nullptr,
+                                   gt ? gt->dW_uT : nullptr);
   }
   TW_CHECK_LAUNCH();
   if (fb) {

@@ -258,6 +258,21 @@ struct GatedPackEpi {
     }
   }
 
+  // the gate (bias applied) and up values of 32 units [c, c + 32) of this thread's row
+  template <int BN>
+  static __device__ __forceinline__ void load_gu32(const Params& p, uint32_t taddr, int col0, int c,
+                                                   uint32_t (&g)[32], uint32_t (&u)[32]) {
+    tmem_ld32(taddr + c, g);
+    tmem_ld32(taddr + BN / 2 + c, u);
+    const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0 + c);
+    uint4 bq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bq[q] = __ldg(bp + q);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) g[i] = __float_as_uint(__uint_as_float(g[i]) + bias_at(bq, i));
+  }
+
   template <int BN>
   static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
                                                int, uint8_t* smem, int et) {
@@ -276,8 +291,8 @@ struct GatedPackEpi {
     int cnt = 0;
 #pragma unroll 1
     for (int c = cb; c < ce; c += 32) {
-      uint32_t h[32];
-      load_h32<BN>(p, taddr, col0, c, h);
+      uint32_t zg[32], zu[32];  // h = zg * zu where zg > 0, else +0
+      load_gu32<BN>(p, taddr, col0, c, zg, zu);
       const int j0 = c % T;
       if (j0 == 0) {
         cnt = 0;
@@ -289,14 +304,24 @@ struct GatedPackEpi {
       }
       uint32_t mask = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) mask |= (fabsf(__uint_as_float(h[i])) > thr ? 1u : 0u) << i;
+      for (int i = 0; i < 32; ++i) {
+        const float g = __uint_as_float(zg[i]);
+        const float h = g > 0.0f ? g * __uint_as_float(zu[i]) : 0.0f;
+        mask |= (fabsf(h) > thr ? 1u : 0u) << i;
+      }
       const int k = __popc(mask);
       if (cnt + k <= C) {
+        // (g, u) of each stored slot, for the backward
+        float* gu = (p.gu && valid)
+                        ? p.gu + (static_cast<int64_t>(row) * p.n_tiles + (col0 + c - j0) / T) * C * 2
+                        : nullptr;
         while (mask) {
           const int i = __ffs(mask) - 1;
           mask &= mask - 1;
-          sv[cnt] = float_to_bf16_bits(__uint_as_float(pick32(h, i)));
+          const float g = __uint_as_float(pick32(zg, i)), u = __uint_as_float(pick32(zu, i));
+          sv[cnt] = float_to_bf16_bits(g * u);
           si[cnt] = static_cast<uint8_t>(j0 + i);
+          if (gu) *reinterpret_cast<float2*>(gu + 2 * cnt) = make_float2(g, u);
           ++cnt;
         }
       } else {
@@ -542,8 +567,63 @@ struct SampleEpi {
           if (j >= 0 && j < 32) {
             const float h = bf16_bits_to_float(p.values[cell * C + s]);
             const float dh = __uint_as_float(pick32(r, j));
-            p.dz_cells[cell * C + s] = h > 0.0f ? dh + p.lambda : 0.0f;
+            if (p.gu) {
+              // gated: stored slots hold h != 0; (dG, dU) = (dh' u, dh' g)
+              const float dhl = dh + (h > 0.0f ? p.lambda : -p.lambda);
+              const float2 gv = *reinterpret_cast<const float2*>(p.gu + (cell * C + s) * 2);
+              reinterpret_cast<float2*>(p.dz_cells)[cell * C + s] =
+                  h != 0.0f ? make_float2(dhl * gv.y, dhl * gv.x) : make_float2(0.0f, 0.0f);
+            } else {
+              p.dz_cells[cell * C + s] = h > 0.0f ? dh + p.lambda : 0.0f;
+            }
           }
+        }
+      } else if (fb < p.fb_cap && p.gu) {
+        // gated fallback row: dense dG and dU over the 32 columns, as high + low bf16 parts
+        const uint4* hp = reinterpret_cast<const uint4*>(p.fb_dense + static_cast<int64_t>(fb) * p.d_ff + col);
+        const float4* gp = reinterpret_cast<const float4*>(p.gu_fb + (static_cast<int64_t>(fb) * p.d_ff + col) * 2);
+        uint4 hq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hq[q] = hp[q];
+        uint32_t ghi[16], glo[16], uhi[16], ulo[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float4 gu2 = gp[i / 2];  // (g, u) of columns i and i + 1
+          float og[2], ou[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float h = bias_at(hq, i + e);
+            const float dhl = __uint_as_float(r[i + e]) + (h > 0.0f ? p.lambda : -p.lambda);
+            og[e] = h != 0.0f ? dhl * (e ? gu2.w : gu2.y) : 0.0f;
+            ou[e] = h != 0.0f ? dhl * (e ? gu2.z : gu2.x) : 0.0f;
+          }
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint16_t gh = float_to_bf16_bits(og[e]);
+            const uint16_t gl = float_to_bf16_bits(og[e] - bf16_bits_to_float(gh));
+            const uint16_t uh = float_to_bf16_bits(ou[e]);
+            const uint16_t ul = float_to_bf16_bits(ou[e] - bf16_bits_to_float(uh));
+            w[0] |= static_cast<uint32_t>(gh) << (16 * e);
+            w[1] |= static_cast<uint32_t>(gl) << (16 * e);
+            w[2] |= static_cast<uint32_t>(uh) << (16 * e);
+            w[3] |= static_cast<uint32_t>(ul) << (16 * e);
+          }
+          ghi[i / 2] = w[0];
+          glo[i / 2] = w[1];
+          uhi[i / 2] = w[2];
+          ulo[i / 2] = w[3];
+        }
+        uint4* g0 = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
+        uint4* g1 = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
+        uint4* u0 = reinterpret_cast<uint4*>(p.du_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
+        uint4* u1 = reinterpret_cast<uint4*>(p.du_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          g0[q] = make_uint4(ghi[4 * q], ghi[4 * q + 1], ghi[4 * q + 2], ghi[4 * q + 3]);
+          g1[q] = make_uint4(glo[4 * q], glo[4 * q + 1], glo[4 * q + 2], glo[4 * q + 3]);
+          u0[q] = make_uint4(uhi[4 * q], uhi[4 * q + 1], uhi[4 * q + 2], uhi[4 * q + 3]);
+          u1[q] = make_uint4(ulo[4 * q], ulo[4 * q + 1], ulo[4 * q + 2], ulo[4 * q + 3]);
         }
       } else if (fb < p.fb_cap) {
         // fallback row: dense dZ over all 32 columns
@@ -581,6 +661,39 @@ struct SampleEpi {
           dl[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
       }
+    }
+  }
+};
+
+// (g, u) of the gated layer's fallback rows (dual-B GEMM: the stage's two B
+// halves are W_g and W_u rows of the same BN / 2 units): each epilogue thread
+// writes its row's units of its half of the tile as (g + b, u) fp32 pairs.
+struct GUEpi {
+  static constexpr bool kDualB = true;
+  using Params = GUEpiParams;
+  static constexpr uint32_t kSmemBytes = 0;
+
+  template <int BN>
+  static __device__ __forceinline__ void apply(const Params& p, uint32_t taddr, int row, int M, int col0, int half,
+                                               int, uint8_t*, int) {
+    constexpr int U = BN / 2;
+    const bool valid = row < M;
+#pragma unroll 1
+    for (int c = half * (U / 2); c < (half + 1) * (U / 2); c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld32(taddr + c, g);
+      tmem_ld32(taddr + U + c, u);
+      const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0 + c);
+      uint4 bq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) bq[q] = __ldg(bp + q);
+      tmem_ld_wait();
+      if (!valid) continue;
+      float4* out = reinterpret_cast<float4*>(p.gu + (static_cast<int64_t>(row) * p.d_ff + col0 + c) * 2);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2)
+        out[i / 2] = make_float4(__uint_as_float(g[i]) + bias_at(bq, i), __uint_as_float(u[i]),
+                                 __uint_as_float(g[i + 1]) + bias_at(bq, i + 1), __uint_as_float(u[i + 1]));
     }
   }
 };
@@ -910,6 +1023,13 @@ int launch_gemm_gated_pack(const uint16_t* A, const uint16_t* Bg, const uint16_t
   if (p.cap > GatedPackEpi::kMaxCap || N % 128 != 0 || 128 % p.tile != 0) return TWELL_ERR_UNSUPPORTED;
   return launch_gemm<256, GatedPackEpi, false, false>(A, Bg, M, nullptr, N, K, 1, p, status, TWELL_KERNEL_UP_PACK, s,
                                                       nullptr, 1, 0, Bu);
+}
+
+int launch_gemm_gu(const uint16_t* A, int64_t lda, const uint16_t* Bg, const uint16_t* Bu, int M, const int32_t* M_dev,
+                   int N, int K, const GUEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s) {
+  if (N % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  return launch_gemm<256, GUEpi, false, false>(A, Bg, M, M_dev, N, K, 1, p, status, kernel_id, s, nullptr, 1, lda,
+                                               Bu);
 }
 
 int launch_gemm_mask(const uint16_t* A, const uint16_t* B, int M, int N, int K, const MaskEpiParams& p,

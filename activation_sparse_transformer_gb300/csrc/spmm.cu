@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "sm103.cuh"
 #include "twell_internal.h"
@@ -58,6 +59,8 @@ struct SpmmArgs {
   // small batches: every row's h as dense bf16 [N][nt * T]; the fallback rows
   // (row_fb >= 0) are then gathered from it here instead of by the fallback path
   const uint16_t* dense_h;
+  // pair entries (float2 values): the second value multiplies this matrix's rows
+  const uint16_t* W2;
 };
 
 // Entry of the per-warp list.  bf16 values: one word, hidden unit j in the low
@@ -84,6 +87,17 @@ struct RowEntry<float> {
   __device__ __forceinline__ void fma(float (&acc)[8], const uint4& wr) const { fma8_f32x2(acc, v, wr); }
 };
 
+// Pair entries (the gated layer's dX): (dG, dU) at hidden unit j meet the rows
+// j of W_g^T and of W_u^T.
+template <>
+struct RowEntry<float2> {
+  int32_t jj;
+  float a, b;
+  int32_t pad;
+  static __device__ __forceinline__ RowEntry make(int j, float2 v) { return RowEntry{j, v.x, v.y, 0}; }
+  __device__ __forceinline__ int j() const { return jj; }
+};
+
 __device__ __forceinline__ uint4 pack8_bf16(const float (&acc)[8]) {
   uint32_t p[4];
 #pragma unroll
@@ -102,23 +116,51 @@ __device__ __forceinline__ float from_bf16<float>(uint16_t v) { return bf16_bits
 
 // acc += sum over list[0, total) of value x (W row j)[c0, c0 + 8), kU rows in flight.
 template <typename VT>
-__device__ __forceinline__ void stream_list(const SpmmArgs& a, const uint16_t* __restrict__ wcol,
+__device__ __forceinline__ void stream_list(const SpmmArgs& a, const uint16_t* __restrict__ W, int c0,
                                             const RowEntry<VT>* list, int total, float (&acc)[8]) {
-  int e = 0;
-  for (; e + kU <= total; e += kU) {
-    uint4 w[kU];
-    RowEntry<VT> en[kU];
+  const uint16_t* __restrict__ wcol = W + c0;
+  if constexpr (std::is_same<VT, float2>::value) {
+    // pairs: two W rows per entry, so half as many entries in flight
+    constexpr int kU2 = kU / 2;
+    const uint16_t* __restrict__ wcol2 = a.W2 + c0;
+    int e = 0;
+    for (; e + kU2 <= total; e += kU2) {
+      uint4 w[kU2], w2[kU2];
+      RowEntry<VT> en[kU2];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      en[u] = list[e + u];
-      w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+      for (int u = 0; u < kU2; ++u) {
+        en[u] = list[e + u];
+        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+        w2[u] = __ldg(reinterpret_cast<const uint4*>(wcol2 + static_cast<int64_t>(en[u].j()) * a.d));
+      }
+#pragma unroll
+      for (int u = 0; u < kU2; ++u) {
+        fma8_f32x2(acc, en[u].a, w[u]);
+        fma8_f32x2(acc, en[u].b, w2[u]);
+      }
     }
+    for (; e < total; ++e) {
+      const RowEntry<VT> en = list[e];
+      fma8_f32x2(acc, en.a, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+      fma8_f32x2(acc, en.b, __ldg(reinterpret_cast<const uint4*>(wcol2 + static_cast<int64_t>(en.j()) * a.d)));
+    }
+  } else {
+    int e = 0;
+    for (; e + kU <= total; e += kU) {
+      uint4 w[kU];
+      RowEntry<VT> en[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
-  }
-  for (; e < total; ++e) {
-    const RowEntry<VT> en = list[e];
-    en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+      for (int u = 0; u < kU; ++u) {
+        en[u] = list[e + u];
+        w[u] = __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en[u].j()) * a.d));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) en[u].fma(acc, w[u]);
+    }
+    for (; e < total; ++e) {
+      const RowEntry<VT> en = list[e];
+      en.fma(acc, __ldg(reinterpret_cast<const uint4*>(wcol + static_cast<int64_t>(en.j()) * a.d)));
+    }
   }
 }
 
@@ -141,7 +183,7 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
     for (int c = t_beg * a.T; c < t_end * a.T; c += 32) {  // T is a multiple of 32
       if (n + 32 > max_entries) {
         __syncwarp();
-        if (active) stream_list<VT>(a, W + c0, list, n, acc);
+        if (active) stream_list<VT>(a, W, c0, list, n, acc);
         __syncwarp();  // the list is free again
         n = 0;
       }
@@ -152,7 +194,7 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
       n += __popc(b);
     }
     __syncwarp();
-    if (active) stream_list<VT>(a, W + c0, list, n, acc);
+    if (active) stream_list<VT>(a, W, c0, list, n, acc);
     __syncwarp();  // the list is rewritten by the warp's next item
     return;
   }
@@ -178,7 +220,7 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
   __syncwarp();
 
   // ---- stream the named W rows, kU loads in flight
-  if (active) stream_list<VT>(a, W + c0, list, total, acc);
+  if (active) stream_list<VT>(a, W, c0, list, total, acc);
 
   // ---- tile-granular hybrid: each dense tile's non-zeros, gathered the same way
   if (a.pool) {
@@ -202,7 +244,7 @@ __device__ __forceinline__ void row_block_sum(const SpmmArgs& a, const uint16_t*
           n += __popc(b);
         }
         __syncwarp();
-        if (active) stream_list<VT>(a, W + c0, list, n, acc);
+        if (active) stream_list<VT>(a, W, c0, list, n, acc);
       }
     }
   }
@@ -352,7 +394,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         const int c0 = cb * 256 + lane * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (c0 < a.d) {
-          stream_list<VT>(a, W + c0, list, total, acc);
+          stream_list<VT>(a, W, c0, list, total, acc);
           *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(row) * a.d + c0) = pack8_bf16(acc);
         }
       }
@@ -362,6 +404,21 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     __syncthreads();  // the list and warp totals are rewritten for the next row
     row = next_row_s[it];
   }
+}
+
+// The CTA-per-row kernel over whole rows (row-granular hybrid, no split).
+template <typename VT>
+int launch_spmm_rowcta(const SpmmArgs& a, const uint16_t* W, int kernel_id, cudaStream_t s) {
+  auto rk = spmm_rowcta_kernel<VT>;
+  const size_t rsmem = static_cast<size_t>(a.nt) * a.C * sizeof(RowEntry<VT>);
+  if (rsmem > kMaxDynSmem) return TWELL_ERR_UNSUPPORTED;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(rk), kMaxDynSmem) != TWELL_OK) return TWELL_ERR_CUDA;
+  const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 4 * static_cast<int64_t>(sm_count()))));
+  {
+    LaunchScope ls(kernel_id, s);
+    if (launch_pdl(rk, dim3(rgrid), dim3(kWarps * 32), rsmem, s, a, W) != cudaSuccess) return TWELL_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
 }
 
 template <typename VT>
@@ -387,19 +444,9 @@ int launch_spmm_rows(const SpmmArgs& a, const uint16_t* W, int nsplit, int kerne
   }
   dim3 grid((a.N + kWarps - 1) / kWarps, (a.d + 255) / 256, nsplit);
   if (nsplit > 1 && static_cast<int64_t>(grid.x) * grid.y > kSpmmMaxArrivals) return TWELL_ERR_UNSUPPORTED;
-  if (nsplit == 1 && !a.pool && !a.dense_h) {
-    // a CTA per row: one shared flatten for all column blocks; persistent, four
-    // CTAs per SM (the register limit)
-    auto rk = spmm_rowcta_kernel<VT>;
-    const size_t rsmem = static_cast<size_t>(a.nt) * a.C * sizeof(RowEntry<VT>);
-    if (set_max_dynamic_smem(reinterpret_cast<const void*>(rk), kMaxDynSmem) != TWELL_OK) return TWELL_ERR_CUDA;
-    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(a.N, 4 * static_cast<int64_t>(sm_count()))));
-    {
-      LaunchScope ls(kernel_id, s);
-      if (launch_pdl(rk, dim3(rgrid), dim3(kWarps * 32), rsmem, s, a, W) != cudaSuccess) return TWELL_ERR_CUDA;
-    }
-    return cudaGetLastError() == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA;
-  }
+  // a CTA per row: one shared flatten for all column blocks; persistent, four
+  // CTAs per SM (the register limit)
+  if (nsplit == 1 && !a.pool && !a.dense_h) return launch_spmm_rowcta<VT>(a, W, kernel_id, s);
   if (nsplit == 1) {
     // persistent: three CTAs per SM (the register limit), warps stride over the items
     const int64_t items = static_cast<int64_t>(a.N) * ((a.d + 255) / 256);
@@ -451,6 +498,17 @@ int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int 
   SpmmArgs a{vals,     L.idx,   L.counts, L.row_fb,         out,    nullptr, nullptr, nullptr, row_counter,
              L.n_rows, d_model, L.d_ff / L.tile, L.tile, L.cap, L.status, nullptr};
   return launch_spmm_rows<float>(a, W, 1, kernel_id, s);
+}
+
+int launch_spmm_f32x2(const twell_t& L, const float* pairs, const uint16_t* W_a, const uint16_t* W_b, int d_model,
+                      uint16_t* out, int32_t* row_counter, int kernel_id, cudaStream_t s) {
+  if (L.hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
+  SpmmArgs a{pairs,    L.idx,   L.counts,        L.row_fb, out,   nullptr,  nullptr, nullptr, row_counter,
+             L.n_rows, d_model, L.d_ff / L.tile, L.tile,   L.cap, L.status, nullptr, W_b};
+  // whole TwELL rows, a CTA per row
+  if (a.N <= 0) return TWELL_OK;
+  if (a.C > 32 || a.d % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  return launch_spmm_rowcta<float2>(a, W_a, kernel_id, s);
 }
 
 }  // namespace twell

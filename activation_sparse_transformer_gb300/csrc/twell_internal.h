@@ -110,6 +110,8 @@ struct PackEpiParams {
   int32_t n_tiles;
   int32_t tile;           // T
   int32_t cap;            // C
+  float* gu;              // gated layer, for its backward: (g, u) fp32 at every stored slot
+                          // [M][n_tiles][C][2] (g with the bias), or null
 };
 
 struct DenseEpiParams {
@@ -151,6 +153,20 @@ struct SampleEpiParams {
   uint16_t* dz_hl;          // [2 * fb_pad][d_ff] bf16 for the fallback rows' dense dZ (0 where h == 0):
                             // row 2s = bf16(dz) (high part), row 2s+1 = bf16(dz - high) (low
                             // part); high + low carry dz to ~2^-17 relative
+  // gated layer (gu non-null): the pattern is h != 0 and dh' = dH + lambda sign(h);
+  // dz_cells then holds (dG, dU) = (dh' u, dh' g) pairs per slot ([M][n_tiles][C][2]),
+  // dz_hl the parts of dG and du_hl those of dU
+  const float* gu;          // (g, u) at the stored slots [M][n_tiles][C][2]
+  const float* gu_fb;       // (g, u) of the fallback rows [fb_pad][d_ff][2]
+  uint16_t* du_hl;
+};
+
+// g = X.W_g + b and u = X.W_u of the gated layer's fallback rows, kept as
+// (g, u) fp32 pairs [M][d_ff][2] (the dual-B GEMM's two halves).
+struct GUEpiParams {
+  const uint16_t* bias;
+  float* gu;
+  int32_t d_ff;
 };
 
 // dZ = dH + lambda where h > 0 (else 0) for the dense comparator: dH the
@@ -178,6 +194,9 @@ int launch_gemm_dense(const uint16_t* A, const uint16_t* B, bool b_n_major, int 
 int launch_gemm_partial_nmajor(const uint16_t* A, const uint16_t* B, int M, const int32_t* M_dev, int N, int K,
                                int ksplit, const PartialEpiParams& p, int32_t* status, int kernel_id,
                                cudaStream_t s, int64_t lda = 0, int b_k_wrap = 0);
+// (g, u) of the gated layer's fallback rows: A = their X rows (lda), B = W_gT and W_uT
+int launch_gemm_gu(const uint16_t* A, int64_t lda, const uint16_t* Bg, const uint16_t* Bu, int M, const int32_t* M_dev,
+                   int N, int K, const GUEpiParams& p, int32_t* status, int kernel_id, cudaStream_t s);
 int launch_gemm_mask(const uint16_t* A, const uint16_t* B, int M, int N, int K, const MaskEpiParams& p,
                      int32_t* status, int kernel_id, cudaStream_t s);
 // db[j] = sum over rows of Z[r][j] (bf16 [M][N], fp32 sums): row-chunk
@@ -233,6 +252,10 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
                 const uint16_t* dense_h = nullptr);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int32_t* row_counter, int kernel_id, cudaStream_t s);
+// out[n] = bf16(sum over row n's TwELL entries e of a_e W_a[j_e] + b_e W_b[j_e]),
+// (a_e, b_e) fp32 pairs per slot ([N][n_tiles][C][2]); fallback rows skipped
+int launch_spmm_f32x2(const twell_t& L, const float* pairs, const uint16_t* W_a, const uint16_t* W_b, int d_model,
+                      uint16_t* out, int32_t* row_counter, int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
 int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_model, uint16_t* out, int kernel_id,
                      cudaStream_t s);
@@ -270,11 +293,26 @@ struct BwdWorkspace {
   float* col_h;           // [capacity] h of each entry
   float* col_dz;          // [capacity] dZ of each entry
   int32_t* row_counter;   // [1] the dX gather's row counter (zeroed by the SDDMM GEMM)
+  // gated layer only (null otherwise); dz_cells is then [N][n_tiles][C][2]
+  // (dG, dU) pairs and part holds 2 ksplit splits (the gate's, then the up's)
+  uint16_t* du_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of the fallback rows' dU
+  float* gu_fb;           // [fb_pad][d_ff][2] (g, u) of the fallback rows, recomputed
+  float* col_du;          // [capacity] dU of each entry
 };
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
-                            void* base);
+                            void* base, bool gated = false);
+
+// The gated layer's extra operands of the backward (H = bf16(g u), g = X.W_g + b > 0,
+// u = X.W_u): W_inT is then W_g^T and dW_inT receives dW_g^T.
+struct GatedBwd {
+  const uint16_t* W_uT;   // [d_ff][d_model] bf16
+  const uint16_t* b;      // [d_ff] bf16 gate bias
+  const float* gu;        // [N][n_tiles][C][2] (g, u) at the stored slots (the training forward's)
+  float* dW_uT;           // [d_ff][d_model] fp32
+};
 int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down, const twell_t& L,
                const uint16_t* dY, float lambda, uint16_t* dX, float* dW_inT, float* dW_down, float* db,
-               int d_model, const BwdWorkspace& ws, cudaStream_t s, bool row_view = false);
+               int d_model, const BwdWorkspace& ws, cudaStream_t s, bool row_view = false,
+               const GatedBwd* gated = nullptr);
 
 }  // namespace twell

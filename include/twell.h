@@ -179,6 +179,17 @@ TWELL_API int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const
                                   int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y,
                                   void* workspace, size_t workspace_bytes, twell_stream_t stream);
 
+/* twell_gated_ffn_fwd for training: also keeps, for every stored slot of a
+ * TwELL cell, the gate g = X.W_g + b and the up value u = X.W_u (fp32) that
+ * twell_gated_ffn_bwd needs (dG = dh u, dU = dh g).
+ *   gu  device, [n_rows][d_ff / tile][cap][2] fp32, 16-byte aligned: (g, u) at
+ *       the slots below the cell's count; other slots (padding, fallback
+ *       rows, overflowed cells) are left as they are. */
+TWELL_API int twell_gated_ffn_fwd_train(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
+                                        const uint16_t* b, const uint16_t* W_down, int32_t n_rows,
+                                        int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y, float* gu,
+                                        void* workspace, size_t workspace_bytes, twell_stream_t stream);
+
 /* The forward pass for callers that cannot allocate device memory.  (The
  * paper and its pages have no counterpart: this is a deployment convenience
  * of this library.)  Some callers have no allocator of their own to hand --
@@ -244,6 +255,38 @@ TWELL_API size_t twell_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int3
 /* Workspace of twell_ffn_bwd for a tile-granular layout: twell_bwd_workspace_bytes
  * plus the row view (routing words, fb_cap slots, fb_cap dense rows). */
 TWELL_API size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
+                                                 int32_t cap, int32_t fb_cap);
+
+/* Backward of the gated layer (the Llama-style "sparse_llama" layer of the
+ * repo-explainer page, "The Repo's Two Jobs") for
+ *   L = sum(Y * dY) + l1_lambda * sum|H|,  Y = H.W_down,
+ *   H = bf16(g u) where g = X.W_g + b > 0 (else 0), u = X.W_u,
+ * with h's bf16 rounding passed straight through and the pattern h != 0 (the
+ * stored entries: h may be negative).  At the pattern
+ *   dh = dY.W_down^T + l1_lambda sign(h),  dG = dh u,  dU = dh g
+ * and 0 elsewhere.  Inputs as for twell_gated_ffn_fwd (row-granular layout
+ * only), plus
+ *   gu   device, what twell_gated_ffn_fwd_train kept for the same call: (g, u)
+ *        fp32 at every stored slot ([n_rows][d_ff / tile][cap][2]); the
+ *        fallback rows' g and u are recomputed here on the tensor cores.
+ * Outputs (all overwritten):
+ *   dX      [n_rows][d_model] bf16   dX[n] = sum_j dG[n][j] W_g^T[j] + dU[n][j] W_u^T[j]
+ *   dW_gT   [d_ff][d_model] fp32     dW_gT[j] = sum_n dG[n][j] X[n]
+ *   dW_uT   [d_ff][d_model] fp32     dW_uT[j] = sum_n dU[n][j] X[n]
+ *   dW_down [d_ff][d_model] fp32     dW_down[j] = sum_n h[n][j] dY[n]
+ *   db      [d_ff] fp32              db[j] = sum_n dG[n][j]  (the bias sits on the gate)
+ * Deterministic as twell_ffn_bwd.  workspace: device, >=
+ * twell_gated_bwd_workspace_bytes(...) bytes, 256-byte aligned.
+ * TWELL_ERR_UNSUPPORTED for a tile-granular layout, d_ff not a multiple of 128,
+ * or n_rows * (d_ff / tile) * cap above 2^31 - 1; TWELL_ERR_MISALIGNED when gu is
+ * not 16-byte aligned. */
+TWELL_API int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
+                                  const uint16_t* b, const uint16_t* W_down, const twell_t* H, const float* gu,
+                                  int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
+                                  float* dW_gT, float* dW_uT, float* dW_down, float* db, void* workspace,
+                                  size_t workspace_bytes, twell_stream_t stream);
+
+TWELL_API size_t twell_gated_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
                                                  int32_t cap, int32_t fb_cap);
 
 /* Dense comparator (not part of the method): Y = ReLU(X.W_in + b).W_down with

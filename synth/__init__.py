@@ -84,6 +84,9 @@ CONFIGS = {
                        forced_frac_rows=0.01, l1_lambda=1e-4),
     # gated (Llama-style) layer, bias at the gate's 99th percentile
     "gated": FFNConfig("gated", 4096, 4096, 14336, 128, 16, seed=2, gated=True),
+    # gated layer's training shape: lognormal row activity, 1% forced-dense rows, L1 on H
+    "gated_train": FFNConfig("gated_train", 4096, 4096, 14336, 128, 16, seed=5, gated=True, row_spread="lognormal",
+                             forced_frac_rows=0.01, l1_lambda=1e-4),
     # decode-shaped step: 16 tokens, bias calibrated on 4096 other tokens
     "decode": FFNConfig("decode", 16, 4096, 14336, 128, 16, seed=3, sparsity=0.995, calib_rows=4096),
 }

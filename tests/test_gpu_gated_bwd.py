@@ -1,0 +1,202 @@
+"""Training path of the gated (Llama-style) layer on the GPU, against the
+oracle: the forward that keeps (g, u) at the stored slots, and the backward
+(dG = dh u, dU = dh g at the pattern h != 0, both dX gathers, the unit-major
+walk with three outputs, the fallback rows' recomputed g and u and their
+tensor-core shares), using the H the GPU's forward produced so both sides share
+the pattern."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from twell_check import assert_close, from_dev_bits, from_dev_f32, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tw():
+    import __graft_entry__ as g
+    g.build()
+    import activation_sparse_transformer_gb300 as m
+    return m
+
+
+def _fwd_train(tw, torch, inp, T, C, fb_cap, train=True):
+    dev = torch.device("cuda")
+    X, Wg, Wu, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "W_uT", "b", "W_down"))
+    N, d = inp["X"].shape
+    f = inp["W_inT"].shape[0]
+    p = tw.alloc_packed(N, f, T, C, fb_cap, dev)
+    Y = torch.full((N, d), 3.0, dtype=torch.bfloat16, device=dev)
+    gu = torch.full((N, f // T, C, 2), 7.0, dtype=torch.float32, device=dev)
+    ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb_cap), dtype=torch.uint8, device=dev)
+    if train:
+        tw.twell_gated_ffn_fwd_train(X, Wg, Wu, b, Wd, p, Y, gu, ws)
+    else:
+        tw.twell_gated_ffn_fwd(X, Wg, Wu, b, Wd, p, Y, ws)
+    assert tw.twell_read_status(p) == 0
+    return p, Y, gu, (X, Wg, Wu, b, Wd)
+
+
+def _bwd(tw, torch, p, gu, dev_inp, dY, lam):
+    dev = torch.device("cuda")
+    X, Wg, Wu, b, Wd = dev_inp
+    N, d = X.shape
+    f, T, C, fb = p.d_ff, p.tile, p.cap, p.fb_cap
+    H = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+    tw.twell_unpack(p, H)
+    dX = torch.full((N, d), 5.0, dtype=torch.bfloat16, device=dev)
+    outs = [torch.full((f, d), 5.0, dtype=torch.float32, device=dev) for _ in range(3)]
+    db = torch.full((f,), 5.0, dtype=torch.float32, device=dev)
+    wsb = torch.full((tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb),), 0x5A, dtype=torch.uint8, device=dev)
+    tw.twell_gated_ffn_bwd(X, Wg, Wu, b, Wd, p, gu, to_dev(dY, torch), lam, dX, outs[0], outs[1], outs[2], db, wsb)
+    assert tw.twell_read_status(p) == 0
+    torch.cuda.synchronize()
+    return (from_dev_bits(H), from_dev_bits(dX), outs[0].cpu().numpy(), outs[1].cpu().numpy(),
+            outs[2].cpu().numpy(), db.cpu().numpy())
+
+
+def _integer_dy(N, d, seed):
+    rng = np.random.default_rng(seed)
+    return synth.f32_to_bf16_bits(rng.integers(-1, 2, size=(N, d)).astype(np.float32))
+
+
+@pytest.mark.parametrize("N,d,f,T,C,sp", [(256, 128, 512, 64, 8, 0.95), (200, 256, 1024, 128, 16, 0.97),
+                                          (130, 128, 512, 32, 4, 0.9)])
+def test_fwd_train_keeps_gate_and_up(tw, N, d, f, T, C, sp):
+    """(g, u) at every stored slot of a TwELL row equal the oracle's g (bias
+    applied) and u = X.W_u (integer layer: exact in fp32); the layout and Y are
+    those of the plain gated forward."""
+    import torch
+    inp = synth.make_integer_inputs(N, d, f, seed=N + f, lo=-1, hi=1, sparsity=sp, gated=True)
+    p, Y, gu, _ = _fwd_train(tw, torch, inp, T, C, N)
+    p0, Y0, _, _ = _fwd_train(tw, torch, inp, T, C, N, train=False)
+    n_fb = int(p.n_fb[0].item())
+    assert n_fb == int(p0.n_fb[0].item())
+    # fb_dense rows past n_fb are never written
+    for a, b in ((p.values, p0.values), (p.idx, p0.idx), (p.counts, p0.counts), (p.row_fb, p0.row_fb),
+                 (p.fb_dense[:n_fb], p0.fb_dense[:n_fb]), (Y, Y0)):
+        assert np.array_equal(from_dev_bits(a), from_dev_bits(b))
+    Zg, Hr = oracle.hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"])
+    U = synth.bf16_bits_to_f32(inp["X"]) @ synth.bf16_bits_to_f32(inp["W_uT"]).T
+    ref = oracle.pack(Hr, T, C, N)
+    gu = gu.cpu().numpy()
+    counts = ref["counts"]
+    idx = ref["idx"].astype(np.int64)
+    n, t, s = np.nonzero(np.arange(C)[None, None, :] < counts[:, :, None])
+    assert len(n) > 0
+    assert (ref["row_fb"][n] < 0).all()       # fallback rows have empty cells
+    j = t * T + idx[n, t, s]
+    assert np.array_equal(gu[n, t, s, 0], Zg[n, j])
+    assert np.array_equal(gu[n, t, s, 1], U[n, j].astype(np.float32))
+    assert (Zg[n, j] > 0).all()
+
+
+@pytest.mark.parametrize("N,d,f,T,C,sp,lam", [(256, 128, 512, 64, 8, 0.92, 1.0),
+                                              (200, 256, 1024, 128, 16, 0.9, 0.0),
+                                              # no fallback rows
+                                              (200, 256, 1024, 128, 16, 0.97, 1.0),
+                                              (130, 128, 512, 32, 4, 0.9, 2.0),
+                                              # a small batch (one M tile, zero-filled)
+                                              (16, 256, 1024, 64, 8, 0.9, 1.0)])
+def test_gated_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
+    """Integer layer and integer dY, lambda an integer: dG, dU and every sum are
+    exact in fp32 (the fallback rows' dG and dU fit the 16 bits of their high +
+    low bf16 parts), so the GPU's gradients equal the oracle's bit for bit."""
+    import torch
+    inp = synth.make_integer_inputs(N, d, f, seed=N + f + 1, lo=-1, hi=1, sparsity=sp, gated=True)
+    dY = _integer_dy(N, d, seed=N)
+    p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, T, C, N)
+    H, dX, dWg, dWu, dWd, db = _bwd(tw, torch, p, gu, dev_inp, dY, lam)
+    _, Hr = oracle.hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"])
+    assert np.array_equal(H, Hr)
+    n_fb = int(p.n_fb[0].item())
+    assert (n_fb > 0) == (sp < 0.97)
+    dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam)
+    assert np.abs(np.concatenate([dG, dU])).max() < 2 ** 15
+    rdX = oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"])
+    rWg, rWu, rWd, rdb = oracle.grad_weights_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], inp["W_down"], H,
+                                                   dY, lam)
+    for a in (rdX, rWg, rWu, rWd, rdb):
+        assert np.abs(a).max() < 2 ** 24
+    assert np.array_equal(dX, oracle.round_bf16(rdX))
+    assert np.array_equal(dWg, rWg)
+    assert np.array_equal(dWu, rWu)
+    assert np.array_equal(dWd, rWd)
+    assert np.array_equal(db, rdb)
+
+
+def test_gated_bwd_random_layer(tw):
+    import torch
+    cfg = synth.FFNConfig("g", 384, 512, 2048, 128, 16, seed=23, gated=True, fb_cap=96, row_spread="lognormal",
+                          forced_frac_rows=0.03)
+    inp = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=3)
+    lam = 1e-2
+    p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, cfg.tile, cfg.cap, cfg.fallback_capacity)
+    assert int(p.n_fb[0].item()) > 0
+    H, dX, dWg, dWu, dWd, db = _bwd(tw, torch, p, gu, dev_inp, dY, lam)
+    dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam)
+    assert_close(synth.bf16_bits_to_f32(dX), oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"]), "dX")
+    rWg, rWu, rWd, rdb = oracle.grad_weights_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], inp["W_down"], H,
+                                                   dY, lam)
+    assert_close(dWg, rWg, "dW_gT")
+    assert_close(dWu, rWu, "dW_uT")
+    assert_close(dWd, rWd, "dW_down")
+    assert_close(db, rdb, "db")
+
+
+def test_gated_bwd_full_size_sampled(tw):
+    """The gated layer's training shape (N = 4096, d_model 4096, d_ff 14336,
+    T 128, C 16, 1% forced-dense rows) checked on sampled rows (dX, with
+    fallback rows among them) and sampled hidden units (dW_g, dW_u, dW_down, db
+    over all rows)."""
+    import torch
+    cfg = synth.CONFIGS["gated_train"]
+    inp = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=78)
+    lam = cfg.l1_lambda
+    p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, cfg.tile, cfg.cap, cfg.fallback_capacity)
+    H, dX, dWg, dWu, dWd, db = _bwd(tw, torch, p, gu, dev_inp, dY, lam)
+    rng = np.random.default_rng(6)
+    rows = rng.choice(cfg.n_rows, size=24, replace=False)
+    fbrows = np.nonzero(from_dev_bits(p.row_fb)[:cfg.n_rows] >= 0)[0][:8]
+    assert len(fbrows) > 0
+    rows = np.unique(np.concatenate([rows, fbrows])).astype(np.int32)
+    dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam,
+                                      rows=rows)
+    assert_close(synth.bf16_bits_to_f32(dX[rows]), oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"]), "dX")
+    cols = np.sort(rng.choice(cfg.d_ff, size=24, replace=False)).astype(np.int32)
+    rWg, rWu, rWd, rdb = oracle.grad_weights_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], inp["W_down"], H,
+                                                   dY, lam, cols=cols)
+    assert_close(dWg[cols], rWg, "dW_gT")
+    assert_close(dWu[cols], rWu, "dW_uT")
+    assert_close(dWd[cols], rWd, "dW_down")
+    assert_close(db[cols], rdb, "db")
+
+
+def test_gated_bwd_refuses(tw):
+    """A tile-granular layout and a short workspace are refused before any launch."""
+    import torch
+    dev = torch.device("cuda")
+    N, d, f, T, C, fb = 64, 128, 512, 64, 8, 16
+    X = torch.zeros((N, d), dtype=torch.bfloat16, device=dev)
+    W = torch.zeros((f, d), dtype=torch.bfloat16, device=dev)
+    b = torch.zeros((f,), dtype=torch.bfloat16, device=dev)
+    gu = torch.zeros((N, f // T, C, 2), dtype=torch.float32, device=dev)
+    dX = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    o = [torch.empty((f, d), dtype=torch.float32, device=dev) for _ in range(3)]
+    db = torch.empty((f,), dtype=torch.float32, device=dev)
+    lib = tw.load_library()
+    need = tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb)
+    assert need > tw.bwd_workspace_bytes(N, d, f, T, C, fb)
+    ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+    for hybrid, nbytes, want in ((tw.HYBRID_ROWS, need - 256, -5), (tw.HYBRID_TILES, need, -3)):
+        p = tw.alloc_packed(N, f, T, C, fb, dev, hybrid=hybrid)
+        st = p.struct()
+        rc = lib.twell_gated_ffn_bwd(X.data_ptr(), W.data_ptr(), W.data_ptr(), b.data_ptr(), W.data_ptr(),
+                                     tw.ctypes.byref(st), gu.data_ptr(), d, X.data_ptr(), 0.0, dX.data_ptr(),
+                                     o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), db.data_ptr(), ws.data_ptr(),
+                                     nbytes, None)
+        assert rc == want, tw.status_string(rc)
