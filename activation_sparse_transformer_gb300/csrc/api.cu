@@ -95,7 +95,8 @@ AuxFork::AuxFork(cudaStream_t s) : s_(s) {
   aux_ = aux_stream_for(dev, s);
   if (!aux_ || cudaEventCreateWithFlags(&fork_, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&join_, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&mid_, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&mid_, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&refork_, cudaEventDisableTiming) != cudaSuccess) {
     rc_ = TWELL_ERR_CUDA;
     return;
   }
@@ -123,10 +124,17 @@ int AuxFork::main_wait_mark() {
   return rc_;
 }
 
+int AuxFork::aux_wait_main() {
+  if (joined_ || rc_ != 0) return rc_;
+  if (cudaEventRecord(refork_, s_) != cudaSuccess || cudaStreamWaitEvent(aux_, refork_, 0) != cudaSuccess)
+    rc_ = TWELL_ERR_CUDA;
+  return rc_;
+}
+
 AuxFork::~AuxFork() {
   join();
   // released by the runtime once the recorded work has completed
-  for (cudaEvent_t e : {fork_, join_, mid_})
+  for (cudaEvent_t e : {fork_, join_, mid_, refork_})
     if (e) cudaEventDestroy(e);
 }
 

@@ -378,6 +378,47 @@ __global__ void fb_operands_kernel(Layout L, const uint16_t* __restrict__ X, con
   }
 }
 
+// The gated layer's fallback rows: dG = dh' u and dU = dh' g from the SDDMM's
+// dense dh' and the recomputed (g, u), as high + low bf16 parts (rows 2 s and
+// 2 s + 1 of dz_hl and du_hl); eight units per thread.
+__global__ void __launch_bounds__(256)
+    gated_fb_parts_kernel(Layout L, const float* __restrict__ dh_fb, const float* __restrict__ gu_fb,
+                          uint16_t* __restrict__ dz_hl, uint16_t* __restrict__ du_hl) {
+  const int nfb = min(*L.n_fb, L.fb_cap);
+  for (int slot = blockIdx.x; slot < nfb; slot += gridDim.x) {
+    for (int j = threadIdx.x * 8; j < L.f; j += blockDim.x * 8) {
+      const int64_t o = static_cast<int64_t>(slot) * L.f + j;
+      const float4* dp = reinterpret_cast<const float4*>(dh_fb + o);
+      const float4* gp = reinterpret_cast<const float4*>(gu_fb + 2 * o);
+      const float4 d0 = dp[0], d1 = dp[1];
+      const float dh[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+      uint32_t w[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 p2 = gp[q];  // (g, u) of units j + 2q and j + 2q + 1
+        const float g[2] = {p2.x, p2.z}, u[2] = {p2.y, p2.w};
+        w[0][q] = w[1][q] = w[2][q] = w[3][q] = 0u;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float dg = dh[2 * q + e] * u[e], du = dh[2 * q + e] * g[e];
+          const uint16_t gh = float_to_bf16_bits(dg), uh = float_to_bf16_bits(du);
+          const uint16_t gl = float_to_bf16_bits(dg - bf16_bits_to_float(gh));
+          const uint16_t ul = float_to_bf16_bits(du - bf16_bits_to_float(uh));
+          w[0][q] |= static_cast<uint32_t>(gh) << (16 * e);
+          w[1][q] |= static_cast<uint32_t>(gl) << (16 * e);
+          w[2][q] |= static_cast<uint32_t>(uh) << (16 * e);
+          w[3][q] |= static_cast<uint32_t>(ul) << (16 * e);
+        }
+      }
+      const int64_t hi = static_cast<int64_t>(2 * slot) * L.f + j, lo = hi + L.f;
+      *reinterpret_cast<uint4*>(dz_hl + hi) = make_uint4(w[0][0], w[0][1], w[0][2], w[0][3]);
+      *reinterpret_cast<uint4*>(dz_hl + lo) = make_uint4(w[1][0], w[1][1], w[1][2], w[1][3]);
+      *reinterpret_cast<uint4*>(du_hl + hi) = make_uint4(w[2][0], w[2][1], w[2][2], w[2][3]);
+      *reinterpret_cast<uint4*>(du_hl + lo) = make_uint4(w[3][0], w[3][1], w[3][2], w[3][3]);
+    }
+  }
+}
+
 // db[j] += sum over the fallback slots of dZ[slot][j] (= high + low part): a
 // CTA covers 32 units, warp w sums slots w, w + 8, ... and the eight partial
 // sums are added in warp order (a fixed order, so the result is deterministic).
@@ -437,6 +478,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t o_cnt = take(sizeof(int32_t));
   const size_t o_duhl = gated ? take(sizeof(uint16_t) * 2 * padf) : 0;
   const size_t o_gufb = gated ? take(sizeof(float) * 2 * padf) : 0;
+  const size_t o_dhfb = gated ? take(sizeof(float) * padf) : 0;
   const size_t o_du = gated ? take(sizeof(float) * cells) : 0;
   if (ws && base) {
     uint8_t* b = static_cast<uint8_t*>(base);
@@ -456,6 +498,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->row_counter = reinterpret_cast<int32_t*>(b + o_cnt);
     ws->du_hl = gated ? reinterpret_cast<uint16_t*>(b + o_duhl) : nullptr;
     ws->gu_fb = gated ? reinterpret_cast<float*>(b + o_gufb) : nullptr;
+    ws->dh_fb = gated ? reinterpret_cast<float*>(b + o_dhfb) : nullptr;
     ws->col_du = gated ? reinterpret_cast<float*>(b + o_du) : nullptr;
   }
   return off;
@@ -479,36 +522,42 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
   const int N = Lh.n_rows;
   const bool fb = Lh.fb_cap > 0 && N > 0;
   const int fb_grid = std::max(1, std::min(2 * ws.fb_pad, 2 * sm_count()));
-  if (gt && fb) {
-    // gated: the fallback rows' operands, then their g and u (recomputed on the
-    // tensor cores from the gathered X rows: row s of xg2 read with stride
-    // 2 d_model), which the SDDMM's epilogue needs for dG = dh' u, dU = dh' g
-    {
-      LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, s);
-      fb_operands_kernel<<<fb_grid, 256, 0, s>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad, ws.du_hl);
-    }
-    TW_CHECK_LAUNCH();
-    GUEpiParams gp{gt->b, ws.gu_fb, f};
-    TW_TRY_RC(launch_gemm_gu(ws.xg2, 2 * static_cast<int64_t>(d), W_inT, gt->W_uT, Lh.fb_cap, Lh.n_fb, f, d, gp,
-                             Lh.status, TWELL_KERNEL_SDDMM, s));
-  }
-  if (N > 0) {
-    // dZ at the pattern (and dense for fallback rows, with its bf16 parts)
-    SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb,  Lh.fb_dense,         Lh.fb_cap,
-                       f / Lh.tile, Lh.tile, Lh.cap,   f,          lambda,              ws.dz_cells,
-                       ws.dz_hl,    gt ? gt->gu : nullptr, gt ? ws.gu_fb : nullptr, gt ? ws.du_hl : nullptr};
-    // its CTA 0 also zeroes the dX gather's row counter
-    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
-  }
   // Second stream: the fallback rows' weight-gradient share (stored into dW
   // first), then dX (the TwELL rows' gather-SpMM, then the fallback rows' GEMM).  This
-  // stream: the unit-major lists (independent of the fallback share), then
+  // stream: the SDDMM, the unit-major lists (independent of the fallback share), then
   // dw_unitcta_kernel adds the TwELL share once the fallback share is in place.
   AuxFork fork(s);
   TW_TRY_RC(fork.status());
   cudaStream_t a = fork.aux();
+  if (gt && fb) {
+    // gated, beside the SDDMM: the fallback rows' operands, then their g and
+    // u, recomputed on the tensor cores from the gathered X rows (row s of xg2
+    // read with stride 2 d_model)
+    {
+      LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, a);
+      fb_operands_kernel<<<fb_grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad, ws.du_hl);
+    }
+    TW_CHECK_LAUNCH();
+    GUEpiParams gp{gt->b, ws.gu_fb, f};
+    TW_TRY_RC(launch_gemm_gu(ws.xg2, 2 * static_cast<int64_t>(d), W_inT, gt->W_uT, Lh.fb_cap, Lh.n_fb, f, d, gp,
+                             Lh.status, TWELL_KERNEL_DW_FALLBACK, a));
+  }
+  if (N > 0) {
+    // dZ at the pattern (and dense for fallback rows: its bf16 parts, or the
+    // gated layer's dh')
+    SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap,
+                       f / Lh.tile, Lh.tile, Lh.cap,   f,         lambda,      ws.dz_cells,
+                       ws.dz_hl,    gt ? gt->gu : nullptr, gt ? ws.dh_fb : nullptr};
+    // its CTA 0 also zeroes the dX gather's row counter
+    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
+  }
+  TW_TRY_RC(fork.aux_wait_main());  // the SDDMM's outputs are in
   if (fb) {
-    if (!gt) {
+    if (gt) {
+      LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, a);
+      gated_fb_parts_kernel<<<std::max(1, std::min(Lh.fb_cap, 2 * sm_count())), 256, 0, a>>>(L, ws.dh_fb, ws.gu_fb,
+                                                                                          ws.dz_hl, ws.du_hl);
+    } else {
       LaunchScope ls(TWELL_KERNEL_DW_FALLBACK, a);
       fb_operands_kernel<<<fb_grid, 256, 0, a>>>(L, X, dY, d, ws.hfb, ws.dyg, ws.xg2, ws.dz_hl, ws.fb_pad, nullptr);
     }

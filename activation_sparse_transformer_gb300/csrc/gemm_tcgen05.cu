@@ -579,51 +579,22 @@ struct SampleEpi {
           }
         }
       } else if (fb < p.fb_cap && p.gu) {
-        // gated fallback row: dense dG and dU over the 32 columns, as high + low bf16 parts
+        // gated fallback row: dense dh' (0 where h == 0); dG and dU are formed
+        // once the fallback rows' g and u are in (a second stream computes them)
         const uint4* hp = reinterpret_cast<const uint4*>(p.fb_dense + static_cast<int64_t>(fb) * p.d_ff + col);
-        const float4* gp = reinterpret_cast<const float4*>(p.gu_fb + (static_cast<int64_t>(fb) * p.d_ff + col) * 2);
         uint4 hq[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) hq[q] = hp[q];
-        uint32_t ghi[16], glo[16], uhi[16], ulo[16];
+        float4* o = reinterpret_cast<float4*>(p.dh_fb + static_cast<int64_t>(fb) * p.d_ff + col);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float4 gu2 = gp[i / 2];  // (g, u) of columns i and i + 1
-          float og[2], ou[2];
+        for (int q = 0; q < 8; ++q) {
+          float v[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float h = bias_at(hq, i + e);
-            const float dhl = __uint_as_float(r[i + e]) + (h > 0.0f ? p.lambda : -p.lambda);
-            og[e] = h != 0.0f ? dhl * (e ? gu2.w : gu2.y) : 0.0f;
-            ou[e] = h != 0.0f ? dhl * (e ? gu2.z : gu2.x) : 0.0f;
+          for (int e = 0; e < 4; ++e) {
+            const float h = bias_at(hq, 4 * q + e);
+            v[e] = h != 0.0f ? __uint_as_float(r[4 * q + e]) + (h > 0.0f ? p.lambda : -p.lambda) : 0.0f;
           }
-          uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const uint16_t gh = float_to_bf16_bits(og[e]);
-            const uint16_t gl = float_to_bf16_bits(og[e] - bf16_bits_to_float(gh));
-            const uint16_t uh = float_to_bf16_bits(ou[e]);
-            const uint16_t ul = float_to_bf16_bits(ou[e] - bf16_bits_to_float(uh));
-            w[0] |= static_cast<uint32_t>(gh) << (16 * e);
-            w[1] |= static_cast<uint32_t>(gl) << (16 * e);
-            w[2] |= static_cast<uint32_t>(uh) << (16 * e);
-            w[3] |= static_cast<uint32_t>(ul) << (16 * e);
-          }
-          ghi[i / 2] = w[0];
-          glo[i / 2] = w[1];
-          uhi[i / 2] = w[2];
-          ulo[i / 2] = w[3];
-        }
-        uint4* g0 = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
-        uint4* g1 = reinterpret_cast<uint4*>(p.dz_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
-        uint4* u0 = reinterpret_cast<uint4*>(p.du_hl + static_cast<int64_t>(2 * fb) * p.d_ff + col);
-        uint4* u1 = reinterpret_cast<uint4*>(p.du_hl + static_cast<int64_t>(2 * fb + 1) * p.d_ff + col);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          g0[q] = make_uint4(ghi[4 * q], ghi[4 * q + 1], ghi[4 * q + 2], ghi[4 * q + 3]);
-          g1[q] = make_uint4(glo[4 * q], glo[4 * q + 1], glo[4 * q + 2], glo[4 * q + 3]);
-          u0[q] = make_uint4(uhi[4 * q], uhi[4 * q + 1], uhi[4 * q + 2], uhi[4 * q + 3]);
-          u1[q] = make_uint4(ulo[4 * q], ulo[4 * q + 1], ulo[4 * q + 2], ulo[4 * q + 3]);
+          o[q] = make_float4(v[0], v[1], v[2], v[3]);
         }
       } else if (fb < p.fb_cap) {
         // fallback row: dense dZ over all 32 columns

@@ -73,11 +73,13 @@ class AuxFork {
   // so s can queue independent work in between
   int mark_aux();
   int main_wait_mark();
+  // aux waits for everything queued on s so far (a second fork point)
+  int aux_wait_main();
 
  private:
   cudaStream_t s_;
   cudaStream_t aux_ = nullptr;
-  cudaEvent_t fork_ = nullptr, join_ = nullptr, mid_ = nullptr;
+  cudaEvent_t fork_ = nullptr, join_ = nullptr, mid_ = nullptr, refork_ = nullptr;
   int rc_ = 0;
   bool joined_ = false;
 };
@@ -154,11 +156,10 @@ struct SampleEpiParams {
                             // row 2s = bf16(dz) (high part), row 2s+1 = bf16(dz - high) (low
                             // part); high + low carry dz to ~2^-17 relative
   // gated layer (gu non-null): the pattern is h != 0 and dh' = dH + lambda sign(h);
-  // dz_cells then holds (dG, dU) = (dh' u, dh' g) pairs per slot ([M][n_tiles][C][2]),
-  // dz_hl the parts of dG and du_hl those of dU
+  // dz_cells then holds (dG, dU) = (dh' u, dh' g) pairs per slot ([M][n_tiles][C][2])
+  // and the fallback rows' dense dh' goes to dh_fb (dz_hl is not written)
   const float* gu;          // (g, u) at the stored slots [M][n_tiles][C][2]
-  const float* gu_fb;       // (g, u) of the fallback rows [fb_pad][d_ff][2]
-  uint16_t* du_hl;
+  float* dh_fb;             // [fb_pad][d_ff] fp32 dh' of the fallback rows (0 where h == 0)
 };
 
 // g = X.W_g + b and u = X.W_u of the gated layer's fallback rows, kept as
@@ -297,6 +298,7 @@ struct BwdWorkspace {
   // (dG, dU) pairs and part holds 2 ksplit splits (the gate's, then the up's)
   uint16_t* du_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of the fallback rows' dU
   float* gu_fb;           // [fb_pad][d_ff][2] (g, u) of the fallback rows, recomputed
+  float* dh_fb;           // [fb_pad][d_ff] fp32 dh' of the fallback rows
   float* col_du;          // [capacity] dU of each entry
 };
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,

@@ -683,7 +683,106 @@ def bench_ours(args, rank, world, local):
     }
     if world == 1 and not args.no_memory:
         result["train_memory"] = bench_train_memory(tw, dev, args)
+        result["gated_train"] = bench_gated_train(tw, dev, args)
     return result
+
+
+def bench_gated_train(tw, dev, args):
+    """One training step of the gated layer (twell_gated_ffn_fwd_train, then
+    twell_gated_ffn_bwd) at its training shape: median time with L2 scrubbed
+    before each step, the per-kernel device times, the allocator's peak over a
+    step (inputs, weights and dY allocated before and not counted), and the
+    tensor-core floor of the GEMM work the step does densely."""
+    import numpy as np
+    import torch
+
+    import synth
+    cfg = synth.CONFIGS["gated_train"]
+    inp = synth.make_ffn_inputs(cfg)
+    N, d, f, T, C, fb = cfg.n_rows, cfg.d_model, cfg.d_ff, cfg.tile, cfg.cap, cfg.fallback_capacity
+    lam = cfg.l1_lambda
+    peaks, peak_src = load_peaks()
+
+    def dt(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    X, Wg, Wu, b, Wd = (dt(inp[k]) for k in ("X", "W_inT", "W_uT", "b", "W_down"))
+    dY = dt(synth.make_grad_output(N, d, seed=cfg.seed + 77))
+    flush = torch.empty(max(2 * torch.cuda.get_device_properties(dev).L2_cache_size, 256 << 20),
+                        dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    packed = tw.alloc_packed(N, f, T, C, fb, dev)
+    gu = torch.empty((N, f // T, C, 2), dtype=torch.float32, device=dev)
+    Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    dW = [torch.empty((f, d), dtype=torch.float32, device=dev) for _ in range(3)]
+    db = torch.empty((f,), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(tw.fwd_workspace_bytes(N, d, f, T, C, fb), tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb)),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        tw.twell_gated_ffn_fwd_train(X, Wg, Wu, b, Wd, packed, Y, gu, ws, stream)
+        tw.twell_gated_ffn_bwd(X, Wg, Wu, b, Wd, packed, gu, dY, lam, dX, dW[0], dW[1], dW[2], db, ws, stream)
+
+    step()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    rc = tw.twell_read_status(packed, stream)
+    if rc != 0:
+        raise RuntimeError(f"gated training step: status {rc}")
+    n_fb = int(packed.n_fb[0].item())
+    nnz = int(packed.counts.to(torch.int64).sum().item())
+    for _ in range(args.warmup):
+        step()
+    k = max(10, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(bb) for a, bb in ev)
+    tw.twell_profile_reset()
+    tw.twell_profile_enable(True)
+    for _ in range(10):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    tw.twell_profile_enable(False)
+    kernels = {}
+    for name in tw.KERNELS:
+        n_l, k_ms = tw.twell_profile_read(name)
+        if n_l:
+            kernels[name] = {"launches": n_l, "avg_us": round(1000.0 * k_ms / n_l, 2)}
+    # dense GEMM work on the tensor cores: gate and up (4 N d f), the SDDMM's dY.W_down^T (2 N d f)
+    floor_us = 6.0 * N * d * f / (peaks["bf16_tflops"] * 1e12) * 1e6
+    dense_floor_us = 18.0 * N * d * f / (peaks["bf16_tflops"] * 1e12) * 1e6
+    kept = packed.values.numel() * 2 + packed.idx.numel() + packed.counts.numel() + fb * f * 2 + gu.numel() * 4
+    out = {
+        "workload": (f"gated layer training step fwd+bwd: N={N} d_model={d} d_ff={f} T={T} C={C}, lognormal rows, "
+                     f"1% rows at 20%, lambda {lam}"),
+        "ms_per_step": round(ms, 4), "tokens_per_s": round(N / (ms * 1e-3), 1),
+        "peak_bytes": int(peak),
+        "kept_for_backward_bytes": int(kept),
+        "dense_h_bytes": N * f * 2,
+        "layer": {"n_fb": n_fb, "twell_entries": nnz},
+        "kernels": kernels,
+        "roofline": {"bound": "tensor (gate + up GEMM and the SDDMM's GEMM)", "time_us": round(floor_us, 2),
+                     "frac": round(floor_us / (ms * 1e3), 4), "peak_source": peak_src,
+                     "dense_step_floor_us": round(dense_floor_us, 2)},
+        "how": ("median of scrubbed steps; kept_for_backward = the packed H and the (g, u) pairs of its stored "
+                "slots (dense_h_bytes: one dense bf16 [N, d_ff] for scale); dense_step_floor_us = 18 N d f at the same peak, the GEMM work of a dense gated fwd+bwd (not "
+                "run)"),
+    }
+    del X, Wg, Wu, b, Wd, dY, packed, gu, Y, dX, dW, db, ws, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_train_memory(tw, dev, args):
@@ -1055,7 +1154,8 @@ def main():
     ap.add_argument("--next", action="store_true",
                     help="forward-only lines for the gated layer and the decode sweep instead of the main step")
     ap.add_argument("--no-memory", action="store_true",
-                    help="skip the training-shape peak-memory comparison against the dense step")
+                    help="skip the training-shape peak-memory comparison against the dense step and the gated "
+                         "layer's training step")
     ap.add_argument("--no-next", action="store_true",
                     help="leave the next shapes' summary (gated layer, decode sweep, tile routing) out of the line")
     ap.add_argument("--min-window", type=float, default=1.0,
