@@ -475,11 +475,13 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const size_t o_rows = take(sizeof(int32_t) * cells);
   const size_t o_h = take(sizeof(float) * cells);
   const size_t o_dz = take(sizeof(float) * cells);
-  const size_t o_cnt = take(sizeof(int32_t));
+  const size_t o_cnt = take(sizeof(int32_t) * 8);  // row counters, one per dX gather pass
   const size_t o_duhl = gated ? take(sizeof(uint16_t) * 2 * padf) : 0;
   const size_t o_gufb = gated ? take(sizeof(float) * 2 * padf) : 0;
   const size_t o_dhfb = gated ? take(sizeof(float) * padf) : 0;
   const size_t o_du = gated ? take(sizeof(float) * cells) : 0;
+  const int dx_passes = gated ? spmm_pair_passes(d_model, d_ff, T) : 1;
+  const size_t o_dxacc = dx_passes > 1 ? take(sizeof(float) * static_cast<size_t>(N) * d_model) : 0;
   if (ws && base) {
     uint8_t* b = static_cast<uint8_t*>(base);
     ws->dz_cells = reinterpret_cast<float*>(b + o_dzc);
@@ -500,6 +502,8 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->gu_fb = gated ? reinterpret_cast<float*>(b + o_gufb) : nullptr;
     ws->dh_fb = gated ? reinterpret_cast<float*>(b + o_dhfb) : nullptr;
     ws->col_du = gated ? reinterpret_cast<float*>(b + o_du) : nullptr;
+    ws->dx_acc = dx_passes > 1 ? reinterpret_cast<float*>(b + o_dxacc) : nullptr;
+    ws->dx_passes = dx_passes;
   }
   return off;
 }
@@ -548,8 +552,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     SampleEpiParams sp{Lh.values, Lh.idx,   Lh.counts, Lh.row_fb, Lh.fb_dense, Lh.fb_cap,
                        f / Lh.tile, Lh.tile, Lh.cap,   f,         lambda,      ws.dz_cells,
                        ws.dz_hl,    gt ? gt->gu : nullptr, gt ? ws.dh_fb : nullptr};
-    // its CTA 0 also zeroes the dX gather's row counter
-    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, 1));
+    // its CTA 0 also zeroes the dX gather's row counters
+    TW_TRY_RC(launch_gemm_sample(dY, W_down, N, f, d, sp, Lh.status, s, ws.row_counter, ws.dx_passes));
   }
   TW_TRY_RC(fork.aux_wait_main());  // the SDDMM's outputs are in
   if (fb) {
@@ -576,7 +580,8 @@ int launch_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_down,
     // the TwELL rows' dX gather first: it needs only the SDDMM's output and,
     // queued after the fallback rows' dX, it waited for SMs held by the dW walk
     if (gt)
-      TW_TRY_RC(launch_spmm_f32x2(Lh, ws.dz_cells, W_inT, gt->W_uT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
+      TW_TRY_RC(launch_spmm_f32x2(Lh, ws.dz_cells, W_inT, gt->W_uT, d, dX, ws.row_counter, ws.dx_acc, ws.dx_passes,
+                                  TWELL_KERNEL_DX, a));
     else
       TW_TRY_RC(launch_spmm_f32(Lh, ws.dz_cells, W_inT, d, dX, ws.row_counter, TWELL_KERNEL_DX, a));
     if (fb) {

@@ -254,9 +254,13 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int32_t* row_counter, int kernel_id, cudaStream_t s);
 // out[n] = bf16(sum over row n's TwELL entries e of a_e W_a[j_e] + b_e W_b[j_e]),
-// (a_e, b_e) fp32 pairs per slot ([N][n_tiles][C][2]); fallback rows skipped
+// (a_e, b_e) fp32 pairs per slot ([N][n_tiles][C][2]); fallback rows skipped.
+// passes > 1: in that many launches over consecutive tile ranges, summed in
+// range order through acc ([N][d_model] fp32); row_counters: one zeroed word
+// per pass (or null)
+int spmm_pair_passes(int d_model, int d_ff, int tile);
 int launch_spmm_f32x2(const twell_t& L, const float* pairs, const uint16_t* W_a, const uint16_t* W_b, int d_model,
-                      uint16_t* out, int32_t* row_counter, int kernel_id, cudaStream_t s);
+                      uint16_t* out, int32_t* row_counters, float* acc, int passes, int kernel_id, cudaStream_t s);
 // out[fb_rows[r]] = bf16(sum over nsplit of part[k][r]) for the fallback rows
 int launch_fb_reduce(const twell_t& L, const float* part, int nsplit, int d_model, uint16_t* out, int kernel_id,
                      cudaStream_t s);
@@ -293,13 +297,15 @@ struct BwdWorkspace {
   int32_t* col_rows;      // [capacity] row of each entry, grouped by unit, rows ascending
   float* col_h;           // [capacity] h of each entry
   float* col_dz;          // [capacity] dZ of each entry
-  int32_t* row_counter;   // [1] the dX gather's row counter (zeroed by the SDDMM GEMM)
+  int32_t* row_counter;   // [dx_passes] the dX gather's row counters (zeroed by the SDDMM GEMM)
   // gated layer only (null otherwise); dz_cells is then [N][n_tiles][C][2]
   // (dG, dU) pairs and part holds 2 ksplit splits (the gate's, then the up's)
   uint16_t* du_hl;        // [2 * fb_pad][d_ff] bf16 high / low parts of the fallback rows' dU
   float* gu_fb;           // [fb_pad][d_ff][2] (g, u) of the fallback rows, recomputed
   float* dh_fb;           // [fb_pad][d_ff] fp32 dh' of the fallback rows
   float* col_du;          // [capacity] dU of each entry
+  float* dx_acc;          // [N][d_model] fp32 sums between the dX gather's passes (null: one pass)
+  int32_t dx_passes;
 };
 size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_cap, BwdWorkspace* ws,
                             void* base, bool gated = false);

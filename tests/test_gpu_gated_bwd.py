@@ -127,6 +127,26 @@ def test_gated_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
     assert np.array_equal(db, rdb)
 
 
+def test_gated_dx_in_passes_integer_bit_exact(tw):
+    """W_g and W_u rows larger than the dX gather's L2 budget (2 x 59 MB at
+    d_model 2048, d_ff 14336) make it run in passes over tile ranges, with the
+    fp32 sums carried between passes: on an integer layer dX (and db) are
+    still the oracle's bits."""
+    import torch
+    N, d, f, T, C, sp, lam = 200, 2048, 14336, 128, 16, 0.95, 1.0
+    inp = synth.make_integer_inputs(N, d, f, seed=77, lo=-1, hi=1, sparsity=sp, gated=True)
+    dY = _integer_dy(N, d, seed=78)
+    p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, T, C, N)
+    H, dX, dWg, dWu, dWd, db = _bwd(tw, torch, p, gu, dev_inp, dY, lam)
+    assert int(p.n_fb[0].item()) > 0
+    dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam)
+    assert np.abs(np.concatenate([dG, dU])).max() < 2 ** 15
+    rdX = oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"])
+    assert np.abs(rdX).max() < 2 ** 24
+    assert np.array_equal(dX, oracle.round_bf16(rdX))
+    assert np.array_equal(db, dG.sum(axis=0, dtype=np.float64).astype(np.float32))
+
+
 def test_gated_bwd_random_layer(tw):
     import torch
     cfg = synth.FFNConfig("g", 384, 512, 2048, 128, 16, seed=23, gated=True, fb_cap=96, row_spread="lognormal",
