@@ -352,9 +352,12 @@ struct FwdWorkspace {
   size_t up_part_off, h_off, arrivals_off;
   int spmm_nsplit;
   size_t spmm_part_off;
+  int spmm_passes;           // whole-row gather in tile-range passes (row-granular layouts)
+  size_t spmm_acc_off;       // their fp32 sums [N][d_model]
 };
 
-FwdWorkspace fwd_workspace_layout(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t fb_cap) {
+FwdWorkspace fwd_workspace_layout(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t fb_cap,
+                                  bool tiles = false) {
   FwdWorkspace w{};
   const int64_t nt = d_ff / tile;
   w.spill_cap = static_cast<int32_t>(std::min<int64_t>(static_cast<int64_t>(fb_cap) * nt, 0xFFFFFF));
@@ -386,6 +389,12 @@ FwdWorkspace fwd_workspace_layout(int32_t n_rows, int32_t d_model, int32_t d_ff,
   if (w.spmm_nsplit > 1) {
     w.spmm_part_off = off;
     off += align256(sizeof(float) * static_cast<size_t>(w.spmm_nsplit) * n_rows * d_model);
+  }
+  // the count word's 256 bytes hold the spill count and one row counter per pass
+  w.spmm_passes = (!w.swap && w.spmm_nsplit == 1 && !tiles) ? spmm_single_passes(d_model, d_ff, tile) : 1;
+  if (w.spmm_passes > 1) {
+    w.spmm_acc_off = off;
+    off += align256(sizeof(float) * static_cast<size_t>(n_rows) * d_model);
   }
   w.total = off;
   return w;
@@ -421,7 +430,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   if (W_uT && 128 % H->tile != 0) return TWELL_ERR_UNSUPPORTED;
   const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
   if (tiles && (W_uT || (n_rows > 0 && n_rows <= kSwapMaxTokens))) return TWELL_ERR_UNSUPPORTED;
-  const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap);
+  const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap, tiles);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
   if (n_rows == 0) return TWELL_OK;
@@ -456,7 +465,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
     // the last CTA of the pack pass also routes the rows
     TW_TRY(launch_pack_partials(up_part, w.up_ksplit, b, Hd, *H, arrivals, s));
   } else {
-    TW_CUDA(cudaMemsetAsync(spill_count, 0, 2 * sizeof(int32_t), s));
+    // the spill count and the gather's row counter(s), one per pass
+    TW_CUDA(cudaMemsetAsync(spill_count, 0, (1 + w.spmm_passes) * sizeof(int32_t), s));
     PackEpiParams pp{b, H->values, H->idx, H->counts, H->row_fb, spill, spill_count, w.spill_cap, H->status,
                      d_ff / H->tile, H->tile, H->cap, gu};
     if (W_uT)
@@ -492,7 +502,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
       TW_TRY(launch_fb_down(*H, W_down, d_model, Y, part, w.ksplit, fork.aux()));
     }
     TW_TRY(launch_spmm(*H, W_down, d_model, Y, spmm_part, w.spmm_nsplit, arrivals ? arrivals + 64 : nullptr,
-                       row_counter, s, swap ? Hd : nullptr));
+                       row_counter, s, swap ? Hd : nullptr, w.spmm_passes,
+                       w.spmm_passes > 1 ? reinterpret_cast<float*>(ws + w.spmm_acc_off) : nullptr));
     TW_TRY(fork.join());
   }
   return TWELL_OK;

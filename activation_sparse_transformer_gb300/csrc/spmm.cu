@@ -492,8 +492,14 @@ int spmm_nsplit(int n_rows, int d_model) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, (4096 + warps - 1) / warps)));
 }
 
+int spmm_single_passes(int d_model, int d_ff, int tile) {
+  const double bytes = 2.0 * d_ff * static_cast<double>(d_model);
+  return std::max(1, std::min({d_ff / tile, 8, static_cast<int>(bytes / (64.0 * 1024 * 1024) + 0.999)}));
+}
+
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
-                int32_t* arrivals, int32_t* row_counter, cudaStream_t s, const uint16_t* dense_h) {
+                int32_t* arrivals, int32_t* row_counter, cudaStream_t s, const uint16_t* dense_h, int passes,
+                float* acc) {
   if (dense_h && (L.hybrid == TWELL_HYBRID_TILES || L.tile % 32 != 0)) return TWELL_ERR_UNSUPPORTED;
   SpmmArgs a{L.values,
              L.idx,
@@ -511,6 +517,22 @@ int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t*
              L.cap,
              L.status,
              dense_h};
+  if (passes > 1) {
+    // whole TwELL rows in tile-range passes (the CTA-per-row kernel)
+    if (nsplit != 1 || a.pool || dense_h || !acc || passes > a.nt) return TWELL_ERR_INVALID_ARG;
+    if (a.N <= 0) return TWELL_OK;
+    if (a.C > 32 || a.d % 128 != 0 || a.nt * a.T > 65536) return TWELL_ERR_UNSUPPORTED;
+    for (int p = 0; p < passes; ++p) {
+      a.t_lo = p * a.nt / passes;
+      a.t_hi = (p + 1) * a.nt / passes;
+      a.row_counter = row_counter ? row_counter + p : nullptr;
+      a.acc = acc;
+      a.acc_mode = p == 0 ? 0 : (p + 1 < passes ? 1 : 2);
+      const int rc = launch_spmm_rowcta<uint16_t>(a, W_down, TWELL_KERNEL_SPMM, s);
+      if (rc != TWELL_OK) return rc;
+    }
+    return TWELL_OK;
+  }
   return launch_spmm_rows<uint16_t>(a, W_down, nsplit, TWELL_KERNEL_SPMM, s);
 }
 

@@ -248,9 +248,15 @@ int launch_fb_assemble(const twell_t& L, const uint16_t* spill, const int32_t* s
 // is given, else by a fixed stride.
 constexpr int kSpmmMaxArrivals = 1024;
 int spmm_nsplit(int n_rows, int d_model);
+// passes > 1 (whole rows of the row-granular hybrid only): the gather runs in
+// that many launches over consecutive tile ranges, summed in range order
+// through acc ([N][d_model] fp32), each with its own zeroed row_counter word
 int launch_spmm(const twell_t& L, const uint16_t* W_down, int d_model, uint16_t* Y, float* part, int nsplit,
                 int32_t* arrivals, int32_t* row_counter, cudaStream_t s,
-                const uint16_t* dense_h = nullptr);
+                const uint16_t* dense_h = nullptr, int passes = 1, float* acc = nullptr);
+// Passes of the forward gather over tile ranges: W_down's rows above ~64 MB
+// do not stay in L2 across one pass over all tiles.
+int spmm_single_passes(int d_model, int d_ff, int tile);
 int launch_spmm_f32(const twell_t& L, const float* vals, const uint16_t* W, int d_model, uint16_t* out,
                     int32_t* row_counter, int kernel_id, cudaStream_t s);
 // out[n] = bf16(sum over row n's TwELL entries e of a_e W_a[j_e] + b_e W_b[j_e]),

@@ -150,7 +150,10 @@ TWELL_API int twell_unpack(const twell_t* in, uint16_t* H, int64_t ldh, twell_st
  * 128-row MMA side and K split over the SMs (its fp32 partial sums added in
  * split order), and the down-projection with each row's tiles cut into ranges
  * added in order; results agree with the large-batch path up to fp32
- * summation order (bit for bit on inputs whose partial sums are exact).
+ * summation order (bit for bit on inputs whose partial sums are exact).  When
+ * W_down is larger than ~64 MB (row-granular layouts, more than 32 rows) the
+ * down-projection gathers in passes over consecutive tile ranges, whose fp32
+ * sums are added in range order, so each pass's W_down rows stay in L2.
  * More fallback rows than fb_cap: the status word reports
  * TWELL_ERR_FALLBACK_OVERFLOW and the rows past fb_cap are stored nowhere
  * (their cells are emptied); their rows of Y are left unwritten, except in

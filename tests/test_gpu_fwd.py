@@ -76,6 +76,9 @@ INT_CASES = [
     # the largest capacity (C = 32), and C = T, where no tile can overflow
     (200, 256, 1024, 64, 32, 0.8, 8),
     (130, 128, 512, 32, 32, 0.5, 9),
+    # W_down (73 MB) above the gather's L2 budget per pass: two tile-range
+    # passes with fp32 sums carried between them
+    (200, 2560, 14336, 128, 16, 0.97, 10),
 ]
 
 

@@ -220,3 +220,37 @@ def test_gated_bwd_refuses(tw):
                                      o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), db.data_ptr(), ws.data_ptr(),
                                      nbytes, None)
         assert rc == want, tw.status_string(rc)
+
+
+def test_bwd_empty_batch_zero_weight_gradients(tw):
+    """No rows: both backward calls succeed and store zero weight gradients
+    (the outputs are overwritten, not accumulated); X, dY and dX have no rows
+    and are never dereferenced."""
+    import ctypes
+    import torch
+    dev = torch.device("cuda")
+    d, f, T, C, fb = 128, 512, 64, 8, 4
+    lib = tw.load_library()
+    W = torch.ones((f, d), dtype=torch.bfloat16, device=dev)
+    b = torch.ones((f,), dtype=torch.bfloat16, device=dev)
+    fake = 0x100   # 256-byte aligned, not null: a row pointer of a zero-row tensor
+    ws = torch.empty(max(tw.bwd_workspace_bytes(0, d, f, T, C, fb), tw.gated_bwd_workspace_bytes(0, d, f, T, C, fb),
+                         256), dtype=torch.uint8, device=dev)
+    p = tw.alloc_packed(0, f, T, C, fb, dev)
+    st = p.struct()
+    o = [torch.full((f, d), 5.0, dtype=torch.float32, device=dev) for _ in range(3)]
+    db = torch.full((f,), 5.0, dtype=torch.float32, device=dev)
+    rc = lib.twell_ffn_bwd(fake, W.data_ptr(), W.data_ptr(), ctypes.byref(st), d, fake, 0.5, fake, o[0].data_ptr(),
+                           o[1].data_ptr(), db.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    torch.cuda.synchronize()
+    assert rc == 0, tw.status_string(rc)
+    assert not o[0].any() and not o[1].any() and not db.any()
+    for t in o + [db]:
+        t.fill_(5.0)
+    gu = torch.empty((16,), dtype=torch.float32, device=dev)
+    rc = lib.twell_gated_ffn_bwd(fake, W.data_ptr(), W.data_ptr(), b.data_ptr(), W.data_ptr(), ctypes.byref(st),
+                                 gu.data_ptr(), d, fake, 0.5, fake, o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(),
+                                 db.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    torch.cuda.synchronize()
+    assert rc == 0, tw.status_string(rc)
+    assert not o[0].any() and not o[1].any() and not o[2].any() and not db.any()
