@@ -46,7 +46,7 @@ EXPORTED = [
     "twell_ffn_fwd_noalloc", "twell_ffn_fwd_noalloc_max_scratch", "twell_gated_ffn_fwd",
     "twell_selftest_wait_timeout", "twell_check_format", "twell_dense_ffn_bwd", "twell_dense_bwd_workspace_bytes",
     "twell_bwd_tiles_workspace_bytes", "twell_gated_ffn_fwd_train", "twell_gated_ffn_bwd",
-    "twell_gated_bwd_workspace_bytes",
+    "twell_gated_bwd_workspace_bytes", "twell_gated_bwd_tiles_workspace_bytes",
 ]
 
 
@@ -104,6 +104,7 @@ def load_library() -> ctypes.CDLL:
         "twell_gated_ffn_bwd": (ctypes.c_int, [P, P, P, P, P, L, P, I32, P, ctypes.c_float, P, P, P, P, P, P, SZ,
                                                P]),
         "twell_gated_bwd_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+        "twell_gated_bwd_tiles_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
         "twell_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "twell_check_format": (ctypes.c_int, [L, P, P]),
         "twell_dense_ffn_bwd": (ctypes.c_int, [P, P, P, P, I32, I32, I32, P, ctypes.c_float, P, P, P, P, P, SZ, P]),
@@ -307,9 +308,11 @@ def twell_ffn_bwd(X, W_inT, W_down, packed: Packed, dY, l1_lambda: float, dX, dW
                                         _stream(stream)), "twell_ffn_bwd")
 
 
-def gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap) -> int:
-    """Workspace of twell_gated_ffn_bwd."""
-    return int(load_library().twell_gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap))
+def gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap, hybrid=None) -> int:
+    """Workspace of twell_gated_ffn_bwd; hybrid=HYBRID_TILES for a tile-granular layout."""
+    lib = load_library()
+    fn = lib.twell_gated_bwd_tiles_workspace_bytes if hybrid == HYBRID_TILES else lib.twell_gated_bwd_workspace_bytes
+    return int(fn(n_rows, d_model, d_ff, tile, cap, fb_cap))
 
 
 def twell_gated_ffn_bwd(X, W_gT, W_uT, b, W_down, packed: Packed, gu, dY, l1_lambda: float, dX, dW_gT, dW_uT,

@@ -429,7 +429,8 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   TW_TRY(check_dense(Y));
   if (W_uT && 128 % H->tile != 0) return TWELL_ERR_UNSUPPORTED;
   const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
-  if (tiles && (W_uT || (n_rows > 0 && n_rows <= kSwapMaxTokens))) return TWELL_ERR_UNSUPPORTED;
+  // the swapped small-batch path has no tile-granular form (the gated layer never takes it)
+  if (tiles && !W_uT && n_rows > 0 && n_rows <= kSwapMaxTokens) return TWELL_ERR_UNSUPPORTED;
   const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap, tiles);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
@@ -510,6 +511,30 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
 }
 }  // namespace
 
+namespace {
+// The row view of a tile-granular layout that the backward builds in its
+// workspace after the base bytes: routing words [n_rows], slots [fb_cap], the
+// count word, and the dense rows [fb_cap][d_ff] bf16.
+size_t row_view_bytes(int32_t n_rows, int32_t d_ff, int32_t fb_cap) {
+  return align256(sizeof(int32_t) * static_cast<size_t>(std::max(n_rows, 1))) +
+         align256(sizeof(int32_t) * static_cast<size_t>(std::max(fb_cap, 1))) + 256 +
+         align256(sizeof(uint16_t) * static_cast<size_t>(std::max(fb_cap, 0)) * static_cast<size_t>(d_ff));
+}
+
+twell_t row_view_in(const twell_t& H, uint8_t* v) {
+  twell_t V = H;
+  V.hybrid = TWELL_HYBRID_ROWS;
+  V.row_fb = reinterpret_cast<int32_t*>(v);
+  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H.n_rows, 1)));
+  V.fb_rows = reinterpret_cast<int32_t*>(v);
+  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H.fb_cap, 1)));
+  V.n_fb = reinterpret_cast<int32_t*>(v);
+  v += 256;
+  V.fb_dense = reinterpret_cast<uint16_t*>(v);
+  return V;
+}
+}  // namespace
+
 extern "C" {
 
 int twell_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,
@@ -570,16 +595,7 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
   // tile-granular layout: the backward of its row view, in which every row
   // holding a dense tile is a fallback row with its dense h (the layer's
   // gradients do not depend on how h is stored)
-  uint8_t* v = static_cast<uint8_t*>(workspace) + base;
-  twell_t V = *H;
-  V.hybrid = TWELL_HYBRID_ROWS;
-  V.row_fb = reinterpret_cast<int32_t*>(v);
-  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H->n_rows, 1)));
-  V.fb_rows = reinterpret_cast<int32_t*>(v);
-  v += align256(sizeof(int32_t) * static_cast<size_t>(std::max(H->fb_cap, 1)));
-  V.n_fb = reinterpret_cast<int32_t*>(v);
-  v += 256;
-  V.fb_dense = reinterpret_cast<uint16_t*>(v);
+  twell_t V = row_view_in(*H, static_cast<uint8_t*>(workspace) + base);
   TW_TRY(launch_tile_row_view(*H, V, s));
   return launch_bwd(X, W_inT, W_down, V, dY, l1_lambda, dX, dW_inT, dW_down, db, d_model, ws, s, true);
 }
@@ -587,15 +603,19 @@ int twell_ffn_bwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_do
 size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
                                        int32_t fb_cap) {
   const size_t base = twell_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap);
-  return base + align256(sizeof(int32_t) * static_cast<size_t>(std::max(n_rows, 1))) +
-         align256(sizeof(int32_t) * static_cast<size_t>(std::max(fb_cap, 1))) + 256 +
-         align256(sizeof(uint16_t) * static_cast<size_t>(std::max(fb_cap, 0)) * static_cast<size_t>(d_ff));
+  return base ? base + row_view_bytes(n_rows, d_ff, fb_cap) : 0;
 }
 
 size_t twell_gated_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile, int32_t cap,
                                        int32_t fb_cap) {
   if (n_rows < 0 || d_ff <= 0 || tile <= 0 || cap <= 0 || fb_cap < 0) return 0;
   return bwd_workspace_layout(n_rows, d_model, d_ff, tile, cap, fb_cap, nullptr, nullptr, true);
+}
+
+size_t twell_gated_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
+                                             int32_t cap, int32_t fb_cap) {
+  const size_t base = twell_gated_bwd_workspace_bytes(n_rows, d_model, d_ff, tile, cap, fb_cap);
+  return base ? base + row_view_bytes(n_rows, d_ff, fb_cap) : 0;
 }
 
 int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT, const uint16_t* b,
@@ -605,7 +625,8 @@ int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t*
                         twell_stream_t stream) {
   TW_TRY(check_layout(H));
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
-  if (d_model % 128 != 0 || H->d_ff % 128 != 0 || H->hybrid != TWELL_HYBRID_ROWS) return TWELL_ERR_UNSUPPORTED;
+  if (d_model % 128 != 0 || H->d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
+  const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
   if (static_cast<int64_t>(H->n_rows) * (H->d_ff / H->tile) * H->cap > INT32_MAX) return TWELL_ERR_UNSUPPORTED;
   for (const void* p : {static_cast<const void*>(X), static_cast<const void*>(W_gT), static_cast<const void*>(W_uT),
                         static_cast<const void*>(b), static_cast<const void*>(W_down), static_cast<const void*>(dY),
@@ -615,14 +636,21 @@ int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t*
     TW_TRY(check_dense(p));
   if (!gu) return TWELL_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(gu) % 16 != 0) return TWELL_ERR_MISALIGNED;
-  const size_t need = twell_gated_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  const size_t base = twell_gated_bwd_workspace_bytes(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap);
+  const size_t need = tiles ? base + row_view_bytes(H->n_rows, H->d_ff, H->fb_cap) : base;
   if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
   BwdWorkspace ws{};
   bwd_workspace_layout(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap, &ws, workspace, true);
   GatedBwd g{W_uT, b, gu, dW_uT};
-  return launch_bwd(X, W_gT, W_down, *H, dY, l1_lambda, dX, dW_gT, dW_down, db, d_model, ws,
-                    reinterpret_cast<cudaStream_t>(stream), false, &g);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!tiles) return launch_bwd(X, W_gT, W_down, *H, dY, l1_lambda, dX, dW_gT, dW_down, db, d_model, ws, s, false, &g);
+  // tile-granular layout: the row view, as for twell_ffn_bwd; its fallback rows
+  // (every row holding a dense tile) get g and u recomputed, its other rows'
+  // slots all have theirs from the forward
+  twell_t V = row_view_in(*H, static_cast<uint8_t*>(workspace) + base);
+  TW_TRY(launch_tile_row_view(*H, V, s));
+  return launch_bwd(X, W_gT, W_down, V, dY, l1_lambda, dX, dW_gT, dW_down, db, d_model, ws, s, true, &g);
 }
 
 int twell_dense_ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* b, const uint16_t* W_down,

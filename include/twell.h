@@ -58,9 +58,10 @@
  *     *n_fb counts dense tiles (may exceed fb_cap * n_tiles; tiles past the
  *     pool are not stored, their cells are left empty, and the status word
  *     reports TWELL_ERR_FALLBACK_OVERFLOW).
- *   - Supported by twell_pack, twell_unpack, twell_ffn_fwd (n_rows > 32) and
- *     twell_ffn_bwd (through a row view, see there); the gated forward and the
- *     small-batch forward return TWELL_ERR_UNSUPPORTED for it.
+ *   - Supported by twell_pack, twell_unpack, twell_ffn_fwd (n_rows > 32), the
+ *     gated forward (any n_rows) and both backward calls (through a row view,
+ *     see twell_ffn_bwd); the small-batch forward of the plain layer returns
+ *     TWELL_ERR_UNSUPPORTED for it.
  */
 #ifndef TWELL_H
 #define TWELL_H
@@ -279,10 +280,13 @@ TWELL_API size_t twell_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model
  *   dW_down [d_ff][d_model] fp32     dW_down[j] = sum_n h[n][j] dY[n]
  *   db      [d_ff] fp32              db[j] = sum_n dG[n][j]  (the bias sits on the gate)
  * Deterministic as twell_ffn_bwd.  workspace: device, >=
- * twell_gated_bwd_workspace_bytes(...) bytes, 256-byte aligned.
- * TWELL_ERR_UNSUPPORTED for a tile-granular layout, d_ff not a multiple of 128,
- * or n_rows * (d_ff / tile) * cap above 2^31 - 1; TWELL_ERR_MISALIGNED when gu is
- * not 16-byte aligned. */
+ * twell_gated_bwd_workspace_bytes(...) bytes, 256-byte aligned; for the
+ * tile-granular variant >= twell_gated_bwd_tiles_workspace_bytes(...).
+ * Tile-granular layouts go through the row view that twell_ffn_bwd describes:
+ * rows holding a dense tile are fallback rows, whose g and u are recomputed.
+ * TWELL_ERR_UNSUPPORTED when d_ff is not a multiple of 128, or n_rows *
+ * (d_ff / tile) * cap is above 2^31 - 1; TWELL_ERR_MISALIGNED when gu is not
+ * 16-byte aligned. */
 TWELL_API int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
                                   const uint16_t* b, const uint16_t* W_down, const twell_t* H, const float* gu,
                                   int32_t d_model, const uint16_t* dY, float l1_lambda, uint16_t* dX,
@@ -291,6 +295,11 @@ TWELL_API int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const
 
 TWELL_API size_t twell_gated_bwd_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff, int32_t tile,
                                                  int32_t cap, int32_t fb_cap);
+
+/* Workspace of twell_gated_ffn_bwd for a tile-granular layout:
+ * twell_gated_bwd_workspace_bytes plus the row view. */
+TWELL_API size_t twell_gated_bwd_tiles_workspace_bytes(int32_t n_rows, int32_t d_model, int32_t d_ff,
+                                                       int32_t tile, int32_t cap, int32_t fb_cap);
 
 /* Dense comparator (not part of the method): Y = ReLU(X.W_in + b).W_down with
  * the same tensor-core GEMM and no sparsity.  W_down is [d_ff][d_model] bf16 as

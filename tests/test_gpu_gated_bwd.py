@@ -22,12 +22,12 @@ def tw():
     return m
 
 
-def _fwd_train(tw, torch, inp, T, C, fb_cap, train=True):
+def _fwd_train(tw, torch, inp, T, C, fb_cap, train=True, hybrid=None):
     dev = torch.device("cuda")
     X, Wg, Wu, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "W_uT", "b", "W_down"))
     N, d = inp["X"].shape
     f = inp["W_inT"].shape[0]
-    p = tw.alloc_packed(N, f, T, C, fb_cap, dev)
+    p = tw.alloc_packed(N, f, T, C, fb_cap, dev, hybrid=tw.HYBRID_ROWS if hybrid is None else hybrid)
     Y = torch.full((N, d), 3.0, dtype=torch.bfloat16, device=dev)
     gu = torch.full((N, f // T, C, 2), 7.0, dtype=torch.float32, device=dev)
     ws = torch.empty(tw.fwd_workspace_bytes(N, d, f, T, C, fb_cap), dtype=torch.uint8, device=dev)
@@ -49,7 +49,8 @@ def _bwd(tw, torch, p, gu, dev_inp, dY, lam):
     dX = torch.full((N, d), 5.0, dtype=torch.bfloat16, device=dev)
     outs = [torch.full((f, d), 5.0, dtype=torch.float32, device=dev) for _ in range(3)]
     db = torch.full((f,), 5.0, dtype=torch.float32, device=dev)
-    wsb = torch.full((tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb),), 0x5A, dtype=torch.uint8, device=dev)
+    wsb = torch.full((tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb, hybrid=p.hybrid),), 0x5A, dtype=torch.uint8,
+                     device=dev)
     tw.twell_gated_ffn_bwd(X, Wg, Wu, b, Wd, p, gu, to_dev(dY, torch), lam, dX, outs[0], outs[1], outs[2], db, wsb)
     assert tw.twell_read_status(p) == 0
     torch.cuda.synchronize()
@@ -197,7 +198,8 @@ def test_gated_bwd_full_size_sampled(tw):
 
 
 def test_gated_bwd_refuses(tw):
-    """A tile-granular layout and a short workspace are refused before any launch."""
+    """A short workspace is refused before any launch, for either layout
+    (the tile-granular one needs room for its row view as well)."""
     import torch
     dev = torch.device("cuda")
     N, d, f, T, C, fb = 64, 128, 512, 64, 8, 16
@@ -212,7 +214,10 @@ def test_gated_bwd_refuses(tw):
     need = tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb)
     assert need > tw.bwd_workspace_bytes(N, d, f, T, C, fb)
     ws = torch.empty((need,), dtype=torch.uint8, device=dev)
-    for hybrid, nbytes, want in ((tw.HYBRID_ROWS, need - 256, -5), (tw.HYBRID_TILES, need, -3)):
+    need_tiles = tw.gated_bwd_workspace_bytes(N, d, f, T, C, fb, hybrid=tw.HYBRID_TILES)
+    assert need_tiles > need
+    ws = torch.empty((need_tiles,), dtype=torch.uint8, device=dev)
+    for hybrid, nbytes, want in ((tw.HYBRID_ROWS, need - 256, -5), (tw.HYBRID_TILES, need_tiles - 256, -5)):
         p = tw.alloc_packed(N, f, T, C, fb, dev, hybrid=hybrid)
         st = p.struct()
         rc = lib.twell_gated_ffn_bwd(X.data_ptr(), W.data_ptr(), W.data_ptr(), b.data_ptr(), W.data_ptr(),
@@ -254,3 +259,79 @@ def test_bwd_empty_batch_zero_weight_gradients(tw):
     torch.cuda.synchronize()
     assert rc == 0, tw.status_string(rc)
     assert not o[0].any() and not o[1].any() and not o[2].any() and not db.any()
+
+
+def test_gated_repeat_calls_bit_identical(tw):
+    """Forward and backward twice on one workspace (fallback rows present):
+    every output has the same bits, as each is summed by one thread in a fixed
+    order (no atomics on outputs)."""
+    import torch
+    cfg = synth.FFNConfig("grep", 300, 512, 2048, 128, 16, seed=29, gated=True, fb_cap=64, row_spread="lognormal",
+                          forced_frac_rows=0.03)
+    inp = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=8)
+    outs = []
+    for _ in range(2):
+        p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, cfg.tile, cfg.cap, cfg.fallback_capacity)
+        assert int(p.n_fb[0].item()) > 0
+        H, dX, dWg, dWu, dWd, db = _bwd(tw, torch, p, gu, dev_inp, dY, 1e-3)
+        outs.append([from_dev_bits(Y), H, dX, dWg.view(np.uint32), dWu.view(np.uint32), dWd.view(np.uint32),
+                     db.view(np.uint32)])
+    for a, c in zip(*outs):
+        assert np.array_equal(a, c)
+
+
+@pytest.mark.parametrize("N,d,f,T,C,sp", [(256, 128, 512, 64, 8, 0.9), (200, 256, 1024, 128, 16, 0.9),
+                                          # a small batch: the gated layer has no separate path for it
+                                          (16, 256, 1024, 64, 8, 0.9)])
+def test_gated_tiles_forward_integer_bit_exact(tw, N, d, f, T, C, sp):
+    """The gated forward on the tile-granular layout: packing (cells, dense
+    tiles of the pool in (row, tile) order) and Y equal the oracle's tile
+    packer and packed product of the oracle's gated h, bit for bit."""
+    import torch
+    inp = synth.make_integer_inputs(N, d, f, seed=N + f + 3, lo=-1, hi=1, sparsity=sp, gated=True)
+    _, Hr = oracle.hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"])
+    fb_cap = N
+    ref = oracle.pack_tiles(Hr, T, C, fb_cap * (f // T))
+    assert ref["n_fb"] > 0
+    Yr = oracle.down_packed(ref, inp["W_down"])
+    assert np.abs(Yr).max() < 2 ** 24
+    p, Y, gu, _ = _fwd_train(tw, torch, inp, T, C, fb_cap, hybrid=tw.HYBRID_TILES)
+    k = min(ref["n_fb"], ref["pool_cap"])
+    assert int(p.n_fb[0].item()) == ref["n_fb"]
+    assert np.array_equal(from_dev_bits(p.values).reshape(ref["values"].shape), ref["values"])
+    assert np.array_equal(from_dev_bits(p.idx), ref["idx"])
+    assert np.array_equal(from_dev_bits(p.counts), ref["counts"])
+    assert np.array_equal(from_dev_bits(p.fb_dense).reshape(-1, T)[:k], ref["pool"][:k])
+    assert np.array_equal(from_dev_bits(Y), oracle.round_bf16(Yr))
+
+
+def test_gated_tiles_backward_equals_rows(tw):
+    """The gated backward of a tile-granular layout runs on its row view: the
+    rows holding a dense tile are exactly the rows row routing sends whole, so
+    every gradient equals the row-routed layout's bit for bit, and both are
+    within tolerance of the oracle."""
+    import torch
+    cfg = synth.FFNConfig("gt", 301, 256, 1024, 64, 8, seed=41, gated=True, row_spread="lognormal",
+                          forced_frac_rows=0.04)
+    inp = synth.make_ffn_inputs(cfg)
+    dY = synth.make_grad_output(cfg.n_rows, cfg.d_model, seed=12)
+    lam = 1e-3
+    outs = {}
+    for name, hybrid in (("rows", tw.HYBRID_ROWS), ("tiles", tw.HYBRID_TILES)):
+        p, Y, gu, dev_inp = _fwd_train(tw, torch, inp, cfg.tile, cfg.cap, cfg.fallback_capacity, hybrid=hybrid)
+        assert int(p.n_fb[0].item()) > 0
+        counts = from_dev_bits(p.counts).copy()
+        outs[name] = _bwd(tw, torch, p, gu, dev_inp, dY, lam)
+        assert np.array_equal(from_dev_bits(p.counts), counts)   # the layout is left as it was
+    for a, c, what in zip(outs["rows"], outs["tiles"], ("H", "dX", "dW_gT", "dW_uT", "dW_down", "db")):
+        assert np.array_equal(a, c), what
+    H, dX, dWg, dWu, dWd, db = outs["tiles"]
+    dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam)
+    assert_close(synth.bf16_bits_to_f32(dX), oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"]), "dX")
+    rWg, rWu, rWd, rdb = oracle.grad_weights_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], inp["W_down"], H,
+                                                   dY, lam)
+    assert_close(dWg, rWg, "dW_gT")
+    assert_close(dWu, rWu, "dW_uT")
+    assert_close(dWd, rWd, "dW_down")
+    assert_close(db, rdb, "db")

@@ -157,8 +157,8 @@ def test_fwd_tiles_1b_sampled(tw):
 
 
 def test_tiles_refused_where_not_built(tw):
-    """The gated forward and the small-batch forward refuse the variant; the
-    backward asks for its own workspace size."""
+    """The plain layer's small-batch forward refuses the variant; the backward
+    asks for its own workspace size."""
     import torch
     lib = tw.load_library()
     N, d, f, T, C = 64, 128, 256, 64, 4
@@ -180,9 +180,6 @@ def test_tiles_refused_where_not_built(tw):
                            None)
     assert rc == -5   # TWELL_ERR_WORKSPACE
     Y = torch.empty((N, d), dtype=torch.bfloat16, device="cuda")
-    rc = lib.twell_gated_ffn_fwd(X.data_ptr(), Wi.data_ptr(), Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), N, d, f,
-                                 ctypes.byref(st), Y.data_ptr(), ws.data_ptr(), ws.numel(), None)
-    assert rc == -3
     small = tw.alloc_packed(8, f, T, C, 8, "cuda", hybrid=tw.HYBRID_TILES)
     ss = small.struct()
     rc = lib.twell_ffn_fwd(X.data_ptr(), Wi.data_ptr(), b.data_ptr(), Wd.data_ptr(), 8, d, f, ctypes.byref(ss),
