@@ -19,6 +19,13 @@
 //             dY_fb and dZ_fb^T . X_fb, dZ as high + low bf16 parts) on the
 //             second stream; dw_unitcta_kernel adds the TwELL share on top; a column
 //             sum adds the fallback share of db
+// The gated layer (h = bf16(g u), g = X.W_g + b > 0, u = X.W_u) runs the same
+// steps with pairs: its SDDMM forms (dG, dU) = (dh' u, dh' g) at the pattern
+// (dh' = dY.W_down^T + lambda sign(h)) from the (g, u) its forward kept; dX
+// gathers two weight rows per entry; the unit lists carry dU beside dG and the
+// walk adds dW_u^T[j] = sum_n dU[n][j] X[n] from the same X loads.  Its
+// fallback rows get g and u recomputed on the tensor cores (GUEpi) beside the
+// SDDMM, then dG, dU as high + low parts, three store GEMMs and two dX GEMMs.
 // No atomics on outputs, so every result is deterministic.
 #include <cuda_runtime.h>
 

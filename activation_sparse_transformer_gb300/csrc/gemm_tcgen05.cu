@@ -1,5 +1,5 @@
 // Persistent warp-specialised bf16 GEMM on the 5th-generation tensor cores
-// (tcgen05 + TMEM), fed by TMA, with four epilogues:
+// (tcgen05 + TMEM), fed by TMA, with these epilogues:
 //   * PackEpi: z = acc + b, h = bf16(z) where z > 0, compaction of each
 //     (row, T-column tile) into TwELL cells (values, tile-local indices,
 //     count) and a per-row overflow flag -- the layer's up-projection with its
@@ -12,9 +12,15 @@
 //   * DenseEpi: bf16 rows with optional bias and ReLU (dense comparator).
 //   * PartialEpi: fp32 stores, per K split when the K range is split (the
 //     fallback rows' down-projection, dX and weight-gradient shares).
-//   * GatedPackEpi: the gated (Llama-style) up-projection with the pack.
+//   * GatedPackEpi: the gated (Llama-style) up-projection with the pack; for
+//     training it also keeps (g, u) fp32 beside every stored value.
 //   * SampleEpi: dH = dY . W_down^T kept only at the TwELL pattern, plus the
-//     L1 term's gradient (bayesiansapien note, TL;DR) -- the backward SDDMM.
+//     L1 term's gradient (bayesiansapien note, TL;DR) -- the backward SDDMM;
+//     for the gated layer it forms (dG, dU) = (dh' u, dh' g) at the pattern.
+//   * GUEpi: g = X.W_g + b and u = X.W_u of the gated layer's fallback rows,
+//     for their share of its backward.
+//   * MaskEpi, PartialTEpi: the dense comparator's masked dZ, and the
+//     small-batch up-projection with swapped operands (fp32 K-split partials).
 //
 // C[M, N] = A[M, K] . B^T; A row-major [M][K] (K-major).  B is either
 // row-major [N][K] (K-major) or row-major [K][N] (N-major, e.g. W_down read as

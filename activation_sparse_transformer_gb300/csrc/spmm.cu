@@ -29,6 +29,14 @@
 // arrival counter, no waiting).  A small batch's fallback rows are gathered
 // here too, from the dense h its pack pass keeps, so no tensor-core fallback
 // GEMM and reduction follow on the second stream.
+//
+// Two more uses of the row kernel.  Pair entries (float2 values) meet two
+// weight matrices at once: the gated layer's dX = dG . W_g + dU . W_u.  And
+// when the rows a gather may name are larger than L2 holds across one pass
+// (two 117 MB matrices for the gated dX, or a 117 MB W_down), the gather runs
+// in consecutive launches over tile ranges -- each range's weight rows stay in
+// L2 for its launch -- with the fp32 sums carried between launches in range
+// order (the last one writes bf16).
 #include <cuda_runtime.h>
 
 #include <algorithm>

@@ -263,11 +263,32 @@ def roofline_entry(work, us, peaks, peak_src):
     return e
 
 
+def _code_lines(text: str):
+    """The lines of a C/CUDA source with // comments and blank lines left out
+    (a // inside a string literal is kept)."""
+    for line in text.splitlines():
+        out, in_str, i = [], False, 0
+        while i < len(line):
+            ch = line[i]
+            if ch == '"' and (i == 0 or line[i - 1] != "\\"):
+                in_str = not in_str
+            elif not in_str and line.startswith("//", i):
+                break
+            out.append(ch)
+            i += 1
+        code = "".join(out).rstrip()
+        if code:
+            yield code
+
+
 def source_digest(name: str) -> str:
-    """First 16 hex digits of the sha256 of a kernel source file (csrc/<name>)."""
+    """First 16 hex digits of the sha256 of a kernel source file's code
+    (csrc/<name>, comments and blank lines left out), so that a capture stays
+    tied to the code it measured across edits of the comments."""
     import hashlib
-    with open(os.path.join(ROOT, "activation_sparse_transformer_gb300", "csrc", name), "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    with open(os.path.join(ROOT, "activation_sparse_transformer_gb300", "csrc", name)) as fh:
+        code = "\n".join(_code_lines(fh.read()))
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, workload: str):

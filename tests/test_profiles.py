@@ -34,3 +34,14 @@ def test_traffic_records_follow_their_sources():
 def test_profiles_are_text_only():
     for name in os.listdir(os.path.join(ROOT, "profiles")):
         assert os.path.splitext(name)[1] in (".md", ".txt"), name
+
+
+def test_digest_follows_code_not_comments():
+    """A comment or blank-line edit keeps a capture's digest; any code edit
+    (a literal with // in it included) changes it."""
+    import bench
+    base = 'int a = 1;  // x\nasm("mov // y");\n'
+    same = '// header\nint a = 1;  // changed comment\n\nasm("mov // y");   \n'
+    assert list(bench._code_lines(base)) == list(bench._code_lines(same))
+    assert list(bench._code_lines(base)) != list(bench._code_lines('int a = 2;  // x\nasm("mov // y");\n'))
+    assert list(bench._code_lines(base)) != list(bench._code_lines('int a = 1;  // x\nasm("mov // z");\n'))
