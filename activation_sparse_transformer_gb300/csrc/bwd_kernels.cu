@@ -84,7 +84,7 @@ __device__ __forceinline__ int cell_idx8(uint2 w, int sl) {
 template <bool kC8, bool kGated>
 __global__ void __launch_bounds__(kListWarps * 32)
     unit_lists_kernel(Layout L, const float* __restrict__ dz_cells, int32_t* __restrict__ col_beg,
-                      int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, float* __restrict__ col_h,
+                      int32_t* __restrict__ col_end, int32_t* __restrict__ col_rows, uint16_t* __restrict__ col_h,
                       float* __restrict__ col_dz, const int32_t* __restrict__ skip_fb, float* __restrict__ col_du) {
   extern __shared__ int32_t lsm[];
   grid_dependency_wait();
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kListWarps * 32)
         const int64_t pos = base + ustart[u] + cur[u] + __popc(m[u] & ((1u << lane) - 1u));
         col_rows[pos] = r;
         if (kC8) {
-          col_h[pos] = bf16_bits_to_float(static_cast<uint16_t>(hw[sl >> 1] >> (16 * (sl & 1))));
+          col_h[pos] = static_cast<uint16_t>(hw[sl >> 1] >> (16 * (sl & 1)));
           if (kGated) {
             col_dz[pos] = dzs[2 * sl];
             col_du[pos] = dzs[2 * sl + 1];
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kListWarps * 32)
             col_dz[pos] = dzs[sl];
           }
         } else {
-          col_h[pos] = bf16_bits_to_float(L.values[cell * L.C + sl]);
+          col_h[pos] = L.values[cell * L.C + sl];
           if (kGated) {
             col_dz[pos] = dz_cells[(cell * L.C + sl) * 2];
             col_du[pos] = dz_cells[(cell * L.C + sl) * 2 + 1];
@@ -251,7 +251,7 @@ template <bool kGated>
 __global__ void __launch_bounds__(kWarps * 32, kGated ? 2 : 3)
     dw_unitcta_kernel(int f, const int32_t* __restrict__ col_beg, const int32_t* __restrict__ col_end,
                       const int32_t* __restrict__ col_rows,
-                      const float* __restrict__ col_h, const float* __restrict__ col_dz,
+                      const uint16_t* __restrict__ col_h, const float* __restrict__ col_dz,
                       const uint16_t* __restrict__ X, const uint16_t* __restrict__ dY, int d,
                       float* __restrict__ dW_inT, float* __restrict__ dW_down, float* __restrict__ db,
                       const int32_t* __restrict__ n_fb, int fb_cap, const float* __restrict__ col_du,
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kWarps * 32, kGated ? 2 : 3)
         __syncthreads();  // the previous chunk has been consumed
         if (static_cast<int>(threadIdx.x) < m) {
           const int q = b + threadIdx.x;
-          stage[threadIdx.x] = UnitEntry{col_rows[q], static_cast<uint32_t>(__float_as_uint(col_h[q]) >> 16),
+          stage[threadIdx.x] = UnitEntry{col_rows[q], static_cast<uint32_t>(col_h[q]),
                                          col_dz[q], kGated ? col_du[q] : 0.f};
         }
         __syncthreads();
@@ -482,19 +482,26 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
   const int pairs = gated ? 2 : 1;
   const size_t o_dzc = take(sizeof(float) * cells * pairs);
   const size_t o_hl = take(sizeof(uint16_t) * 2 * padf);
-  const size_t o_hfb = take(sizeof(uint16_t) * padf);
-  const size_t o_dyg = take(sizeof(uint16_t) * padd);
-  const size_t o_xg = take(sizeof(uint16_t) * 2 * padd);
-  const size_t o_part = take(sizeof(float) * pairs * ksplit * static_cast<size_t>(fb_cap) * d_model);
+  // The fallback rows' gathered operands (and, gated, their recomputed (g, u)
+  // and dh') are dead once the store GEMMs have run; the split-K partials of
+  // their dX are written after those GEMMs on the same stream, so both share
+  // one region.
+  const size_t s_hfb = align256(sizeof(uint16_t) * padf), s_dyg = align256(sizeof(uint16_t) * padd);
+  const size_t s_xg = align256(sizeof(uint16_t) * 2 * padd);
+  const size_t s_gufb = gated ? align256(sizeof(float) * 2 * padf) : 0;
+  const size_t s_dhfb = gated ? align256(sizeof(float) * padf) : 0;
+  const size_t s_part = sizeof(float) * pairs * ksplit * static_cast<size_t>(fb_cap) * d_model;
+  const size_t o_opnd = take(std::max(s_hfb + s_dyg + s_xg + s_gufb + s_dhfb, s_part));
+  const size_t o_hfb = o_opnd, o_dyg = o_hfb + s_hfb, o_xg = o_dyg + s_dyg;
+  const size_t o_gufb = o_xg + s_xg, o_dhfb = o_gufb + s_gufb;
+  const size_t o_part = o_opnd;
   const size_t o_beg = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
   const size_t o_end = take(sizeof(int32_t) * static_cast<size_t>(d_ff));
   const size_t o_rows = take(sizeof(int32_t) * cells);
-  const size_t o_h = take(sizeof(float) * cells);
+  const size_t o_h = take(sizeof(uint16_t) * cells);
   const size_t o_dz = take(sizeof(float) * cells);
   const size_t o_cnt = take(sizeof(int32_t) * 8);  // row counters, one per dX gather pass
   const size_t o_duhl = gated ? take(sizeof(uint16_t) * 2 * padf) : 0;
-  const size_t o_gufb = gated ? take(sizeof(float) * 2 * padf) : 0;
-  const size_t o_dhfb = gated ? take(sizeof(float) * padf) : 0;
   const size_t o_du = gated ? take(sizeof(float) * cells) : 0;
   const int dx_passes = gated ? spmm_pair_passes(d_model, d_ff, T) : 1;
   const size_t o_dxacc = dx_passes > 1 ? take(sizeof(float) * static_cast<size_t>(N) * d_model) : 0;
@@ -511,7 +518,7 @@ size_t bwd_workspace_layout(int N, int d_model, int d_ff, int T, int C, int fb_c
     ws->col_beg = reinterpret_cast<int32_t*>(b + o_beg);
     ws->col_end = reinterpret_cast<int32_t*>(b + o_end);
     ws->col_rows = reinterpret_cast<int32_t*>(b + o_rows);
-    ws->col_h = reinterpret_cast<float*>(b + o_h);
+    ws->col_h = reinterpret_cast<uint16_t*>(b + o_h);
     ws->col_dz = reinterpret_cast<float*>(b + o_dz);
     ws->row_counter = reinterpret_cast<int32_t*>(b + o_cnt);
     ws->du_hl = gated ? reinterpret_cast<uint16_t*>(b + o_duhl) : nullptr;

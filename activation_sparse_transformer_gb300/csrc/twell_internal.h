@@ -297,11 +297,13 @@ struct BwdWorkspace {
   uint16_t* xg2;          // [2 * fb_pad][d_model] X of the fallback rows, each row twice
   int32_t fb_pad;         // fb_cap rounded up to 64
   float* part;            // [ksplit][fb_cap][d_model] fp32 partial sums of the fallback rows' dX
+                          // (shares its region with hfb, dyg, xg2 and, gated, gu_fb, dh_fb,
+                          // which are dead before it is written)
   int32_t ksplit;
   int32_t* col_beg;       // [d_ff] start of each hidden unit's entry list (tile t's lists in [t N C, (t + 1) N C))
   int32_t* col_end;       // [d_ff] end of each hidden unit's entry list
   int32_t* col_rows;      // [capacity] row of each entry, grouped by unit, rows ascending
-  float* col_h;           // [capacity] h of each entry
+  uint16_t* col_h;        // [capacity] h of each entry (bf16 bits)
   float* col_dz;          // [capacity] dZ of each entry
   int32_t* row_counter;   // [dx_passes] the dX gather's row counters (zeroed by the SDDMM GEMM)
   // gated layer only (null otherwise); dz_cells is then [N][n_tiles][C][2]
