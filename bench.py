@@ -223,7 +223,8 @@ def kernel_work(N, d, f, T, C, nnz_tw, n_fb):
         "dx": {"bound": "hbm", "bytes": cells * C * 4 + cells * C + cells + f * d * 2 + N * d * 2,
                "l2_gather_bytes": nnz_tw * row,
                "what": "dX gather of the TwELL rows (fp32 dZ entries x W_in^T rows)"},
-        "dw": {"bound": "hbm", "bytes": 2 * N * d * 2 + 2 * f * d * 4 + nnz_tw * 12 + f * 4,
+        # the lists hold per entry its row (int32), h (bf16 bits) and dZ (fp32)
+        "dw": {"bound": "hbm", "bytes": 2 * N * d * 2 + 2 * f * d * 4 + nnz_tw * 10 + f * 4,
                "l2_gather_bytes": 2 * nnz_tw * row,
                "what": "unit-major walk: the TwELL rows' dW_down, dW_in^T (fp32, added to the fallback share "
                        "stored before it) and db"},
