@@ -99,6 +99,9 @@ def test_fwd_train_keeps_gate_and_up(tw, N, d, f, T, C, sp):
                                               # no fallback rows
                                               (200, 256, 1024, 128, 16, 0.97, 1.0),
                                               (130, 128, 512, 32, 4, 0.9, 2.0),
+                                              # d_ff a multiple of 128 but not of 256: the
+                                              # SDDMM on 128-wide tiles
+                                              (200, 128, 1152, 64, 8, 0.93, 1.0),
                                               # a small batch (one M tile, zero-filled)
                                               (16, 256, 1024, 64, 8, 0.9, 1.0)])
 def test_gated_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
