@@ -340,9 +340,11 @@ int twell_check_format(const twell_t* layout, int32_t* violations, twell_stream_
 }
 
 namespace {
-// Forward workspace: [spill tiles][spill counter][fallback down-projection
-// partials] then, for small batches, [up-projection K-split partials][dense H]
-// and [SpMM tile-range partials].
+// Forward workspace: [spill tiles][spill counter and the gather's row
+// counters][fallback down-projection partials] then, for small batches,
+// [up-projection K-split partials][dense H] and [SpMM tile-range partials], or,
+// when W_down is too large for L2, [fp32 sums carried between the gather's
+// tile-range passes].
 struct FwdWorkspace {
   size_t spill_off, count_off, part_off, total;
   int32_t spill_cap;
