@@ -254,7 +254,8 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_layout(const twell_t* L) {
+// The layout's fields (no device query).
+int check_layout_fields(const twell_t* L) {
   if (!L) return TWELL_ERR_INVALID_ARG;
   if (L->n_rows < 0 || L->d_ff <= 0 || L->fb_cap < 0) return TWELL_ERR_INVALID_ARG;
   if (L->hybrid != TWELL_HYBRID_ROWS && L->hybrid != TWELL_HYBRID_TILES) return TWELL_ERR_INVALID_ARG;
@@ -272,8 +273,14 @@ int check_layout(const twell_t* L) {
   if (!aligned16(L->values) || !aligned16(L->idx) || !aligned16(L->counts) || !aligned16(L->row_fb))
     return TWELL_ERR_MISALIGNED;
   if (L->fb_cap > 0 && (!aligned16(L->fb_rows) || !aligned16(L->fb_dense))) return TWELL_ERR_MISALIGNED;
-  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
   return TWELL_OK;
+}
+
+// The layout's fields, then the device (an sm_103a GPU current).
+int check_layout(const twell_t* L) {
+  const int rc = check_layout_fields(L);
+  if (rc != TWELL_OK) return rc;
+  return device_is_sm103() ? TWELL_OK : TWELL_ERR_NO_DEVICE;
 }
 
 int check_dense(const void* p) {
@@ -419,7 +426,7 @@ namespace {
 int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, const uint16_t* b,
             const uint16_t* W_down, int32_t n_rows, int32_t d_model, int32_t d_ff, const twell_t* H, uint16_t* Y,
             void* workspace, size_t workspace_bytes, twell_stream_t stream, float* gu = nullptr) {
-  TW_TRY(check_layout(H));
+  TW_TRY(check_layout_fields(H));
   if (n_rows < 0 || d_model <= 0 || d_ff <= 0) return TWELL_ERR_INVALID_ARG;
   if (H->n_rows != n_rows || H->d_ff != d_ff) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0) return TWELL_ERR_UNSUPPORTED;
@@ -436,6 +443,7 @@ int ffn_fwd(const uint16_t* X, const uint16_t* W_inT, const uint16_t* W_uT, cons
   const FwdWorkspace w = fwd_workspace_layout(n_rows, d_model, d_ff, H->tile, H->fb_cap, tiles);
   if (!workspace || workspace_bytes < w.total) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
+  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
   if (n_rows == 0) return TWELL_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -625,7 +633,7 @@ int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t*
                         const uint16_t* dY, float l1_lambda, uint16_t* dX, float* dW_gT, float* dW_uT,
                         float* dW_down, float* db, void* workspace, size_t workspace_bytes,
                         twell_stream_t stream) {
-  TW_TRY(check_layout(H));
+  TW_TRY(check_layout_fields(H));
   if (d_model <= 0) return TWELL_ERR_INVALID_ARG;
   if (d_model % 128 != 0 || H->d_ff % 128 != 0) return TWELL_ERR_UNSUPPORTED;
   const bool tiles = H->hybrid == TWELL_HYBRID_TILES;
@@ -642,6 +650,7 @@ int twell_gated_ffn_bwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t*
   const size_t need = tiles ? base + row_view_bytes(H->n_rows, H->d_ff, H->fb_cap) : base;
   if (!workspace || workspace_bytes < need) return TWELL_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TWELL_ERR_MISALIGNED;
+  if (!device_is_sm103()) return TWELL_ERR_NO_DEVICE;
   BwdWorkspace ws{};
   bwd_workspace_layout(H->n_rows, d_model, H->d_ff, H->tile, H->cap, H->fb_cap, &ws, workspace, true);
   GatedBwd g{W_uT, b, gu, dW_uT};

@@ -142,3 +142,38 @@ def test_binding_rejects_short_buffers(lib):
         tw.twell_pack(torch.empty((N - 1, f), **bf), p)
     with pytest.raises(ValueError, match="^violations: "):
         tw.twell_check_format(p, torch.empty(0, dtype=torch.int32))
+
+
+def test_gated_host_argument_checks_without_gpu(lib):
+    """The gated calls refuse bad arguments on the host, before any launch:
+    no up matrix, no or misaligned (g, u) buffer, a tile wider than the gated
+    GEMM's 128-unit halves, a short or misaligned workspace."""
+    import activation_sparse_transformer_gb300 as tw
+    P = ctypes.c_void_p
+    a = P(0x10000)   # aligned fake device pointers, never dereferenced
+    N, d, f = 16, 128, 1024
+    L = tw.twell_t(N, f, 64, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    ws = 1 << 30
+    # forward: no W_u, no (g, u), misaligned (g, u), T = 256
+    assert lib.twell_gated_ffn_fwd(a, a, None, a, a, N, d, f, ctypes.byref(L), a, a, ws, None) == -1
+    assert lib.twell_gated_ffn_fwd_train(a, a, a, a, a, N, d, f, ctypes.byref(L), a, None, a, ws, None) == -1
+    assert lib.twell_gated_ffn_fwd_train(a, a, a, a, a, N, d, f, ctypes.byref(L), a, P(0x10008), a, ws,
+                                         None) == -2
+    wide = tw.twell_t(N, f, 256, 8, 4, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    assert lib.twell_gated_ffn_fwd(a, a, a, a, a, N, d, f, ctypes.byref(wide), a, a, ws, None) == -3
+
+    def bwd(layout, gu, workspace, nbytes):
+        return lib.twell_gated_ffn_bwd(a, a, a, a, a, ctypes.byref(layout), gu, d, a, ctypes.c_float(0.0), a, a, a,
+                                       a, a, workspace, nbytes, None)
+
+    need = tw.gated_bwd_workspace_bytes(N, d, f, 64, 8, 4)
+    assert need > tw.bwd_workspace_bytes(N, d, f, 64, 8, 4)
+    assert tw.gated_bwd_workspace_bytes(N, d, f, 64, 8, 4, hybrid=tw.HYBRID_TILES) > need
+    assert bwd(L, None, a, need) == -1
+    assert bwd(L, P(0x10004), a, need) == -2
+    assert bwd(L, a, a, need - 256) == -5
+    assert bwd(L, a, None, need) == -5
+    assert bwd(L, a, P(0x10010), need) == -2
+    tiles = tw.twell_t(N, f, 64, 8, 4, tw.HYBRID_TILES, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000,
+                       0x8000)
+    assert bwd(tiles, a, a, need) == -5   # the row view needs room beyond the row layout's workspace
