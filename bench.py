@@ -1066,6 +1066,11 @@ def next_summary(args, steps=50):
     return out
 
 
+def synth_configs():
+    import synth
+    return synth.CONFIGS
+
+
 def cpu_sample_rows(default):
     return int(os.environ.get("TWELL_CPU_SAMPLE_ROWS", default))
 
@@ -1167,7 +1172,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="1b")
+    # the main step times the plain layer; the gated layer is timed by the
+    # gated_train block of the line and by --next
+    ap.add_argument("--config", default="1b",
+                    choices=sorted(k for k, c in synth_configs().items() if not c.gated))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-energy", action="store_true",
                     help="skip the energy loops (e.g. to keep an ncu launch list to the timed steps)")
