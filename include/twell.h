@@ -176,7 +176,8 @@ TWELL_API size_t twell_fwd_workspace_bytes(int32_t n_rows, int32_t d_model, int3
  * (the pages name a sparse "sparse_llama" model configuration, repo-explainer
  * "The Repo's Two Jobs").  W_gT and W_uT are [d_ff][d_model] bf16; b applies to
  * the gate.  h = bf16(zg * zu) where zg = X.W_g + b > 0 (fp32), else +0, so h
- * may be negative; "non-zero" is h != 0.  The tile must divide 128.  Same
+ * may be negative; "non-zero" is h != 0.  The tile must divide 128.  Both
+ * hybrid variants, at any n_rows (there is no separate small-batch path).  Same
  * workspace as twell_ffn_fwd. */
 TWELL_API int twell_gated_ffn_fwd(const uint16_t* X, const uint16_t* W_gT, const uint16_t* W_uT,
                                   const uint16_t* b, const uint16_t* W_down, int32_t n_rows,
