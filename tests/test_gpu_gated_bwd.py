@@ -103,7 +103,11 @@ def test_fwd_train_keeps_gate_and_up(tw, N, d, f, T, C, sp):
                                               # SDDMM on 128-wide tiles
                                               (200, 128, 1152, 64, 8, 0.93, 1.0),
                                               # a small batch (one M tile, zero-filled)
-                                              (16, 256, 1024, 64, 8, 0.9, 1.0)])
+                                              (16, 256, 1024, 64, 8, 0.9, 1.0),
+                                              # the epilogue's largest capacity (C = 32), and C = T,
+                                              # where no tile can overflow
+                                              (160, 128, 512, 64, 32, 0.6, 1.0),
+                                              (160, 128, 512, 32, 32, 0.5, 1.0)])
 def test_gated_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
     """Integer layer and integer dY, lambda an integer: dG, dU and every sum are
     exact in fp32 (the fallback rows' dG and dU fit the 16 bits of their high +
@@ -116,7 +120,7 @@ def test_gated_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
     _, Hr = oracle.hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"])
     assert np.array_equal(H, Hr)
     n_fb = int(p.n_fb[0].item())
-    assert (n_fb > 0) == (sp < 0.97)
+    assert (n_fb > 0) == (sp < 0.97 and C < T)
     dG, dU = oracle.grad_hidden_gated(inp["X"], inp["W_inT"], inp["W_uT"], inp["b"], dY, inp["W_down"], H, lam)
     assert np.abs(np.concatenate([dG, dU])).max() < 2 ** 15
     rdX = oracle.grad_input_gated(dG, dU, inp["W_inT"], inp["W_uT"])
