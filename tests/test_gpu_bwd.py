@@ -165,3 +165,49 @@ def test_train_shape_full_size_sampled(tw):
     assert_close(dWi[cols], rWi, "dW_inT")
     assert_close(dWd[cols], rWd, "dW_down")
     assert_close(db[cols], rdb, "db")
+
+
+@pytest.mark.parametrize("N,d,f,T,C,sp,lam", [(256, 128, 512, 64, 8, 0.92, 1.0), (200, 256, 1024, 128, 16, 0.9, 0.0),
+                                              (130, 128, 512, 32, 4, 0.9, 2.0),
+                                              # a small batch: its forward takes the small-batch path
+                                              (16, 256, 1024, 64, 8, 0.9, 1.0),
+                                              # wide rows, most of them routed to the fallback
+                                              (300, 2048, 1024, 128, 8, 0.95, 1.0)])
+def test_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
+    """Integer layer, integer dY and lambda: every dZ, every product and every
+    partial sum is an exact fp32 integer (the fallback rows' dZ fit the 16 bits
+    of their high + low bf16 parts), so dX, dW_in^T, dW_down and db equal the
+    oracle's bit for bit, TwELL rows and fallback rows alike."""
+    import torch
+    dev = torch.device("cuda")
+    inp = synth.make_integer_inputs(N, d, f, seed=N + f + 5, lo=-1, hi=1, sparsity=sp)
+    rng = np.random.default_rng(N + 1)
+    dY = synth.f32_to_bf16_bits(rng.integers(-1, 2, size=(N, d)).astype(np.float32))
+    X, Wi, b, Wd = (to_dev(inp[k], torch) for k in ("X", "W_inT", "b", "W_down"))
+    p = tw.alloc_packed(N, f, T, C, N, dev)
+    Y = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(tw.fwd_workspace_bytes(N, d, f, T, C, N), tw.bwd_workspace_bytes(N, d, f, T, C, N)),
+                     dtype=torch.uint8, device=dev)
+    tw.twell_ffn_fwd(X, Wi, b, Wd, p, Y, ws)
+    assert tw.twell_read_status(p) == 0
+    assert int(p.n_fb[0].item()) > 0
+    dX = torch.full((N, d), 5.0, dtype=torch.bfloat16, device=dev)
+    dWi = torch.full((f, d), 5.0, dtype=torch.float32, device=dev)
+    dWd = torch.full((f, d), 5.0, dtype=torch.float32, device=dev)
+    db = torch.full((f,), 5.0, dtype=torch.float32, device=dev)
+    tw.twell_ffn_bwd(X, Wi, Wd, p, to_dev(dY, torch), lam, dX, dWi, dWd, db, ws)
+    torch.cuda.synchronize()
+    _, H = oracle.hidden(inp["X"], inp["W_inT"], inp["b"])
+    Hg = torch.empty((N, f), dtype=torch.bfloat16, device=dev)
+    tw.twell_unpack(p, Hg)
+    assert np.array_equal(from_dev_bits(Hg), H)
+    _, dZ = oracle.grad_hidden(dY, inp["W_down"], H, lam)
+    assert np.abs(dZ).max() < 2 ** 15
+    rdX = oracle.grad_input(dZ, inp["W_inT"])
+    rWi, rWd, rdb = oracle.grad_weights(inp["X"], inp["W_down"], H, dY, lam)
+    for a in (rdX, rWi, rWd, rdb):
+        assert np.abs(a).max() < 2 ** 24
+    assert np.array_equal(from_dev_bits(dX), oracle.round_bf16(rdX))
+    assert np.array_equal(dWi.cpu().numpy(), rWi)
+    assert np.array_equal(dWd.cpu().numpy(), rWd)
+    assert np.array_equal(db.cpu().numpy(), rdb)
