@@ -172,7 +172,9 @@ def test_train_shape_full_size_sampled(tw):
                                               # a small batch: its forward takes the small-batch path
                                               (16, 256, 1024, 64, 8, 0.9, 1.0),
                                               # wide rows, most of them routed to the fallback
-                                              (300, 2048, 1024, 128, 8, 0.95, 1.0)])
+                                              (300, 2048, 1024, 128, 8, 0.95, 1.0),
+                                              # the widest tile (the unit lists' largest shared memory)
+                                              (200, 256, 1024, 256, 16, 0.95, 1.0)])
 def test_bwd_integer_bit_exact(tw, N, d, f, T, C, sp, lam):
     """Integer layer, integer dY and lambda: every dZ, every product and every
     partial sum is an exact fp32 integer (the fallback rows' dZ fit the 16 bits
